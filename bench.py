@@ -1,0 +1,457 @@
+"""Throughput of the sparse-MoE FFN forward on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one forward pass of the whole layer (router GEMM + selection,
+dispatch, grouped expert GEMMs, shared experts, combine, balance statistic)
+over one batch of seeded synthetic tokens.  The default workload is the
+Qwen3-style layer: 16384 tokens, d_model 2048, 128 SwiGLU experts of width
+768, top-8 with Zipf-skewed routing.
+
+`value` is tokens/s with inputs resident in HBM, timed with CUDA events on
+the launching stream over the K steps (each stage bracketed by its own
+events, which also give the per-stage times and the roofline of the
+dominant kernel).  `e2e` is the same metric through moe_forward_host: the
+timed region includes the copy of x from page-locked host memory and the
+copy of the output back.  The layer's working set (x, 1.2 GB of expert
+weights, the 1.3 GB of grouped intermediates) is far larger than the 126 MB
+L2, so no flush is needed between steps.
+
+Several GPUs run independent replicas (the layer has no exchange step
+without a global capacity): one process per GPU under torchrun, a barrier
+and the max over ranks around the timed region, and `value` counts the
+tokens of all ranks.
+
+`--impl reference` times the CPU oracle (the only reference there is) on a
+bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from routing_dispatch_expert_05_b300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; grouped-GEMM % bf16 peak; routing % HBM BW"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
+                  "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.out = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        try:
+            with open(self.out) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    if self.uuid and parts[1] != self.uuid:
+                        continue
+                    rows.append(parts)
+            os.unlink(self.out)
+        except OSError:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def oracle_sample(shape, inputs, target_s=12.0, max_tokens=None):
+    """Time the CPU oracle's forward on the first n tokens of the workload
+    (same layer parameters), n grown until one run takes ~target_s."""
+    from oracle import moe_oracle as O
+    n = min(64, shape.n_tokens)
+    elapsed = 0.0
+    while True:
+        sub = inputs.first_tokens(n)
+        t0 = time.perf_counter()
+        O.forward(sub.shape, sub.values)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= target_s / 4 or n >= shape.n_tokens or (max_tokens and n >= max_tokens):
+            break
+        n = min(shape.n_tokens, n * 4)
+    return n, elapsed
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [os.cpu_count() or 1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def kernel_launches_per_step(shape):
+    """Kernels the library launches for one moe_forward of this layer."""
+    router = 3          # logits GEMM, selection, statistic finalize
+    dispatch = 4        # count, scan, rank, gather
+    experts = 2         # grouped up (with activation), grouped down
+    shared = 2 if shape.n_shared > 0 else 0
+    combine = 1
+    return router + dispatch + experts + shared + combine
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, shape, peaks, peaks_kind):
+    import torch
+    import torch.distributed as dist
+    from routing_dispatch_expert_05_b300 import moe as M
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    inputs = W.make_inputs(shape)
+    t = M.upload(inputs, device=dev)
+    cfg = M.make_config(shape)
+    weights = M.make_weights(t)
+    ws = M.MoEWorkspace(cfg, device=dev)
+    N, d, E, k, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.top_k, shape.d_ff
+    td = M.torch_dtype(shape.dtype)
+    es = 2 if shape.dtype == W.DTYPE_BF16 else 4
+    x = t["x"]
+    # stage buffers (views of nothing: separate allocations for the staged step)
+    idx = torch.empty(N, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(N, k, dtype=torch.float32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ros = torch.empty(N * k, dtype=torch.int32, device=dev)
+    tor = torch.empty(N * k, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(N * k, d, dtype=td, device=dev)
+    h = torch.empty(N * k, F, dtype=td, device=dev)
+    y = torch.empty(N * k, d, dtype=torch.float32, device=dev)
+    out = torch.empty(N, d, dtype=td, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    kept = torch.empty(E, dtype=torch.int32, device=dev)
+    dropped = torch.empty(E, dtype=torch.int32, device=dev)
+    bal = torch.empty(1, dtype=torch.float32, device=dev)
+    hs = so = None
+    if shape.n_shared > 0:
+        hs = torch.empty(N, shape.n_shared * shape.d_ff_shared, dtype=td, device=dev)
+        so = torch.empty(N, d, dtype=torch.float32, device=dev)
+    rstats = M.make_stats(counts=counts, balance=bal)
+    dstats = M.make_stats(kept=kept, dropped=dropped)
+    fstats = M.make_stats(counts=counts, kept=kept, dropped=dropped, balance=bal)
+    stream = torch.cuda.current_stream(dev)
+    stages = ["router", "dispatch", "expert_up", "expert_down"] + \
+        (["shared"] if shape.n_shared > 0 else []) + ["combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        M.moe_router_topk(cfg, x, weights, None, idx, wts, rstats, ws)
+        mark(1)
+        M.moe_dispatch_permute(cfg, idx, x, offsets, ros, tor, x_perm, dstats, ws)
+        mark(2)
+        M.moe_expert_up(cfg, x_perm, offsets, weights, h, ws)
+        mark(3)
+        M.moe_expert_down(cfg, h, offsets, weights, y, ws)
+        i = 4
+        mark(i)
+        if so is not None:
+            M.moe_shared_ffn(cfg, x, weights, hs, so, ws)
+            i += 1
+            mark(i)
+        M.moe_combine(cfg, y, ros, wts, so, out, ws)
+        mark(i + 1)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if ws_n > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    n_ev = len(stages) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+           for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = {name: statistics.median(
+        [evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)])
+        for i, name in enumerate(stages)}
+    stage_mean = {name: sum(evs[s][i].elapsed_time(evs[s][i + 1])
+                            for s in range(args.steps)) / args.steps
+                  for i, name in enumerate(stages)}
+    ms_step = total_ms / args.steps
+    if ws_n > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    # the same step through the single moe_forward call
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        M.moe_forward(cfg, x, weights, out, fstats, ws)
+    f1.record(stream)
+    barrier()
+    fwd_ms = f0.elapsed_time(f1) / args.steps
+
+    # end to end through moe_forward_host: H2D of x and D2H of out inside
+    xh = x.cpu().pin_memory()
+    oh = torch.empty(N, d, dtype=td).pin_memory()
+    for _ in range(2):
+        M.moe_forward_host(cfg, xh, weights, oh, fstats, ws)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        M.moe_forward_host(cfg, xh, weights, oh, fstats, ws)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if ws_n > 1:
+        tt = torch.tensor([e2e_ms, fwd_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms, fwd_ms = float(tt[0].item()), float(tt[1].item())
+    err = M.moe_read_device_error(ws)
+    if err != M.MOE_OK:
+        raise RuntimeError(f"device error word set: {M.STATUS_NAMES.get(err, err)}")
+
+    # roofline of the dominant kernel: the grouped up projection (2/3 of the
+    # routed FLOPs): 2 * d * (2F for SwiGLU, F otherwise) per kept assignment
+    m_kept = int(kept.sum().item())
+    up_cols = 2 * F if shape.expert == W.EXPERT_SWIGLU else F
+    up_flop = 2.0 * m_kept * d * up_cols
+    down_flop = 2.0 * m_kept * F * d
+    up_ms = stage_mean["expert_up"]
+    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved = up_flop / (up_ms * 1e-3) / 1e12
+    traffic = args.up_traffic_bytes
+    roofline = {"bound": "tensor", "kernel": "grouped expert up-projection (tcgen05)",
+                "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved / peak_tf, 4),
+                "peak_kind": f"{peaks_kind} sustained bf16",
+                "frac_of_burst": round(achieved / peaks.get("bf16_tflops", peak_tf), 4),
+                "algorithmic_flop_per_launch": up_flop,
+                "traffic": traffic}
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    # algorithmic bytes of the HBM-bound stages (per step)
+    router_bytes = N * d * es + E * d * es + N * k * 8
+    dispatch_bytes = N * d * es + m_kept * d * es + N * k * 4 * 3
+    combine_bytes = m_kept * d * 4 + N * d * es + N * k * 8 + \
+        (N * d * 4 if shape.n_shared > 0 else 0)
+    stage_report = {}
+    for name in stages:
+        entry = {"ms": round(stage_ms[name], 4)}
+        if name == "expert_up":
+            entry["tflops"] = round(up_flop / (stage_ms[name] * 1e-3) / 1e12, 1)
+        if name == "expert_down":
+            entry["tflops"] = round(down_flop / (stage_ms[name] * 1e-3) / 1e12, 1)
+        if name == "shared":
+            sf = 2.0 * N * d * 3 * shape.n_shared * shape.d_ff_shared
+            entry["tflops"] = round(sf / (stage_ms[name] * 1e-3) / 1e12, 1)
+        if name in ("router", "dispatch", "combine"):
+            b = {"router": router_bytes, "dispatch": dispatch_bytes,
+                 "combine": combine_bytes}[name]
+            gbs = b / (stage_ms[name] * 1e-3) / 1e9
+            entry["gbs"] = round(gbs, 1)
+            entry["hbm_frac"] = round(gbs / hbm, 4)
+        stage_report[name] = entry
+    grouped_flop = up_flop + down_flop
+    grouped_ms = stage_ms["expert_up"] + stage_ms["expert_down"]
+
+    res = {
+        "metric": METRIC,
+        "value": round(N * ws_n / (ms_step * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if shape.dtype == W.DTYPE_BF16 else "f32",
+        "data": "synthetic (seeded PCG64; random-init weights of the layer's shapes)",
+        "config": {"workload": shape.name, "n_tokens": N, "d_model": d,
+                   "n_experts": E, "top_k": k, "d_ff": F,
+                   "n_shared": shape.n_shared, "route": shape.route,
+                   "capacity_factor": shape.capacity_factor,
+                   "parallelism": f"replicas x{ws_n}",
+                   "l2": "working set > 126 MB L2 (no flush needed)",
+                   "forward_api_ms_per_step": round(fwd_ms, 4),
+                   "grouped_gemm_tflops": round(grouped_flop / (grouped_ms * 1e-3) / 1e12, 1),
+                   "grouped_gemm_frac_of_sustained": round(
+                       grouped_flop / (grouped_ms * 1e-3) / 1e12 / peak_tf, 4),
+                   "stages": stage_report},
+        "roofline": roofline,
+        "e2e": {"value": round(N * ws_n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": N * d * es, "d2h_bytes_per_step": N * d * es,
+                "ms_per_step": round(e2e_ms, 4), "api": "moe_forward_host"},
+        "gpu_launches": kernel_launches_per_step(shape) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        n_s, el = oracle_sample(shape, inputs, target_s=args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(n_s / el, 2), "unit": "tokens/s",
+                               "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"first {n_s} tokens of the workload, one "
+                                         f"forward, {el:.2f} s"}
+    if ws_n > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return res, rank
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args, shape):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None, rank
+    inputs = W.make_inputs(shape)
+    from oracle import moe_oracle as O
+    n_s, el = oracle_sample(shape, inputs, target_s=max(1.0, args.cpu_seconds / 2),
+                            max_tokens=args.ref_tokens)
+    sub = inputs.first_tokens(n_s)
+    for _ in range(args.warmup):
+        O.forward(sub.shape, sub.values)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        O.forward(sub.shape, sub.values)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    v = round(n_s / sec, 2)
+    cores = blas_threads()
+    res = {
+        "impl": "reference",
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.dtype == W.DTYPE_BF16 else "f32",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": shape.name, "n_tokens": shape.n_tokens,
+                   "sample_tokens": n_s},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"first {n_s} tokens of the workload per step"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return res, rank
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3_moe", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=1024)
+    ap.add_argument("--up-traffic-bytes", type=float, default=None,
+                    help="DRAM bytes per launch of the up projection from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res, rank = run_reference(args, shape)
+    else:
+        from routing_dispatch_expert_05_b300 import build as B
+        B.build()
+        peaks, kind = load_peaks()
+        res, rank = run_ours(args, shape, peaks, kind)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

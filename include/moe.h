@@ -1,0 +1,288 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN forward.
+ *
+ * The layer (one GPU, one CUDA stream, no host synchronisation):
+ *
+ *   logits = x W_r^T + b_r                         router GEMM
+ *   idx, w = select(logits)                        top-k in one of three modes
+ *   offsets, row_of_slot, x_perm = dispatch(idx)   histogram, scan, stable
+ *                                                  permutation, capacity drop
+ *   h = act(x_perm W1^T [, x_perm W3^T])           grouped expert GEMM (up)
+ *   y = h W2^T (+ b2)                              grouped expert GEMM (down)
+ *   S = sum_s SwiGLU_s(x)                          always-on shared experts
+ *   out[t] = sum_j w[t,j] y[row_of_slot[t,j]] + S[t]   weighted combine
+ *   balance = coef * sum_e (count_e / N) * (mean_t p[t,e])
+ *
+ * Sources (page titles and sections):
+ *   - "Hands-on build guide: pure-Python MoE router with load-balanced top-k
+ *     gating", Architecture Overview and steps 2 and 5 (gate, combine).
+ *   - "Expert Networks > Code Implementation", In[7] (SiLU-MLP expert with
+ *     bias) and In[10] (capacity = int(cf * (N // E)), token-order drop).
+ *   - "DeepSeek 5.7: MoE from scratch", sections 1-4 (SwiGLU expert, sigmoid
+ *     selection with a selection-only balancing bias, dispatch/combine,
+ *     shared experts) and Failure modes (empty expert batches are legal).
+ *   - "Tutorial -- MoE SER Expert Routing", sections 3-4 (tokens per expert,
+ *     load-balancing statistic).
+ *   - "Implementing Mixed Expert (MoE) layers", Core Algorithmic Steps
+ *     (topk on raw gate scores, softmax over the k, grouping by expert,
+ *     SwiGLU expert, index_add_ combine).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" point to GPU memory of the current device; the
+ *     caller allocates and frees all of it.  Entry points never allocate,
+ *     free or synchronise (moe_read_device_error is the one exception: it
+ *     waits for the stream to read one word back).
+ *   - All work is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and is asynchronous; results are valid once the
+ *     stream has reached that point.
+ *   - Tensors are dense row-major.  Weights use the PyTorch Linear layout
+ *     [out, in], stacked over experts.  Every device pointer must be 16-byte
+ *     aligned.  x, weights, biases (except sel_bias), the hidden activations
+ *     h and out are in the layer dtype (fp32 or bf16); logits, w, sel_bias,
+ *     the expert outputs y and the shared-expert sum S are fp32; indices are
+ *     int32.
+ *   - Accumulation is fp32, and it runs from the down projection through
+ *     the weighted combine: y is not rounded to bf16, the layer output is
+ *     rounded once.  bf16 tensors are rounded to nearest even.
+ *   - A status other than MOE_OK is returned before anything is enqueued
+ *     when arguments are invalid (MOE_ERR_INVALID_ARG / _UNSUPPORTED /
+ *     _WORKSPACE); MOE_ERR_CUDA reports a failed launch.  Problems found on
+ *     the device (an expert index outside [0, E), a bounded wait that ran
+ *     out) set a sticky error word at the start of the workspace instead;
+ *     read it with moe_read_device_error.
+ *   - The workspace `ws` must be zero-filled once when it is allocated (its
+ *     first word is the device error word); after that no call needs it
+ *     cleared.  Calls that share a workspace must be ordered on one stream.
+ *   - n_tokens == 0 is legal: outputs are empty, counts/kept/dropped are
+ *     zero-filled, balance is 0.
+ */
+#ifndef MOE_B300_H_
+#define MOE_B300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+typedef int32_t moe_status_t;
+#define MOE_OK                 0
+#define MOE_ERR_INVALID_ARG   -1  /* bad size, null or misaligned pointer */
+#define MOE_ERR_UNSUPPORTED   -2  /* valid layer the library does not run */
+#define MOE_ERR_WORKSPACE     -3  /* ws_bytes smaller than required        */
+#define MOE_ERR_CUDA          -4  /* a CUDA launch or copy failed          */
+#define MOE_ERR_TIMEOUT       -5  /* device error word: a bounded wait ran out */
+#define MOE_ERR_DEVICE_CHECK  -6  /* device error word: bad index seen    */
+
+/* ---- enumerations (stored as int32 in moe_config_t) ---------------- */
+#define MOE_F32   0
+#define MOE_BF16  1
+
+/* Selection modes.
+ * SOFTMAX_TOPK: p = softmax over all E logits; the k experts with the
+ *   largest logits (equivalently largest p) are chosen; w_j = p_j / sum of
+ *   the chosen p ("Hands-on build guide", step 2, and its test that the
+ *   weights sum to 1).
+ * TOPK_SOFTMAX: the k largest raw logits are chosen; w = softmax over those
+ *   k logits ("Implementing Mixed Expert (MoE) layers", Core Algorithmic
+ *   Steps).
+ * SIGMOID_BIAS: s_e = sigmoid(logit_e), evaluated in double and rounded to
+ *   fp32; the k largest keys s_e + sel_bias_e (fp32 add) are chosen;
+ *   w_j = s_j / sum of the chosen s -- the bias never enters a weight
+ *   ("DeepSeek 5.7", section 2).
+ * In every mode equal keys go to the lower expert index, and slot j of a
+ * token holds its j-th best expert (key descending). */
+#define MOE_ROUTE_SOFTMAX_TOPK  0
+#define MOE_ROUTE_TOPK_SOFTMAX  1
+#define MOE_ROUTE_SIGMOID_BIAS  2
+
+/* Expert kinds.
+ * SILU_MLP: y = W2 silu(W1 x + b1) + b2 ("Expert Networks", In[7]).
+ * SWIGLU:   y = W2 (silu(W1 x) * (W3 x)) (no bias) ("Implementing Mixed
+ *           Expert (MoE) layers", expert forward pass; "DeepSeek 5.7" s.1). */
+#define MOE_EXPERT_SILU_MLP  0
+#define MOE_EXPERT_SWIGLU    1
+
+/* Limits of this build. */
+#define MOE_MAX_EXPERTS  256
+
+/* Layer description.  All fields are read, none is written. */
+typedef struct moe_config {
+  int64_t n_tokens;        /* N >= 0 (batch * sequence, flattened)            */
+  int32_t d_model;         /* d >= 1; multiple of 8 (bf16) or 4 (fp32)        */
+  int32_t n_experts;       /* E in [1, MOE_MAX_EXPERTS]                        */
+  int32_t top_k;           /* k in [1, E]                                      */
+  int32_t d_ff;            /* F >= 1; multiple of 8 (bf16) or 4 (fp32)        */
+  int32_t n_shared;        /* number of always-on shared SwiGLU experts (>= 0) */
+  int32_t d_ff_shared;     /* their hidden width Fs (multiple of 64 if > 0)    */
+  float   capacity_factor; /* <= 0: no limit; else capacity =
+                              int(capacity_factor * (N / E)), N / E integer
+                              division ("Expert Networks", In[10])            */
+  int32_t route;           /* MOE_ROUTE_*                                      */
+  int32_t expert;          /* MOE_EXPERT_*                                     */
+  int32_t dtype;           /* MOE_F32 or MOE_BF16                              */
+  int32_t has_bias;        /* SiLU-MLP only: 1 = b1 and b2 are present         */
+  float   balance_coef;    /* coefficient of the balance statistic (0.01 in
+                              "Tutorial -- MoE SER Expert Routing")           */
+} moe_config_t;
+
+/* Device weights (PyTorch Linear layout [out, in], experts stacked). */
+typedef struct moe_weights {
+  const void  *w_router;   /* [E, d]                                  required */
+  const void  *b_router;   /* [E] router bias / logit offset          nullable */
+  const float *sel_bias;   /* [E] fp32 selection-only bias, required in
+                              SIGMOID_BIAS mode, ignored otherwise             */
+  const void  *w1;         /* [E, F, d] gate (SwiGLU) / first layer  required */
+  const void  *b1;         /* [E, F]   SiLU-MLP with has_bias                   */
+  const void  *w3;         /* [E, F, d] up projection, SwiGLU only             */
+  const void  *w2;         /* [E, d, F] down projection               required */
+  const void  *b2;         /* [E, d]   SiLU-MLP with has_bias                   */
+  const void  *ws1;        /* [S, Fs, d] shared gate     (n_shared > 0)        */
+  const void  *ws3;        /* [S, Fs, d] shared up       (n_shared > 0)        */
+  const void  *ws2;        /* [S, d, Fs] shared down     (n_shared > 0)        */
+} moe_weights_t;
+
+/* Device statistics outputs; every pointer is nullable. */
+typedef struct moe_stats {
+  int32_t *counts;   /* [E] selections per expert, before any drop          */
+  int32_t *kept;     /* [E] assignments processed (<= capacity)              */
+  int32_t *dropped;  /* [E] assignments dropped by the capacity              */
+  float   *balance;  /* [1] coef * sum_e (counts_e / N) * mean_t p[t, e]     */
+} moe_stats_t;
+
+/* ---- sizes ------------------------------------------------------------ */
+
+/* Bytes of scratch the stage calls below need in `ws` (error word, router
+ * and dispatch partial sums, a logits buffer).  Never fails for a valid
+ * config; returns MOE_ERR_INVALID_ARG otherwise. */
+MOE_API moe_status_t moe_scratch_size(const moe_config_t *cfg, size_t *bytes);
+
+/* Bytes of workspace moe_forward / moe_forward_host need: the scratch plus
+ * every intermediate of the layer sized for the worst case M = N * k
+ * (idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, and for shared
+ * experts their hidden activations and fp32 sum; host staging for x, out). */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
+
+/* ---- stages ----------------------------------------------------------- */
+
+/* Router GEMM plus selection.
+ * x [N, d] (device, layer dtype); weights->w_router, ->b_router,
+ * ->sel_bias used.  Writes idx [N, k] int32 and w [N, k] fp32 (device), and
+ * if non-NULL logits [N, E] fp32 (device).  stats->counts receives the
+ * selections per expert and stats->balance the balance statistic (both
+ * optional).  ws: scratch of moe_scratch_size bytes. */
+MOE_API moe_status_t moe_router_topk(const moe_config_t *cfg, const void *x,
+                             const moe_weights_t *weights, float *logits,
+                             int32_t *idx, float *w, moe_stats_t *stats,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* Selection alone, from given logits [N, E] fp32 (device): the same
+ * selection, weights and statistics as moe_router_topk.  sel_bias [E] fp32
+ * (device) is required in SIGMOID_BIAS mode. */
+MOE_API moe_status_t moe_route_logits(const moe_config_t *cfg, const float *logits,
+                              const float *sel_bias, int32_t *idx, float *w,
+                              moe_stats_t *stats, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* Grouping by expert with the capacity drop ("Expert Networks", In[10];
+ * "DeepSeek 5.7", section 3).  idx [N, k] int32 (device); x [N, d].
+ * Assignments are taken in token order, slot order within a token.  The
+ * r-th assignment (r from 0) of expert e is kept iff r < capacity; kept
+ * assignments of e occupy rows offsets[e] .. offsets[e+1]-1 in arrival
+ * order.  Writes offsets [E+1], row_of_slot [N*k] (-1 = dropped),
+ * token_of_row [N*k] (first offsets[E] entries valid) and
+ * x_perm [N*k, d] (first offsets[E] rows valid), and the stats
+ * counts/kept/dropped.  An index outside [0, E) is treated as dropped and
+ * sets MOE_ERR_DEVICE_CHECK in the error word. */
+MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t *idx,
+                                  const void *x, int32_t *offsets,
+                                  int32_t *row_of_slot, int32_t *token_of_row,
+                                  void *x_perm, moe_stats_t *stats, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/* Expert up-projection and activation on the expert-sorted rows:
+ * for each expert e and row r in [offsets[e], offsets[e+1]):
+ *   SwiGLU:   h[r] = silu(W1[e] x_perm[r]) * (W3[e] x_perm[r])
+ *   SiLU-MLP: h[r] = silu(W1[e] x_perm[r] + b1[e])
+ * x_perm [N*k, d], offsets [E+1] (device, read on the device), h [N*k, F]. */
+MOE_API moe_status_t moe_expert_up(const moe_config_t *cfg, const void *x_perm,
+                           const int32_t *offsets, const moe_weights_t *weights,
+                           void *h, void *ws, size_t ws_bytes, void *stream);
+
+/* Expert down-projection: y[r] = W2[e] h[r] (+ b2[e]); y [N*k, d] fp32. */
+MOE_API moe_status_t moe_expert_down(const moe_config_t *cfg, const void *h,
+                             const int32_t *offsets,
+                             const moe_weights_t *weights, float *y,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* moe_expert_up followed by moe_expert_down (h is caller memory). */
+MOE_API moe_status_t moe_grouped_ffn(const moe_config_t *cfg, const void *x_perm,
+                             const int32_t *offsets,
+                             const moe_weights_t *weights, void *h, float *y,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* Always-on shared experts ("DeepSeek 5.7", section 4):
+ * S[t] = sum_s W2s[s] (silu(W1s[s] x[t]) * (W3s[s] x[t])), each with weight
+ * one.  Computed as one SwiGLU of width S*Fs (row-concatenated gate/up,
+ * column-concatenated down).  x [N, d]; h_shared [N, S*Fs] layer dtype
+ * (device scratch, caller memory); shared_out [N, d] fp32. */
+MOE_API moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x,
+                            const moe_weights_t *weights, void *h_shared,
+                            float *shared_out, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/* Weighted combine back to token order ("Implementing Mixed Expert (MoE)
+ * layers", weighted aggregation; "Hands-on build guide", step 5):
+ *   out[t] = sum_{j : row_of_slot[t*k+j] >= 0} w[t,j] * y[row_of_slot[t*k+j]]
+ *            (+ shared_out[t])
+ * accumulated in fp32 in slot order, one rounding to the layer dtype.
+ * y [N*k, d] fp32; row_of_slot [N*k]; w [N, k] fp32; shared_out [N, d] fp32
+ * (nullable); out [N, d]. */
+MOE_API moe_status_t moe_combine(const moe_config_t *cfg, const float *y,
+                         const int32_t *row_of_slot, const float *w,
+                         const float *shared_out, void *out, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* ---- the whole layer ---------------------------------------------------- */
+
+/* All stages above on one stream, intermediates in `ws`
+ * (moe_workspace_size bytes).  x [N, d] and out [N, d] are device memory. */
+MOE_API moe_status_t moe_forward(const moe_config_t *cfg, const void *x,
+                         const moe_weights_t *weights, void *out,
+                         moe_stats_t *stats, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/* moe_forward for callers whose activations live in host memory: copies
+ * x_host [N, d] into the workspace, runs the layer and copies the result to
+ * out_host [N, d], all enqueued on `stream` (use page-locked host memory
+ * for asynchronous copies).  Weights and stats are device memory. */
+MOE_API moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_host,
+                              const moe_weights_t *weights, void *out_host,
+                              moe_stats_t *stats, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* ---- diagnostics -------------------------------------------------------- */
+
+/* Waits for `stream`, then reads and clears the device error word at the
+ * start of `ws`: *code = MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT. */
+MOE_API moe_status_t moe_read_device_error(void *ws, int32_t *code, void *stream);
+
+/* Static description of a status code (never NULL). */
+MOE_API const char *moe_status_string(moe_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MOE_API int32_t moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H_ */

@@ -23,7 +23,9 @@ Page citations (titles as printed on the pages):
   index_add_ combine).
 
 Readings where the pages are silent or disagree (each also listed in the
-design notes): capacity is int(cf * (N // E)) applied per expert with
+design notes): storage points are x, weights, h and the output in the layer
+dtype, logits, weights w, the expert outputs y and the shared sum S in
+fp32; capacity is int(cf * (N // E)) applied per expert with
 assignments taken in token order; dropped assignments contribute zero and the
 surviving weights are not renormalised; ties go to the lowest expert index;
 the softmax modes select on the raw logit; the sigmoid is evaluated in
@@ -259,12 +261,16 @@ def permute_rows(x, token_of_row) -> np.ndarray:
 
 def expert_ffn(x_rows, w1, w2, kind: int, dtype: int, w3=None, b1=None,
                b2=None):
-    """One expert applied to a block of rows; returns (h, y), both rounded.
+    """One expert applied to a block of rows; returns (h, y).
 
     SiLU-MLP: h = silu(W1 x + b1), y = W2 h + b2   [EXPERT In[7]].
     SwiGLU:   h = silu(W1 x) * (W3 x), y = W2 h     [QWEN expert forward pass;
               DSEEK s.1].
-    h and y are rounded to the layer's storage type (bf16 or fp32).
+    h is rounded to the layer's storage type (bf16 or fp32).  y is rounded
+    to fp32 only: it is an fp32 accumulation that feeds the weighted
+    combine, itself part of the same fp32 accumulation (the layer is "bf16
+    weights/activations, fp32 accumulation"), and the layer output is
+    rounded once, at the end.
     """
     x = np.asarray(x_rows, np.float64)
     a = x @ np.asarray(w1, np.float64).T
@@ -278,7 +284,7 @@ def expert_ffn(x_rows, w1, w2, kind: int, dtype: int, w3=None, b1=None,
     y = h @ np.asarray(w2, np.float64).T
     if kind != SWIGLU and b2 is not None:
         y = y + np.asarray(b2, np.float64)[None, :]
-    return h, round_to(dtype, y)
+    return h, round_f32(y)
 
 
 def grouped_ffn(x_perm, offsets, p: dict, kind: int, dtype: int):
@@ -355,7 +361,9 @@ def forward(shape, values: dict) -> dict:
 
     ``shape`` is any object with the workload fields (n_tokens, n_experts,
     top_k, expert, route, dtype, capacity_factor, n_shared, balance_coef);
-    ``values`` holds the fp32 arrays the layer sees.
+    ``values`` holds the fp32 arrays the layer sees.  ``out`` is rounded to
+    the layer's storage type; ``out_exact`` is the same sum before that last
+    rounding.
     """
     x = values["x"]
     n_tokens = x.shape[0]
@@ -368,12 +376,12 @@ def forward(shape, values: dict) -> dict:
     if shape.n_shared > 0:
         shared = round_f32(shared_ffn(x, values["ws1"], values["ws3"],
                                       values["ws2"], shape.dtype))
-    out = combine(y, disp["row_of_slot"], w, shared)
-    out = round_to(shape.dtype, out)
+    out_exact = combine(y, disp["row_of_slot"], w, shared)
+    out = round_to(shape.dtype, out_exact)
     bal = balance_statistic(disp["counts"], p, n_tokens, shape.balance_coef) \
         if n_tokens > 0 else 0.0
     res = dict(logits=logits, idx=idx, w=w, p=p, x_perm=x_perm, h=h, y=y,
-               shared=shared, out=out, balance=bal)
+               shared=shared, out=out, out_exact=out_exact, balance=bal)
     res.update(disp)
     return res
 
@@ -404,4 +412,5 @@ def forward_tokens(shape, values: dict, tokens) -> dict:
     if shape.n_shared > 0:
         out += round_f32(shared_ffn(x, values["ws1"], values["ws3"],
                                     values["ws2"], shape.dtype))
-    return dict(logits=logits, idx=idx, w=w, out=round_to(shape.dtype, out))
+    return dict(logits=logits, idx=idx, w=w, out=round_to(shape.dtype, out),
+                out_exact=out)

@@ -1,0 +1,103 @@
+"""Build the CUDA library ``libmoe_b300.so`` in-tree for sm_103a.
+
+Each ``csrc/*.cu`` is compiled to an object under ``_build/`` (in parallel),
+then linked with ``nvcc -shared``.  The CUDA runtime is linked statically;
+the driver API (tensor-map encoding) is reached at run time through
+``cudaGetDriverEntryPoint``, so the library loads on a machine without a
+GPU (nothing in it runs there).
+
+    python -m routing_dispatch_expert_05_b300.build [--force] [--verbose]
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+import sys
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG_DIR)
+CSRC = os.path.join(PKG_DIR, "csrc")
+BUILD_DIR = os.path.join(ROOT, "_build")
+LIB_NAME = "libmoe_b300.so"
+LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+          "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
+          "-I", os.path.join(ROOT, "include")]
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build")
+
+
+def _sources():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _deps():
+    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
+        sorted(glob.glob(os.path.join(CSRC, "*.h"))) + \
+        [os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return False
+    t = os.path.getmtime(LIB_PATH)
+    return all(os.path.getmtime(p) <= t for p in _deps())
+
+
+def _run(cmd, verbose):
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError("command failed:\n" + " ".join(cmd) + "\n" + r.stdout)
+    if verbose and r.stdout.strip():
+        print(r.stdout, flush=True)
+    return r.stdout
+
+
+def build(force: bool = False, verbose: bool = False,
+          ptxas_verbose: bool = False) -> str:
+    """Compile and link the library if any source is newer; return its path."""
+    if not force and up_to_date():
+        return LIB_PATH
+    nvcc = _nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    jobs = []
+    for src in _sources():
+        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        jobs.append((obj, [nvcc, "-c", src, "-o", obj] + ARCH + CFLAGS + extra))
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        outs = list(ex.map(lambda j: _run(j[1], verbose), jobs))
+    if ptxas_verbose:
+        for (obj, _), out in zip(jobs, outs):
+            print("==", os.path.basename(obj), "\n", out)
+    tmp = LIB_PATH + ".tmp"
+    _run([nvcc, "-shared", "-o", tmp] + [o for o, _ in jobs] + ARCH +
+         ["-Xcompiler", "-fPIC"], verbose)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--ptxas", action="store_true", help="print ptxas -v")
+    a = ap.parse_args(argv)
+    print(build(force=a.force, verbose=a.verbose, ptxas_verbose=a.ptxas))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,635 @@
+// The exported C ABI (include/moe.h): argument checks, workspace layout and
+// the order of launches.  No entry point allocates, frees or waits (except
+// moe_read_device_error, which waits to read one word back).
+#include <cmath>
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t elem_size(const moe_config_t& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  // scratch (shared by all stage calls)
+  size_t err, route_psum, route_cnt, chunk_cnt, chunk_base, logits, scratch_end;
+  // intermediates of moe_forward
+  size_t idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, h_shared,
+      shared_out, x_stage, out_stage, total;
+  int route_parts, chunks;
+};
+
+Layout layout_of(const moe_config_t& c) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model,
+                F = c.d_ff;
+  const size_t es = elem_size(c);
+  L.route_parts = (int)ceil_div64(N, kRouteTokensPerPartial);
+  L.chunks = (int)ceil_div64(N, kDispatchTokensPerChunk);
+  L.err = take(kAlign);
+  L.route_psum = take((size_t)L.route_parts * E * 4);
+  L.route_cnt = take((size_t)L.route_parts * E * 4);
+  L.chunk_cnt = take((size_t)L.chunks * E * 4);
+  L.chunk_base = take((size_t)L.chunks * E * 4);
+  L.logits = take((size_t)N * E * 4);
+  L.scratch_end = o;
+  L.idx = take((size_t)N * k * 4);
+  L.w = take((size_t)N * k * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.row_of_slot = take((size_t)N * k * 4);
+  L.token_of_row = take((size_t)N * k * 4);
+  L.x_perm = take((size_t)N * k * d * es);
+  L.h = take((size_t)N * k * F * es);
+  L.y = take((size_t)N * k * d * 4);   // expert outputs stay fp32
+  if (c.n_shared > 0) {
+    L.h_shared = take((size_t)N * c.n_shared * c.d_ff_shared * es);
+    L.shared_out = take((size_t)N * d * 4);
+  }
+  L.x_stage = take((size_t)N * d * es);
+  L.out_stage = take((size_t)N * d * es);
+  L.total = o;
+  return L;
+}
+
+moe_status_t check_config(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens < 0 || c->d_model < 1 || c->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->n_experts > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->route < MOE_ROUTE_SOFTMAX_TOPK || c->route > MOE_ROUTE_SIGMOID_BIAS)
+    return MOE_ERR_INVALID_ARG;
+  if (c->expert != MOE_EXPERT_SILU_MLP && c->expert != MOE_EXPERT_SWIGLU)
+    return MOE_ERR_INVALID_ARG;
+  if (c->has_bias != 0 && c->has_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (c->has_bias && c->expert != MOE_EXPERT_SILU_MLP) return MOE_ERR_INVALID_ARG;
+  const int vec = c->dtype == MOE_BF16 ? 8 : 4;  // elements per 16 bytes
+  if (c->d_model % vec != 0 || c->d_ff % vec != 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared > 0 && (c->d_ff_shared < 1 || c->d_ff_shared % vec != 0))
+    return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->balance_coef))
+    return MOE_ERR_INVALID_ARG;
+  // row indices are int32: every assignment must fit
+  if ((double)c->n_tokens * (double)c->top_k > 2147483647.0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// all listed pointers non-null and 16-byte aligned
+moe_status_t need(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+// listed pointers may be null; non-null ones must be aligned
+moe_status_t maybe(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                        \
+  do {                                       \
+    const moe_status_t s_ = (expr);          \
+    if (s_ != MOE_OK) return s_;             \
+  } while (0)
+
+moe_status_t check_router_weights(const moe_config_t& c, const moe_weights_t* w) {
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need({w->w_router}));
+  MOE_TRY(maybe({w->b_router}));
+  if (c.route == MOE_ROUTE_SIGMOID_BIAS) MOE_TRY(need({w->sel_bias}));
+  return MOE_OK;
+}
+moe_status_t check_up_weights(const moe_config_t& c, const moe_weights_t* w) {
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need({w->w1}));
+  if (c.expert == MOE_EXPERT_SWIGLU) MOE_TRY(need({w->w3}));
+  if (c.has_bias) MOE_TRY(need({w->b1}));
+  return MOE_OK;
+}
+moe_status_t check_down_weights(const moe_config_t& c, const moe_weights_t* w) {
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need({w->w2}));
+  if (c.has_bias) MOE_TRY(need({w->b2}));
+  return MOE_OK;
+}
+moe_status_t check_shared_weights(const moe_config_t& c, const moe_weights_t* w) {
+  if (c.n_shared == 0) return MOE_OK;
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  return need({w->ws1, w->ws3, w->ws2});
+}
+moe_status_t check_stats(const moe_stats_t* s) {
+  if (s == nullptr) return MOE_OK;
+  return maybe({s->counts, s->kept, s->dropped, s->balance});
+}
+
+moe_status_t check_ws(void* ws, size_t ws_bytes, size_t needed) {
+  if (ws == nullptr || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < needed) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t last_cuda() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 148;
+  return n > 0 ? n : 148;
+}
+
+template <typename T> T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int32_t* err_word(void* ws) { return static_cast<int32_t*>(ws); }
+
+int64_t capacity_of(const moe_config_t& c) {
+  if (!(c.capacity_factor > 0.f)) return -1;
+  const int64_t base = c.n_tokens / c.n_experts;
+  return (int64_t)((double)c.capacity_factor * (double)base);
+}
+
+// zero the requested per-expert stats (used when there are no tokens)
+moe_status_t zero_stats(const moe_config_t& c, moe_stats_t* s, cudaStream_t st) {
+  if (s == nullptr) return MOE_OK;
+  const size_t eb = (size_t)c.n_experts * 4;
+  if (s->counts) cudaMemsetAsync(s->counts, 0, eb, st);
+  if (s->kept) cudaMemsetAsync(s->kept, 0, eb, st);
+  if (s->dropped) cudaMemsetAsync(s->dropped, 0, eb, st);
+  if (s->balance) cudaMemsetAsync(s->balance, 0, 4, st);
+  return last_cuda();
+}
+
+// ---- stage bodies (arguments already checked) -----------------------------
+void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
+                 float* logits, int32_t* idx, float* wts, moe_stats_t* stats,
+                 void* ws, cudaStream_t st, bool gemm) {
+  const Layout L = layout_of(c);
+  float* lg = logits ? logits : at<float>(ws, L.logits);
+  if (gemm) {
+    GemmProblem p{};
+    p.A = x;
+    p.B0 = w.w_router;
+    p.k_sub = c.d_model;
+    p.bias = w.b_router;
+    p.bias_group_stride = 0;
+    p.C = lg;
+    p.c_is_f32 = 1;
+    p.offsets = nullptr;
+    p.n_groups = 1;
+    p.rows = c.n_tokens;
+    p.N = c.n_experts;
+    p.K = c.d_model;
+    p.epilogue = kEpiNone;
+    p.is_bf16 = c.dtype == MOE_BF16;
+    launch_simt_gemm(p, st);
+  }
+  launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route,
+                           w.sel_bias, idx, wts, at<float>(ws, L.route_psum),
+                           at<int32_t>(ws, L.route_cnt), st);
+  launch_balance_finalize(at<float>(ws, L.route_psum), at<int32_t>(ws, L.route_cnt),
+                          L.route_parts, c.n_experts, c.n_tokens, c.balance_coef,
+                          stats ? stats->counts : nullptr,
+                          stats ? stats->balance : nullptr, st);
+}
+
+void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
+                   int32_t* offsets, int32_t* ros, int32_t* tor, void* x_perm,
+                   moe_stats_t* stats, void* ws, cudaStream_t st) {
+  const Layout L = layout_of(c);
+  launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c),
+                  at<int32_t>(ws, L.chunk_cnt), at<int32_t>(ws, L.chunk_base),
+                  offsets, ros, tor, stats ? stats->counts : nullptr,
+                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr,
+                  at<int32_t>(ws, L.err), st);
+  launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
+                     c.n_tokens * c.top_k, x_perm, num_sms(), st);
+}
+
+// bf16 expert GEMMs run on the tensor cores; fp32 ones on the CUDA cores
+moe_status_t run_gemm(const moe_config_t& c, const TcProblem& tq, const GemmProblem& sq,
+                      cudaStream_t st) {
+  if (c.dtype == MOE_BF16 && tc_gemm_supported(tq))
+    return launch_tc_gemm(tq, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+  launch_simt_gemm(sq, st);
+  return MOE_OK;
+}
+
+moe_status_t up_body(const moe_config_t& c, const void* x_perm, const int32_t* offsets,
+                     const moe_weights_t& w, void* h, int32_t* err, cudaStream_t st) {
+  const bool swiglu = c.expert == MOE_EXPERT_SWIGLU;
+  GemmProblem p{};
+  p.A = x_perm;
+  p.B0 = w.w1;
+  p.B1 = swiglu ? w.w3 : nullptr;
+  p.b_group_stride = (int64_t)c.d_ff * c.d_model;
+  p.k_sub = c.d_model;
+  p.bias = c.has_bias ? w.b1 : nullptr;
+  p.bias_group_stride = c.d_ff;
+  p.C = h;
+  p.offsets = offsets;
+  p.n_groups = c.n_experts;
+  p.rows = c.n_tokens * c.top_k;
+  p.N = c.d_ff;
+  p.K = c.d_model;
+  p.epilogue = swiglu ? kEpiSwiglu : kEpiSiluBias;
+  p.is_bf16 = c.dtype == MOE_BF16;
+  TcProblem q{};
+  q.A = x_perm;
+  q.a_rows = c.n_tokens * c.top_k;
+  q.K = c.d_model;
+  q.B0 = w.w1;
+  q.B1 = p.B1;
+  q.b_groups = c.n_experts;
+  q.b_rows = c.d_ff;
+  q.k_sub = c.d_model;
+  q.n_sub = 1;
+  q.offsets = offsets;
+  q.n_groups = c.n_experts;
+  q.rows = q.a_rows;
+  q.n_out = c.d_ff;
+  q.swiglu = swiglu;
+  q.epilogue = p.epilogue;
+  q.bias = p.bias;
+  q.bias_stride = c.d_ff;
+  q.C = h;
+  q.err = err;
+  return run_gemm(c, q, p, st);
+}
+
+moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offsets,
+                       const moe_weights_t& w, float* y, int32_t* err, cudaStream_t st) {
+  GemmProblem p{};
+  p.A = h;
+  p.B0 = w.w2;
+  p.b_group_stride = (int64_t)c.d_model * c.d_ff;
+  p.k_sub = c.d_ff;
+  p.bias = c.has_bias ? w.b2 : nullptr;
+  p.bias_group_stride = c.d_model;
+  p.C = y;
+  p.c_is_f32 = 1;
+  p.offsets = offsets;
+  p.n_groups = c.n_experts;
+  p.rows = c.n_tokens * c.top_k;
+  p.N = c.d_model;
+  p.K = c.d_ff;
+  p.epilogue = kEpiNone;
+  p.is_bf16 = c.dtype == MOE_BF16;
+  TcProblem q{};
+  q.A = h;
+  q.a_rows = c.n_tokens * c.top_k;
+  q.K = c.d_ff;
+  q.B0 = w.w2;
+  q.b_groups = c.n_experts;
+  q.b_rows = c.d_model;
+  q.k_sub = c.d_ff;
+  q.n_sub = 1;
+  q.offsets = offsets;
+  q.n_groups = c.n_experts;
+  q.rows = q.a_rows;
+  q.n_out = c.d_model;
+  q.epilogue = kEpiNone;
+  q.bias = p.bias;
+  q.bias_stride = c.d_model;
+  q.C = y;
+  q.c_is_f32 = 1;
+  q.err = err;
+  return run_gemm(c, q, p, st);
+}
+
+moe_status_t shared_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
+                         void* h_shared, float* shared_out, int32_t* err,
+                         cudaStream_t st) {
+  const int fs_total = c.n_shared * c.d_ff_shared;
+  GemmProblem up{};
+  up.A = x;
+  up.B0 = w.ws1;  // [S, Fs, d] read as [S*Fs, d]
+  up.B1 = w.ws3;
+  up.k_sub = c.d_model;
+  up.C = h_shared;
+  up.n_groups = 1;
+  up.rows = c.n_tokens;
+  up.N = fs_total;
+  up.K = c.d_model;
+  up.epilogue = kEpiSwiglu;
+  up.is_bf16 = c.dtype == MOE_BF16;
+  TcProblem uq{};
+  uq.A = x;
+  uq.a_rows = c.n_tokens;
+  uq.K = c.d_model;
+  uq.B0 = w.ws1;
+  uq.B1 = w.ws3;
+  uq.b_groups = 1;
+  uq.b_rows = fs_total;
+  uq.k_sub = c.d_model;
+  uq.n_sub = 1;
+  uq.n_groups = 1;
+  uq.rows = c.n_tokens;
+  uq.n_out = fs_total;
+  uq.swiglu = 1;
+  uq.epilogue = kEpiSwiglu;
+  uq.C = h_shared;
+  uq.err = err;
+  MOE_TRY(run_gemm(c, uq, up, st));
+  GemmProblem dn{};
+  dn.A = h_shared;
+  dn.B0 = w.ws2;  // [S, d, Fs]: column block s of the concatenated down
+  dn.k_sub = c.d_ff_shared;
+  dn.sub_stride = (int64_t)c.d_model * c.d_ff_shared;
+  dn.C = shared_out;
+  dn.c_is_f32 = 1;
+  dn.n_groups = 1;
+  dn.rows = c.n_tokens;
+  dn.N = c.d_model;
+  dn.K = fs_total;
+  dn.epilogue = kEpiNone;
+  dn.is_bf16 = c.dtype == MOE_BF16;
+  TcProblem dq{};
+  dq.A = h_shared;
+  dq.a_rows = c.n_tokens;
+  dq.K = fs_total;
+  dq.B0 = w.ws2;  // viewed as [S*d, Fs]
+  dq.b_groups = 1;
+  dq.b_rows = c.d_model;
+  dq.k_sub = c.d_ff_shared;
+  dq.n_sub = c.n_shared;
+  dq.n_groups = 1;
+  dq.rows = c.n_tokens;
+  dq.n_out = c.d_model;
+  dq.epilogue = kEpiNone;
+  dq.C = shared_out;
+  dq.c_is_f32 = 1;
+  dq.err = err;
+  return run_gemm(c, dq, dn, st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_scratch_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_of(*cfg).scratch_end;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_of(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x,
+                             const moe_weights_t* weights, float* logits,
+                             int32_t* idx, float* w, moe_stats_t* stats, void* ws,
+                             size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_router_weights(c, weights));
+  MOE_TRY(check_stats(stats));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) return zero_stats(c, stats, st);
+  MOE_TRY(need({x, idx, w}));
+  MOE_TRY(maybe({logits}));
+  router_body(c, x, *weights, logits, idx, w, stats, ws, st, true);
+  return last_cuda();
+}
+
+moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits,
+                              const float* sel_bias, int32_t* idx, float* w,
+                              moe_stats_t* stats, void* ws, size_t ws_bytes,
+                              void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  if (c.route == MOE_ROUTE_SIGMOID_BIAS) MOE_TRY(need({sel_bias}));
+  MOE_TRY(check_stats(stats));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) return zero_stats(c, stats, st);
+  MOE_TRY(need({logits, idx, w}));
+  moe_weights_t wt{};
+  wt.sel_bias = sel_bias;
+  router_body(c, nullptr, wt, const_cast<float*>(logits), idx, w, stats, ws, st, false);
+  return last_cuda();
+}
+
+moe_status_t moe_dispatch_permute(const moe_config_t* cfg, const int32_t* idx,
+                                  const void* x, int32_t* offsets,
+                                  int32_t* row_of_slot, int32_t* token_of_row,
+                                  void* x_perm, moe_stats_t* stats, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_stats(stats));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  MOE_TRY(need({offsets}));
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) {
+    cudaMemsetAsync(offsets, 0, (size_t)(c.n_experts + 1) * 4, st);
+    MOE_TRY(last_cuda());
+    return zero_stats(c, stats, st);
+  }
+  MOE_TRY(need({idx, x, row_of_slot, token_of_row, x_perm}));
+  dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats, ws, st);
+  return last_cuda();
+}
+
+moe_status_t moe_expert_up(const moe_config_t* cfg, const void* x_perm,
+                           const int32_t* offsets, const moe_weights_t* weights,
+                           void* h, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_up_weights(c, weights));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({x_perm, offsets, h}));
+  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), static_cast<cudaStream_t>(stream)));
+  return last_cuda();
+}
+
+moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h,
+                             const int32_t* offsets, const moe_weights_t* weights,
+                             float* y, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_down_weights(c, weights));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({h, offsets, y}));
+  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), static_cast<cudaStream_t>(stream)));
+  return last_cuda();
+}
+
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm,
+                             const int32_t* offsets, const moe_weights_t* weights,
+                             void* h, float* y, void* ws, size_t ws_bytes,
+                             void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_up_weights(c, weights));
+  MOE_TRY(check_down_weights(c, weights));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({x_perm, offsets, h, y}));
+  auto st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), st));
+  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
+  return last_cuda();
+}
+
+moe_status_t moe_shared_ffn(const moe_config_t* cfg, const void* x,
+                            const moe_weights_t* weights, void* h_shared,
+                            float* shared_out, void* ws, size_t ws_bytes,
+                            void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  if (c.n_shared == 0) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_shared_weights(c, weights));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({x, h_shared, shared_out}));
+  MOE_TRY(shared_body(c, x, *weights, h_shared, shared_out, err_word(ws),
+                      static_cast<cudaStream_t>(stream)));
+  return last_cuda();
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const float* y,
+                         const int32_t* row_of_slot, const float* w,
+                         const float* shared_out, void* out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({y, row_of_slot, w, out}));
+  MOE_TRY(maybe({shared_out}));
+  launch_combine(y, row_of_slot, w, shared_out, out, c.n_tokens, c.top_k, c.d_model,
+                 c.dtype == MOE_BF16, num_sms(), static_cast<cudaStream_t>(stream));
+  return last_cuda();
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
+                         const moe_weights_t* weights, void* out,
+                         moe_stats_t* stats, void* ws, size_t ws_bytes,
+                         void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_router_weights(c, weights));
+  MOE_TRY(check_up_weights(c, weights));
+  MOE_TRY(check_down_weights(c, weights));
+  MOE_TRY(check_shared_weights(c, weights));
+  MOE_TRY(check_stats(stats));
+  const Layout L = layout_of(c);
+  MOE_TRY(check_ws(ws, ws_bytes, L.total));
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) return zero_stats(c, stats, st);
+  MOE_TRY(need({x, out}));
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* wts = at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* ros = at<int32_t>(ws, L.row_of_slot);
+  int32_t* tor = at<int32_t>(ws, L.token_of_row);
+  void* x_perm = at<char>(ws, L.x_perm);
+  void* h = at<char>(ws, L.h);
+  float* y = at<float>(ws, L.y);
+  float* shared_out = c.n_shared > 0 ? at<float>(ws, L.shared_out) : nullptr;
+  // the balance statistic and pre-drop counts come from the router, the
+  // kept/dropped counts from the dispatch
+  moe_stats_t rs{};
+  if (stats) {
+    rs.counts = stats->counts;
+    rs.balance = stats->balance;
+  }
+  router_body(c, x, *weights, nullptr, idx, wts, &rs, ws, st, true);
+  moe_stats_t ds{};
+  if (stats) {
+    ds.kept = stats->kept;
+    ds.dropped = stats->dropped;
+  }
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, ws, st);
+  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), st));
+  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
+  if (c.n_shared > 0)
+    MOE_TRY(shared_body(c, x, *weights, at<char>(ws, L.h_shared), shared_out,
+                        err_word(ws), st));
+  launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
+                 c.dtype == MOE_BF16, num_sms(), st);
+  return last_cuda();
+}
+
+moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host,
+                              const moe_weights_t* weights, void* out_host,
+                              moe_stats_t* stats, void* ws, size_t ws_bytes,
+                              void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  const Layout L = layout_of(c);
+  MOE_TRY(check_ws(ws, ws_bytes, L.total));
+  if (c.n_tokens > 0 && (x_host == nullptr || out_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)c.n_tokens * c.d_model * elem_size(c);
+  void* xd = at<char>(ws, L.x_stage);
+  void* od = at<char>(ws, L.out_stage);
+  if (bytes > 0 && cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  MOE_TRY(moe_forward(cfg, xd, weights, od, stats, ws, ws_bytes, stream));
+  if (bytes > 0 && cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_read_device_error(void* ws, int32_t* code, void* stream) {
+  if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0 && cudaMemsetAsync(ws, 0, sizeof(v), st) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v == kDevOk ? MOE_OK : v == kDevTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t moe_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// Weighted combine back to token order.
+//
+// out[t] = sum_{j : row_of_slot[t*k+j] >= 0} w[t,j] * y[row_of_slot[t*k+j]] + S[t]
+// ("Implementing Mixed Expert (MoE) layers", weighted aggregation with
+// index_add_; "Hands-on build guide", step 5; "DeepSeek 5.7", s.3-4).
+//
+// Written as a gather-reduce rather than a scatter-add: each token reads its
+// own k expert rows, so there are no atomics, the fp32 sum runs in slot order
+// j = 0..k-1 and the result is rounded and written once.  The expert outputs
+// y are fp32 (the combine continues their fp32 accumulation).  A CTA owns a
+// run of whole tokens; a thread owns C consecutive columns (8 for a bf16
+// output, 4 for fp32), and the loads of four slots are issued before their
+// multiply-adds so they are in flight together.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int NV>
+__device__ __forceinline__ void load_cols(const float* p, float4 (&v)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = __ldcs(reinterpret_cast<const float4*>(p) + i);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot,
+               const float* __restrict__ w, const float* __restrict__ shared,
+               T* __restrict__ out, int64_t n_tokens, int top_k, int d_model) {
+  constexpr int C = sizeof(T) == 2 ? 8 : 4;  // columns per thread step
+  constexpr int NV = C / 4;                  // float4 per row segment
+  const int nvec = d_model / C;
+  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
+    const int32_t* rows = row_of_slot + t * top_k;
+    const float* wt = w + t * top_k;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const int64_t col = (int64_t)v * C;
+      float acc[C];
+#pragma unroll
+      for (int i = 0; i < C; ++i) acc[i] = 0.f;
+      int j = 0;
+      for (; j + 4 <= top_k; j += 4) {
+        float4 val[4][NV];
+        int r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          r[q] = rows[j + q];
+          if (r[q] >= 0) load_cols<NV>(y + (int64_t)r[q] * d_model + col, val[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (r[q] < 0) continue;
+          const float wj = wt[j + q];
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            acc[4 * i + 0] = fmaf(wj, val[q][i].x, acc[4 * i + 0]);
+            acc[4 * i + 1] = fmaf(wj, val[q][i].y, acc[4 * i + 1]);
+            acc[4 * i + 2] = fmaf(wj, val[q][i].z, acc[4 * i + 2]);
+            acc[4 * i + 3] = fmaf(wj, val[q][i].w, acc[4 * i + 3]);
+          }
+        }
+      }
+      for (; j < top_k; ++j) {
+        const int r = rows[j];
+        if (r < 0) continue;
+        float4 val[NV];
+        load_cols<NV>(y + (int64_t)r * d_model + col, val);
+        const float wj = wt[j];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          acc[4 * i + 0] = fmaf(wj, val[i].x, acc[4 * i + 0]);
+          acc[4 * i + 1] = fmaf(wj, val[i].y, acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(wj, val[i].z, acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(wj, val[i].w, acc[4 * i + 3]);
+        }
+      }
+      if (shared != nullptr) {
+        float4 s[NV];
+        load_cols<NV>(shared + t * d_model + col, s);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          acc[4 * i + 0] += s[i].x;
+          acc[4 * i + 1] += s[i].y;
+          acc[4 * i + 2] += s[i].z;
+          acc[4 * i + 3] += s[i].w;
+        }
+      }
+      T* op = out + t * d_model + col;
+      if constexpr (C == 4) {
+        *reinterpret_cast<float4*>(op) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      } else {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        st_vec16(op, o);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
+                    const float* shared, void* out, int64_t n_tokens, int top_k,
+                    int d_model, int is_bf16, int num_sms, cudaStream_t st) {
+  if (n_tokens <= 0) return;
+  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 16);
+  if (is_bf16)
+    combine_kernel<bf16><<<blocks, kThreads, 0, st>>>(
+        y, row_of_slot, w, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
+  else
+    combine_kernel<float><<<blocks, kThreads, 0, st>>>(
+        y, row_of_slot, w, shared, static_cast<float*>(out), n_tokens, top_k, d_model);
+}
+
+}  // namespace moe

@@ -1,0 +1,215 @@
+// Grouping assignments by expert with a capacity limit.
+//
+// "Expert Networks > Code Implementation", In[10]: assignments are visited in
+// token order; expert e processes an assignment while it has processed fewer
+// than `capacity`, otherwise the assignment is dropped and counted.  So the
+// assignment of token t to expert e is kept iff its rank r -- the number of
+// earlier assignments to e -- is below the capacity, and kept assignments
+// of e fill rows offsets[e] + r in arrival order ("DeepSeek 5.7", s.3;
+// "Implementing Mixed Expert (MoE) layers", grouping by expert).
+//
+// Three passes over idx (flattened slot order s = t*k + j; an expert occurs
+// at most once per token, so slot order within a token does not change any
+// rank):
+//   1. count:  per chunk of tokens, assignments per expert (smem atomics);
+//   2. scan:   per expert, chunk bases (exclusive scan over chunks), totals,
+//              kept = min(total, capacity), dropped, offsets = exclusive
+//              scan of kept -- one CTA, fixed order;
+//   3. rank:   per chunk, each warp owns a contiguous run of slots; ranks
+//              inside a 32-slot step come from __match_any_sync (lanes with
+//              the same expert) and a running per-(warp, expert) counter;
+//              warp bases are an exclusive scan over the chunk's warps.
+// A fourth kernel copies x rows into x_perm (16-byte vectors).
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRankWarps = 8;
+
+__global__ void __launch_bounds__(256)
+dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
+                      int n_experts, int32_t* __restrict__ chunk_cnt,
+                      int32_t* __restrict__ err) {
+  __shared__ int s_cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < n_experts; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kDispatchTokensPerChunk;
+  const int64_t t1 = min(n_tokens, t0 + kDispatchTokensPerChunk);
+  for (int64_t s = t0 * top_k + threadIdx.x; s < t1 * top_k; s += blockDim.x) {
+    const int e = idx[s];
+    if (e < 0 || e >= n_experts) {
+      set_device_error(err, kDevBadExpert);
+      continue;
+    }
+    atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n_experts; e += blockDim.x)
+    chunk_cnt[(int64_t)blockIdx.x * n_experts + e] = s_cnt[e];
+}
+
+__global__ void __launch_bounds__(kMaxExperts)
+dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
+                     int n_experts, int64_t capacity,
+                     int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
+                     int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+                     int32_t* __restrict__ dropped) {
+  __shared__ int s_kept[kMaxExperts];
+  const int e = threadIdx.x;
+  if (e < n_experts) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int64_t o = (int64_t)c * n_experts + e;
+      const int v = chunk_cnt[o];
+      chunk_base[o] = run;
+      run += v;
+    }
+    const int kp = capacity < 0 ? run : (int)min((int64_t)run, capacity);
+    s_kept[e] = kp;
+    if (counts) counts[e] = run;
+    if (kept) kept[e] = kp;
+    if (dropped) dropped[e] = run - kp;
+  }
+  __syncthreads();
+  if (e == 0) {
+    int acc = 0;
+    for (int q = 0; q < n_experts; ++q) {
+      offsets[q] = acc;
+      acc += s_kept[q];
+    }
+    offsets[n_experts] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(kRankWarps * 32)
+dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
+                     int n_experts, int64_t capacity,
+                     const int32_t* __restrict__ chunk_base,
+                     const int32_t* __restrict__ offsets,
+                     int32_t* __restrict__ row_of_slot,
+                     int32_t* __restrict__ token_of_row) {
+  __shared__ int s_w[kRankWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kRankWarps * kMaxExperts; i += blockDim.x)
+    (&s_w[0][0])[i] = 0;
+  __syncthreads();
+
+  const int64_t t0 = (int64_t)blockIdx.x * kDispatchTokensPerChunk;
+  const int64_t t1 = min(n_tokens, t0 + kDispatchTokensPerChunk);
+  const int64_t s0 = t0 * top_k, s1 = t1 * top_k;
+  const int64_t per_warp = ceil_div64(s1 - s0, kRankWarps);
+  const int64_t ws0 = s0 + warp * per_warp;
+  const int64_t ws1 = min(s1, ws0 + per_warp);
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // pass 1: assignments per (warp, expert)
+  for (int64_t base = ws0; base < ws1; base += 32) {
+    const int64_t s = base + lane;
+    int e = s < ws1 ? idx[s] : -1;
+    if (e >= n_experts) e = -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    if (e >= 0 && (m & lt_mask) == 0) s_w[warp][e] += __popc(m);
+    __syncwarp();
+  }
+  __syncthreads();
+  // warp bases: chunk base + exclusive scan over the chunk's warps
+  for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+    int run = chunk_base[(int64_t)blockIdx.x * n_experts + e];
+#pragma unroll
+    for (int q = 0; q < kRankWarps; ++q) {
+      const int v = s_w[q][e];
+      s_w[q][e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // pass 2: ranks, keep/drop, rows
+  for (int64_t base = ws0; base < ws1; base += 32) {
+    const int64_t s = base + lane;
+    int e = s < ws1 ? idx[s] : -1;
+    if (e >= n_experts) e = -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    int rank = 0;
+    if (e >= 0) rank = s_w[warp][e] + __popc(m & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (m & lt_mask) == 0) s_w[warp][e] += __popc(m);
+    __syncwarp();
+    if (s < ws1) {
+      int32_t row = -1;
+      if (e >= 0 && (capacity < 0 || rank < capacity)) {
+        row = offsets[e] + rank;
+        token_of_row[row] = (int32_t)(s / top_k);
+      }
+      row_of_slot[s] = row;
+    }
+  }
+}
+
+// x_perm[r] = x[token_of_row[r]] for r < offsets[E]; one warp per row,
+// 16-byte vectors, up to 4 vectors in flight per lane.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
+                   const int32_t* __restrict__ token_of_row,
+                   const int32_t* __restrict__ offsets, int n_experts,
+                   uint8_t* __restrict__ x_perm) {
+  const int64_t rows = offsets[n_experts];
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nvec = row_bytes >> 4;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += warps_total) {
+    const int64_t t = token_of_row[r];
+    const uint8_t* src = x + t * row_bytes;
+    uint8_t* dst = x_perm + r * row_bytes;
+    int64_t v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 a = ld_vec16_nc(src + (v << 4));
+      const uint4 b = ld_vec16_nc(src + ((v + 32) << 4));
+      const uint4 c = ld_vec16_nc(src + ((v + 64) << 4));
+      const uint4 d = ld_vec16_nc(src + ((v + 96) << 4));
+      st_vec16(dst + (v << 4), a);
+      st_vec16(dst + ((v + 32) << 4), b);
+      st_vec16(dst + ((v + 64) << 4), c);
+      st_vec16(dst + ((v + 96) << 4), d);
+    }
+    for (; v < nvec; v += 32) st_vec16(dst + (v << 4), ld_vec16_nc(src + (v << 4)));
+  }
+}
+
+}  // namespace
+
+void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
+                     int n_experts, int64_t capacity, int32_t* chunk_cnt,
+                     int32_t* chunk_base, int32_t* offsets, int32_t* row_of_slot,
+                     int32_t* token_of_row, int32_t* counts, int32_t* kept,
+                     int32_t* dropped, int32_t* err, cudaStream_t st) {
+  const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
+  if (chunks > 0)
+    dispatch_count_kernel<<<chunks, 256, 0, st>>>(idx, n_tokens, top_k, n_experts,
+                                                  chunk_cnt, err);
+  dispatch_scan_kernel<<<1, kMaxExperts, 0, st>>>(chunk_cnt, chunks, n_experts,
+                                                  capacity, chunk_base, offsets,
+                                                  counts, kept, dropped);
+  if (chunks > 0)
+    dispatch_rank_kernel<<<chunks, kRankWarps * 32, 0, st>>>(
+        idx, n_tokens, top_k, n_experts, capacity, chunk_base, offsets,
+        row_of_slot, token_of_row);
+}
+
+void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
+                        const int32_t* offsets, int n_experts, int64_t max_rows,
+                        void* x_perm, int num_sms, cudaStream_t st) {
+  if (max_rows <= 0) return;
+  const int64_t blocks_needed = ceil_div64(max_rows, 8);
+  const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)num_sms * 8);
+  gather_rows_kernel<<<blocks, 256, 0, st>>>(
+      static_cast<const uint8_t*>(x), row_bytes, token_of_row, offsets, n_experts,
+      static_cast<uint8_t*>(x_perm));
+}
+
+}  // namespace moe

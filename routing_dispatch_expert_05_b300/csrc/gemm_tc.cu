@@ -1,0 +1,554 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (sm_103a):
+//   C = epilogue(A B^T), A rows grouped by expert, fp32 accumulation in TMEM.
+//
+// This is the expert FFN of the layer ("Implementing Mixed Expert (MoE)
+// layers", expert forward pass: silu(fc1 x) * fc2 x, then fc3; "DeepSeek
+// 5.7", s.1 and s.5: grouped GEMMs over expert-sorted token buffers;
+// "Expert Networks", In[7]: the SiLU-MLP with biases).
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (bf16,
+//              128-byte swizzle) per k-block into a 4-stage smem ring;
+//   warp 1     owns 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//              one lane issues tcgen05.mma (M=128, N=256, K=16, kind::f16);
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31 = tile rows), apply the activation, store bf16.
+// The accumulator is double-buffered, so the epilogue of one tile overlaps
+// the main loop of the next.
+//
+// SwiGLU: the B tile holds 128 rows of W1 (gate) and the same 128 rows of
+// W3 (up); accumulator columns 0..127 are gate, 128..255 up, and the
+// epilogue writes h = silu(gate) * up -- 128 output columns per tile.
+//
+// Groups: expert e owns rows offsets[e] .. offsets[e+1]-1 (read on the
+// device).  Tile t is mapped to (expert, m-tile, n-tile) through a prefix of
+// per-expert tile counts; rows of a tile past the expert's end are computed
+// (they read the next expert's rows, or zeros past the buffer) but never
+// stored.  Empty experts own no tile.
+//
+// Every wait on an mbarrier is bounded in time: on expiry the CTA records
+// kDevTimeout in the error word, the other roles leave their loops, in-flight
+// copies and MMAs are waited for (again bounded) and TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileA = BM * BK * 2;            // 16 KB
+constexpr uint32_t kTileB = BN * BK * 2;            // 32 KB
+constexpr uint32_t kStageBytes = kTileA + kTileB;   // 48 KB
+constexpr uint32_t kTmemCols = 2 * BN;              // two accumulators
+constexpr uint64_t kTimeoutNs = 2000000000ull;      // 2 s
+constexpr int kBarBytes = 1024;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes +
+                           2 * (kMaxExperts + 1) * 4 + 1024 /* alignment */;
+
+struct Params {
+  const int32_t* offsets;     // [G+1] device or null (one group of `rows`)
+  int n_groups;
+  int rows;
+  int K;                      // reduction length (multiple of 64 per sub-block)
+  int n_out;                  // output columns
+  int swiglu;                 // 1: B = (W1 rows, W3 rows), epilogue silu(g)*u
+  int epilogue;               // kEpiNone / kEpiSiluBias / kEpiSwiglu
+  int b_rows;                 // rows of B per group (and per sub-block)
+  int k_sub;                  // K-split width (K itself unless split)
+  int n_sub;                  // K / k_sub
+  const bf16* bias;           // [G][n_out] or null
+  int64_t bias_stride;
+  void* C;                    // [rows, n_out]
+  int c_is_f32;
+  int32_t* err;
+};
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of `bar` with parity `parity` to complete, giving up
+// when another role aborted or after kTimeoutNs (then abort everyone).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        set_device_error(err, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
+                                            uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
+        "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core-matrix groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                             // leading byte offset (unused)
+  d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset
+  d |= (uint64_t)1 << 46;                             // descriptor version
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      ::"r"(smem_u32(bar)) : "memory");
+}
+#define MOE_TMEM_LD32(taddr, r)                                                     \
+  asm volatile(                                                                     \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                     \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"                     \
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"    \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),     \
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),   \
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),            \
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),            \
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),            \
+        "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
+      : "r"(taddr))
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tiles
+struct Tile {
+  int g, row0, row_end, n;
+};
+
+__device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int* off,
+                                        int G, int nt) {
+  int lo = 0, hi = G - 1;  // largest g with tile_start[g] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int local = t - tile_start[lo];
+  Tile r;
+  r.g = lo;
+  r.row0 = off[lo] + (local / nt) * BM;
+  r.row_end = off[lo + 1];
+  r.n = local % nt;
+  return r;
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+               const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kTileA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_tile_start = reinterpret_cast<int*>(smem + kStages * kStageBytes + kBarBytes);
+  int* s_off = s_tile_start + kMaxExperts + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.offsets ? p.n_groups : 1;
+  const int nt_cols = p.swiglu ? BN / 2 : BN;       // output columns per tile
+  const int nt = (p.n_out + nt_cols - 1) / nt_cols;  // n-tiles per group
+  const int nkb = (p.K + BK - 1) / BK;
+  const int kb_per_sub = p.k_sub / BK;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 4);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&tmA);
+    prefetch_map(&tmB0);
+    if (p.swiglu) prefetch_map(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
+  if (warp == 2) {
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int gg = base + lane;
+      int m = 0;
+      if (gg < G) {
+        const int o0 = p.offsets ? p.offsets[gg] : 0;
+        const int o1 = p.offsets ? p.offsets[gg + 1] : p.rows;
+        s_off[gg] = o0;
+        m = o1 - o0;
+      }
+      const int tiles = (m + BM - 1) / BM * nt;
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (gg < G) s_tile_start[gg] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_tile_start[G] = carry;
+      s_off[G] = p.offsets ? p.offsets[G] : p.rows;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = s_tile_start[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[kStages];
+      bool used[kStages];
+      for (int s = 0; s < kStages; ++s) used[s] = false, last_phase[s] = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
+          mbar_expect_tx(&full[stage], kStageBytes);
+          uint8_t* a = sA + stage * kTileA;
+          uint8_t* b = sB + stage * kTileB;
+          tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
+          if (p.swiglu) {
+            const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
+            tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
+            tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
+          } else {
+            const int sub = kb / kb_per_sub;
+            const int kk = (kb - sub * kb_per_sub) * BK;
+            const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN;
+            tma_load_2d(b, &tmB0, &full[stage], kk, brow);
+          }
+          used[stage] = true;
+          last_phase[stage] = phase;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // every issued copy has landed before the CTA can exit
+      for (int s = 0; s < kStages; ++s) {
+        if (!used[s]) continue;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&full[s], last_phase[s])) {
+          if (globaltimer() - t0 > kTimeoutNs) {
+            set_device_error(p.err, kDevTimeout);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&full[stage], phase, s_abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kTileA);
+          const uint32_t b0 = smem_u32(sB + stage * kTileB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
+                 (kb | kk) != 0);
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // all MMAs issued by this thread are complete before TMEM is freed
+      umma_commit(drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+          set_device_error(p.err, kDevTimeout);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
+      if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
+      tc_fence_after();
+      const int row = tl.row0 + q * 32 + lane;
+      const bool valid = row < tl.row_end;
+      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if (p.swiglu) {
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 2 / 32; ++ch) {
+          uint32_t g[32], u[32];
+          MOE_TMEM_LD32(tb + ch * 32, g);
+          MOE_TMEM_LD32(tb + BN / 2 + ch * 32, u);
+          tmem_ld_wait();
+          const int col0 = tl.n * (BN / 2) + ch * 32;
+          if (valid) {
+            bf16* out = static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 >= p.n_out) break;
+              uint4 o;
+              uint32_t* ow = &o.x;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int c = v * 8 + j * 2;
+                const float h0 = silu_f32(__uint_as_float(g[c])) * __uint_as_float(u[c]);
+                const float h1 =
+                    silu_f32(__uint_as_float(g[c + 1])) * __uint_as_float(u[c + 1]);
+                ow[j] = pack_bf16x2(h0, h1);
+              }
+              st_vec16(out + v * 8, o);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          MOE_TMEM_LD32(tb + ch * 32, r);
+          tmem_ld_wait();
+          const int col0 = tl.n * BN + ch * 32;
+          if (valid && col0 < p.n_out) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            if (p.bias) {
+              const bf16* bp = p.bias + (int64_t)tl.g * p.bias_stride + col0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < p.n_out) v[j] += __bfloat162float(bp[j]);
+            }
+            if (p.epilogue == kEpiSiluBias) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
+            }
+            if (p.c_is_f32) {
+              float* out = static_cast<float*>(p.C) + (int64_t)row * p.n_out + col0;
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) {
+                if (col0 + q4 * 4 >= p.n_out) break;
+                *reinterpret_cast<float4*>(out + q4 * 4) =
+                    make_float4(v[q4 * 4], v[q4 * 4 + 1], v[q4 * 4 + 2], v[q4 * 4 + 3]);
+              }
+            } else {
+              bf16* out = static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0;
+#pragma unroll
+              for (int q8 = 0; q8 < 4; ++q8) {
+                if (col0 + q8 * 8 >= p.n_out) break;
+                uint4 o;
+                o.x = pack_bf16x2(v[q8 * 8 + 0], v[q8 * 8 + 1]);
+                o.y = pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]);
+                o.z = pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]);
+                o.w = pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]);
+                st_vec16(out + q8 * 8, o);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 2-D bf16 map: `inner` contiguous elements per row, `outer` rows
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_gemm_supported(const TcProblem& q) {
+  if (q.K < 1 || q.n_out < 8 || q.n_out % 8 != 0) return false;
+  if (q.k_sub % tc::BK != 0 && q.n_sub > 1) return false;
+  if (q.n_groups > kMaxExperts) return false;
+  return tc::encode_fn() != nullptr;
+}
+
+bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
+  using namespace tc;
+  CUtensorMap ma, mb0, mb1;
+  // A [a_rows, K]
+  if (!make_map(&ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2, BM))
+    return false;
+  const int ksub = q.n_sub > 1 ? q.k_sub : q.K;
+  const uint64_t brows_total = (uint64_t)q.b_groups * q.n_sub * q.b_rows;
+  if (q.swiglu) {
+    if (!make_map(&mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2) ||
+        !make_map(&mb1, q.B1, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2))
+      return false;
+  } else {
+    if (!make_map(&mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN))
+      return false;
+    mb1 = mb0;
+  }
+  Params p{};
+  p.offsets = q.offsets;
+  p.n_groups = q.n_groups;
+  p.rows = (int)q.rows;
+  p.K = q.K;
+  p.n_out = q.n_out;
+  p.swiglu = q.swiglu;
+  p.epilogue = q.epilogue;
+  p.b_rows = q.b_rows;
+  p.k_sub = ksub;
+  p.n_sub = q.n_sub;
+  p.bias = static_cast<const bf16*>(q.bias);
+  p.bias_stride = q.bias_stride;
+  p.C = q.C;
+  p.c_is_f32 = q.c_is_f32;
+  p.err = q.err;
+  if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return false;
+  tc_gemm_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb0, mb1, p);
+  return cudaGetLastError() == cudaSuccess;
+}
+
+}  // namespace moe

@@ -1,0 +1,105 @@
+// Internal (C++) launch interface between the ABI layer and the kernels.
+// Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens whose selection statistics one router partial covers.
+constexpr int kRouteTokensPerPartial = 128;
+// Tokens per dispatch chunk (the unit of the per-chunk histogram).
+constexpr int kDispatchTokensPerChunk = 256;
+constexpr int kMaxExperts = 256;
+
+// ---- router ---------------------------------------------------------------
+// logits[N, E] (fp32) -> idx, w, per-partial selection counts and
+// probability sums ([P][E], P = ceil(N / kRouteTokensPerPartial)).
+void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_experts,
+                              int top_k, int mode, const float* sel_bias,
+                              int32_t* idx, float* w, float* psum_part,
+                              int32_t* cnt_part, cudaStream_t st);
+// sums the partials in a fixed order: counts[E] (optional) and the balance
+// statistic (optional).
+void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
+                             int n_parts, int n_experts, int64_t n_tokens,
+                             float coef, int32_t* counts, float* balance,
+                             cudaStream_t st);
+
+// ---- dispatch -------------------------------------------------------------
+void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
+                     int n_experts, int64_t capacity /* <0: none */,
+                     int32_t* chunk_cnt, int32_t* chunk_base, int32_t* offsets,
+                     int32_t* row_of_slot, int32_t* token_of_row,
+                     int32_t* counts, int32_t* kept, int32_t* dropped,
+                     int32_t* err, cudaStream_t st);
+void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
+                        const int32_t* offsets, int n_experts, int64_t max_rows,
+                        void* x_perm, int num_sms, cudaStream_t st);
+
+// ---- SIMT GEMM (fp32 and bf16 storage, fp32 accumulation) ----------------
+enum Epilogue : int {
+  kEpiNone = 0,      // C = A B^T (+ bias)
+  kEpiSiluBias = 1,  // C = silu(A B^T + bias)
+  kEpiSwiglu = 2,    // C = silu(A B0^T) * (A B1^T)
+};
+
+struct GemmProblem {
+  const void* A;             // [rows, K] row-major, lda = K
+  const void* B0;            // group g: B0 + g * b_group_stride, [N, ...]
+  const void* B1;            // second operand (SwiGLU up), same layout
+  int64_t b_group_stride;    // elements between groups
+  // element (n, k) of group g's B sits at
+  //   B + g*b_group_stride + (k / k_sub) * sub_stride + n * k_sub + (k % k_sub)
+  // (k_sub = K for one plain [N, K] matrix; the shared down projection is
+  // S column blocks of width k_sub = Fs)
+  int k_sub;
+  int64_t sub_stride;
+  const void* bias;          // [G][N] or null
+  int64_t bias_group_stride;
+  void* C;                   // [rows, N] row-major
+  int c_is_f32;              // 1: C is fp32 regardless of the storage type
+  const int32_t* offsets;    // [G+1] device (row ranges) or null: one group
+  int n_groups;
+  int64_t rows;              // rows when offsets == null, else max rows
+  int N, K;
+  int epilogue;
+  int is_bf16;               // storage type of A, B, bias (and C unless c_is_f32)
+};
+void launch_simt_gemm(const GemmProblem& p, cudaStream_t st);
+
+// ---- tcgen05 grouped GEMM (bf16 storage, fp32 accumulation in TMEM) -------
+struct TcProblem {
+  const void* A;             // [a_rows, K] bf16 row-major
+  int64_t a_rows;
+  int K;
+  const void* B0;            // [b_groups * n_sub * b_rows, k_sub] bf16
+  const void* B1;            // SwiGLU up projection, same layout as B0
+  int b_groups;              // groups stacked in B
+  int b_rows;                // rows of B per (group, sub-block)
+  int k_sub;                 // K-split width (K when n_sub == 1)
+  int n_sub;                 // K = n_sub * k_sub; block s of K reads sub-block s
+  const int32_t* offsets;    // [n_groups+1] device row ranges, or null
+  int n_groups;
+  int64_t rows;              // rows when offsets == null
+  int n_out;                 // output columns (multiple of 8)
+  int swiglu;                // 1: out = silu(A B0^T) * (A B1^T)
+  int epilogue;              // Epilogue
+  const void* bias;          // [n_groups][n_out] bf16 or null
+  int64_t bias_stride;
+  void* C;                   // [rows, n_out] bf16 (or fp32 if c_is_f32)
+  int c_is_f32;
+  int32_t* err;              // device error word
+};
+bool tc_gemm_supported(const TcProblem& p);
+bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
+
+// ---- combine ----------------------------------------------------------------
+// y: fp32 expert outputs [N*k, d]; out: layer dtype [N, d]
+void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
+                    const float* shared, void* out, int64_t n_tokens, int top_k,
+                    int d_model, int is_bf16, int num_sms, cudaStream_t st);
+
+}  // namespace moe

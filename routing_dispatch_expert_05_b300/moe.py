@@ -1,0 +1,295 @@
+"""Python binding of the C ABI in ``include/moe.h`` (ctypes).
+
+Argument marshalling only: every function here turns torch tensors into
+device pointers, passes the current CUDA stream and raises ``MoEError`` on a
+non-OK status.  All computation runs in ``libmoe_b300.so``; there is no CPU
+path.  If the library has not been built, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libmoe_b300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = -1, -2, -3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK = -4, -5, -6
+STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
+                -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_TIMEOUT",
+                -6: "MOE_ERR_DEVICE_CHECK"}
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ROUTE_SOFTMAX_TOPK, MOE_ROUTE_TOPK_SOFTMAX, MOE_ROUTE_SIGMOID_BIAS = 0, 1, 2
+MOE_EXPERT_SILU_MLP, MOE_EXPERT_SWIGLU = 0, 1
+
+# every function include/moe.h declares (checked by the tests)
+EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
+            "moe_route_logits", "moe_dispatch_permute", "moe_expert_up",
+            "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
+            "moe_forward", "moe_forward_host", "moe_read_device_error",
+            "moe_status_string", "moe_version")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class MoEConfig(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int64), ("d_model", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+                ("d_ff_shared", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("route", ctypes.c_int32), ("expert", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
+                ("balance_coef", ctypes.c_float)]
+
+
+class MoEWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "b_router", "sel_bias", "w1", "b1", "w3", "w2", "b2",
+                 "ws1", "ws3", "ws2")]
+
+
+class MoEStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("counts", "kept", "dropped", "balance")]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library once; raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library not built: {path} is missing "
+            "(run `python -m routing_dispatch_expert_05_b300.build`)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    cfgp, wp, sp = P(MoEConfig), P(MoEWeights), P(MoEStats)
+    sig = {
+        "moe_scratch_size": [cfgp, P(sz)],
+        "moe_workspace_size": [cfgp, P(sz)],
+        "moe_router_topk": [cfgp, vp, wp, vp, vp, vp, sp, vp, sz, vp],
+        "moe_route_logits": [cfgp, vp, vp, vp, vp, sp, vp, sz, vp],
+        "moe_dispatch_permute": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp],
+        "moe_expert_up": [cfgp, vp, vp, wp, vp, vp, sz, vp],
+        "moe_expert_down": [cfgp, vp, vp, wp, vp, vp, sz, vp],
+        "moe_grouped_ffn": [cfgp, vp, vp, wp, vp, vp, vp, sz, vp],
+        "moe_shared_ffn": [cfgp, vp, wp, vp, vp, vp, sz, vp],
+        "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp, sz, vp],
+        "moe_forward": [cfgp, vp, wp, vp, sp, vp, sz, vp],
+        "moe_forward_host": [cfgp, vp, wp, vp, sp, vp, sz, vp],
+        "moe_read_device_error": [vp, P(ctypes.c_int32), vp],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int32
+    lib.moe_status_string.argtypes = [ctypes.c_int32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_version.argtypes = []
+    lib.moe_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- helpers
+def ptr(t) -> Optional[int]:
+    """Device (or host) address of a tensor; None for None; ints pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "tensor"):        # MoEWorkspace
+        t = t.tensor
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+def make_config(shape, n_tokens: Optional[int] = None) -> MoEConfig:
+    """moe_config_t from a workload description (fields as in workloads.MoEShape)."""
+    return MoEConfig(
+        n_tokens=shape.n_tokens if n_tokens is None else n_tokens,
+        d_model=shape.d_model, n_experts=shape.n_experts, top_k=shape.top_k,
+        d_ff=shape.d_ff, n_shared=shape.n_shared, d_ff_shared=shape.d_ff_shared,
+        capacity_factor=shape.capacity_factor, route=shape.route,
+        expert=shape.expert, dtype=shape.dtype, has_bias=int(shape.has_bias),
+        balance_coef=shape.balance_coef)
+
+
+def make_weights(tensors: Dict[str, torch.Tensor]) -> MoEWeights:
+    w = MoEWeights()
+    for name, _ in MoEWeights._fields_:
+        setattr(w, name, ptr(tensors.get(name)))
+    return w
+
+
+def make_stats(counts=None, kept=None, dropped=None, balance=None) -> MoEStats:
+    return MoEStats(ptr(counts), ptr(kept), ptr(dropped), ptr(balance))
+
+
+def scratch_size(cfg: MoEConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().moe_scratch_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_scratch_size")
+    return n.value
+
+
+def workspace_size(cfg: MoEConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_workspace_size")
+    return n.value
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    if hasattr(ws, "tensor"):
+        ws = ws.tensor
+    return ptr(ws), ws.numel() * ws.element_size()
+
+
+# ---------------------------------------------------------------- stages
+def moe_router_topk(cfg, x, weights: MoEWeights, logits, idx, w, stats, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_router_topk(
+        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(logits), ptr(idx),
+        ptr(w), ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_router_topk")
+
+
+def moe_route_logits(cfg, logits, sel_bias, idx, w, stats, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_route_logits(
+        ctypes.byref(cfg), ptr(logits), ptr(sel_bias), ptr(idx), ptr(w),
+        ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_route_logits")
+
+
+def moe_dispatch_permute(cfg, idx, x, offsets, row_of_slot, token_of_row, x_perm,
+                         stats, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_dispatch_permute(
+        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(offsets), ptr(row_of_slot),
+        ptr(token_of_row), ptr(x_perm),
+        ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_dispatch_permute")
+
+
+def moe_expert_up(cfg, x_perm, offsets, weights: MoEWeights, h, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_expert_up(
+        ctypes.byref(cfg), ptr(x_perm), ptr(offsets), ctypes.byref(weights), ptr(h),
+        wp, wb, _stream(stream)), "moe_expert_up")
+
+
+def moe_expert_down(cfg, h, offsets, weights: MoEWeights, y, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_expert_down(
+        ctypes.byref(cfg), ptr(h), ptr(offsets), ctypes.byref(weights), ptr(y),
+        wp, wb, _stream(stream)), "moe_expert_down")
+
+
+def moe_grouped_ffn(cfg, x_perm, offsets, weights: MoEWeights, h, y, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_grouped_ffn(
+        ctypes.byref(cfg), ptr(x_perm), ptr(offsets), ctypes.byref(weights), ptr(h),
+        ptr(y), wp, wb, _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_shared_ffn(cfg, x, weights: MoEWeights, h_shared, shared_out, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_shared_ffn(
+        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(h_shared),
+        ptr(shared_out), wp, wb, _stream(stream)), "moe_shared_ffn")
+
+
+def moe_combine(cfg, y, row_of_slot, w, shared_out, out, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_combine(
+        ctypes.byref(cfg), ptr(y), ptr(row_of_slot), ptr(w), ptr(shared_out),
+        ptr(out), wp, wb, _stream(stream)), "moe_combine")
+
+
+def moe_forward(cfg, x, weights: MoEWeights, out, stats, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_forward(
+        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(out),
+        ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(cfg, x_host, weights: MoEWeights, out_host, stats, ws,
+                     stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_forward_host(
+        ctypes.byref(cfg), ptr(x_host), ctypes.byref(weights), ptr(out_host),
+        ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_forward_host")
+
+
+def moe_read_device_error(ws, stream=None) -> int:
+    code = ctypes.c_int32()
+    _check(load_library().moe_read_device_error(ptr(ws), ctypes.byref(code),
+                                                _stream(stream)),
+           "moe_read_device_error")
+    return code.value
+
+
+def status_string(status: int) -> str:
+    return load_library().moe_status_string(status).decode()
+
+
+# ------------------------------------------------------ device residency
+def torch_dtype(dtype_code: int):
+    return torch.bfloat16 if dtype_code == MOE_BF16 else torch.float32
+
+
+def upload(inputs, device="cuda") -> Dict[str, torch.Tensor]:
+    """Copy a workloads.MoEInputs to device tensors in the layer dtype.
+
+    bf16 tensors are uploaded from their exact bit patterns.
+    """
+    out = {}
+    for name in inputs.values:
+        if name in inputs.bits:
+            t = torch.from_numpy(inputs.bits[name].view("int16").copy())
+            out[name] = t.to(device).view(torch.bfloat16)
+        else:
+            out[name] = torch.from_numpy(inputs.values[name].copy()).to(device)
+    return out
+
+
+class MoEWorkspace:
+    """A zero-filled workspace for moe_forward of one configuration."""
+
+    def __init__(self, cfg: MoEConfig, device="cuda", forward: bool = True):
+        n = workspace_size(cfg) if forward else scratch_size(cfg)
+        self.tensor = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+    @property
+    def nbytes(self) -> int:
+        return self.tensor.numel()

@@ -27,9 +27,11 @@ The shapes follow the pages' workloads:
 
 Randomness: NumPy ``default_rng(seed)`` (PCG64).  Values are drawn in fp32 and,
 for bf16 workloads, rounded to bf16 (round to nearest even) before either side
-sees them, so both sides start from identical bit patterns.  Draw order:
-x, router weight, router bias (or logit offset), selection bias, then the
-expert stacks W1 (gate), b1, W3 (up), W2 (down), b2, then the shared stacks.
+sees them, so both sides start from identical bit patterns.  Draw order: the
+expert stacks W1 (gate), b1, W3 (up), W2 (down), b2, the shared stacks, the
+router weight, the router bias (or logit offset), the selection bias, and x
+last -- so the layer's parameters do not depend on the number of tokens, and
+the two 128-expert workloads (same seed) share their expert weights.
 """
 from __future__ import annotations
 
@@ -106,7 +108,7 @@ WORKLOADS: Dict[str, MoEShape] = {
     "decode_stream": MoEShape(
         name="decode_stream", n_tokens=64, d_model=2048, n_experts=128,
         top_k=8, d_ff=768, expert=EXPERT_SWIGLU, route=ROUTE_TOPK_SOFTMAX,
-        dtype=DTYPE_BF16, seed=5),
+        dtype=DTYPE_BF16, seed=4),
 }
 
 
@@ -142,6 +144,15 @@ class MoEInputs:
     values: Dict[str, np.ndarray]
     bits: Dict[str, np.ndarray]
 
+    def first_tokens(self, n: int) -> "MoEInputs":
+        """The same layer applied to the first n tokens only (views, no copy)."""
+        v = dict(self.values)
+        b = dict(self.bits)
+        v["x"] = self.values["x"][:n]
+        if "x" in b:
+            b["x"] = self.bits["x"][:n]
+        return MoEInputs(shape=self.shape.replace(n_tokens=n), values=v, bits=b)
+
     def device_array(self, name: str) -> np.ndarray:
         """The array to upload: bf16 bits for bf16 parameters, fp32 otherwise."""
         if name in self.bits:
@@ -161,18 +172,6 @@ def make_inputs(shape: MoEShape, seed: Optional[int] = None,
     rng = np.random.default_rng(s.seed if seed is None else seed)
     N, d, E, F = s.n_tokens, s.d_model, s.n_experts, s.d_ff
     v: Dict[str, np.ndarray] = {}
-    v["x"] = _normal(rng, (N, d), 1.0)
-    v["w_router"] = _normal(rng, (E, d), 1.0 / math.sqrt(d))
-    if s.router_bias == "normal":
-        v["b_router"] = _normal(rng, (E,), 1.0 / math.sqrt(d))
-    elif s.router_bias == "offset_normal":
-        v["b_router"] = _normal(rng, (E,), s.router_offset_std)
-    elif s.router_bias == "zipf":
-        rank = rng.permutation(E).astype(np.float64) + 1.0
-        v["b_router"] = (-s.zipf_s * np.log(rank)).astype(np.float32)
-    if s.route == ROUTE_SIGMOID_BIAS:
-        r = s.sel_bias_range
-        v["sel_bias"] = rng.uniform(-r, r, size=(E,)).astype(np.float32)
     v["w1"] = _normal(rng, (E, F, d), 1.0 / math.sqrt(d))
     if s.has_bias:
         v["b1"] = _normal(rng, (E, F), 1.0 / math.sqrt(d))
@@ -186,6 +185,18 @@ def make_inputs(shape: MoEShape, seed: Optional[int] = None,
         v["ws1"] = _normal(rng, (S, Fs, d), 1.0 / math.sqrt(d))
         v["ws3"] = _normal(rng, (S, Fs, d), 1.0 / math.sqrt(d))
         v["ws2"] = _normal(rng, (S, d, Fs), 1.0 / math.sqrt(Fs))
+    v["w_router"] = _normal(rng, (E, d), 1.0 / math.sqrt(d))
+    if s.router_bias == "normal":
+        v["b_router"] = _normal(rng, (E,), 1.0 / math.sqrt(d))
+    elif s.router_bias == "offset_normal":
+        v["b_router"] = _normal(rng, (E,), s.router_offset_std)
+    elif s.router_bias == "zipf":
+        rank = rng.permutation(E).astype(np.float64) + 1.0
+        v["b_router"] = (-s.zipf_s * np.log(rank)).astype(np.float32)
+    if s.route == ROUTE_SIGMOID_BIAS:
+        r = s.sel_bias_range
+        v["sel_bias"] = rng.uniform(-r, r, size=(E,)).astype(np.float32)
+    v["x"] = _normal(rng, (N, d), 1.0)
     bits: Dict[str, np.ndarray] = {}
     if s.dtype == DTYPE_BF16:
         for name in PARAM_NAMES:

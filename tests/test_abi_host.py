@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every function include/moe.h declares,
+and rejects invalid arguments on the host -- no GPU needed (no call here
+reaches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routing_dispatch_expert_05_b300 import build as B
+from routing_dispatch_expert_05_b300 import moe as M
+from routing_dispatch_expert_05_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return M.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_functions():
+    assert _declared_functions() == sorted(M.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.moe_version() >= 100
+    for code in M.STATUS_NAMES:
+        assert lib.moe_status_string(code).decode()
+    assert lib.moe_status_string(12345).decode() == "unknown status"
+
+
+def test_config_struct_layout_matches_header():
+    # int64 + 6 int32 + float + 4 int32 + float = 8 + 24 + 4 + 16 + 4 = 56
+    assert ctypes.sizeof(M.MoEConfig) == 56
+    assert ctypes.sizeof(M.MoEWeights) == 11 * 8
+    assert ctypes.sizeof(M.MoEStats) == 4 * 8
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_workspace_sizes_cover_the_intermediates(lib, name):
+    shape = W.WORKLOADS[name]
+    cfg = M.make_config(shape)
+    scratch = M.scratch_size(cfg)
+    total = M.workspace_size(cfg)
+    es = 2 if shape.dtype == W.DTYPE_BF16 else 4
+    nk = shape.n_tokens * shape.top_k
+    floor = nk * (shape.d_model * 2 + shape.d_ff) * es
+    assert scratch >= shape.n_tokens * shape.n_experts * 4
+    assert total >= scratch + floor
+
+
+def _bad(**kw):
+    base = dict(W.WORKLOADS["toy_top2_fp32"].__dict__)
+    base.update(kw)
+    return M.make_config(W.MoEShape(**base))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(top_k=0), dict(top_k=9), dict(n_experts=0), dict(n_experts=300),
+    dict(d_model=0), dict(d_model=66), dict(d_ff=130), dict(dtype=5),
+    dict(route=3), dict(expert=2), dict(n_tokens=-1), dict(n_shared=-1),
+    dict(n_shared=1, d_ff_shared=0), dict(expert=W.EXPERT_SWIGLU, has_bias=True),
+    dict(capacity_factor=float("nan"))])
+def test_invalid_config_rejected(lib, kw):
+    cfg = _bad(**kw)
+    n = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == -1
+
+
+def test_bf16_needs_multiple_of_8(lib):
+    cfg = _bad(dtype=W.DTYPE_BF16, d_model=68)   # 68 % 8 != 0
+    n = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == -1
+
+
+def test_too_many_assignments_unsupported(lib):
+    cfg = _bad(n_tokens=2 ** 31, top_k=2)
+    n = ctypes.c_size_t()
+    assert lib.moe_scratch_size(ctypes.byref(cfg), ctypes.byref(n)) == -2
+
+
+def test_stage_calls_reject_bad_pointers_before_the_device(lib):
+    cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
+    w = M.MoEWeights()
+    buf = ctypes.create_string_buffer(1 << 20)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    # missing router weight
+    st = lib.moe_router_topk(ctypes.byref(cfg), addr, ctypes.byref(w), None, addr,
+                             addr, None, addr, 1 << 19, None)
+    assert st == -1
+    # misaligned x
+    w.w_router = addr
+    st = lib.moe_router_topk(ctypes.byref(cfg), addr + 4, ctypes.byref(w), None,
+                             addr, addr, None, addr, 1 << 19, None)
+    assert st == -1
+    # workspace too small
+    st = lib.moe_router_topk(ctypes.byref(cfg), addr, ctypes.byref(w), None, addr,
+                             addr, None, addr, 16, None)
+    assert st == -3
+    # sigmoid mode without the selection bias
+    cfg2 = _bad(route=W.ROUTE_SIGMOID_BIAS)
+    st = lib.moe_route_logits(ctypes.byref(cfg2), addr, None, addr, addr, None,
+                              addr, 1 << 19, None)
+    assert st == -1
+    # shared experts requested but absent
+    st = lib.moe_shared_ffn(ctypes.byref(cfg), addr, ctypes.byref(w), addr, addr,
+                            addr, 1 << 19, None)
+    assert st == -1
+    # forward with a SwiGLU layer but no up projection
+    cfg3 = _bad(expert=W.EXPERT_SWIGLU, has_bias=False)
+    w.w1 = addr
+    w.w2 = addr
+    st = lib.moe_forward(ctypes.byref(cfg3), addr, ctypes.byref(w), addr, None,
+                         addr, 1 << 40, None)
+    assert st == -1

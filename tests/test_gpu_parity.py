@@ -1,0 +1,415 @@
+"""Parity of every stage of the CUDA path with the CPU oracle, on identical
+seeded inputs, through the C ABI.  Sizes span several tiles and end in a
+ragged tail; edge cases cover empty experts, N < E, k = E, E = 1, N = 0 and
+capacity drops."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from routing_dispatch_expert_05_b300 import build as B
+from routing_dispatch_expert_05_b300 import moe as M
+from routing_dispatch_expert_05_b300 import workloads as W
+from tests.parity_util import (BALANCE_REL, Device, ambiguous_tokens,
+                               assert_close_rms, assert_output_close,
+                               assert_within_ulp,
+                               check_selection_valid, dev, inputs_for,
+                               logit_margin, rel_tol, set_ambiguous_tokens,
+                               to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    M.load_library()
+    torch.cuda.init()
+
+
+def _cfg(**kw):
+    base = dict(name="t", n_tokens=100, d_model=64, n_experts=8, top_k=2, d_ff=64,
+                expert=W.EXPERT_SWIGLU, route=W.ROUTE_SOFTMAX_TOPK,
+                dtype=W.DTYPE_F32)
+    base.update(kw)
+    return W.MoEShape(**base)
+
+
+# ------------------------------------------------ selection from logits
+ROUTE_CASES = [(8, 2), (5, 3), (33, 4), (64, 6), (128, 8), (256, 8), (8, 8),
+               (1, 1), (200, 1), (40, 40)]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("E,k", ROUTE_CASES)
+@pytest.mark.parametrize("kind", ["normal", "ties", "signed_zero"])
+def test_route_logits_bit_exact(mode, E, k, kind):
+    N = 1000
+    seed = 1000 * mode + 10 * E + k
+    logits = W.make_logits(N, E, seed=seed, kind=kind)
+    bias = np.random.default_rng(seed).uniform(-0.1, 0.1, E).astype(np.float32) \
+        if mode == 2 else None
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, route=mode)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    idx = torch.full((N, k), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((N, k), dtype=torch.float32, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    bal = torch.zeros(1, dtype=torch.float32, device="cuda")
+    M.moe_route_logits(cfg, dev(logits), dev(bias) if bias is not None else None,
+                       idx, w, M.make_stats(counts=counts, balance=bal), ws)
+    torch.cuda.synchronize()
+    i_o, w_o, p_o = O.route(logits, mode, k, bias)
+    assert np.array_equal(to_np(idx), i_o)
+    assert np.allclose(to_np(w), w_o, rtol=2e-6, atol=2e-7)
+    cnt_o = np.bincount(i_o.reshape(-1), minlength=E)
+    assert np.array_equal(to_np(counts), cnt_o)
+    b_o = O.balance_statistic(cnt_o, p_o, N, shape.balance_coef)
+    assert abs(float(to_np(bal)[0]) - b_o) <= BALANCE_REL * abs(b_o)
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+
+
+def test_route_logits_empty_and_tail():
+    for N in (0, 1, 127, 129):
+        shape = _cfg(n_tokens=N, n_experts=16, top_k=4)
+        cfg = M.make_config(shape)
+        ws = M.MoEWorkspace(cfg, forward=False)
+        logits = W.make_logits(max(N, 1), 16, seed=N)[:N]
+        idx = torch.full((max(N, 1), 4), -1, dtype=torch.int32, device="cuda")
+        w = torch.zeros((max(N, 1), 4), dtype=torch.float32, device="cuda")
+        counts = torch.full((16,), 5, dtype=torch.int32, device="cuda")
+        bal = torch.full((1,), 5.0, device="cuda")
+        lg = dev(logits) if N else torch.zeros(16, device="cuda")
+        M.moe_route_logits(cfg, lg, None, idx, w, M.make_stats(counts=counts, balance=bal), ws)
+        torch.cuda.synchronize()
+        i_o, _, _ = O.route(logits, 0, 4) if N else (np.zeros((0, 4)), None, None)
+        assert np.array_equal(to_np(idx)[:N], i_o)
+        assert to_np(counts).sum() == 4 * N
+        if N == 0:
+            assert float(to_np(bal)[0]) == 0.0
+
+
+# ------------------------------------------------------------- dispatch
+DISPATCH_CASES = [
+    # N, E, k, capacity_factor, zipf
+    (1000, 8, 2, 1.25, 0.0),
+    (1000, 8, 2, 0.0, 0.0),
+    (777, 64, 6, 0.0, 1.1),
+    (4096, 8, 2, 1.25, 1.5),
+    (3, 8, 2, 1.25, 0.0),      # N < E: capacity 0, everything dropped
+    (1, 1, 1, 0.0, 0.0),       # E = 1
+    (300, 16, 16, 0.0, 0.0),   # k = E
+    (513, 128, 8, 0.0, 1.1),   # many empty experts
+    (2000, 256, 4, 2.0, 1.2),
+    (600, 7, 3, 1.0, 0.8),
+]
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("N,E,k,cf,zipf", DISPATCH_CASES)
+def test_dispatch_bit_exact(N, E, k, cf, zipf, dtype):
+    d = 64
+    idx = W.make_assignments(N, E, k, seed=N + E + k, zipf_s=zipf)
+    x = np.random.default_rng(N).standard_normal((N, d)).astype(np.float32)
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d, capacity_factor=cf,
+                 dtype=dtype)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    td = M.torch_dtype(dtype)
+    xd = dev(x, dtype)
+    offsets = torch.full((E + 1,), -5, dtype=torch.int32, device="cuda")
+    ros = torch.full((N * k,), -5, dtype=torch.int32, device="cuda")
+    tor = torch.full((N * k,), -5, dtype=torch.int32, device="cuda")
+    x_perm = torch.zeros((N * k, d), dtype=td, device="cuda")
+    st = {n: torch.full((E,), -5, dtype=torch.int32, device="cuda")
+          for n in ("counts", "kept", "dropped")}
+    M.moe_dispatch_permute(cfg, dev(idx), xd, offsets, ros, tor, x_perm,
+                           M.make_stats(**st), ws)
+    torch.cuda.synchronize()
+    # the config stores capacity_factor as fp32; the oracle gets the same value
+    res = O.dispatch(idx, E, float(np.float32(cf)))
+    assert np.array_equal(to_np(offsets), res["offsets"])
+    assert np.array_equal(to_np(ros), res["row_of_slot"])
+    m = int(res["offsets"][-1])
+    assert np.array_equal(to_np(tor)[:m], res["token_of_row"])
+    for n in ("counts", "kept", "dropped"):
+        assert np.array_equal(to_np(st[n]), res[n]), n
+    got = x_perm[:m].view(torch.int16 if dtype == W.DTYPE_BF16 else torch.int32)
+    ref = xd[torch.from_numpy(res["token_of_row"]).cuda()].view(got.dtype) if m else got
+    assert torch.equal(got, ref)
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+
+
+def test_dispatch_flags_bad_expert_index():
+    N, E, k, d = 64, 8, 2, 32
+    idx = W.make_assignments(N, E, k, seed=3)
+    idx[5, 1] = 8       # out of range
+    idx[9, 0] = -1      # out of range
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    x = torch.randn(N, d, device="cuda")
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    ros = torch.zeros(N * k, dtype=torch.int32, device="cuda")
+    tor = torch.zeros(N * k, dtype=torch.int32, device="cuda")
+    xp = torch.zeros(N * k, d, device="cuda")
+    M.moe_dispatch_permute(cfg, dev(idx), x, offsets, ros, tor, xp, None, ws)
+    assert M.moe_read_device_error(ws) == M.MOE_ERR_DEVICE_CHECK
+    assert M.moe_read_device_error(ws) == M.MOE_OK      # read clears it
+    r = to_np(ros)
+    assert r[5 * k + 1] == -1 and r[9 * k + 0] == -1
+    assert int(to_np(offsets)[-1]) == N * k - 2
+
+
+# ---------------------------------------------------------- expert FFNs
+FFN_CASES = [("toy_top2_fp32", 64), ("capacity_top2_fp32", 700),
+             ("capacity_top2_bf16", 700), ("deepseek_v3_block", 300),
+             ("qwen3_moe", 200)]
+
+
+def _oracle_dispatch_inputs(shape, inp, zipf=1.1, seed=77):
+    idx = W.make_assignments(shape.n_tokens, shape.n_experts, shape.top_k, seed=seed,
+                             zipf_s=zipf)
+    disp = O.dispatch(idx, shape.n_experts, float(np.float32(shape.capacity_factor)))
+    x_perm = O.permute_rows(inp.values["x"], disp["token_of_row"])
+    return idx, disp, x_perm
+
+
+def _padded(a, rows):
+    out = np.zeros((rows,) + a.shape[1:], a.dtype)
+    out[:a.shape[0]] = a
+    return out
+
+
+@pytest.mark.parametrize("name,N", FFN_CASES)
+def test_expert_up_down_parity(name, N):
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    _, disp, x_perm = _oracle_dispatch_inputs(shape, inp)
+    h_o, y_o = O.grouped_ffn(x_perm, disp["offsets"], inp.values, shape.expert,
+                             shape.dtype)
+    rows = shape.n_tokens * shape.top_k
+    m = int(disp["offsets"][-1])
+    xp = dev(_padded(x_perm.astype(np.float32), rows), shape.dtype)
+    off = dev(disp["offsets"].astype(np.int32))
+    h = D.empty(rows, shape.d_ff)
+    M.moe_expert_up(D.cfg, xp, off, D.weights, h, D.ws)
+    # down on the oracle's h, so the two projections are checked separately
+    hd = dev(_padded(h_o.astype(np.float32), rows), shape.dtype)
+    y = D.empty(rows, shape.d_model, dtype=torch.float32)
+    M.moe_expert_down(D.cfg, hd, off, D.weights, y, D.ws)
+    torch.cuda.synchronize()
+    assert_within_ulp(to_np(h)[:m], h_o, shape.dtype, "h")
+    # y is an fp32 accumulation of exactly the same bf16 products
+    assert_close_rms(to_np(y)[:m], y_o, 1e-4, "y")
+    # both together: y also carries the GPU h's one-ulp differences, each
+    # scaled by a down-projection weight, so the layer tolerance applies
+    y2 = D.empty(rows, shape.d_model, dtype=torch.float32)
+    M.moe_grouped_ffn(D.cfg, xp, off, D.weights, h, y2, D.ws)
+    torch.cuda.synchronize()
+    assert_close_rms(to_np(y2)[:m], y_o, rel_tol(shape.dtype), "y (grouped)")
+    assert D.device_error() == M.MOE_OK
+
+
+def test_shared_ffn_parity():
+    inp = inputs_for("deepseek_v3_block", 300)
+    shape = inp.shape
+    D = Device(inp)
+    hs = D.empty(shape.n_tokens, shape.n_shared * shape.d_ff_shared)
+    so = torch.empty(shape.n_tokens, shape.d_model, device="cuda")
+    M.moe_shared_ffn(D.cfg, D.t["x"], D.weights, hs, so, D.ws)
+    torch.cuda.synchronize()
+    ref = O.shared_ffn(inp.values["x"], inp.values["ws1"], inp.values["ws3"],
+                       inp.values["ws2"], shape.dtype)
+    assert_close_rms(to_np(so), ref, rel_tol(shape.dtype), "shared")
+
+
+# -------------------------------------------------------------- combine
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+@pytest.mark.parametrize("shared", [False, True])
+@pytest.mark.parametrize("cf", [0.0, 1.0])
+def test_combine_parity(dtype, shared, cf):
+    N, E, k, d = 1000, 16, 4, 256
+    rng = np.random.default_rng(5)
+    idx = W.make_assignments(N, E, k, seed=8, zipf_s=1.0)
+    disp = O.dispatch(idx, E, cf)
+    m = int(disp["offsets"][-1])
+    y = rng.standard_normal((N * k, d)).astype(np.float32)
+    w = rng.random((N, k)).astype(np.float32)
+    s = rng.standard_normal((N, d)).astype(np.float32) if shared else None
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d, dtype=dtype,
+                 capacity_factor=cf)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    out = torch.empty(N, d, dtype=M.torch_dtype(dtype), device="cuda")
+    M.moe_combine(cfg, dev(y), dev(disp["row_of_slot"].astype(np.int32)),
+                  dev(w), dev(s) if shared else None, out, ws)
+    torch.cuda.synchronize()
+    exact = O.combine(y, disp["row_of_slot"], w, s)
+    assert_output_close(to_np(out), exact, dtype, "out")
+    # the fp32 sum itself is far inside the tolerance: a bf16 output is the
+    # correctly rounded value except where the fp32 sum straddles a boundary
+    if dtype == W.DTYPE_BF16:
+        assert np.mean(to_np(out) != O.round_bf16(exact)) < 0.01
+
+
+# ------------------------------------------- router GEMM + selection
+ROUTER_CASES = [("toy_top2_fp32", None), ("capacity_top2_fp32", None),
+                ("capacity_top2_bf16", None), ("deepseek_v3_block", 1000),
+                ("qwen3_moe", 1000), ("decode_stream", None)]
+
+
+@pytest.mark.parametrize("name,N", ROUTER_CASES)
+def test_router_topk_parity(name, N):
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    n, E, k = shape.n_tokens, shape.n_experts, shape.top_k
+    logits = torch.empty(n, E, device="cuda")
+    idx = torch.empty(n, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(n, k, device="cuda")
+    st, sts = D.stats()
+    M.moe_router_topk(D.cfg, D.t["x"], D.weights, logits, idx, w, sts, D.ws)
+    torch.cuda.synchronize()
+    v = inp.values
+    lg_o = O.router_logits(v["x"], v["w_router"], v.get("b_router"))
+    lg = to_np(logits)
+    tol_logit = 1e-4 if shape.dtype == W.DTYPE_BF16 else 1e-5
+    assert np.max(np.abs(lg - lg_o)) <= tol_logit * max(1.0, np.abs(lg_o).max())
+    keys = O.selection_keys(lg_o, shape.route, v.get("sel_bias"))
+    margin = logit_margin(lg, lg_o)
+    amb = ambiguous_tokens(keys, k, margin)
+    i_o, w_o, p_o = O.route(lg_o, shape.route, k, v.get("sel_bias"))
+    ig = to_np(idx)
+    assert np.array_equal(ig[~amb], i_o[~amb])
+    check_selection_valid(ig[amb], keys[amb], k, margin)
+    assert np.allclose(to_np(w)[~amb], w_o[~amb], rtol=1e-3, atol=1e-5)
+    # the counts are those of the GPU's own selection
+    cnt = np.bincount(ig.reshape(-1), minlength=E)
+    assert np.array_equal(to_np(st["counts"]), cnt)
+    if not amb.any():
+        b_ref = O.balance_statistic(cnt, p_o, n, shape.balance_coef)
+        assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
+
+
+# --------------------------------------------------------- whole layer
+FORWARD_CASES = [("toy_top2_fp32", None), ("capacity_top2_fp32", None),
+                 ("capacity_top2_bf16", None), ("deepseek_v3_block", 640),
+                 ("qwen3_moe", 640), ("decode_stream", None)]
+
+
+def _router_margin(D, ref_logits):
+    """The near-tie margin of this layer's router: from the GPU router's
+    logits (the same kernel moe_forward runs) against the oracle's."""
+    shape = D.shape
+    n, E, k = shape.n_tokens, shape.n_experts, shape.top_k
+    logits = torch.zeros(n, E, device="cuda")
+    idx = torch.zeros(n, k, dtype=torch.int32, device="cuda")
+    w = torch.zeros(n, k, device="cuda")
+    M.moe_router_topk(D.cfg, D.t["x"], D.weights, logits, idx, w, None, D.ws)
+    torch.cuda.synchronize()
+    return logit_margin(to_np(logits), ref_logits)
+
+
+def _forward(D, stats=True):
+    shape = D.shape
+    out = D.empty(shape.n_tokens, shape.d_model)
+    st, sts = D.stats()
+    M.moe_forward(D.cfg, D.t["x"], D.weights, out, sts if stats else None, D.ws)
+    torch.cuda.synchronize()
+    return out, st
+
+
+@pytest.mark.parametrize("name,N", FORWARD_CASES)
+def test_forward_parity(name, N):
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    out, st = _forward(D)
+    ref = O.forward(shape, inp.values)
+    margin = _router_margin(D, ref["logits"])
+    keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
+    # a near-tie at the k-th key may swap one expert for another; with a
+    # capacity that also moves later drops of the experts involved, so those
+    # experts' tokens are left out of the exact comparison
+    amb, swap = set_ambiguous_tokens(keys, shape.top_k, margin)
+    keep = ~amb
+    if shape.capacity_factor > 0 and swap:
+        keep &= ~np.isin(ref["idx"], sorted(swap)).any(axis=1)
+    if shape.capacity_factor > 0:
+        others = np.array([e not in swap for e in range(shape.n_experts)])
+        for n in ("kept", "dropped"):
+            assert np.array_equal(to_np(st[n])[others], ref[n][others]), n
+    assert keep.mean() > 0.9
+    o = to_np(out)
+    assert_output_close(o[keep], ref["out_exact"][keep], shape.dtype, name)
+    cnt = to_np(st["counts"])
+    assert cnt.sum() == shape.n_tokens * shape.top_k
+    assert np.abs(cnt - ref["counts"]).sum() <= 2 * amb.sum()
+    b = float(to_np(st["balance"])[0])
+    if not amb.any():
+        assert abs(b - ref["balance"]) <= BALANCE_REL * abs(ref["balance"])
+    assert D.device_error() == M.MOE_OK
+
+
+def test_forward_host_matches_forward():
+    inp = inputs_for("capacity_top2_bf16", None)
+    D = Device(inp)
+    out, _ = _forward(D)
+    shape = inp.shape
+    xh = D.t["x"].cpu().pin_memory()
+    oh = torch.empty(shape.n_tokens, shape.d_model, dtype=D.tdtype).pin_memory()
+    M.moe_forward_host(D.cfg, xh, D.weights, oh, None, D.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, out.cpu())
+
+
+def test_forward_is_deterministic():
+    inp = inputs_for("deepseek_v3_block", 256)
+    D = Device(inp)
+    a, sa = _forward(D)
+    b, sb = _forward(D)
+    assert torch.equal(a, b)
+    assert torch.equal(sa["balance"], sb["balance"])
+
+
+def test_forward_zero_tokens():
+    inp = inputs_for("toy_top2_fp32", 0)
+    D = Device(inp)
+    out, st = _forward(D)
+    assert out.numel() == 0
+    assert (to_np(st["counts"]) == 0).all() and float(to_np(st["balance"])[0]) == 0.0
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (4, 4)])
+def test_forward_special_cases(E, k):
+    """E = 1, k = 1 is the dense FFN; k = E with no capacity is the dense
+    all-expert weighted sum -- both reach the same values as the oracle."""
+    shape = _cfg(n_tokens=300, n_experts=E, top_k=k, d_model=64, d_ff=96)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, _ = _forward(D)
+    ref = O.forward(shape, inp.values)
+    assert_output_close(to_np(out), ref["out_exact"], shape.dtype, "special")
+
+
+# -------------------------------------------- full-size sampled checks
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["qwen3_moe", "deepseek_v3_block"])
+def test_forward_full_size_sampled(name):
+    inp = inputs_for(name, None)
+    shape = inp.shape
+    D = Device(inp)
+    out, st = _forward(D)
+    rng = np.random.default_rng(0)
+    tokens = np.unique(np.concatenate([rng.choice(shape.n_tokens, 48, replace=False),
+                                       [0, shape.n_tokens - 1]]))
+    ref = O.forward_tokens(shape, inp.values, tokens)
+    keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
+    amb, _ = set_ambiguous_tokens(keys, shape.top_k, 4e-4)   # logits agree to 1e-4
+    o = to_np(out)[tokens]
+    assert_output_close(o[~amb], ref["out_exact"][~amb], shape.dtype, name)
+    cnt = to_np(st["counts"])
+    assert cnt.sum() == shape.n_tokens * shape.top_k
+    assert D.device_error() == M.MOE_OK
