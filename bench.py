@@ -152,8 +152,8 @@ def blas_threads():
 def kernel_launches_per_step(shape):
     """Kernels the library launches for one moe_forward of this layer."""
     router = 3          # logits GEMM, selection, statistic finalize
-    dispatch = 4        # count, scan, rank, gather
-    experts = 2         # grouped up (with activation), grouped down
+    dispatch = 3        # count, scan, rank (the row gather is fused into up)
+    experts = 2         # grouped up (row gather + activation), grouped down
     shared = 2 if shape.n_shared > 0 else 0
     combine = 1
     return router + dispatch + experts + shared + combine
@@ -186,7 +186,6 @@ def run_ours(args, shape, peaks, peaks_kind):
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     ros = torch.empty(N * k, dtype=torch.int32, device=dev)
     tor = torch.empty(N * k, dtype=torch.int32, device=dev)
-    x_perm = torch.empty(N * k, d, dtype=td, device=dev)
     h = torch.empty(N * k, F, dtype=td, device=dev)
     y = torch.empty(N * k, d, dtype=torch.float32, device=dev)
     out = torch.empty(N, d, dtype=td, device=dev)
@@ -212,9 +211,11 @@ def run_ours(args, shape, peaks, peaks_kind):
         mark(0)
         M.moe_router_topk(cfg, x, weights, None, idx, wts, rstats, ws)
         mark(1)
-        M.moe_dispatch_permute(cfg, idx, x, offsets, ros, tor, x_perm, dstats, ws)
+        # the launches of moe_forward: grouping without a copy, then the up
+        # projection gathers the token rows itself
+        M.moe_dispatch_permute(cfg, idx, None, offsets, ros, tor, None, dstats, ws)
         mark(2)
-        M.moe_expert_up(cfg, x_perm, offsets, weights, h, ws)
+        M.moe_expert_up_gather(cfg, x, tor, offsets, weights, h, ws)
         mark(3)
         M.moe_expert_down(cfg, h, offsets, weights, y, ws)
         i = 4
@@ -321,7 +322,8 @@ def run_ours(args, shape, peaks, peaks_kind):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     # algorithmic bytes of the HBM-bound stages (per step)
     router_bytes = N * d * es + E * d * es + N * k * 8
-    dispatch_bytes = N * d * es + m_kept * d * es + N * k * 4 * 3
+    # idx read twice, row_of_slot and token_of_row written
+    dispatch_bytes = N * k * 4 * 4
     combine_bytes = m_kept * d * 4 + N * d * es + N * k * 8 + \
         (N * d * 4 if shape.n_shared > 0 else 0)
     stage_report = {}
@@ -438,10 +440,14 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1024)
     ap.add_argument("--up-traffic-bytes", type=float, default=None,
                     help="DRAM bytes per launch of the up projection from an ncu capture")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the token count (smaller cases for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     shape = W.WORKLOADS[args.workload]
+    if args.tokens is not None and args.tokens != shape.n_tokens:
+        shape = shape.replace(name=f"{shape.name}@{args.tokens}tok", n_tokens=args.tokens)
     if args.impl == "reference":
         res, rank = run_reference(args, shape)
     else:

@@ -167,8 +167,10 @@ MOE_API moe_status_t moe_scratch_size(const moe_config_t *cfg, size_t *bytes);
 
 /* Bytes of workspace moe_forward / moe_forward_host need: the scratch plus
  * every intermediate of the layer sized for the worst case M = N * k
- * (idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, and for shared
- * experts their hidden activations and fp32 sum; host staging for x, out). */
+ * (idx, w, offsets, row_of_slot, token_of_row, h, y, and for shared
+ * experts their hidden activations and fp32 sum; host staging for x, out).
+ * moe_forward does not materialise x_perm: its up projection reads the
+ * token rows of x directly (see moe_expert_up_gather). */
 MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
 /* ---- stages ----------------------------------------------------------- */
@@ -199,9 +201,11 @@ MOE_API moe_status_t moe_route_logits(const moe_config_t *cfg, const float *logi
  * assignments of e occupy rows offsets[e] .. offsets[e+1]-1 in arrival
  * order.  Writes offsets [E+1], row_of_slot [N*k] (-1 = dropped),
  * token_of_row [N*k] (first offsets[E] entries valid) and
- * x_perm [N*k, d] (first offsets[E] rows valid), and the stats
- * counts/kept/dropped.  An index outside [0, E) is treated as dropped and
- * sets MOE_ERR_DEVICE_CHECK in the error word. */
+ * x_perm [N*k, d] (first offsets[E] rows valid, x_perm[r] = x[token_of_row[r]]),
+ * and the stats counts/kept/dropped.  x and x_perm may both be NULL: then
+ * the rows are not copied (moe_expert_up_gather reads them from x).  An
+ * index outside [0, E) is treated as dropped and sets MOE_ERR_DEVICE_CHECK
+ * in the error word. */
 MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t *idx,
                                   const void *x, int32_t *offsets,
                                   int32_t *row_of_slot, int32_t *token_of_row,
@@ -216,6 +220,18 @@ MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t
 MOE_API moe_status_t moe_expert_up(const moe_config_t *cfg, const void *x_perm,
                            const int32_t *offsets, const moe_weights_t *weights,
                            void *h, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_expert_up with the grouping gather fused into the GEMM's operand
+ * loads: row r of expert e reads token row x[token_of_row[r]] straight from
+ * x [N, d] instead of x_perm[r], so the expert-sorted copy of the tokens is
+ * never written.  token_of_row [N*k] and offsets [E+1] as written by
+ * moe_dispatch_permute (device, read on the device); h [N*k, F].  The
+ * result equals moe_expert_up on the materialised x_perm. */
+MOE_API moe_status_t moe_expert_up_gather(const moe_config_t *cfg, const void *x,
+                                  const int32_t *token_of_row,
+                                  const int32_t *offsets,
+                                  const moe_weights_t *weights, void *h,
+                                  void *ws, size_t ws_bytes, void *stream);
 
 /* Expert down-projection: y[r] = W2[e] h[r] (+ b2[e]); y [N*k, d] fp32. */
 MOE_API moe_status_t moe_expert_down(const moe_config_t *cfg, const void *h,

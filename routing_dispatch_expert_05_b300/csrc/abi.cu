@@ -23,7 +23,7 @@ struct Layout {
   // scratch (shared by all stage calls)
   size_t err, route_psum, route_cnt, chunk_cnt, chunk_base, logits, scratch_end;
   // intermediates of moe_forward
-  size_t idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, h_shared,
+  size_t idx, w, offsets, row_of_slot, token_of_row, h, y, h_shared,
       shared_out, x_stage, out_stage, total;
   int route_parts, chunks;
 };
@@ -53,7 +53,7 @@ Layout layout_of(const moe_config_t& c) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.row_of_slot = take((size_t)N * k * 4);
   L.token_of_row = take((size_t)N * k * 4);
-  L.x_perm = take((size_t)N * k * d * es);
+  // moe_forward gathers token rows inside the up projection: no x_perm
   L.h = take((size_t)N * k * F * es);
   L.y = take((size_t)N * k * d * 4);   // expert outputs stay fp32
   if (c.n_shared > 0) {
@@ -186,6 +186,28 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
                  void* ws, cudaStream_t st, bool gemm) {
   const Layout L = layout_of(c);
   float* lg = logits ? logits : at<float>(ws, L.logits);
+  if (gemm && c.dtype == MOE_BF16) {
+    // bf16 router: one dense tcgen05 GEMM, fp32 logits (N = E columns)
+    TcProblem q{};
+    q.A = x;
+    q.a_rows = c.n_tokens;
+    q.K = c.d_model;
+    q.B0 = w.w_router;
+    q.b_groups = 1;
+    q.b_rows = c.n_experts;
+    q.k_sub = c.d_model;
+    q.n_sub = 1;
+    q.n_groups = 1;
+    q.rows = c.n_tokens;
+    q.n_out = c.n_experts;
+    q.epilogue = kEpiNone;
+    q.bias = w.b_router;
+    q.bias_stride = 0;
+    q.C = lg;
+    q.c_is_f32 = 1;
+    q.err = err_word(ws);
+    if (tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) gemm = false;
+  }
   if (gemm) {
     GemmProblem p{};
     p.A = x;
@@ -222,8 +244,9 @@ void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                   offsets, ros, tor, stats ? stats->counts : nullptr,
                   stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr,
                   at<int32_t>(ws, L.err), st);
-  launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
-                     c.n_tokens * c.top_k, x_perm, num_sms(), st);
+  if (x_perm != nullptr)
+    launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
+                       c.n_tokens * c.top_k, x_perm, num_sms(), st);
 }
 
 // bf16 expert GEMMs run on the tensor cores; fp32 ones on the CUDA cores
@@ -235,11 +258,17 @@ moe_status_t run_gemm(const moe_config_t& c, const TcProblem& tq, const GemmProb
   return MOE_OK;
 }
 
-moe_status_t up_body(const moe_config_t& c, const void* x_perm, const int32_t* offsets,
-                     const moe_weights_t& w, void* h, int32_t* err, cudaStream_t st) {
+// The up projection reads its rows either from the expert-sorted buffer
+// (row_map == null, a = x_perm) or straight from the token rows
+// (a = x, row r reads token row_map[r]).
+moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_map,
+                     const int32_t* offsets, const moe_weights_t& w, void* h,
+                     int32_t* err, cudaStream_t st) {
   const bool swiglu = c.expert == MOE_EXPERT_SWIGLU;
+  const int64_t a_rows = row_map ? c.n_tokens : c.n_tokens * c.top_k;
   GemmProblem p{};
-  p.A = x_perm;
+  p.A = a;
+  p.a_row_map = row_map;
   p.B0 = w.w1;
   p.B1 = swiglu ? w.w3 : nullptr;
   p.b_group_stride = (int64_t)c.d_ff * c.d_model;
@@ -255,8 +284,9 @@ moe_status_t up_body(const moe_config_t& c, const void* x_perm, const int32_t* o
   p.epilogue = swiglu ? kEpiSwiglu : kEpiSiluBias;
   p.is_bf16 = c.dtype == MOE_BF16;
   TcProblem q{};
-  q.A = x_perm;
-  q.a_rows = c.n_tokens * c.top_k;
+  q.A = a;
+  q.a_rows = a_rows;
+  q.a_row_map = row_map;
   q.K = c.d_model;
   q.B0 = w.w1;
   q.B1 = p.B1;
@@ -266,7 +296,7 @@ moe_status_t up_body(const moe_config_t& c, const void* x_perm, const int32_t* o
   q.n_sub = 1;
   q.offsets = offsets;
   q.n_groups = c.n_experts;
-  q.rows = q.a_rows;
+  q.rows = c.n_tokens * c.top_k;
   q.n_out = c.d_ff;
   q.swiglu = swiglu;
   q.epilogue = p.epilogue;
@@ -455,7 +485,10 @@ moe_status_t moe_dispatch_permute(const moe_config_t* cfg, const int32_t* idx,
     MOE_TRY(last_cuda());
     return zero_stats(c, stats, st);
   }
-  MOE_TRY(need({idx, x, row_of_slot, token_of_row, x_perm}));
+  MOE_TRY(need({idx, row_of_slot, token_of_row}));
+  // x and x_perm: both present (rows are gathered) or both NULL (no gather)
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(maybe({x, x_perm}));
   dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats, ws, st);
   return last_cuda();
 }
@@ -469,7 +502,23 @@ moe_status_t moe_expert_up(const moe_config_t* cfg, const void* x_perm,
   MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
   if (c.n_tokens == 0) return MOE_OK;
   MOE_TRY(need({x_perm, offsets, h}));
-  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), static_cast<cudaStream_t>(stream)));
+  MOE_TRY(up_body(c, x_perm, nullptr, offsets, *weights, h, err_word(ws),
+                  static_cast<cudaStream_t>(stream)));
+  return last_cuda();
+}
+
+moe_status_t moe_expert_up_gather(const moe_config_t* cfg, const void* x,
+                                  const int32_t* token_of_row, const int32_t* offsets,
+                                  const moe_weights_t* weights, void* h, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_up_weights(c, weights));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({x, token_of_row, offsets, h}));
+  MOE_TRY(up_body(c, x, token_of_row, offsets, *weights, h, err_word(ws),
+                  static_cast<cudaStream_t>(stream)));
   return last_cuda();
 }
 
@@ -498,7 +547,7 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm,
   if (c.n_tokens == 0) return MOE_OK;
   MOE_TRY(need({x_perm, offsets, h, y}));
   auto st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), st));
+  MOE_TRY(up_body(c, x_perm, nullptr, offsets, *weights, h, err_word(ws), st));
   MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
   return last_cuda();
 }
@@ -555,7 +604,6 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* ros = at<int32_t>(ws, L.row_of_slot);
   int32_t* tor = at<int32_t>(ws, L.token_of_row);
-  void* x_perm = at<char>(ws, L.x_perm);
   void* h = at<char>(ws, L.h);
   float* y = at<float>(ws, L.y);
   float* shared_out = c.n_shared > 0 ? at<float>(ws, L.shared_out) : nullptr;
@@ -572,8 +620,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
     ds.kept = stats->kept;
     ds.dropped = stats->dropped;
   }
-  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, ws, st);
-  MOE_TRY(up_body(c, x_perm, offsets, *weights, h, err_word(ws), st));
+  // grouping without a copy: the up projection gathers the token rows
+  dispatch_body(c, idx, nullptr, offsets, ros, tor, nullptr, &ds, ws, st);
+  MOE_TRY(up_body(c, x, tor, offsets, *weights, h, err_word(ws), st));
   MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
   if (c.n_shared > 0)
     MOE_TRY(shared_body(c, x, *weights, at<char>(ws, L.h_shared), shared_out,

@@ -89,7 +89,12 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmProblem p) {
       const int r = li >> 4, kk = li & 15;
       const int64_t gr = row0 + r;
       const int gk = k0 + kk;
-      As[kk][r] = (gr < row_end && gk < K) ? ld_elem<T>(p.A, gr * K + gk) : 0.f;
+      float v = 0.f;
+      if (gr < row_end && gk < K) {
+        const int64_t src = p.a_row_map ? (int64_t)p.a_row_map[gr] : gr;
+        v = ld_elem<T>(p.A, src * K + gk);
+      }
+      As[kk][r] = v;
     }
 #pragma unroll
     for (int b = 0; b < NB; ++b) {

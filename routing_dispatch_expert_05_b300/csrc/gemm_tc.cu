@@ -48,8 +48,25 @@ constexpr uint32_t kStageBytes = kTileA + kTileB;   // 48 KB
 constexpr uint32_t kTmemCols = 2 * BN;              // two accumulators
 constexpr uint64_t kTimeoutNs = 2000000000ull;      // 2 s
 constexpr int kBarBytes = 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes +
-                           2 * (kMaxExperts + 1) * 4 + 1024 /* alignment */;
+// per-group tile starts and row offsets, padded so what follows stays
+// 128-byte aligned
+constexpr int kTableBytes = (2 * (kMaxExperts + 1) * 4 + 127) / 128 * 128;
+// Epilogue staging: each epilogue warp turns its 32 rows x 32 columns chunk
+// (one row per lane after tcgen05.ld) into row-contiguous global stores.
+// Rows are padded (fp32: 36 words, bf16: 20 words) so that both the
+// row-per-lane writes and the column-per-lane reads are free of bank
+// conflicts (up to a 2-way conflict on a quarter of the bf16 reads).
+constexpr int kStgF32Stride = 36;                  // floats per staged row
+constexpr int kStgB16Stride = 20;                  // 32-bit words per staged row
+constexpr int kStgWarpBytes = 32 * kStgF32Stride * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kTableBytes +
+                           4 * kStgWarpBytes + 1024 /* alignment */;
+static_assert((kStages * kStageBytes + kBarBytes + kTableBytes) % 16 == 0,
+              "epilogue staging must be 16-byte aligned (vector stores)");
+static_assert(kStgWarpBytes % 16 == 0 && (kStgF32Stride * 4) % 16 == 0 &&
+                  (kStgB16Stride * 4) % 16 == 0,
+              "staged rows must keep 16-byte alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
   const int32_t* offsets;     // [G+1] device or null (one group of `rows`)
@@ -67,6 +84,8 @@ struct Params {
   void* C;                    // [rows, n_out]
   int c_is_f32;
   int32_t* err;
+  const int32_t* a_row_map;   // null: A rows are the tile rows; else A row r
+                              // is row a_row_map[r] of the A tensor
 };
 
 // ---------------------------------------------------------------- PTX
@@ -125,6 +144,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
       " [%0], [%1, {%3, %4}], [%2];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
         "r"(c0), "r"(c1)
+      : "memory");
+}
+// Four rows r0..r3 (each one box of BK columns starting at column c0) into
+// consecutive 128-byte rows of shared memory; the map's box is one row high.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
+        "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -231,6 +261,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_tile_start = reinterpret_cast<int*>(smem + kStages * kStageBytes + kBarBytes);
   int* s_off = s_tile_start + kMaxExperts + 1;
+  uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.offsets ? p.n_groups : 1;
@@ -290,21 +321,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t last_phase[kStages];
-      bool used[kStages];
-      for (int s = 0; s < kStages; ++s) used[s] = false, last_phase[s] = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
+    // Lane 0 waits for free stages and loads B (and a plain A tile).  With a
+    // row map, the A tile is gathered: lane l loads rows 4l..4l+3 of the
+    // tile (tokens row_map[row]) with one gather4 per k-block.
+    const bool gather = p.a_row_map != nullptr;
+    const int m_total = s_off[G];
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t last_phase[kStages];
+    bool used[kStages];
+    for (int s = 0; s < kStages; ++s) used[s] = false, last_phase[s] = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
+      int src[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          // rows past the last kept row read token 0; they are never stored
+          const int row = tl.row0 + lane * 4 + i;
+          src[i] = row < m_total ? __ldg(p.a_row_map + row) : 0;
+        }
+      }
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        int good = 1;
+        if (lane == 0) good = wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err);
+        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        uint8_t* a = sA + stage * kTileA;
+        if (lane == 0) {
           mbar_expect_tx(&full[stage], kStageBytes);
-          uint8_t* a = sA + stage * kTileA;
           uint8_t* b = sB + stage * kTileB;
-          tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
+          if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
           if (p.swiglu) {
             const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
             tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
@@ -317,11 +364,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           used[stage] = true;
           last_phase[stage] = phase;
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (gather)
+          tma_gather4(a + lane * 4 * (BK * 2), &tmA, &full[stage], kb * BK, src[0], src[1],
+                      src[2], src[3]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-      // every issued copy has landed before the CTA can exit
+      if (!ok) break;
+    }
+    // every issued copy has landed before the CTA can exit
+    if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         if (!used[s]) continue;
         const uint64_t t0 = globaltimer();
@@ -376,86 +429,94 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ------------------------------------------------------ epilogue
     const int q = warp & 3;
+    float* stg_f = reinterpret_cast<float*>(s_stage + (warp - 2) * kStgWarpBytes);
+    uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg_f);
+    const int cols_tile = p.swiglu ? BN / 2 : BN;   // output columns per tile
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
       if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
       tc_fence_after();
-      const int row = tl.row0 + q * 32 + lane;
-      const bool valid = row < tl.row_end;
+      const int row_base = tl.row0 + q * 32;         // this warp's 32 rows
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      if (p.swiglu) {
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 2 / 32; ++ch) {
+      for (int ch = 0; ch < cols_tile / 32; ++ch) {
+        const int col0 = tl.n * cols_tile + ch * 32;
+        if (col0 >= p.n_out) break;                  // warp-uniform
+        float v[32];
+        if (p.swiglu) {
           uint32_t g[32], u[32];
           MOE_TMEM_LD32(tb + ch * 32, g);
           MOE_TMEM_LD32(tb + BN / 2 + ch * 32, u);
           tmem_ld_wait();
-          const int col0 = tl.n * (BN / 2) + ch * 32;
-          if (valid) {
-            bf16* out = static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (col0 + v * 8 >= p.n_out) break;
-              uint4 o;
-              uint32_t* ow = &o.x;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int c = v * 8 + j * 2;
-                const float h0 = silu_f32(__uint_as_float(g[c])) * __uint_as_float(u[c]);
-                const float h1 =
-                    silu_f32(__uint_as_float(g[c + 1])) * __uint_as_float(u[c + 1]);
-                ow[j] = pack_bf16x2(h0, h1);
-              }
-              st_vec16(out + v * 8, o);
-            }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+          for (int j = 0; j < 32; ++j)
+            v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+        } else {
           uint32_t r[32];
           MOE_TMEM_LD32(tb + ch * 32, r);
           tmem_ld_wait();
-          const int col0 = tl.n * BN + ch * 32;
-          if (valid && col0 < p.n_out) {
-            float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-            if (p.bias) {
-              const bf16* bp = p.bias + (int64_t)tl.g * p.bias_stride + col0;
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if (p.bias) {
+            const bf16* bp = p.bias + (int64_t)tl.g * p.bias_stride + col0;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < p.n_out) v[j] += __bfloat162float(bp[j]);
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.n_out) v[j] += __bfloat162float(bp[j]);
+          }
+          if (p.epilogue == kEpiSiluBias) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
+          }
+        }
+        // lane = row: stage the row's 32 values
+        if (p.c_is_f32) {
+          float4* dst = reinterpret_cast<float4*>(stg_f + lane * kStgF32Stride);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(stg_w + lane * kStgB16Stride);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+        __syncwarp();
+        // lane = 16-byte column piece: whole row segments per store
+        if (p.c_is_f32) {
+          const int c4 = lane & 7;
+          const bool col_ok = col0 + c4 * 4 < p.n_out;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + (lane >> 3);
+            const int row = row_base + r;
+            if (col_ok && row < tl.row_end) {
+              const float4 val =
+                  *reinterpret_cast<const float4*>(stg_f + r * kStgF32Stride + c4 * 4);
+              *reinterpret_cast<float4*>(static_cast<float*>(p.C) + (int64_t)row * p.n_out +
+                                         col0 + c4 * 4) = val;
             }
-            if (p.epilogue == kEpiSiluBias) {
+          }
+        } else {
+          const int c8 = lane & 3;
+          const bool col_ok = col0 + c8 * 8 < p.n_out;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
-            }
-            if (p.c_is_f32) {
-              float* out = static_cast<float*>(p.C) + (int64_t)row * p.n_out + col0;
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                if (col0 + q4 * 4 >= p.n_out) break;
-                *reinterpret_cast<float4*>(out + q4 * 4) =
-                    make_float4(v[q4 * 4], v[q4 * 4 + 1], v[q4 * 4 + 2], v[q4 * 4 + 3]);
-              }
-            } else {
-              bf16* out = static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0;
-#pragma unroll
-              for (int q8 = 0; q8 < 4; ++q8) {
-                if (col0 + q8 * 8 >= p.n_out) break;
-                uint4 o;
-                o.x = pack_bf16x2(v[q8 * 8 + 0], v[q8 * 8 + 1]);
-                o.y = pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]);
-                o.z = pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]);
-                o.w = pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]);
-                st_vec16(out + q8 * 8, o);
-              }
+          for (int it = 0; it < 4; ++it) {
+            const int r = it * 8 + (lane >> 2);
+            const int row = row_base + r;
+            if (col_ok && row < tl.row_end) {
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(stg_w + r * kStgB16Stride + c8 * 4);
+              st_vec16(static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0 + c8 * 8,
+                       val);
             }
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -515,7 +576,9 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   using namespace tc;
   CUtensorMap ma, mb0, mb1;
   // A [a_rows, K]
-  if (!make_map(&ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2, BM))
+  // a gathered A is read one row per box (four boxes per gather4)
+  if (!make_map(&ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2,
+                q.a_row_map ? 1u : (uint32_t)BM))
     return false;
   const int ksub = q.n_sub > 1 ? q.k_sub : q.K;
   const uint64_t brows_total = (uint64_t)q.b_groups * q.n_sub * q.b_rows;
@@ -544,6 +607,7 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.C = q.C;
   p.c_is_f32 = q.c_is_f32;
   p.err = q.err;
+  p.a_row_map = q.a_row_map;
   if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return false;

@@ -67,6 +67,9 @@ struct GemmProblem {
   int N, K;
   int epilogue;
   int is_bf16;               // storage type of A, B, bias (and C unless c_is_f32)
+  // Optional row map (fused dispatch gather): row r of the grouped problem
+  // reads row a_row_map[r] of A.  null: A is in grouped row order.
+  const int32_t* a_row_map;
 };
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st);
 
@@ -92,6 +95,10 @@ struct TcProblem {
   void* C;                   // [rows, n_out] bf16 (or fp32 if c_is_f32)
   int c_is_f32;
   int32_t* err;              // device error word
+  // Optional row map (fused dispatch gather): A row r of the grouped problem
+  // is row a_row_map[r] of A ([a_rows, K], e.g. the token rows x), for
+  // r < offsets[n_groups].  null: A is already in grouped row order.
+  const int32_t* a_row_map;
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);

@@ -29,7 +29,7 @@ MOE_EXPERT_SILU_MLP, MOE_EXPERT_SWIGLU = 0, 1
 # every function include/moe.h declares (checked by the tests)
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_route_logits", "moe_dispatch_permute", "moe_expert_up",
-            "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
+            "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_host", "moe_read_device_error",
             "moe_status_string", "moe_version")
 
@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route_logits": [cfgp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_dispatch_permute": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_expert_up": [cfgp, vp, vp, wp, vp, vp, sz, vp],
+        "moe_expert_up_gather": [cfgp, vp, vp, vp, wp, vp, vp, sz, vp],
         "moe_expert_down": [cfgp, vp, vp, wp, vp, vp, sz, vp],
         "moe_grouped_ffn": [cfgp, vp, vp, wp, vp, vp, vp, sz, vp],
         "moe_shared_ffn": [cfgp, vp, wp, vp, vp, vp, sz, vp],
@@ -204,6 +205,14 @@ def moe_expert_up(cfg, x_perm, offsets, weights: MoEWeights, h, ws, stream=None)
     _check(load_library().moe_expert_up(
         ctypes.byref(cfg), ptr(x_perm), ptr(offsets), ctypes.byref(weights), ptr(h),
         wp, wb, _stream(stream)), "moe_expert_up")
+
+
+def moe_expert_up_gather(cfg, x, token_of_row, offsets, weights: MoEWeights, h, ws,
+                         stream=None):
+    wp, wb = _ws(ws)
+    _check(load_library().moe_expert_up_gather(
+        ctypes.byref(cfg), ptr(x), ptr(token_of_row), ptr(offsets),
+        ctypes.byref(weights), ptr(h), wp, wb, _stream(stream)), "moe_expert_up_gather")
 
 
 def moe_expert_down(cfg, h, offsets, weights: MoEWeights, y, ws, stream=None):

@@ -212,6 +212,39 @@ def test_expert_up_down_parity(name, N):
     assert D.device_error() == M.MOE_OK
 
 
+@pytest.mark.parametrize("name,N", FFN_CASES)
+def test_expert_up_gather_matches_materialised_rows(name, N):
+    """The up projection reading token rows through token_of_row equals the
+    one reading the expert-sorted copy x_perm bit for bit (same products,
+    same accumulation order), and so matches the oracle's h."""
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    idx, disp, x_perm = _oracle_dispatch_inputs(shape, inp)
+    rows = shape.n_tokens * shape.top_k
+    m = int(disp["offsets"][-1])
+    off = torch.zeros(shape.n_experts + 1, dtype=torch.int32, device="cuda")
+    ros = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    tor = torch.full((rows,), -3, dtype=torch.int32, device="cuda")
+    xp = D.empty(rows, shape.d_model)
+    M.moe_dispatch_permute(D.cfg, dev(idx), D.t["x"], off, ros, tor, xp, None, D.ws)
+    # the same grouping without the copy leaves x_perm alone
+    tor2 = torch.full((rows,), -3, dtype=torch.int32, device="cuda")
+    M.moe_dispatch_permute(D.cfg, dev(idx), None, off, ros, tor2, None, None, D.ws)
+    h_ref = D.empty(rows, shape.d_ff)
+    M.moe_expert_up(D.cfg, xp, off, D.weights, h_ref, D.ws)
+    h = D.empty(rows, shape.d_ff)
+    M.moe_expert_up_gather(D.cfg, D.t["x"], tor2, off, D.weights, h, D.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(tor[:m], tor2[:m])
+    assert np.array_equal(to_np(tor2)[:m], disp["token_of_row"])
+    assert torch.equal(h[:m], h_ref[:m])
+    h_o, _ = O.grouped_ffn(x_perm, disp["offsets"], inp.values, shape.expert,
+                           shape.dtype)
+    assert_within_ulp(to_np(h)[:m], h_o, shape.dtype, "h (gathered)")
+    assert D.device_error() == M.MOE_OK
+
+
 def test_shared_ffn_parity():
     inp = inputs_for("deepseek_v3_block", 300)
     shape = inp.shape
