@@ -151,9 +151,12 @@ def blas_threads():
 
 def kernel_launches_per_step(shape):
     """Kernels the library launches for one moe_forward of this layer."""
-    router = 3          # logits GEMM, selection, statistic finalize
-    dispatch = 3        # count, scan, rank (the row gather is fused into up)
-    experts = 2         # grouped up (row gather + activation), grouped down
+    # bf16: logits GEMM with the selection epilogue + statistic finalize;
+    # fp32: logits GEMM, selection kernel, finalize
+    fused = shape.dtype == W.DTYPE_BF16 and shape.n_experts % 8 == 0 and shape.top_k <= 8
+    router = 2 if fused else 3
+    dispatch = 4        # count, scan, rank, row gather
+    experts = 2         # grouped up (with activation), grouped down
     shared = 2 if shape.n_shared > 0 else 0
     combine = 1
     return router + dispatch + experts + shared + combine
@@ -180,52 +183,14 @@ def run_ours(args, shape, peaks, peaks_kind):
     td = M.torch_dtype(shape.dtype)
     es = 2 if shape.dtype == W.DTYPE_BF16 else 4
     x = t["x"]
-    # stage buffers (views of nothing: separate allocations for the staged step)
-    idx = torch.empty(N, k, dtype=torch.int32, device=dev)
-    wts = torch.empty(N, k, dtype=torch.float32, device=dev)
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    ros = torch.empty(N * k, dtype=torch.int32, device=dev)
-    tor = torch.empty(N * k, dtype=torch.int32, device=dev)
-    h = torch.empty(N * k, F, dtype=td, device=dev)
-    y = torch.empty(N * k, d, dtype=torch.float32, device=dev)
     out = torch.empty(N, d, dtype=td, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     kept = torch.empty(E, dtype=torch.int32, device=dev)
     dropped = torch.empty(E, dtype=torch.int32, device=dev)
     bal = torch.empty(1, dtype=torch.float32, device=dev)
-    hs = so = None
-    if shape.n_shared > 0:
-        hs = torch.empty(N, shape.n_shared * shape.d_ff_shared, dtype=td, device=dev)
-        so = torch.empty(N, d, dtype=torch.float32, device=dev)
-    rstats = M.make_stats(counts=counts, balance=bal)
-    dstats = M.make_stats(kept=kept, dropped=dropped)
     fstats = M.make_stats(counts=counts, kept=kept, dropped=dropped, balance=bal)
     stream = torch.cuda.current_stream(dev)
-    stages = ["router", "dispatch", "expert_up", "expert_down"] + \
-        (["shared"] if shape.n_shared > 0 else []) + ["combine"]
-
-    def step(ev=None):
-        def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        M.moe_router_topk(cfg, x, weights, None, idx, wts, rstats, ws)
-        mark(1)
-        # the launches of moe_forward: grouping without a copy, then the up
-        # projection gathers the token rows itself
-        M.moe_dispatch_permute(cfg, idx, None, offsets, ros, tor, None, dstats, ws)
-        mark(2)
-        M.moe_expert_up_gather(cfg, x, tor, offsets, weights, h, ws)
-        mark(3)
-        M.moe_expert_down(cfg, h, offsets, weights, y, ws)
-        i = 4
-        mark(i)
-        if so is not None:
-            M.moe_shared_ffn(cfg, x, weights, hs, so, ws)
-            i += 1
-            mark(i)
-        M.moe_combine(cfg, y, ros, wts, so, out, ws)
-        mark(i + 1)
+    stages = [s_ for s_ in M.FORWARD_STAGES if s_ != "shared" or shape.n_shared > 0]
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -234,11 +199,14 @@ def run_ours(args, shape, peaks, peaks_kind):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step()
+        M.moe_forward(cfg, x, weights, out, fstats, ws)
     barrier()
-    n_ev = len(stages) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    # one event before the layer and one after each stage, per step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(M.MOE_FORWARD_EVENTS)]
            for _ in range(args.steps)]
+    for row in evs:
+        for ev in row:
+            ev.record(stream)          # creates the CUDA events before timing
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -251,25 +219,27 @@ def run_ours(args, shape, peaks, peaks_kind):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for s in range(args.steps):
-        step(evs[s])
+    for s_ in range(args.steps):
+        M.moe_forward_timed(cfg, x, weights, out, fstats, ws, evs[s_])
     t_end.record(stream)
     barrier()
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
-    stage_ms = {name: statistics.median(
-        [evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)])
-        for i, name in enumerate(stages)}
-    stage_mean = {name: sum(evs[s][i].elapsed_time(evs[s][i + 1])
-                            for s in range(args.steps)) / args.steps
-                  for i, name in enumerate(stages)}
+    names = list(M.FORWARD_STAGES)
+
+    def stage_times(name):
+        i = names.index(name)
+        return [evs[s_][i].elapsed_time(evs[s_][i + 1]) for s_ in range(args.steps)]
+
+    stage_ms = {name: statistics.median(stage_times(name)) for name in stages}
+    stage_mean = {name: sum(stage_times(name)) / args.steps for name in stages}
     ms_step = total_ms / args.steps
     if ws_n > 1:
         tt = torch.tensor([ms_step], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_step = float(tt.item())
 
-    # the same step through the single moe_forward call
+    # the plain moe_forward call, eager and replayed from a CUDA graph
     barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
@@ -279,6 +249,26 @@ def run_ours(args, shape, peaks, peaks_kind):
     f1.record(stream)
     barrier()
     fwd_ms = f0.elapsed_time(f1) / args.steps
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                M.moe_forward(cfg, x, weights, out, fstats, ws)
+        stream.wait_stream(cap)
+        for _ in range(2):
+            g.replay()
+        barrier()
+        f0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        f1.record(stream)
+        barrier()
+        graph_ms = f0.elapsed_time(f1) / args.steps
+    except Exception as exc:  # report, do not hide, a capture failure
+        graph_ms = f"capture failed: {exc}"
 
     # end to end through moe_forward_host: H2D of x and D2H of out inside
     xh = x.cpu().pin_memory()
@@ -322,9 +312,11 @@ def run_ours(args, shape, peaks, peaks_kind):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     # algorithmic bytes of the HBM-bound stages (per step)
     router_bytes = N * d * es + E * d * es + N * k * 8
-    # idx read twice, row_of_slot and token_of_row written
-    dispatch_bytes = N * k * 4 * 4
-    combine_bytes = m_kept * d * 4 + N * d * es + N * k * 8 + \
+    # idx read twice, row_of_slot and token_of_row written, rows copied
+    dispatch_bytes = N * k * 4 * 4 + N * d * es + m_kept * d * es
+    # expert outputs: fp16 + one fp32 scale per 256 columns (bf16 layers) or fp32
+    y_row_bytes = d * 2 + 4 * ((d + 255) // 256) if shape.dtype == W.DTYPE_BF16 else d * 4
+    combine_bytes = m_kept * y_row_bytes + N * d * es + N * k * 8 + \
         (N * d * 4 if shape.n_shared > 0 else 0)
     stage_report = {}
     for name in stages:
@@ -366,6 +358,9 @@ def run_ours(args, shape, peaks, peaks_kind):
                    "parallelism": f"replicas x{ws_n}",
                    "l2": "working set > 126 MB L2 (no flush needed)",
                    "forward_api_ms_per_step": round(fwd_ms, 4),
+                   "forward_graph_ms_per_step": (round(graph_ms, 4)
+                                                 if isinstance(graph_ms, float) else graph_ms),
+                   "timed_api": "moe_forward_timed (events between stages)",
                    "grouped_gemm_tflops": round(grouped_flop / (grouped_ms * 1e-3) / 1e12, 1),
                    "grouped_gemm_frac_of_sustained": round(
                        grouped_flop / (grouped_ms * 1e-3) / 1e12 / peak_tf, 4),

@@ -167,10 +167,8 @@ MOE_API moe_status_t moe_scratch_size(const moe_config_t *cfg, size_t *bytes);
 
 /* Bytes of workspace moe_forward / moe_forward_host need: the scratch plus
  * every intermediate of the layer sized for the worst case M = N * k
- * (idx, w, offsets, row_of_slot, token_of_row, h, y, and for shared
- * experts their hidden activations and fp32 sum; host staging for x, out).
- * moe_forward does not materialise x_perm: its up projection reads the
- * token rows of x directly (see moe_expert_up_gather). */
+ * (idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, and for shared
+ * experts their hidden activations and fp32 sum; host staging for x, out). */
 MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
 /* ---- stages ----------------------------------------------------------- */
@@ -226,7 +224,9 @@ MOE_API moe_status_t moe_expert_up(const moe_config_t *cfg, const void *x_perm,
  * x [N, d] instead of x_perm[r], so the expert-sorted copy of the tokens is
  * never written.  token_of_row [N*k] and offsets [E+1] as written by
  * moe_dispatch_permute (device, read on the device); h [N*k, F].  The
- * result equals moe_expert_up on the materialised x_perm. */
+ * result equals moe_expert_up on the materialised x_perm bit for bit.  It
+ * saves the N*k*d buffer, not time: the per-row loads (TMA gather4, four
+ * rows per copy) feed the tensor cores more slowly than 128-row boxes. */
 MOE_API moe_status_t moe_expert_up_gather(const moe_config_t *cfg, const void *x,
                                   const int32_t *token_of_row,
                                   const int32_t *offsets,
@@ -275,6 +275,18 @@ MOE_API moe_status_t moe_forward(const moe_config_t *cfg, const void *x,
                          const moe_weights_t *weights, void *out,
                          moe_stats_t *stats, void *ws, size_t ws_bytes,
                          void *stream);
+
+/* moe_forward that also records caller-created CUDA events (cudaEvent_t
+ * handles, passed as void*) on `stream` between its stages, for per-stage
+ * timing of exactly the launches moe_forward makes: events[0] before the
+ * router, then one after each of router+selection, dispatch, expert up,
+ * expert down, shared experts (recorded even without shared experts) and
+ * combine.  n_events must be MOE_FORWARD_EVENTS. */
+#define MOE_FORWARD_EVENTS 7
+MOE_API moe_status_t moe_forward_timed(const moe_config_t *cfg, const void *x,
+                               const moe_weights_t *weights, void *out,
+                               moe_stats_t *stats, void *ws, size_t ws_bytes,
+                               void *stream, void *const *events, int32_t n_events);
 
 /* moe_forward for callers whose activations live in host memory: copies
  * x_host [N, d] into the workspace, runs the layer and copies the result to

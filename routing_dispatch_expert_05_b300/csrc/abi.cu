@@ -21,9 +21,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   // scratch (shared by all stage calls)
-  size_t err, route_psum, route_cnt, chunk_cnt, chunk_base, logits, scratch_end;
+  size_t err, fin_ticket, fin_terms, route_psum, route_cnt, chunk_cnt, chunk_base, logits,
+      scratch_end;
   // intermediates of moe_forward
-  size_t idx, w, offsets, row_of_slot, token_of_row, h, y, h_shared,
+  size_t idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, y_e8, h_shared,
       shared_out, x_stage, out_stage, total;
   int route_parts, chunks;
 };
@@ -42,6 +43,8 @@ Layout layout_of(const moe_config_t& c) {
   L.route_parts = (int)ceil_div64(N, kRouteTokensPerPartial);
   L.chunks = (int)ceil_div64(N, kDispatchTokensPerChunk);
   L.err = take(kAlign);
+  L.fin_ticket = L.err + 64;   // inside the first (zero-filled) block
+  L.fin_terms = take((size_t)E * 8);
   L.route_psum = take((size_t)L.route_parts * E * 4);
   L.route_cnt = take((size_t)L.route_parts * E * 4);
   L.chunk_cnt = take((size_t)L.chunks * E * 4);
@@ -53,9 +56,12 @@ Layout layout_of(const moe_config_t& c) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.row_of_slot = take((size_t)N * k * 4);
   L.token_of_row = take((size_t)N * k * 4);
-  // moe_forward gathers token rows inside the up projection: no x_perm
+  L.x_perm = take((size_t)N * k * d * es);
   L.h = take((size_t)N * k * F * es);
-  L.y = take((size_t)N * k * d * 4);   // expert outputs stay fp32
+  // expert outputs: fp32, or (bf16 layers on the tensor cores) fp16 with an
+  // exponent byte per (row, 32-column block) -- either fits here
+  L.y = take((size_t)N * k * d * 4);
+  L.y_e8 = take((size_t)N * k * ceil_div64(d, kYScaleBlock));
   if (c.n_shared > 0) {
     L.h_shared = take((size_t)N * c.n_shared * c.d_ff_shared * es);
     L.shared_out = take((size_t)N * d * 4);
@@ -186,8 +192,12 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
                  void* ws, cudaStream_t st, bool gemm) {
   const Layout L = layout_of(c);
   float* lg = logits ? logits : at<float>(ws, L.logits);
+  float* psum = at<float>(ws, L.route_psum);
+  int32_t* cnt = at<int32_t>(ws, L.route_cnt);
+  bool selected = false;
   if (gemm && c.dtype == MOE_BF16) {
-    // bf16 router: one dense tcgen05 GEMM, fp32 logits (N = E columns)
+    // bf16 router: one dense tcgen05 GEMM (N = E columns) whose epilogue
+    // selects the experts; logits are stored only if the caller asked
     TcProblem q{};
     q.A = x;
     q.a_rows = c.n_tokens;
@@ -203,10 +213,20 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     q.epilogue = kEpiNone;
     q.bias = w.b_router;
     q.bias_stride = 0;
-    q.C = lg;
+    q.C = logits;
     q.c_is_f32 = 1;
     q.err = err_word(ws);
-    if (tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) gemm = false;
+    q.route.idx = idx;
+    q.route.w = wts;
+    q.route.psum_part = psum;
+    q.route.cnt_part = cnt;
+    q.route.sel_bias = w.sel_bias;
+    q.route.mode = c.route;
+    q.route.top_k = c.top_k;
+    if (c.top_k <= kRouteMaxK && tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) {
+      gemm = false;
+      selected = true;
+    }
   }
   if (gemm) {
     GemmProblem p{};
@@ -226,13 +246,13 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     p.is_bf16 = c.dtype == MOE_BF16;
     launch_simt_gemm(p, st);
   }
-  launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route,
-                           w.sel_bias, idx, wts, at<float>(ws, L.route_psum),
-                           at<int32_t>(ws, L.route_cnt), st);
-  launch_balance_finalize(at<float>(ws, L.route_psum), at<int32_t>(ws, L.route_cnt),
-                          L.route_parts, c.n_experts, c.n_tokens, c.balance_coef,
-                          stats ? stats->counts : nullptr,
-                          stats ? stats->balance : nullptr, st);
+  if (!selected)
+    launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route, w.sel_bias,
+                             idx, wts, psum, cnt, st);
+  launch_balance_finalize(psum, cnt, L.route_parts, c.n_experts, c.n_tokens,
+                          c.balance_coef, stats ? stats->counts : nullptr,
+                          stats ? stats->balance : nullptr, at<double>(ws, L.fin_terms),
+                          at<unsigned>(ws, L.fin_ticket), st);
 }
 
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
@@ -307,8 +327,11 @@ moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_ma
   return run_gemm(c, q, p, st);
 }
 
+// y_e8 != null asks for the compact expert outputs (fp16 + exponents); it
+// returns MOE_ERR_UNSUPPORTED (nothing launched) where only fp32 y is made.
 moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offsets,
-                       const moe_weights_t& w, float* y, int32_t* err, cudaStream_t st) {
+                       const moe_weights_t& w, void* y, uint8_t* y_e8, int32_t* err,
+                       cudaStream_t st) {
   GemmProblem p{};
   p.A = h;
   p.B0 = w.w2;
@@ -344,6 +367,13 @@ moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offs
   q.C = y;
   q.c_is_f32 = 1;
   q.err = err;
+  if (y_e8 != nullptr) {
+    q.c_is_f32 = 0;
+    q.c_e8 = y_e8;
+    q.e8_cols = (int)ceil_div64(c.d_model, kYScaleBlock);
+    if (c.dtype != MOE_BF16 || !tc_gemm_supported(q)) return MOE_ERR_UNSUPPORTED;
+    return launch_tc_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+  }
   return run_gemm(c, q, p, st);
 }
 
@@ -531,7 +561,8 @@ moe_status_t moe_expert_down(const moe_config_t* cfg, const void* h,
   MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
   if (c.n_tokens == 0) return MOE_OK;
   MOE_TRY(need({h, offsets, y}));
-  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), static_cast<cudaStream_t>(stream)));
+  MOE_TRY(down_body(c, h, offsets, *weights, y, nullptr, err_word(ws),
+                    static_cast<cudaStream_t>(stream)));
   return last_cuda();
 }
 
@@ -548,7 +579,7 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm,
   MOE_TRY(need({x_perm, offsets, h, y}));
   auto st = static_cast<cudaStream_t>(stream);
   MOE_TRY(up_body(c, x_perm, nullptr, offsets, *weights, h, err_word(ws), st));
-  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
+  MOE_TRY(down_body(c, h, offsets, *weights, y, nullptr, err_word(ws), st));
   return last_cuda();
 }
 
@@ -583,10 +614,15 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y,
   return last_cuda();
 }
 
-moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
-                         const moe_weights_t* weights, void* out,
-                         moe_stats_t* stats, void* ws, size_t ws_bytes,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+// The whole layer; ev (if not null) receives kForwardEvents events: the
+// start, then one after each stage (router, dispatch, up, down, shared,
+// combine -- "shared" coincides with "down" when there is none).
+moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
+                          const moe_weights_t* weights, void* out, moe_stats_t* stats,
+                          void* ws, size_t ws_bytes, void* stream, cudaEvent_t const* ev) {
   MOE_TRY(check_config(cfg));
   const moe_config_t& c = *cfg;
   MOE_TRY(check_router_weights(c, weights));
@@ -604,6 +640,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* ros = at<int32_t>(ws, L.row_of_slot);
   int32_t* tor = at<int32_t>(ws, L.token_of_row);
+  void* x_perm = at<char>(ws, L.x_perm);
   void* h = at<char>(ws, L.h);
   float* y = at<float>(ws, L.y);
   float* shared_out = c.n_shared > 0 ? at<float>(ws, L.shared_out) : nullptr;
@@ -614,23 +651,69 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
     rs.counts = stats->counts;
     rs.balance = stats->balance;
   }
+  auto mark = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], st);
+  };
+  mark(0);
   router_body(c, x, *weights, nullptr, idx, wts, &rs, ws, st, true);
+  mark(1);
   moe_stats_t ds{};
   if (stats) {
     ds.kept = stats->kept;
     ds.dropped = stats->dropped;
   }
-  // grouping without a copy: the up projection gathers the token rows
-  dispatch_body(c, idx, nullptr, offsets, ros, tor, nullptr, &ds, ws, st);
-  MOE_TRY(up_body(c, x, tor, offsets, *weights, h, err_word(ws), st));
-  MOE_TRY(down_body(c, h, offsets, *weights, y, err_word(ws), st));
+  // the expert-sorted copy of the token rows is written once and read by
+  // the up projection as whole 128-row TMA boxes (a per-row gather inside
+  // the GEMM -- moe_expert_up_gather -- saves that memory, not time)
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, ws, st);
+  mark(2);
+  MOE_TRY(up_body(c, x_perm, nullptr, offsets, *weights, h, err_word(ws), st));
+  mark(3);
+  // bf16 layers keep the expert outputs compact (half the bytes of fp32)
+  uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
+  moe_status_t ds_ = c.dtype == MOE_BF16
+                         ? down_body(c, h, offsets, *weights, y, y_e8, err_word(ws), st)
+                         : MOE_ERR_UNSUPPORTED;
+  const bool compact = ds_ == MOE_OK;
+  if (ds_ == MOE_ERR_UNSUPPORTED)
+    ds_ = down_body(c, h, offsets, *weights, y, nullptr, err_word(ws), st);
+  MOE_TRY(ds_);
+  mark(4);
   if (c.n_shared > 0)
     MOE_TRY(shared_body(c, x, *weights, at<char>(ws, L.h_shared), shared_out,
                         err_word(ws), st));
-  launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
-                 c.dtype == MOE_BF16, num_sms(), st);
+  mark(5);
+  if (compact)
+    launch_combine_compact(y, y_e8, ros, wts, shared_out, out, c.n_tokens, c.top_k,
+                           c.d_model, c.dtype == MOE_BF16, num_sms(), st);
+  else
+    launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
+                   c.dtype == MOE_BF16, num_sms(), st);
+  mark(6);
   return last_cuda();
 }
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x,
+                         const moe_weights_t* weights, void* out,
+                         moe_stats_t* stats, void* ws, size_t ws_bytes,
+                         void* stream) {
+  return forward_impl(cfg, x, weights, out, stats, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status_t moe_forward_timed(const moe_config_t* cfg, const void* x,
+                               const moe_weights_t* weights, void* out,
+                               moe_stats_t* stats, void* ws, size_t ws_bytes,
+                               void* stream, void* const* events, int32_t n_events) {
+  if (events == nullptr || n_events != MOE_FORWARD_EVENTS) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i)
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, weights, out, stats, ws, ws_bytes, stream,
+                      reinterpret_cast<cudaEvent_t const*>(events));
+}
+
 
 moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host,
                               const moe_weights_t* weights, void* out_host,

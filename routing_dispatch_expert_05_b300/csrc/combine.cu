@@ -13,6 +13,8 @@
 // multiply-adds so they are in flight together.
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -105,7 +107,96 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_s
   }
 }
 
+// The same gather-reduce over compact expert outputs: y16 [N*k, d] fp16 and
+// one exponent byte per (row, 32 columns), value = y16 * 2^(e8 - 127).  The
+// power of two folds into the weight (an exact product), so the fp32 sum is
+// sum_j (w_j * 2^(e8_j - 127)) * y16_j in slot order, as for fp32 y.  The
+// k rows of a token (up to 8 at a time) are loaded before their FMAs.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+combine_compact_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
+                       const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
+                       const float* __restrict__ shared, T* __restrict__ out,
+                       int64_t n_tokens, int top_k, int d_model) {
+  constexpr int C = 8;                       // columns per thread step (16 B of fp16)
+  constexpr int KB = 8;                      // slots in flight
+  const int nvec = d_model / C;
+  const int e8_cols = (d_model + kYScaleBlock - 1) / kYScaleBlock;
+  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
+    const int32_t* rows = row_of_slot + t * top_k;
+    const float* wt = w + t * top_k;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const int64_t col = (int64_t)v * C;
+      const int blk = (int)(col / kYScaleBlock);
+      float acc[C];
+#pragma unroll
+      for (int i = 0; i < C; ++i) acc[i] = 0.f;
+      for (int j0 = 0; j0 < top_k; j0 += KB) {
+        uint4 val[KB];
+        float cj[KB];
+#pragma unroll
+        for (int q = 0; q < KB; ++q) {
+          const int j = j0 + q;
+          const int r = j < top_k ? rows[j] : -1;
+          cj[q] = 0.f;
+          val[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (r >= 0) {
+            val[q] = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
+            const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
+            cj[q] = wt[j] * __uint_as_float(e8 << 23);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < KB; ++q) {
+          if (j0 + q >= top_k || cj[q] == 0.f && rows[j0 + q] < 0) continue;
+          const __half2* h2 = reinterpret_cast<const __half2*>(&val[q]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(h2[i]);
+            acc[2 * i] = fmaf(cj[q], f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(cj[q], f.y, acc[2 * i + 1]);
+          }
+        }
+      }
+      if (shared != nullptr) {
+        const float4* sp = reinterpret_cast<const float4*>(shared + t * d_model + col);
+        const float4 s0 = __ldcs(sp), s1 = __ldcs(sp + 1);
+        acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+        acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+      }
+      T* op = out + t * d_model + col;
+      if constexpr (sizeof(T) == 4) {
+        reinterpret_cast<float4*>(op)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        reinterpret_cast<float4*>(op)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        st_vec16(op, o);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+void launch_combine_compact(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
+                            const float* w, const float* shared, void* out, int64_t n_tokens,
+                            int top_k, int d_model, int is_bf16, int num_sms,
+                            cudaStream_t st) {
+  if (n_tokens <= 0) return;
+  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 16);
+  const __half* y = static_cast<const __half*>(y16);
+  if (is_bf16)
+    combine_compact_kernel<bf16><<<blocks, kThreads, 0, st>>>(
+        y, y_e8, row_of_slot, w, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
+  else
+    combine_compact_kernel<float><<<blocks, kThreads, 0, st>>>(
+        y, y_e8, row_of_slot, w, shared, static_cast<float*>(out), n_tokens, top_k,
+        d_model);
+}
 
 void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
                     const float* shared, void* out, int64_t n_tokens, int top_k,

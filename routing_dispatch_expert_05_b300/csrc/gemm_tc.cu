@@ -34,6 +34,8 @@
 
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -59,8 +61,12 @@ constexpr int kTableBytes = (2 * (kMaxExperts + 1) * 4 + 127) / 128 * 128;
 constexpr int kStgF32Stride = 36;                  // floats per staged row
 constexpr int kStgB16Stride = 20;                  // 32-bit words per staged row
 constexpr int kStgWarpBytes = 32 * kStgF32Stride * 4;
+// Routing epilogue: per-warp selection counters (each epilogue warp owns the
+// statistics partial of its 32 tokens, so the warps never wait on each other)
+// and the router / selection biases as fp32.
+constexpr int kRouteSmemBytes = 4 * kMaxExperts * 4 + 2 * kMaxExperts * 4;
 constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kTableBytes +
-                           4 * kStgWarpBytes + 1024 /* alignment */;
+                           4 * kStgWarpBytes + kRouteSmemBytes + 1024 /* alignment */;
 static_assert((kStages * kStageBytes + kBarBytes + kTableBytes) % 16 == 0,
               "epilogue staging must be 16-byte aligned (vector stores)");
 static_assert(kStgWarpBytes % 16 == 0 && (kStgF32Stride * 4) % 16 == 0 &&
@@ -83,9 +89,12 @@ struct Params {
   int64_t bias_stride;
   void* C;                    // [rows, n_out]
   int c_is_f32;
+  uint8_t* c_e8;              // compact fp16 output: per (row, 32 columns) exponent
+  int e8_cols;                // ceil(n_out / 32)
   int32_t* err;
   const int32_t* a_row_map;   // null: A rows are the tile rows; else A row r
                               // is row a_row_map[r] of the A tensor
+  RouteEpilogue route;        // route.idx != null: the routing epilogue
 };
 
 // ---------------------------------------------------------------- PTX
@@ -242,11 +251,311 @@ __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int*
   return r;
 }
 
+// ------------------------------------------------------- epilogue helpers
+// Writes the warp's staged 32 rows x 32 fp32 columns (row r at
+// stg + r * kStgF32Stride) as whole 128-byte row segments: lane = (row
+// quarter, 16-byte piece).
+__device__ __forceinline__ void store_staged_f32(const float* stg, int lane, int row_base,
+                                                 int row_end, int col0, int n_out, float* C) {
+  const int c4 = lane & 7;
+  const bool col_ok = col0 + c4 * 4 < n_out;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3);
+    const int row = row_base + r;
+    if (col_ok && row < row_end) {
+      const float4 val = *reinterpret_cast<const float4*>(stg + r * kStgF32Stride + c4 * 4);
+      *reinterpret_cast<float4*>(C + (int64_t)row * n_out + col0 + c4 * 4) = val;
+    }
+  }
+}
+
+// Writes the warp's staged 32 rows x 32 16-bit columns (row r at
+// stg + r * kStgB16Stride words) as whole 64-byte row segments.
+__device__ __forceinline__ void store_staged_b16(const uint32_t* stg, int lane, int row_base,
+                                                 int row_end, int col0, int n_out, void* C) {
+  const int c8 = lane & 3;
+  const bool col_ok = col0 + c8 * 8 < n_out;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2);
+    const int row = row_base + r;
+    if (col_ok && row < row_end) {
+      const uint4 val = *reinterpret_cast<const uint4*>(stg + r * kStgB16Stride + c8 * 4);
+      st_vec16(static_cast<uint16_t*>(C) + (int64_t)row * n_out + col0 + c8 * 8, val);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Compact output of one tile, one pass over the accumulator: for each 32
+// columns of a row, the largest |v| picks a power of two 2^s that brings it
+// into [2^14, 2^15); v * 2^s (exact) is rounded once to fp16, and the biased
+// exponent of 2^-s (one byte, an E8 shared exponent) is stored beside it.
+__device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, int lane,
+                                             int row_base, uint32_t tb, uint32_t* stg) {
+  const int row = row_base + lane;
+  const bf16* bp = p.bias ? p.bias + (int64_t)tl.g * p.bias_stride : nullptr;
+  uint32_t e8lo = 0u, e8hi = 0u;                   // this row's 8 exponents of the tile
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    const int c0 = tl.n * BN + ch * 32;
+    if (c0 >= p.n_out) break;                      // warp-uniform
+    uint32_t r[32];
+    MOE_TMEM_LD32(tb + ch * 32, r);
+    tmem_ld_wait();
+    float v[32];
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = __uint_as_float(r[j]);
+      if (bp != nullptr && c0 + j < p.n_out) v[j] += __bfloat162float(bp[c0 + j]);
+      mx = fmaxf(mx, fabsf(v[j]));                 // columns past n_out hold 0
+    }
+    int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+    e = min(max(e, -100), 127);                    // zero / tiny blocks: bounded scale
+    const float scale = __uint_as_float((uint32_t)(127 + 14 - e) << 23);   // 2^(14-e)
+    const uint32_t e8 = (uint32_t)(e + 113) << (8 * (ch & 3));             // 2^(e-14)
+    if (ch < 4) e8lo |= e8; else e8hi |= e8;
+    uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgB16Stride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = make_uint4(pack_half2(v[8 * j] * scale, v[8 * j + 1] * scale),
+                          pack_half2(v[8 * j + 2] * scale, v[8 * j + 3] * scale),
+                          pack_half2(v[8 * j + 4] * scale, v[8 * j + 5] * scale),
+                          pack_half2(v[8 * j + 6] * scale, v[8 * j + 7] * scale));
+    __syncwarp();
+    store_staged_b16(stg, lane, row_base, tl.row_end, c0, p.n_out, p.C);
+    __syncwarp();
+  }
+  if (row < tl.row_end) {
+    uint8_t* ep = p.c_e8 + (int64_t)row * p.e8_cols + tl.n * (BN / 32);
+    const int n8 = min(BN / 32, p.e8_cols - tl.n * (BN / 32));
+    if (n8 == 8 && (reinterpret_cast<uintptr_t>(ep) & 7u) == 0) {
+      *reinterpret_cast<uint2*>(ep) = make_uint2(e8lo, e8hi);
+    } else {
+      for (int i = 0; i < n8; ++i) ep[i] = (uint8_t)((i < 4 ? e8lo : e8hi) >> (8 * (i & 3)));
+    }
+  }
+}
+
+// Sum of 32 per-lane vectors, transposed: on return v[0] of lane l is the
+// sum over the 32 lanes of their v[l].  A fixed butterfly (31 shuffles), so
+// the summation order -- and the result -- is the same on every run.
+__device__ __forceinline__ void warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+}
+
+// Insert (key, e, aux) into a list sorted by key descending in which equal
+// keys keep arrival order.  Experts arrive in ascending index order, so ties
+// go to the lower expert index.  Slots >= k are never filled (idx -1 = empty).
+template <int KM>
+__device__ __forceinline__ void topk_insert(float (&tk)[KM], int (&ti)[KM], float (&ta)[KM],
+                                            int k, float key, int e, float aux) {
+  bool shifting = false;   // once placed, every later entry moves down one slot
+#pragma unroll
+  for (int i = 0; i < KM; ++i) {
+    if (i < k && (shifting || ti[i] < 0 || key > tk[i])) {
+      const float kk = tk[i], aa = ta[i];
+      const int ii = ti[i];
+      tk[i] = key; ti[i] = e; ta[i] = aux;
+      key = kk; e = ii; aux = aa;
+      shifting = true;
+      if (e < 0) break;    // filled an empty slot: nothing left to move
+    }
+  }
+}
+
+// sigmoid in double, rounded once to fp32: the selection key's definition
+__device__ __forceinline__ float sigmoid_exact(float l) {
+  return (float)(1.0 / (1.0 + exp(-(double)l)));
+}
+// fp32 sigmoid: expf (<= 2 ulp), one add and a correctly rounded divide; its
+// distance to sigmoid_exact stays far below kSigmoidSlack
+__device__ __forceinline__ float sigmoid_fast(float l) {
+  return 1.0f / (1.0f + expf(-l));
+}
+constexpr float kSigmoidSlack = 1.0f / 65536.0f;   // bound used for candidates
+
+// The routing epilogue of the router GEMM: the accumulator holds the fp32
+// logits of 128 tokens x E experts (E <= 256, one n-tile).  Lane = token.
+//   pass 1: logits (+ router bias), optional logits store, selection keys,
+//           running top-k, softmax max / normaliser (online) or sum of s;
+//   pass 2 (sigmoid mode): exact keys for the candidates (see below);
+//   pass 3: routing probabilities p[t, e] -> per-expert sums over the
+//           warp's 32 tokens (one statistics partial per warp).
+// The sigmoid key is sigmoid(l) + b with sigmoid evaluated in double and
+// rounded to fp32.  Double is slow here, so pass 1 ranks fp32 keys ka whose
+// distance to the exact keys is below delta = kSigmoidSlack; every expert of
+// the exact top k then has ka >= (k-th largest ka) - 2 delta, and only those
+// candidates get exact keys -- the selection equals the all-double one.
+__device__ __forceinline__ void route_tile(const Params& p, const Tile& tl, int q, int lane,
+                                           uint32_t tb, float* stg, int* cnt,
+                                           const float* s_rb, const float* s_sb) {
+  constexpr int KM = kRouteMaxK;
+  const RouteEpilogue& R = p.route;
+  const int E = p.n_out, k = R.top_k, mode = R.mode;
+  const int nch = (E + 31) / 32;
+  const int row_base = tl.row0 + q * 32;
+  const int row = row_base + lane;
+  const bool valid = row < tl.row_end;
+  const bool warp_has_rows = row_base < tl.row_end;
+  const int part = row_base / kRouteTokensPerPartial;   // this warp's statistics partial
+
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+
+  float tk[KM], ta[KM];
+  int ti[KM];
+#pragma unroll
+  for (int i = 0; i < KM; ++i) tk[i] = -INFINITY, ta[i] = 0.f, ti[i] = -1;
+  float m = -INFINITY, z = 0.f;                     // softmax max and sum exp(l - m)
+  float ssum = 0.f;                                 // sigmoid: sum of s (fp32 s)
+
+  // ---- pass 1
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const int col0 = ch * 32;
+    uint32_t r[32];
+    MOE_TMEM_LD32(tb + col0, r);
+    tmem_ld_wait();
+    float l[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = col0 + j;
+      l[j] = __uint_as_float(r[j]) + s_rb[e];
+    }
+    if (p.C != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(stg + lane * kStgF32Stride);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(l[4 * j], l[4 * j + 1], l[4 * j + 2], l[4 * j + 3]);
+      __syncwarp();
+      store_staged_f32(stg, lane, row_base, tl.row_end, col0, E, static_cast<float*>(p.C));
+      __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = col0 + j;
+      if (e >= E) break;
+      if (mode == 2) {
+        const float sa = sigmoid_fast(l[j]);
+        ssum += sa;
+        topk_insert<KM>(tk, ti, ta, k, __fadd_rn(sa, s_sb[e]), e, 0.f);
+      } else {
+        if (l[j] > m) {
+          z = z * expf(m - l[j]) + 1.f;
+          m = l[j];
+        } else {
+          z += expf(l[j] - m);
+        }
+        topk_insert<KM>(tk, ti, ta, k, l[j], e, 0.f);
+      }
+    }
+  }
+
+  // ---- pass 2 (sigmoid): exact keys of the candidates
+  if (mode == 2) {
+    float kth = tk[0];                              // the k-th fp32 key (unrolled pick)
+#pragma unroll
+    for (int i = 1; i < KM; ++i)
+      if (i == k - 1) kth = tk[i];
+    const float thr = kth - 4.f * kSigmoidSlack;
+#pragma unroll
+    for (int i = 0; i < KM; ++i) tk[i] = -INFINITY, ta[i] = 0.f, ti[i] = -1;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+      const int col0 = ch * 32;
+      uint32_t r[32];
+      MOE_TMEM_LD32(tb + col0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = col0 + j;
+        if (e >= E) break;
+        const float l = __uint_as_float(r[j]) + s_rb[e];
+        const float b = s_sb[e];
+        if (__fadd_rn(sigmoid_fast(l), b) >= thr) {
+          const float s = sigmoid_exact(l);
+          topk_insert<KM>(tk, ti, ta, k, __fadd_rn(s, b), e, s);
+        }
+      }
+    }
+  }
+
+  // ---- selection outputs: idx, weights, counts
+  if (valid) {
+    float wsum = 0.f, wv[KM];
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+      wv[i] = 0.f;
+      if (i < k) {
+        wv[i] = mode == 2 ? ta[i] : expf(tk[i] - tk[0]);
+        wsum += wv[i];
+      }
+    }
+    const int64_t o = (int64_t)row * k;
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+      if (i < k) {
+        R.idx[o + i] = ti[i];
+        R.w[o + i] = wv[i] / wsum;
+        atomicAdd(&cnt[ti[i]], 1);
+      }
+    }
+  }
+
+  // ---- pass 3: probabilities, summed per expert over this warp's tokens
+  const float inv = mode == 2 ? 1.f / ssum : 1.f / z;
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const int col0 = ch * 32;
+    uint32_t r[32];
+    MOE_TMEM_LD32(tb + col0, r);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = col0 + j;
+      float pv = 0.f;
+      if (valid && e < E) {
+        const float l = __uint_as_float(r[j]) + s_rb[e];
+        pv = (mode == 2 ? sigmoid_fast(l) : expf(l - m)) * inv;
+      }
+      v[j] = pv;
+    }
+    warp_transpose_sum32(v, lane);
+    if (warp_has_rows && col0 + lane < E)
+      R.psum_part[(int64_t)part * E + col0 + lane] = v[0];
+  }
+  __syncwarp();
+  if (warp_has_rows)
+    for (int e = lane; e < E; e += 32) R.cnt_part[(int64_t)part * E + e] = cnt[e];
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------- kernel
+// Epilogue kinds, one kernel instantiation each.
+enum : int { kEkStore = 0, kEkCompact = 1, kEkRoute = 2 };
+
+template <int EK>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB0,
-               const __grid_constant__ CUtensorMap tmB1, const Params p) {
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,6 +571,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   int* s_tile_start = reinterpret_cast<int*>(smem + kStages * kStageBytes + kBarBytes);
   int* s_off = s_tile_start + kMaxExperts + 1;
   uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
+  int* s_rcnt = reinterpret_cast<int*>(s_stage + 4 * kStgWarpBytes);  // [4][kMaxExperts]
+  float* s_rb = reinterpret_cast<float*>(s_rcnt + 4 * kMaxExperts);   // router bias [256]
+  float* s_sb = s_rb + kMaxExperts;                                    // selection bias
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.offsets ? p.n_groups : 1;
@@ -287,6 +599,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (p.swiglu) prefetch_map(&tmB1);
   }
   if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
+  if (EK == kEkRoute && warp == 3) {
+    for (int e = lane; e < kMaxExperts; e += 32) {
+      const bool in = e < p.n_out;
+      s_rb[e] = in && p.bias != nullptr ? __bfloat162float(p.bias[e]) : 0.f;
+      s_sb[e] = in && p.route.mode == 2 ? p.route.sel_bias[e] : 0.f;
+    }
+  }
   if (warp == 2) {
     int carry = 0;
     for (int base = 0; base < G; base += 32) {
@@ -328,57 +647,59 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int m_total = s_off[G];
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t last_phase[kStages];
-    bool used[kStages];
-    for (int s = 0; s < kStages; ++s) used[s] = false, last_phase[s] = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
-      int src[4] = {0, 0, 0, 0};
-      if (gather) {
+    uint32_t used = 0, last_phases = 0;             // per-stage bits
+    if (gather || lane == 0) {
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const Tile tl = tile_of(t, s_tile_start, s_off, G, nt);
+        int src[4] = {0, 0, 0, 0};
+        if (gather) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // rows past the last kept row read token 0; they are never stored
-          const int row = tl.row0 + lane * 4 + i;
-          src[i] = row < m_total ? __ldg(p.a_row_map + row) : 0;
-        }
-      }
-      bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        int good = 1;
-        if (lane == 0) good = wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err);
-        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
-        uint8_t* a = sA + stage * kTileA;
-        if (lane == 0) {
-          mbar_expect_tx(&full[stage], kStageBytes);
-          uint8_t* b = sB + stage * kTileB;
-          if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
-          if (p.swiglu) {
-            const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
-            tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
-            tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
-          } else {
-            const int sub = kb / kb_per_sub;
-            const int kk = (kb - sub * kb_per_sub) * BK;
-            const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN;
-            tma_load_2d(b, &tmB0, &full[stage], kk, brow);
+          for (int i = 0; i < 4; ++i) {
+            // rows past the last kept row read token 0; they are never stored
+            const int row = tl.row0 + lane * 4 + i;
+            src[i] = row < m_total ? __ldg(p.a_row_map + row) : 0;
           }
-          used[stage] = true;
-          last_phase[stage] = phase;
         }
-        __syncwarp();
-        if (gather)
-          tma_gather4(a + lane * 4 * (BK * 2), &tmA, &full[stage], kb * BK, src[0], src[1],
-                      src[2], src[3]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          int good = 1;
+          if (lane == 0) good = wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err);
+          if (gather) good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) { ok = false; break; }
+          uint8_t* a = sA + stage * kTileA;
+          if (lane == 0) {
+            mbar_expect_tx(&full[stage], kStageBytes);
+            uint8_t* b = sB + stage * kTileB;
+            if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
+            if (p.swiglu) {
+              const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
+              tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
+              tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
+            } else {
+              const int sub = kb / kb_per_sub;
+              const int kk = (kb - sub * kb_per_sub) * BK;
+              const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN;
+              tma_load_2d(b, &tmB0, &full[stage], kk, brow);
+            }
+            used |= 1u << stage;
+            last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
+          }
+          if (gather) {
+            __syncwarp();
+            tma_gather4(a + lane * 4 * (BK * 2), &tmA, &full[stage], kb * BK, src[0], src[1],
+                        src[2], src[3]);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
-      if (!ok) break;
     }
     // every issued copy has landed before the CTA can exit
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
-        if (!used[s]) continue;
+        if (!(used >> s & 1u)) continue;
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&full[s], last_phase[s])) {
+        while (!mbar_try_wait(&full[s], last_phases >> s & 1u)) {
           if (globaltimer() - t0 > kTimeoutNs) {
             set_device_error(p.err, kDevTimeout);
             break;
@@ -440,6 +761,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tc_fence_after();
       const int row_base = tl.row0 + q * 32;         // this warp's 32 rows
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if constexpr (EK == kEkRoute) {
+        route_tile(p, tl, q, lane, tb, stg_f, s_rcnt + (warp - 2) * kMaxExperts, s_rb, s_sb);
+      } else if constexpr (EK == kEkCompact) {
+        compact_tile(p, tl, lane, row_base, tb, stg_w);
+      } else {
 #pragma unroll 1
       for (int ch = 0; ch < cols_tile / 32; ++ch) {
         const int col0 = tl.n * cols_tile + ch * 32;
@@ -488,19 +814,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
         // lane = 16-byte column piece: whole row segments per store
         if (p.c_is_f32) {
-          const int c4 = lane & 7;
-          const bool col_ok = col0 + c4 * 4 < p.n_out;
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int r = it * 4 + (lane >> 3);
-            const int row = row_base + r;
-            if (col_ok && row < tl.row_end) {
-              const float4 val =
-                  *reinterpret_cast<const float4*>(stg_f + r * kStgF32Stride + c4 * 4);
-              *reinterpret_cast<float4*>(static_cast<float*>(p.C) + (int64_t)row * p.n_out +
-                                         col0 + c4 * 4) = val;
-            }
-          }
+          store_staged_f32(stg_f, lane, row_base, tl.row_end, col0, p.n_out,
+                           static_cast<float*>(p.C));
         } else {
           const int c8 = lane & 3;
           const bool col_ok = col0 + c8 * 8 < p.n_out;
@@ -517,6 +832,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
         __syncwarp();
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -569,6 +885,13 @@ bool tc_gemm_supported(const TcProblem& q) {
   if (q.K < 1 || q.n_out < 8 || q.n_out % 8 != 0) return false;
   if (q.k_sub % tc::BK != 0 && q.n_sub > 1) return false;
   if (q.n_groups > kMaxExperts) return false;
+  // the routing epilogue: one group, all E columns in one accumulator tile
+  // compact output: one exponent per 32 columns, no SwiGLU pairing
+  if (q.c_e8 != nullptr && (q.swiglu || q.e8_cols != (q.n_out + 31) / 32)) return false;
+  if (q.route.idx != nullptr &&
+      (q.n_out > tc::BN || q.offsets != nullptr || q.swiglu || q.n_sub != 1 ||
+       q.route.top_k < 1 || q.route.top_k > kRouteMaxK || q.route.top_k > q.n_out))
+    return false;
   return tc::encode_fn() != nullptr;
 }
 
@@ -606,12 +929,18 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.bias_stride = q.bias_stride;
   p.C = q.C;
   p.c_is_f32 = q.c_is_f32;
+  p.c_e8 = q.c_e8;
+  p.e8_cols = q.e8_cols;
   p.err = q.err;
   p.a_row_map = q.a_row_map;
-  if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
+  p.route = q.route;
+  auto kern = q.route.idx != nullptr ? tc_gemm_kernel<kEkRoute>
+             : q.c_e8 != nullptr       ? tc_gemm_kernel<kEkCompact>
+                                       : tc_gemm_kernel<kEkStore>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
     return false;
-  tc_gemm_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb0, mb1, p);
+  kern<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb0, mb1, p);
   return cudaGetLastError() == cudaSuccess;
 }
 

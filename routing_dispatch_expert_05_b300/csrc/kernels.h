@@ -8,8 +8,9 @@
 
 namespace moe {
 
-// Tokens whose selection statistics one router partial covers.
-constexpr int kRouteTokensPerPartial = 128;
+// Tokens whose selection statistics one router partial covers (one warp of
+// the routing epilogue, or of the selection kernel).
+constexpr int kRouteTokensPerPartial = 32;
 // Tokens per dispatch chunk (the unit of the per-chunk histogram).
 constexpr int kDispatchTokensPerChunk = 256;
 constexpr int kMaxExperts = 256;
@@ -22,11 +23,12 @@ void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_exper
                               int32_t* idx, float* w, float* psum_part,
                               int32_t* cnt_part, cudaStream_t st);
 // sums the partials in a fixed order: counts[E] (optional) and the balance
-// statistic (optional).
+// statistic (optional).  terms: [E] doubles of scratch; ticket: one counter
+// that is zero on entry (and is left zero).
 void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
                              int n_parts, int n_experts, int64_t n_tokens,
                              float coef, int32_t* counts, float* balance,
-                             cudaStream_t st);
+                             double* terms, unsigned* ticket, cudaStream_t st);
 
 // ---- dispatch -------------------------------------------------------------
 void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
@@ -74,6 +76,20 @@ struct GemmProblem {
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st);
 
 // ---- tcgen05 grouped GEMM (bf16 storage, fp32 accumulation in TMEM) -------
+// Routing epilogue of the router GEMM (one group, n_out = E <= 256): instead
+// of (or as well as, if C != null) storing the logits, the epilogue selects
+// each token's k experts, writes idx / w and one statistics partial per 32
+// tokens (same layout and meaning as launch_route_from_logits).
+constexpr int kRouteMaxK = 8;
+struct RouteEpilogue {
+  int32_t* idx;              // [N, k]; null: no routing epilogue
+  float* w;                  // [N, k]
+  float* psum_part;          // [ceil(N/32), E]
+  int32_t* cnt_part;         // [ceil(N/32), E]
+  const float* sel_bias;     // [E] (mode 2)
+  int mode;                  // MOE_ROUTE_*
+  int top_k;                 // 1..kRouteMaxK
+};
 struct TcProblem {
   const void* A;             // [a_rows, K] bf16 row-major
   int64_t a_rows;
@@ -92,13 +108,20 @@ struct TcProblem {
   int epilogue;              // Epilogue
   const void* bias;          // [n_groups][n_out] bf16 or null
   int64_t bias_stride;
-  void* C;                   // [rows, n_out] bf16 (or fp32 if c_is_f32)
+  void* C;                   // [rows, n_out] bf16 (or fp32 if c_is_f32, fp16 if c_scale)
   int c_is_f32;
+  // Compact output (non-SwiGLU only): C holds fp16 values v * 2^s with one
+  // power of two per (row, 32-column block), chosen so that the block's
+  // largest magnitude lands in [2^14, 2^15); c_e8[row * e8_cols + block] is
+  // the biased fp32 exponent of 2^-s (value = fp16 * 2^(c_e8 - 127)).
+  uint8_t* c_e8;
+  int e8_cols;               // ceil(n_out / 32)
   int32_t* err;              // device error word
   // Optional row map (fused dispatch gather): A row r of the grouped problem
   // is row a_row_map[r] of A ([a_rows, K], e.g. the token rows x), for
   // r < offsets[n_groups].  null: A is already in grouped row order.
   const int32_t* a_row_map;
+  RouteEpilogue route;
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
@@ -108,5 +131,12 @@ bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
 void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
                     const float* shared, void* out, int64_t n_tokens, int top_k,
                     int d_model, int is_bf16, int num_sms, cudaStream_t st);
+// the same with compact expert outputs: y16 [N*k, d] fp16 and
+// y_e8 [N*k, ceil(d/32)] (value = y16 * 2^(y_e8 - 127) for its 32 columns)
+void launch_combine_compact(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
+                            const float* w, const float* shared, void* out, int64_t n_tokens,
+                            int top_k, int d_model, int is_bf16, int num_sms,
+                            cudaStream_t st);
+constexpr int kYScaleBlock = 32;    // columns per compact-output exponent
 
 }  // namespace moe

@@ -35,9 +35,43 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// sigmoid evaluated in double, rounded once to fp32
+// sigmoid evaluated in double, rounded once to fp32 (the selection key's
+// definition)
 __device__ __forceinline__ float sigmoid_f32_via_f64(float l) {
   return (float)(1.0 / (1.0 + exp(-(double)l)));
+}
+// fp32 sigmoid: expf (<= 2 ulp), an add and a correctly rounded divide; its
+// distance to sigmoid_f32_via_f64 is far below kSlack
+__device__ __forceinline__ float sigmoid_fast(float l) { return 1.0f / (1.0f + expf(-l)); }
+constexpr float kSlack = 1.0f / 65536.0f;
+
+// One selection round: the lane holding the best remaining candidate (key
+// desc, index asc) among all lanes; returns its expert index (INT_MAX if
+// none is left).
+template <int EPL>
+__device__ __forceinline__ int warp_best(const float (&key)[EPL], const int (&slot)[EPL],
+                                         int lane, int E, float* best_key) {
+  float bk = -INFINITY;
+  int bi = INT_MAX;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && slot[i] < 0 && (bi == INT_MAX || key[i] > bk)) {
+      bk = key[i];
+      bi = e;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ok = __shfl_xor_sync(kFull, bk, off);
+    const int oi = __shfl_xor_sync(kFull, bi, off);
+    if (oi != INT_MAX && (bi == INT_MAX || ok > bk || (ok == bk && oi < bi))) {
+      bk = ok;
+      bi = oi;
+    }
+  }
+  *best_key = __shfl_sync(kFull, bk, 0);
+  return __shfl_sync(kFull, bi, 0);
 }
 
 template <int EPL>
@@ -74,19 +108,36 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
       slot[i] = -1;
     }
     if (mode == 2) {
-      float s[EPL];
+      // Rank fp32 keys first (within kSlack of the exact ones); the exact top
+      // k lies among the experts whose fp32 key is within 2 kSlack of the
+      // k-th fp32 key, so only those get the double-precision sigmoid.
+      float sa[EPL];
       float part = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const bool v = lane + 32 * i < E;
-        s[i] = v ? sigmoid_f32_via_f64(l[i]) : 0.f;
-        key[i] = __fadd_rn(s[i], bias[i]);
-        num[i] = s[i];
-        part += s[i];
+        sa[i] = v ? sigmoid_fast(l[i]) : 0.f;
+        key[i] = __fadd_rn(sa[i], bias[i]);
+        part += sa[i];
       }
       const float ssum = warp_sum_bcast(part);
+      float kth = -INFINITY;
+      for (int j = 0; j < top_k; ++j) {
+        const int bi = warp_best<EPL>(key, slot, lane, E, &kth);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) p[i] = s[i] / ssum;
+        for (int i = 0; i < EPL; ++i)
+          if (lane + 32 * i == bi) slot[i] = j;
+      }
+      const float thr = kth - 4.f * kSlack;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const bool cand = lane + 32 * i < E && key[i] >= thr;
+        const float s = cand ? sigmoid_f32_via_f64(l[i]) : 0.f;
+        num[i] = s;
+        key[i] = cand ? __fadd_rn(s, bias[i]) : -INFINITY;
+        slot[i] = cand ? -1 : 0x7fff;      // non-candidates never selected
+        p[i] = sa[i] / ssum;
+      }
     } else {
       float m = -INFINITY;
 #pragma unroll
@@ -111,27 +162,8 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
     for (int i = 0; i < EPL; ++i) ps[i] += (lane + 32 * i < E) ? p[i] : 0.f;
 
     for (int j = 0; j < top_k; ++j) {
-      float bk = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && slot[i] < 0 && (bi == INT_MAX || key[i] > bk)) {
-          bk = key[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ok = __shfl_xor_sync(kFull, bk, off);
-        const int oi = __shfl_xor_sync(kFull, bi, off);
-        if (oi != INT_MAX &&
-            (bi == INT_MAX || ok > bk || (ok == bk && oi < bi))) {
-          bk = ok;
-          bi = oi;
-        }
-      }
-      bi = __shfl_sync(kFull, bi, 0);
+      float bk;
+      const int bi = warp_best<EPL>(key, slot, lane, E, &bk);
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
         if (lane + 32 * i == bi) slot[i] = j;
@@ -139,11 +171,11 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
 
     float part = 0.f;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) part += slot[i] >= 0 ? num[i] : 0.f;
+    for (int i = 0; i < EPL; ++i) part += (slot[i] >= 0 && slot[i] < top_k) ? num[i] : 0.f;
     const float zsel = warp_sum_bcast(part);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      if (slot[i] >= 0) {
+      if (slot[i] >= 0 && slot[i] < top_k) {
         const int e = lane + 32 * i;
         idx[t * top_k + slot[i]] = e;
         w[t * top_k + slot[i]] = num[i] / zsel;
@@ -164,30 +196,51 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
   }
 }
 
-__global__ void balance_finalize_kernel(const float* __restrict__ psum_part,
-                                        const int32_t* __restrict__ cnt_part,
-                                        int n_parts, int n_experts,
-                                        int64_t n_tokens, float coef,
-                                        int32_t* __restrict__ counts,
-                                        float* __restrict__ balance) {
-  __shared__ double s_term[kMaxExperts];
-  const int e = threadIdx.x;
-  if (e < n_experts) {
-    double ps = 0.0;
-    long long cnt = 0;
-    for (int q = 0; q < n_parts; ++q) {
-      ps += (double)psum_part[(int64_t)q * n_experts + e];
-      cnt += cnt_part[(int64_t)q * n_experts + e];
+// Per-expert totals of the partials (block e, fixed-order tree), then the
+// last block to finish sums the per-expert terms in expert order: the
+// statistic is the same on every run.  `ticket` (zero when the workspace
+// was allocated) is reset by that last block.
+constexpr int kFinThreads = 256;
+__global__ void __launch_bounds__(kFinThreads)
+balance_finalize_kernel(const float* __restrict__ psum_part,
+                        const int32_t* __restrict__ cnt_part, int n_parts,
+                        int n_experts, int64_t n_tokens, float coef,
+                        int32_t* __restrict__ counts, float* __restrict__ balance,
+                        double* __restrict__ terms, unsigned* __restrict__ ticket) {
+  __shared__ double s_ps[kFinThreads];
+  __shared__ long long s_cnt[kFinThreads];
+  __shared__ bool s_last;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  double ps = 0.0;
+  long long cnt = 0;
+  for (int q = tid; q < n_parts; q += kFinThreads) {
+    ps += (double)psum_part[(int64_t)q * n_experts + e];
+    cnt += cnt_part[(int64_t)q * n_experts + e];
+  }
+  s_ps[tid] = ps;
+  s_cnt[tid] = cnt;
+  __syncthreads();
+  for (int h = kFinThreads / 2; h > 0; h >>= 1) {
+    if (tid < h) {
+      s_ps[tid] += s_ps[tid + h];
+      s_cnt[tid] += s_cnt[tid + h];
     }
-    if (counts) counts[e] = (int32_t)cnt;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if (counts) counts[e] = (int32_t)s_cnt[0];
     const double n = n_tokens > 0 ? (double)n_tokens : 1.0;
-    s_term[e] = ((double)cnt / n) * (ps / n);
+    terms[e] = ((double)s_cnt[0] / n) * (s_ps[0] / n);
+    __threadfence();
+    s_last = atomicAdd(ticket, 1u) == (unsigned)(n_experts - 1);
   }
   __syncthreads();
-  if (e == 0 && balance) {
+  if (s_last && tid == 0) {
+    __threadfence();
     double acc = 0.0;
-    for (int q = 0; q < n_experts; ++q) acc += s_term[q];
-    balance[0] = n_tokens > 0 ? (float)((double)coef * acc) : 0.f;
+    for (int q = 0; q < n_experts; ++q) acc += ((volatile double*)terms)[q];
+    if (balance) balance[0] = n_tokens > 0 ? (float)((double)coef * acc) : 0.f;
+    *ticket = 0u;
   }
 }
 
@@ -217,10 +270,11 @@ void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_exper
 void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
                              int n_parts, int n_experts, int64_t n_tokens,
                              float coef, int32_t* counts, float* balance,
-                             cudaStream_t st) {
+                             double* terms, unsigned* ticket, cudaStream_t st) {
   if (!counts && !balance) return;
-  balance_finalize_kernel<<<1, kMaxExperts, 0, st>>>(
-      psum_part, cnt_part, n_parts, n_experts, n_tokens, coef, counts, balance);
+  balance_finalize_kernel<<<n_experts, kFinThreads, 0, st>>>(
+      psum_part, cnt_part, n_parts, n_experts, n_tokens, coef, counts, balance, terms,
+      ticket);
 }
 
 }  // namespace moe

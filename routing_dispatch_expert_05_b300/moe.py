@@ -30,7 +30,8 @@ MOE_EXPERT_SILU_MLP, MOE_EXPERT_SWIGLU = 0, 1
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_route_logits", "moe_dispatch_permute", "moe_expert_up",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
-            "moe_forward", "moe_forward_host", "moe_read_device_error",
+            "moe_forward", "moe_forward_timed", "moe_forward_host",
+            "moe_read_device_error",
             "moe_status_string", "moe_version")
 
 
@@ -90,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine": [cfgp, vp, vp, vp, vp, vp, vp, sz, vp],
         "moe_forward": [cfgp, vp, wp, vp, sp, vp, sz, vp],
         "moe_forward_host": [cfgp, vp, wp, vp, sp, vp, sz, vp],
+        "moe_forward_timed": [cfgp, vp, wp, vp, sp, vp, sz, vp, P(vp), ctypes.c_int32],
         "moe_read_device_error": [vp, P(ctypes.c_int32), vp],
     }
     for name, args in sig.items():
@@ -249,6 +251,29 @@ def moe_forward(cfg, x, weights: MoEWeights, out, stats, ws, stream=None):
         ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(out),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_forward")
+
+
+FORWARD_STAGES = ("router", "dispatch", "expert_up", "expert_down", "shared", "combine")
+MOE_FORWARD_EVENTS = len(FORWARD_STAGES) + 1
+
+
+def moe_forward_timed(cfg, x, weights: MoEWeights, out, stats, ws, events, stream=None):
+    """moe_forward recording ``events`` (MOE_FORWARD_EVENTS torch.cuda.Event
+    objects with timing enabled): before the layer and after each stage in
+    FORWARD_STAGES."""
+    if len(events) != MOE_FORWARD_EVENTS:
+        raise ValueError(f"need {MOE_FORWARD_EVENTS} events")
+    handles = []
+    for ev in events:
+        if not ev.cuda_event:            # torch creates the CUDA event lazily
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    wp, wb = _ws(ws)
+    _check(load_library().moe_forward_timed(
+        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(out),
+        ctypes.byref(stats) if stats is not None else None, wp, wb, _stream(stream),
+        arr, len(handles)), "moe_forward_timed")
 
 
 def moe_forward_host(cfg, x_host, weights: MoEWeights, out_host, stats, ws,

@@ -56,9 +56,9 @@ def test_workspace_sizes_cover_the_intermediates(lib, name):
     total = M.workspace_size(cfg)
     es = 2 if shape.dtype == W.DTYPE_BF16 else 4
     nk = shape.n_tokens * shape.top_k
-    # the forward keeps h [N*k, F] in the layer dtype and y [N*k, d] in fp32
-    # (token rows are gathered inside the up projection: no x_perm)
-    floor = nk * shape.d_ff * es + nk * shape.d_model * 4
+    # the forward keeps x_perm [N*k, d] and h [N*k, F] in the layer dtype and
+    # the expert outputs y [N*k, d] in at least 16 bits
+    floor = nk * (shape.d_model + shape.d_ff) * es + nk * shape.d_model * 2
     assert scratch >= shape.n_tokens * shape.n_experts * 4
     assert total >= scratch + floor
 
@@ -127,3 +127,15 @@ def test_stage_calls_reject_bad_pointers_before_the_device(lib):
     st = lib.moe_forward(ctypes.byref(cfg3), addr, ctypes.byref(w), addr, None,
                          addr, 1 << 40, None)
     assert st == -1
+
+
+def test_forward_timed_rejects_a_wrong_event_count(lib):
+    cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
+    w = M.MoEWeights()
+    evs = (ctypes.c_void_p * 3)(1, 2, 3)
+    st = lib.moe_forward_timed(ctypes.byref(cfg), None, ctypes.byref(w), None, None,
+                               None, 0, None, evs, 3)
+    assert st == M.MOE_ERR_INVALID_ARG
+    st = lib.moe_forward_timed(ctypes.byref(cfg), None, ctypes.byref(w), None, None,
+                               None, 0, None, None, M.MOE_FORWARD_EVENTS)
+    assert st == M.MOE_ERR_INVALID_ARG

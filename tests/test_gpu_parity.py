@@ -318,12 +318,58 @@ def test_router_topk_parity(name, N):
     assert np.array_equal(ig[~amb], i_o[~amb])
     check_selection_valid(ig[amb], keys[amb], k, margin)
     assert np.allclose(to_np(w)[~amb], w_o[~amb], rtol=1e-3, atol=1e-5)
+    # selection runs on exactly the logits the router wrote: on those, every
+    # token's experts and slot order equal the oracle's, ties included
+    i_g, w_g, _ = O.route(lg, shape.route, k, v.get("sel_bias"))
+    assert np.array_equal(ig, i_g)
+    assert np.allclose(to_np(w), w_g, rtol=1e-3, atol=1e-5)
+    # without the logits output the selection is the same
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    M.moe_router_topk(D.cfg, D.t["x"], D.weights, None, idx2, w2, None, D.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(idx2, idx) and torch.equal(w2, w)
     # the counts are those of the GPU's own selection
     cnt = np.bincount(ig.reshape(-1), minlength=E)
     assert np.array_equal(to_np(st["counts"]), cnt)
     if not amb.any():
         b_ref = O.balance_statistic(cnt, p_o, n, shape.balance_coef)
         assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_F32])
+def test_router_ties_from_duplicated_experts(mode, dtype):
+    """Experts with identical router rows (and selection bias) produce exactly
+    equal keys: the lower expert index must win, on the tensor-core router
+    (bf16) as on the CUDA-core one (fp32)."""
+    E, k, d, N = 64, 6, 256, 333
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d, d_ff=64, dtype=dtype,
+                 route=mode, sel_bias_range=0.1 if mode == 2 else 0.0)
+    inp = W.make_inputs(shape)
+    v = inp.values
+    for src, dst in ((3, 40), (3, 17), (9, 10), (0, 63)):
+        v["w_router"][dst] = v["w_router"][src]
+        if "w_router" in inp.bits:
+            inp.bits["w_router"][dst] = inp.bits["w_router"][src]
+        if mode == 2:
+            v["sel_bias"][dst] = v["sel_bias"][src]
+    D = Device(inp)
+    logits = torch.empty(N, E, device="cuda")
+    idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(N, k, device="cuda")
+    st, sts = D.stats()
+    M.moe_router_topk(D.cfg, D.t["x"], D.weights, logits, idx, w, sts, D.ws)
+    torch.cuda.synchronize()
+    lg = to_np(logits)
+    assert np.array_equal(lg[:, 40], lg[:, 3]) and np.array_equal(lg[:, 63], lg[:, 0])
+    i_o, w_o, p_o = O.route(lg, mode, k, v.get("sel_bias"))
+    assert np.array_equal(to_np(idx), i_o)
+    assert np.allclose(to_np(w), w_o, rtol=1e-3, atol=1e-5)
+    cnt = np.bincount(i_o.reshape(-1), minlength=E)
+    assert np.array_equal(to_np(st["counts"]), cnt)
+    b_ref = O.balance_statistic(cnt, p_o, N, shape.balance_coef)
+    assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
 
 
 # --------------------------------------------------------- whole layer
@@ -396,6 +442,26 @@ def test_forward_host_matches_forward():
     M.moe_forward_host(D.cfg, xh, D.weights, oh, None, D.ws)
     torch.cuda.synchronize()
     assert torch.equal(oh, out.cpu())
+
+
+def test_forward_timed_matches_forward():
+    """The instrumented entry point makes the same launches: identical output
+    and statistics, and its events bracket every stage in order."""
+    inp = inputs_for("deepseek_v3_block", 300)
+    D = Device(inp)
+    a, sa = _forward(D)
+    out = D.empty(D.shape.n_tokens, D.shape.d_model)
+    st, sts = D.stats()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(M.MOE_FORWARD_EVENTS)]
+    M.moe_forward_timed(D.cfg, D.t["x"], D.weights, out, sts, D.ws, evs)
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
+    for name in ("counts", "kept", "dropped", "balance"):
+        assert torch.equal(st[name], sa[name]), name
+    gaps = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
+    assert all(g >= 0.0 for g in gaps) and sum(gaps) > 0.0
+    with pytest.raises(ValueError):
+        M.moe_forward_timed(D.cfg, D.t["x"], D.weights, out, sts, D.ws, evs[:3])
 
 
 def test_forward_is_deterministic():
