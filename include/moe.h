@@ -210,6 +210,29 @@ MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t
                                   void *x_perm, moe_stats_t *stats, void *ws,
                                   size_t ws_bytes, void *stream);
 
+/* moe_dispatch_permute for callers that cannot give the library any device
+ * memory of its own: a serving engine that has already claimed the GPU's
+ * memory for its own pool, or a hot loop that must not call cudaMalloc
+ * (which can stall the whole device).  The pages have no counterpart; this
+ * is a deployment variant of the grouping step above, with the same
+ * arguments minus the workspace and bit-identical outputs.
+ *   - Its per-chunk histogram lives in a fixed 512 KB array inside the
+ *     library (allocated on every GPU that loads it, kept until exit), so
+ *     n_tokens is limited to 65536: larger layers get MOE_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up that array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Calls share the array: calls whose GPU work may overlap (other
+ *     streams, other host threads) race and must be ordered by the caller.
+ *   - With no workspace there is no device error word: an expert index
+ *     outside [0, E) is dropped without being flagged.
+ * It allocates and frees nothing. */
+MOE_API moe_status_t moe_dispatch_permute_noalloc(const moe_config_t *cfg,
+                                  const int32_t *idx, const void *x,
+                                  int32_t *offsets, int32_t *row_of_slot,
+                                  int32_t *token_of_row, void *x_perm,
+                                  moe_stats_t *stats, void *stream);
+
 /* Expert up-projection and activation on the expert-sorted rows:
  * for each expert e and row r in [offsets[e], offsets[e+1]):
  *   SwiGLU:   h[r] = silu(W1[e] x_perm[r]) * (W3[e] x_perm[r])

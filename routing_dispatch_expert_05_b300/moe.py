@@ -28,7 +28,8 @@ MOE_EXPERT_SILU_MLP, MOE_EXPERT_SWIGLU = 0, 1
 
 # every function include/moe.h declares (checked by the tests)
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
-            "moe_route_logits", "moe_dispatch_permute", "moe_expert_up",
+            "moe_route_logits", "moe_dispatch_permute",
+            "moe_dispatch_permute_noalloc", "moe_expert_up",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_timed", "moe_forward_host",
             "moe_read_device_error",
@@ -83,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_router_topk": [cfgp, vp, wp, vp, vp, vp, sp, vp, sz, vp],
         "moe_route_logits": [cfgp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_dispatch_permute": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp],
+        "moe_dispatch_permute_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp],
         "moe_expert_up": [cfgp, vp, vp, wp, vp, vp, sz, vp],
         "moe_expert_up_gather": [cfgp, vp, vp, vp, wp, vp, vp, sz, vp],
         "moe_expert_down": [cfgp, vp, vp, wp, vp, vp, sz, vp],
@@ -200,6 +202,18 @@ def moe_dispatch_permute(cfg, idx, x, offsets, row_of_slot, token_of_row, x_perm
         ptr(token_of_row), ptr(x_perm),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_dispatch_permute")
+
+
+def moe_dispatch_permute_noalloc(cfg, idx, x, offsets, row_of_slot, token_of_row,
+                                 x_perm, stats, stream=None):
+    """moe_dispatch_permute without a workspace, for callers that cannot give
+    the library device memory (its scratch is a fixed array in the library:
+    n_tokens <= 65536; overlapping calls race)."""
+    _check(load_library().moe_dispatch_permute_noalloc(
+        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(offsets), ptr(row_of_slot),
+        ptr(token_of_row), ptr(x_perm),
+        ctypes.byref(stats) if stats is not None else None, _stream(stream)),
+        "moe_dispatch_permute_noalloc")
 
 
 def moe_expert_up(cfg, x_perm, offsets, weights: MoEWeights, h, ws, stream=None):
