@@ -151,10 +151,7 @@ def blas_threads():
 
 def kernel_launches_per_step(shape):
     """Kernels the library launches for one moe_forward of this layer."""
-    # bf16: logits GEMM with the selection epilogue + statistic finalize;
-    # fp32: logits GEMM, selection kernel, finalize
-    fused = shape.dtype == W.DTYPE_BF16 and shape.n_experts % 8 == 0 and shape.top_k <= 8
-    router = 2 if fused else 3
+    router = 3          # logits GEMM, selection kernel, statistic finalize
     dispatch = 4        # count, scan, rank, row gather
     experts = 2         # grouped up (with activation), grouped down
     shared = 2 if shape.n_shared > 0 else 0

@@ -194,10 +194,17 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
   float* lg = logits ? logits : at<float>(ws, L.logits);
   float* psum = at<float>(ws, L.route_psum);
   int32_t* cnt = at<int32_t>(ws, L.route_cnt);
-  bool selected = false;
+  if (gemm && c.n_tokens < kRouterSmallTokens && c.d_model * elem_size(c) * 2 <= 48 * 1024) {
+    // a few tokens: every expert's dot product at once on the CUDA cores
+    launch_router_small(x, w.w_router, w.b_router, lg, c.n_tokens, c.n_experts, c.d_model,
+                        c.dtype == MOE_BF16, st);
+    gemm = false;
+  }
   if (gemm && c.dtype == MOE_BF16) {
-    // bf16 router: one dense tcgen05 GEMM (N = E columns) whose epilogue
-    // selects the experts; logits are stored only if the caller asked
+    // bf16 router: one dense tcgen05 GEMM (N = E columns) writing fp32
+    // logits; the selection kernel reads them.  (Selecting inside the GEMM's
+    // epilogue, one thread per token, measured 1.8x slower: the serial
+    // insertion chains of four warps per SM cannot hide their latency.)
     TcProblem q{};
     q.A = x;
     q.a_rows = c.n_tokens;
@@ -213,20 +220,10 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     q.epilogue = kEpiNone;
     q.bias = w.b_router;
     q.bias_stride = 0;
-    q.C = logits;
+    q.C = lg;
     q.c_is_f32 = 1;
     q.err = err_word(ws);
-    q.route.idx = idx;
-    q.route.w = wts;
-    q.route.psum_part = psum;
-    q.route.cnt_part = cnt;
-    q.route.sel_bias = w.sel_bias;
-    q.route.mode = c.route;
-    q.route.top_k = c.top_k;
-    if (c.top_k <= kRouteMaxK && tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) {
-      gemm = false;
-      selected = true;
-    }
+    if (tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) gemm = false;
   }
   if (gemm) {
     GemmProblem p{};
@@ -246,9 +243,8 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     p.is_bf16 = c.dtype == MOE_BF16;
     launch_simt_gemm(p, st);
   }
-  if (!selected)
-    launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route, w.sel_bias,
-                             idx, wts, psum, cnt, st);
+  launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route, w.sel_bias, idx,
+                           wts, psum, cnt, st);
   launch_balance_finalize(psum, cnt, L.route_parts, c.n_experts, c.n_tokens,
                           c.balance_coef, stats ? stats->counts : nullptr,
                           stats ? stats->balance : nullptr, at<double>(ws, L.fin_terms),
@@ -267,6 +263,12 @@ void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
   if (x_perm != nullptr)
     launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
                        c.n_tokens * c.top_k, x_perm, num_sms(), st);
+}
+
+// CTA pairs (256-row tiles) pay off when experts hold enough rows; with a
+// few rows per expert most of a 256-row tile would be padding
+bool pairs_pay(const moe_config_t& c) {
+  return (double)c.n_tokens * c.top_k / c.n_experts >= 128.0;
 }
 
 // bf16 expert GEMMs run on the tensor cores; fp32 ones on the CUDA cores
@@ -324,6 +326,7 @@ moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_ma
   q.bias_stride = c.d_ff;
   q.C = h;
   q.err = err;
+  q.use_pairs = pairs_pay(c);
   return run_gemm(c, q, p, st);
 }
 
@@ -367,6 +370,7 @@ moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offs
   q.C = y;
   q.c_is_f32 = 1;
   q.err = err;
+  q.use_pairs = pairs_pay(c);
   if (y_e8 != nullptr) {
     q.c_is_f32 = 0;
     q.c_e8 = y_e8;
@@ -410,6 +414,7 @@ moe_status_t shared_body(const moe_config_t& c, const void* x, const moe_weights
   uq.epilogue = kEpiSwiglu;
   uq.C = h_shared;
   uq.err = err;
+  uq.use_pairs = c.n_tokens >= 128;
   MOE_TRY(run_gemm(c, uq, up, st));
   GemmProblem dn{};
   dn.A = h_shared;
@@ -440,6 +445,7 @@ moe_status_t shared_body(const moe_config_t& c, const void* x, const moe_weights
   dq.C = shared_out;
   dq.c_is_f32 = 1;
   dq.err = err;
+  dq.use_pairs = c.n_tokens >= 128;
   return run_gemm(c, dq, dn, st);
 }
 

@@ -7,6 +7,8 @@
 // each CTA maps its tile index to (group, m-tile) from a prefix over the
 // groups' tile counts, so no host synchronisation is needed to size it.
 // Empty groups own no tile.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -170,7 +172,67 @@ void launch_typed(const GemmProblem& p, cudaStream_t st) {
   }
 }
 
+// Router logits for a few tokens: logits[t, e] = sum_i x[t, i] W[e, i] (+ b[e]),
+// fp32 accumulation.  One CTA per kSmallTok tokens (staged in shared memory),
+// one thread per expert; each thread streams its router row in 16-byte
+// pieces.  With few tokens the tensor-core router runs one tile whose k-loop
+// is a serial chain; here every expert's dot product runs at once.
+constexpr int kSmallTok = 2;
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* __restrict__ b,
+                    float* __restrict__ logits, int64_t n_tokens, int n_experts, int d) {
+  extern __shared__ __align__(16) uint8_t sx_raw[];
+  T* sx = reinterpret_cast<T*>(sx_raw);              // [kSmallTok][d]
+  const int64_t t0 = (int64_t)blockIdx.x * kSmallTok;
+  const int nt = (int)min((int64_t)kSmallTok, n_tokens - t0);
+  constexpr int V = 16 / sizeof(T);                  // elements per 16 bytes
+  const int nv = d / V;
+  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) {
+    const int tt = i / nv, v = i - tt * nv;
+    reinterpret_cast<uint4*>(sx + (int64_t)tt * d)[v] =
+        reinterpret_cast<const uint4*>(x + (t0 + tt) * d)[v];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+    const uint4* wr = reinterpret_cast<const uint4*>(W + (int64_t)e * d);
+    float acc[kSmallTok];
+#pragma unroll
+    for (int tt = 0; tt < kSmallTok; ++tt) acc[tt] = 0.f;
+    for (int v = 0; v < nv; ++v) {
+      const uint4 wv = __ldg(wr + v);
+      const T* wp = reinterpret_cast<const T*>(&wv);
+#pragma unroll
+      for (int tt = 0; tt < kSmallTok; ++tt) {
+        if (tt >= nt) break;
+        const uint4 xv = reinterpret_cast<const uint4*>(sx + (int64_t)tt * d)[v];
+        const T* xp = reinterpret_cast<const T*>(&xv);
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[tt] = fmaf(to_f32(xp[j]), to_f32(wp[j]), acc[tt]);
+      }
+    }
+    const float bias = b ? to_f32(b[e]) : 0.f;
+    for (int tt = 0; tt < nt; ++tt) logits[(t0 + tt) * n_experts + e] = acc[tt] + bias;
+  }
+}
+
 }  // namespace
+
+void launch_router_small(const void* x, const void* w, const void* b, float* logits,
+                         int64_t n_tokens, int n_experts, int d, int is_bf16, cudaStream_t st) {
+  if (n_tokens <= 0) return;
+  const int blocks = (int)ceil_div64(n_tokens, kSmallTok);
+  const int threads = std::min(256, (n_experts + 31) / 32 * 32);
+  const size_t smem = (size_t)kSmallTok * d * (is_bf16 ? 2 : 4);
+  if (is_bf16)
+    router_small_kernel<bf16><<<blocks, threads, smem, st>>>(
+        static_cast<const bf16*>(x), static_cast<const bf16*>(w), static_cast<const bf16*>(b),
+        logits, n_tokens, n_experts, d);
+  else
+    router_small_kernel<float><<<blocks, threads, smem, st>>>(
+        static_cast<const float*>(x), static_cast<const float*>(w),
+        static_cast<const float*>(b), logits, n_tokens, n_experts, d);
+}
 
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st) {
   if (p.is_bf16) launch_typed<bf16>(p, st);

@@ -43,7 +43,11 @@ namespace moe {
 namespace tc {
 
 constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
-constexpr int kThreads = 192;
+// warp 0 TMA producer, warp 1 MMA issuer, warps 2.. epilogue: two epilogue
+// warps per TMEM lane quadrant (warp w may read lanes 32*(w%4)..), each
+// taking half of the tile's output columns
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTileA = BM * BK * 2;            // 16 KB
 constexpr uint32_t kTileB = BN * BK * 2;            // 32 KB
 constexpr uint32_t kStageBytes = kTileA + kTileB;   // 48 KB
@@ -58,20 +62,17 @@ constexpr int kTableBytes = (2 * (kMaxExperts + 1) * 4 + 127) / 128 * 128;
 // Rows are padded (fp32: 36 words, bf16: 20 words) so that both the
 // row-per-lane writes and the column-per-lane reads are free of bank
 // conflicts (up to a 2-way conflict on a quarter of the bf16 reads).
-constexpr int kStgF32Stride = 36;                  // floats per staged row
-constexpr int kStgB16Stride = 20;                  // 32-bit words per staged row
-constexpr int kStgWarpBytes = 32 * kStgF32Stride * 4;
-// Routing epilogue: per-warp selection counters (each epilogue warp owns the
-// statistics partial of its 32 tokens, so the warps never wait on each other)
-// and the router / selection biases as fp32.
-constexpr int kRouteSmemBytes = 4 * kMaxExperts * 4 + 2 * kMaxExperts * 4;
+constexpr int kStgF32Stride = 20;                  // words per staged row (16 fp32)
+constexpr int kStgB16Stride = 20;                  // words per staged row (32 x 16-bit)
+constexpr int kStgWarpBytes = 32 * kStgB16Stride * 4;
 constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kTableBytes +
-                           4 * kStgWarpBytes + kRouteSmemBytes + 1024 /* alignment */;
+                           kEpiWarps * kStgWarpBytes + 1024 /* alignment */;
 static_assert((kStages * kStageBytes + kBarBytes + kTableBytes) % 16 == 0,
               "epilogue staging must be 16-byte aligned (vector stores)");
 static_assert(kStgWarpBytes % 16 == 0 && (kStgF32Stride * 4) % 16 == 0 &&
-                  (kStgB16Stride * 4) % 16 == 0,
-              "staged rows must keep 16-byte alignment");
+                  (kStgB16Stride * 4) % 16 == 0 && kStgF32Stride >= 16 && kStgB16Stride >= 16,
+              "staged rows must keep 16-byte alignment and hold 64 bytes");
+static_assert(kEpiWarps == 8, "two epilogue warps per TMEM lane quadrant");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
@@ -94,7 +95,6 @@ struct Params {
   int32_t* err;
   const int32_t* a_row_map;   // null: A rows are the tile rows; else A row r
                               // is row a_row_map[r] of the A tensor
-  RouteEpilogue route;        // route.idx != null: the routing epilogue
 };
 
 // ---------------------------------------------------------------- PTX
@@ -236,7 +236,7 @@ struct Tile {
 };
 
 __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int* off,
-                                        int G, int nt) {
+                                        int G, int nt, int bm = BM) {
   int lo = 0, hi = G - 1;  // largest g with tile_start[g] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -245,23 +245,23 @@ __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int*
   const int local = t - tile_start[lo];
   Tile r;
   r.g = lo;
-  r.row0 = off[lo] + (local / nt) * BM;
+  r.row0 = off[lo] + (local / nt) * bm;
   r.row_end = off[lo + 1];
   r.n = local % nt;
   return r;
 }
 
 // ------------------------------------------------------- epilogue helpers
-// Writes the warp's staged 32 rows x 32 fp32 columns (row r at
-// stg + r * kStgF32Stride) as whole 128-byte row segments: lane = (row
-// quarter, 16-byte piece).
+// Writes the warp's staged 32 rows x 16 fp32 columns (row r at
+// stg + r * kStgF32Stride) as whole 64-byte row segments: lane = (row of an
+// 8-row group, 16-byte piece).
 __device__ __forceinline__ void store_staged_f32(const float* stg, int lane, int row_base,
                                                  int row_end, int col0, int n_out, float* C) {
-  const int c4 = lane & 7;
+  const int c4 = lane & 3;
   const bool col_ok = col0 + c4 * 4 < n_out;
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int r = it * 4 + (lane >> 3);
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2);
     const int row = row_base + r;
     if (col_ok && row < row_end) {
       const float4 val = *reinterpret_cast<const float4*>(stg + r * kStgF32Stride + c4 * 4);
@@ -296,13 +296,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // columns of a row, the largest |v| picks a power of two 2^s that brings it
 // into [2^14, 2^15); v * 2^s (exact) is rounded once to fp16, and the biased
 // exponent of 2^-s (one byte, an E8 shared exponent) is stored beside it.
-__device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, int lane,
+// The warp takes half `half` of the tile's 256 columns (4 exponents).
+__device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, int lane, int half,
                                              int row_base, uint32_t tb, uint32_t* stg) {
   const int row = row_base + lane;
   const bf16* bp = p.bias ? p.bias + (int64_t)tl.g * p.bias_stride : nullptr;
-  uint32_t e8lo = 0u, e8hi = 0u;                   // this row's 8 exponents of the tile
+  uint32_t e8w = 0u;                               // this row's 4 exponents
 #pragma unroll 1
-  for (int ch = 0; ch < BN / 32; ++ch) {
+  for (int ci = 0; ci < BN / 32 / 2; ++ci) {
+    const int ch = half * (BN / 32 / 2) + ci;
     const int c0 = tl.n * BN + ch * 32;
     if (c0 >= p.n_out) break;                      // warp-uniform
     uint32_t r[32];
@@ -319,8 +321,7 @@ __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, in
     int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
     e = min(max(e, -100), 127);                    // zero / tiny blocks: bounded scale
     const float scale = __uint_as_float((uint32_t)(127 + 14 - e) << 23);   // 2^(14-e)
-    const uint32_t e8 = (uint32_t)(e + 113) << (8 * (ch & 3));             // 2^(e-14)
-    if (ch < 4) e8lo |= e8; else e8hi |= e8;
+    e8w |= (uint32_t)(e + 113) << (8 * ci);                                // 2^(e-14)
     uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgB16Stride);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -333,223 +334,88 @@ __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, in
     __syncwarp();
   }
   if (row < tl.row_end) {
-    uint8_t* ep = p.c_e8 + (int64_t)row * p.e8_cols + tl.n * (BN / 32);
-    const int n8 = min(BN / 32, p.e8_cols - tl.n * (BN / 32));
-    if (n8 == 8 && (reinterpret_cast<uintptr_t>(ep) & 7u) == 0) {
-      *reinterpret_cast<uint2*>(ep) = make_uint2(e8lo, e8hi);
+    const int b0 = tl.n * (BN / 32) + half * (BN / 32 / 2);   // first exponent index
+    const int n4 = min(BN / 32 / 2, p.e8_cols - b0);
+    uint8_t* ep = p.c_e8 + (int64_t)row * p.e8_cols + b0;
+    if (n4 == 4 && (reinterpret_cast<uintptr_t>(ep) & 3u) == 0) {
+      *reinterpret_cast<uint32_t*>(ep) = e8w;
     } else {
-      for (int i = 0; i < n8; ++i) ep[i] = (uint8_t)((i < 4 ? e8lo : e8hi) >> (8 * (i & 3)));
+      for (int i = 0; i < n4; ++i) ep[i] = (uint8_t)(e8w >> (8 * i));
     }
   }
 }
 
-// Sum of 32 per-lane vectors, transposed: on return v[0] of lane l is the
-// sum over the 32 lanes of their v[l].  A fixed butterfly (31 shuffles), so
-// the summation order -- and the result -- is the same on every run.
-__device__ __forceinline__ void warp_transpose_sum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const float send = upper ? v[i] : v[i + s];
-      const float keep = upper ? v[i + s] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-}
-
-// Insert (key, e, aux) into a list sorted by key descending in which equal
-// keys keep arrival order.  Experts arrive in ascending index order, so ties
-// go to the lower expert index.  Slots >= k are never filled (idx -1 = empty).
-template <int KM>
-__device__ __forceinline__ void topk_insert(float (&tk)[KM], int (&ti)[KM], float (&ta)[KM],
-                                            int k, float key, int e, float aux) {
-  bool shifting = false;   // once placed, every later entry moves down one slot
-#pragma unroll
-  for (int i = 0; i < KM; ++i) {
-    if (i < k && (shifting || ti[i] < 0 || key > tk[i])) {
-      const float kk = tk[i], aa = ta[i];
-      const int ii = ti[i];
-      tk[i] = key; ti[i] = e; ta[i] = aux;
-      key = kk; e = ii; aux = aa;
-      shifting = true;
-      if (e < 0) break;    // filled an empty slot: nothing left to move
-    }
-  }
-}
-
-// sigmoid in double, rounded once to fp32: the selection key's definition
-__device__ __forceinline__ float sigmoid_exact(float l) {
-  return (float)(1.0 / (1.0 + exp(-(double)l)));
-}
-// fp32 sigmoid: expf (<= 2 ulp), one add and a correctly rounded divide; its
-// distance to sigmoid_exact stays far below kSigmoidSlack
-__device__ __forceinline__ float sigmoid_fast(float l) {
-  return 1.0f / (1.0f + expf(-l));
-}
-constexpr float kSigmoidSlack = 1.0f / 65536.0f;   // bound used for candidates
-
-// The routing epilogue of the router GEMM: the accumulator holds the fp32
-// logits of 128 tokens x E experts (E <= 256, one n-tile).  Lane = token.
-//   pass 1: logits (+ router bias), optional logits store, selection keys,
-//           running top-k, softmax max / normaliser (online) or sum of s;
-//   pass 2 (sigmoid mode): exact keys for the candidates (see below);
-//   pass 3: routing probabilities p[t, e] -> per-expert sums over the
-//           warp's 32 tokens (one statistics partial per warp).
-// The sigmoid key is sigmoid(l) + b with sigmoid evaluated in double and
-// rounded to fp32.  Double is slow here, so pass 1 ranks fp32 keys ka whose
-// distance to the exact keys is below delta = kSigmoidSlack; every expert of
-// the exact top k then has ka >= (k-th largest ka) - 2 delta, and only those
-// candidates get exact keys -- the selection equals the all-double one.
-__device__ __forceinline__ void route_tile(const Params& p, const Tile& tl, int q, int lane,
-                                           uint32_t tb, float* stg, int* cnt,
-                                           const float* s_rb, const float* s_sb) {
-  constexpr int KM = kRouteMaxK;
-  const RouteEpilogue& R = p.route;
-  const int E = p.n_out, k = R.top_k, mode = R.mode;
-  const int nch = (E + 31) / 32;
-  const int row_base = tl.row0 + q * 32;
-  const int row = row_base + lane;
-  const bool valid = row < tl.row_end;
-  const bool warp_has_rows = row_base < tl.row_end;
-  const int part = row_base / kRouteTokensPerPartial;   // this warp's statistics partial
-
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
-
-  float tk[KM], ta[KM];
-  int ti[KM];
-#pragma unroll
-  for (int i = 0; i < KM; ++i) tk[i] = -INFINITY, ta[i] = 0.f, ti[i] = -1;
-  float m = -INFINITY, z = 0.f;                     // softmax max and sum exp(l - m)
-  float ssum = 0.f;                                 // sigmoid: sum of s (fp32 s)
-
-  // ---- pass 1
+// Plain output of one tile (bf16, or fp32 if c_is_f32): SwiGLU / SiLU+bias /
+// identity epilogue, staged per 32-row chunk for row-contiguous stores.  The
+// warp takes half `half` of the tile's output columns.
+__device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int lane, int half,
+                                           int row_base, uint32_t tb, float* stg_f,
+                                           uint32_t* stg_w) {
+  const int cols_tile = p.swiglu ? BN / 2 : BN;   // output columns per tile
+  const int nch = cols_tile / 32 / 2;              // chunks per half
 #pragma unroll 1
-  for (int ch = 0; ch < nch; ++ch) {
-    const int col0 = ch * 32;
-    uint32_t r[32];
-    MOE_TMEM_LD32(tb + col0, r);
-    tmem_ld_wait();
-    float l[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = col0 + j;
-      l[j] = __uint_as_float(r[j]) + s_rb[e];
-    }
-    if (p.C != nullptr) {
-      float4* dst = reinterpret_cast<float4*>(stg + lane * kStgF32Stride);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = make_float4(l[4 * j], l[4 * j + 1], l[4 * j + 2], l[4 * j + 3]);
-      __syncwarp();
-      store_staged_f32(stg, lane, row_base, tl.row_end, col0, E, static_cast<float*>(p.C));
-      __syncwarp();
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = col0 + j;
-      if (e >= E) break;
-      if (mode == 2) {
-        const float sa = sigmoid_fast(l[j]);
-        ssum += sa;
-        topk_insert<KM>(tk, ti, ta, k, __fadd_rn(sa, s_sb[e]), e, 0.f);
-      } else {
-        if (l[j] > m) {
-          z = z * expf(m - l[j]) + 1.f;
-          m = l[j];
-        } else {
-          z += expf(l[j] - m);
-        }
-        topk_insert<KM>(tk, ti, ta, k, l[j], e, 0.f);
-      }
-    }
-  }
-
-  // ---- pass 2 (sigmoid): exact keys of the candidates
-  if (mode == 2) {
-    float kth = tk[0];                              // the k-th fp32 key (unrolled pick)
-#pragma unroll
-    for (int i = 1; i < KM; ++i)
-      if (i == k - 1) kth = tk[i];
-    const float thr = kth - 4.f * kSigmoidSlack;
-#pragma unroll
-    for (int i = 0; i < KM; ++i) tk[i] = -INFINITY, ta[i] = 0.f, ti[i] = -1;
-#pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-      const int col0 = ch * 32;
-      uint32_t r[32];
-      MOE_TMEM_LD32(tb + col0, r);
+  for (int ci = 0; ci < nch; ++ci) {
+    const int ch = half * nch + ci;
+    const int col0 = tl.n * cols_tile + ch * 32;
+    if (col0 >= p.n_out) break;                  // warp-uniform
+    float v[32];
+    if (p.swiglu) {
+      uint32_t g[32], u[32];
+      MOE_TMEM_LD32(tb + ch * 32, g);
+      MOE_TMEM_LD32(tb + BN / 2 + ch * 32, u);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = col0 + j;
-        if (e >= E) break;
-        const float l = __uint_as_float(r[j]) + s_rb[e];
-        const float b = s_sb[e];
-        if (__fadd_rn(sigmoid_fast(l), b) >= thr) {
-          const float s = sigmoid_exact(l);
-          topk_insert<KM>(tk, ti, ta, k, __fadd_rn(s, b), e, s);
-        }
+      for (int j = 0; j < 32; ++j)
+        v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+    } else {
+      uint32_t r[32];
+      MOE_TMEM_LD32(tb + ch * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      if (p.bias) {
+        const bf16* bp = p.bias + (int64_t)tl.g * p.bias_stride + col0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < p.n_out) v[j] += __bfloat162float(bp[j]);
       }
+      if (p.epilogue == kEpiSiluBias) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
+      }
+    }
+    if (p.c_is_f32) {
+      // two 16-column halves through the staging rows
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float4* dst = reinterpret_cast<float4*>(stg_f + lane * kStgF32Stride);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(v[16 * hh + 4 * j], v[16 * hh + 4 * j + 1],
+                               v[16 * hh + 4 * j + 2], v[16 * hh + 4 * j + 3]);
+        __syncwarp();
+        store_staged_f32(stg_f, lane, row_base, tl.row_end, col0 + 16 * hh, p.n_out,
+                         static_cast<float*>(p.C));
+        __syncwarp();
+      }
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(stg_w + lane * kStgB16Stride);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                            pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                            pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                            pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+      __syncwarp();
+      store_staged_b16(stg_w, lane, row_base, tl.row_end, col0, p.n_out, p.C);
+      __syncwarp();
     }
   }
-
-  // ---- selection outputs: idx, weights, counts
-  if (valid) {
-    float wsum = 0.f, wv[KM];
-#pragma unroll
-    for (int i = 0; i < KM; ++i) {
-      wv[i] = 0.f;
-      if (i < k) {
-        wv[i] = mode == 2 ? ta[i] : expf(tk[i] - tk[0]);
-        wsum += wv[i];
-      }
-    }
-    const int64_t o = (int64_t)row * k;
-#pragma unroll
-    for (int i = 0; i < KM; ++i) {
-      if (i < k) {
-        R.idx[o + i] = ti[i];
-        R.w[o + i] = wv[i] / wsum;
-        atomicAdd(&cnt[ti[i]], 1);
-      }
-    }
-  }
-
-  // ---- pass 3: probabilities, summed per expert over this warp's tokens
-  const float inv = mode == 2 ? 1.f / ssum : 1.f / z;
-#pragma unroll 1
-  for (int ch = 0; ch < nch; ++ch) {
-    const int col0 = ch * 32;
-    uint32_t r[32];
-    MOE_TMEM_LD32(tb + col0, r);
-    tmem_ld_wait();
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = col0 + j;
-      float pv = 0.f;
-      if (valid && e < E) {
-        const float l = __uint_as_float(r[j]) + s_rb[e];
-        pv = (mode == 2 ? sigmoid_fast(l) : expf(l - m)) * inv;
-      }
-      v[j] = pv;
-    }
-    warp_transpose_sum32(v, lane);
-    if (warp_has_rows && col0 + lane < E)
-      R.psum_part[(int64_t)part * E + col0 + lane] = v[0];
-  }
-  __syncwarp();
-  if (warp_has_rows)
-    for (int e = lane; e < E; e += 32) R.cnt_part[(int64_t)part * E + e] = cnt[e];
-  __syncwarp();
 }
 
 // ---------------------------------------------------------------- kernel
 // Epilogue kinds, one kernel instantiation each.
-enum : int { kEkStore = 0, kEkCompact = 1, kEkRoute = 2 };
+enum : int { kEkStore = 0, kEkCompact = 1 };
 
 template <int EK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -571,9 +437,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   int* s_tile_start = reinterpret_cast<int*>(smem + kStages * kStageBytes + kBarBytes);
   int* s_off = s_tile_start + kMaxExperts + 1;
   uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
-  int* s_rcnt = reinterpret_cast<int*>(s_stage + 4 * kStgWarpBytes);  // [4][kMaxExperts]
-  float* s_rb = reinterpret_cast<float*>(s_rcnt + 4 * kMaxExperts);   // router bias [256]
-  float* s_sb = s_rb + kMaxExperts;                                    // selection bias
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.offsets ? p.n_groups : 1;
@@ -589,7 +452,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 4);
+      mbar_init(&tempty[s], kEpiWarps);
     }
     mbar_init(drain, 1);
     *s_abort = 0;
@@ -599,13 +462,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (p.swiglu) prefetch_map(&tmB1);
   }
   if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
-  if (EK == kEkRoute && warp == 3) {
-    for (int e = lane; e < kMaxExperts; e += 32) {
-      const bool in = e < p.n_out;
-      s_rb[e] = in && p.bias != nullptr ? __bfloat162float(p.bias[e]) : 0.f;
-      s_sb[e] = in && p.route.mode == 2 ? p.route.sel_bias[e] : 0.f;
-    }
-  }
   if (warp == 2) {
     int carry = 0;
     for (int base = 0; base < G; base += 32) {
@@ -749,10 +605,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   } else {
     // ------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                          // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;                // which half of the columns
     float* stg_f = reinterpret_cast<float*>(s_stage + (warp - 2) * kStgWarpBytes);
     uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg_f);
-    const int cols_tile = p.swiglu ? BN / 2 : BN;   // output columns per tile
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -761,78 +617,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tc_fence_after();
       const int row_base = tl.row0 + q * 32;         // this warp's 32 rows
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      if constexpr (EK == kEkRoute) {
-        route_tile(p, tl, q, lane, tb, stg_f, s_rcnt + (warp - 2) * kMaxExperts, s_rb, s_sb);
-      } else if constexpr (EK == kEkCompact) {
-        compact_tile(p, tl, lane, row_base, tb, stg_w);
+      if constexpr (EK == kEkCompact) {
+        compact_tile(p, tl, lane, half, row_base, tb, stg_w);
       } else {
-#pragma unroll 1
-      for (int ch = 0; ch < cols_tile / 32; ++ch) {
-        const int col0 = tl.n * cols_tile + ch * 32;
-        if (col0 >= p.n_out) break;                  // warp-uniform
-        float v[32];
-        if (p.swiglu) {
-          uint32_t g[32], u[32];
-          MOE_TMEM_LD32(tb + ch * 32, g);
-          MOE_TMEM_LD32(tb + BN / 2 + ch * 32, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-        } else {
-          uint32_t r[32];
-          MOE_TMEM_LD32(tb + ch * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          if (p.bias) {
-            const bf16* bp = p.bias + (int64_t)tl.g * p.bias_stride + col0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.n_out) v[j] += __bfloat162float(bp[j]);
-          }
-          if (p.epilogue == kEpiSiluBias) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
-          }
-        }
-        // lane = row: stage the row's 32 values
-        if (p.c_is_f32) {
-          float4* dst = reinterpret_cast<float4*>(stg_f + lane * kStgF32Stride);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(stg_w + lane * kStgB16Stride);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-        }
-        __syncwarp();
-        // lane = 16-byte column piece: whole row segments per store
-        if (p.c_is_f32) {
-          store_staged_f32(stg_f, lane, row_base, tl.row_end, col0, p.n_out,
-                           static_cast<float*>(p.C));
-        } else {
-          const int c8 = lane & 3;
-          const bool col_ok = col0 + c8 * 8 < p.n_out;
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int r = it * 8 + (lane >> 2);
-            const int row = row_base + r;
-            if (col_ok && row < tl.row_end) {
-              const uint4 val =
-                  *reinterpret_cast<const uint4*>(stg_w + r * kStgB16Stride + c8 * 4);
-              st_vec16(static_cast<bf16*>(p.C) + (int64_t)row * p.n_out + col0 + c8 * 8,
-                       val);
-            }
-          }
-        }
-        __syncwarp();
-      }
+        store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
       }
       tc_fence_before();
       __syncwarp();
@@ -847,6 +635,292 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// The same grouped GEMM on pairs of SMs (a cluster of two CTAs) with
+// tcgen05.mma.cta_group::2: a pair computes a 256-row x 256-column tile.
+// CTA r of the pair loads rows 128r..128r+127 of A and half of the B tile
+// (SwiGLU: r = 0 the gate rows, r = 1 the up rows; otherwise columns
+// 128r..128r+127), each 128 x 64 per k-block into a 6-stage ring, and holds
+// rows 128r.. of the accumulator in its own TMEM.  Per SM, a k-block moves 32
+// KB through shared memory instead of 48 KB for the same tensor work, which
+// is what bounds the single-CTA kernel.
+//   * both CTAs' copies complete on the leader's (rank 0) full barrier, which
+//     expects the bytes of both; the leader's MMA thread issues the MMAs and
+//     commits to the empty / accumulator-full barriers of both CTAs at once;
+//   * each CTA's epilogue warps read their own TMEM rows and release the
+//     accumulator on the leader's barrier (remote arrive from rank 1);
+//   * TMEM is allocated and freed by one warp in each CTA, collectively.
+// Waits are bounded exactly as in the single-CTA kernel.
+constexpr int BM2 = 256;
+constexpr int kStages2 = 6;
+constexpr uint32_t kTileA2 = 128 * BK * 2;         // this CTA's 128 rows of A
+constexpr uint32_t kTileB2 = 128 * BK * 2;         // this CTA's half of B
+constexpr uint32_t kStageBytes2 = kTileA2 + kTileB2;
+constexpr int kSmemBytes2 =
+    kStages2 * kStageBytes2 + kBarBytes + kTableBytes + kEpiWarps * kStgWarpBytes + 1024;
+static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA (pairs)");
+static_assert((kStages2 * kStageBytes2 + kBarBytes + kTableBytes) % 16 == 0, "staging alignment");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// tile load into this CTA's shared memory, completing on an mbarrier of
+// either CTA of the pair (a shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive once on `bar` (same offset) in every CTA of `mask` when all prior
+// MMAs of this thread are complete
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+               ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+template <int EK>
+__global__ void __launch_bounds__(kThreads, 1)
+tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages2 * kTileA2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStageBytes2);
+  uint64_t* empty = full + kStages2;
+  uint64_t* tfull = empty + kStages2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_tile_start = reinterpret_cast<int*>(smem + kStages2 * kStageBytes2 + kBarBytes);
+  int* s_off = s_tile_start + kMaxExperts + 1;
+  uint8_t* s_stage = smem + kStages2 * kStageBytes2 + kBarBytes + kTableBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int G = p.offsets ? p.n_groups : 1;
+  const int nt_cols = p.swiglu ? BN / 2 : BN;       // output columns per tile
+  const int nt = (p.n_out + nt_cols - 1) / nt_cols;  // n-tiles per group
+  const int nkb = (p.K + BK - 1) / BK;
+  const int kb_per_sub = p.k_sub / BK;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 2 * kEpiWarps);        // the epilogue warps of both CTAs
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&tmA);
+    prefetch_map(&tmB0);
+    if (p.swiglu) prefetch_map(&tmB1);
+  }
+  if (warp == 1) tmem_alloc_pair(s_tmem, kTmemCols);
+  if (warp == 2) {
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int gg = base + lane;
+      int m = 0;
+      if (gg < G) {
+        const int o0 = p.offsets ? p.offsets[gg] : 0;
+        const int o1 = p.offsets ? p.offsets[gg + 1] : p.rows;
+        s_off[gg] = o0;
+        m = o1 - o0;
+      }
+      const int tiles = (m + BM2 - 1) / BM2 * nt;
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (gg < G) s_tile_start[gg] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_tile_start[G] = carry;
+      s_off[G] = p.offsets ? p.offsets[G] : p.rows;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                  // both CTAs' barriers exist
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = s_tile_start[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_phases = 0;
+      for (int t = pair; t < total; t += n_pairs) {
+        const Tile tl = tile_of(t, s_tile_start, s_off, G, nt, BM2);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
+          const uint32_t bar = map_to_rank(&full[stage], 0);
+          if (leader) mbar_expect_tx(&full[stage], 2 * kStageBytes2);
+          uint8_t* a = sA + stage * kTileA2;
+          uint8_t* b = sB + stage * kTileB2;
+          tma_load_2d_pair(a, &tmA, bar, kb * BK, tl.row0 + (int)rank * 128);
+          if (p.swiglu) {
+            const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
+            tma_load_2d_pair(b, rank ? &tmB1 : &tmB0, bar, kb * BK, brow);
+          } else {
+            const int sub = kb / kb_per_sub;
+            const int kk = (kb - sub * kb_per_sub) * BK;
+            const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN + (int)rank * 128;
+            tma_load_2d_pair(b, &tmB0, bar, kk, brow);
+          }
+          used |= 1u << stage;
+          last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // the leader's full barriers count both CTAs' copies: every issued
+      // copy of the pair has landed once they complete
+      if (leader) {
+        for (int s = 0; s < kStages2; ++s) {
+          if (!(used >> s & 1u)) continue;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&full[s], last_phases >> s & 1u)) {
+            if (globaltimer() - t0 > kTimeoutNs) {
+              set_device_error(p.err, kDevTimeout);
+              break;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM2, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = pair; t < total; t += n_pairs) {
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&full[stage], phase, s_abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kTileA2);
+          const uint32_t b0 = smem_u32(sB + stage * kTileB2);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_pair(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
+                      (kb | kk) != 0);
+          umma_commit_pair(&empty[stage], 0x3);
+          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      umma_commit_pair(drain, 0x1);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+          set_device_error(p.err, kDevTimeout);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;                          // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;                // which half of the columns
+    float* stg_f = reinterpret_cast<float*>(s_stage + (warp - 2) * kStgWarpBytes);
+    uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg_f);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < total; t += n_pairs) {
+      const Tile tl = tile_of(t, s_tile_start, s_off, G, nt, BM2);
+      if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
+      tc_fence_after();
+      const int row_base = tl.row0 + (int)rank * 128 + q * 32;
+      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if constexpr (EK == kEkCompact) {
+        compact_tile(p, tl, lane, half, row_base, tb, stg_w);
+      } else {
+        store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                  // no CTA leaves while its peer works
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -885,35 +959,36 @@ bool tc_gemm_supported(const TcProblem& q) {
   if (q.K < 1 || q.n_out < 8 || q.n_out % 8 != 0) return false;
   if (q.k_sub % tc::BK != 0 && q.n_sub > 1) return false;
   if (q.n_groups > kMaxExperts) return false;
-  // the routing epilogue: one group, all E columns in one accumulator tile
   // compact output: one exponent per 32 columns, no SwiGLU pairing
   if (q.c_e8 != nullptr && (q.swiglu || q.e8_cols != (q.n_out + 31) / 32)) return false;
-  if (q.route.idx != nullptr &&
-      (q.n_out > tc::BN || q.offsets != nullptr || q.swiglu || q.n_sub != 1 ||
-       q.route.top_k < 1 || q.route.top_k > kRouteMaxK || q.route.top_k > q.n_out))
-    return false;
   return tc::encode_fn() != nullptr;
 }
 
+namespace {
+// CTA pairs that can be resident at once for the pair kernel (0: none)
+int pair_grid(const void* kern, int num_sms) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(num_sms & ~1);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmemBytes2;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return std::min(clusters, num_sms / 2);
+}
+}  // namespace
+
 bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   using namespace tc;
-  CUtensorMap ma, mb0, mb1;
-  // A [a_rows, K]
-  // a gathered A is read one row per box (four boxes per gather4)
-  if (!make_map(&ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2,
-                q.a_row_map ? 1u : (uint32_t)BM))
-    return false;
-  const int ksub = q.n_sub > 1 ? q.k_sub : q.K;
-  const uint64_t brows_total = (uint64_t)q.b_groups * q.n_sub * q.b_rows;
-  if (q.swiglu) {
-    if (!make_map(&mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2) ||
-        !make_map(&mb1, q.B1, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2))
-      return false;
-  } else {
-    if (!make_map(&mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN))
-      return false;
-    mb1 = mb0;
-  }
   Params p{};
   p.offsets = q.offsets;
   p.n_groups = q.n_groups;
@@ -923,7 +998,7 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.swiglu = q.swiglu;
   p.epilogue = q.epilogue;
   p.b_rows = q.b_rows;
-  p.k_sub = ksub;
+  p.k_sub = q.n_sub > 1 ? q.k_sub : q.K;
   p.n_sub = q.n_sub;
   p.bias = static_cast<const bf16*>(q.bias);
   p.bias_stride = q.bias_stride;
@@ -933,10 +1008,51 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.e8_cols = q.e8_cols;
   p.err = q.err;
   p.a_row_map = q.a_row_map;
-  p.route = q.route;
-  auto kern = q.route.idx != nullptr ? tc_gemm_kernel<kEkRoute>
-             : q.c_e8 != nullptr       ? tc_gemm_kernel<kEkCompact>
-                                       : tc_gemm_kernel<kEkStore>;
+  const int ksub = p.k_sub;
+  const uint64_t brows_total = (uint64_t)q.b_groups * q.n_sub * q.b_rows;
+  // A [a_rows, K] (a gathered A is read one row per box, four per gather4);
+  // B: SwiGLU halves of 128 rows, otherwise 256 rows (128 per CTA of a pair)
+  auto maps = [&](bool pair_tiles, CUtensorMap* ma, CUtensorMap* mb0, CUtensorMap* mb1) {
+    if (!make_map(ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2,
+                  q.a_row_map ? 1u : (uint32_t)BM))
+      return false;
+    if (q.swiglu)
+      return make_map(mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2) &&
+             make_map(mb1, q.B1, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2);
+    if (!make_map(mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2,
+                  pair_tiles ? BN / 2 : BN))
+      return false;
+    *mb1 = *mb0;
+    return true;
+  };
+  CUtensorMap ma, mb0, mb1;
+  // CTA pairs for grouped row order (not a gathered A); the single-CTA
+  // kernel runs if pairs cannot be launched here
+  if (q.use_pairs && q.a_row_map == nullptr) {
+    auto kern2 = q.c_e8 != nullptr ? tc2_gemm_kernel<kEkCompact> : tc2_gemm_kernel<kEkStore>;
+    int n_pairs = 0;
+    if (cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes2) == cudaSuccess)
+      n_pairs = pair_grid(reinterpret_cast<const void*>(kern2), num_sms);
+    if (n_pairs >= 1 && maps(true, &ma, &mb0, &mb1)) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(2 * n_pairs);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemBytes2;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, kern2, ma, mb0, mb1, p) == cudaSuccess) return true;
+    }
+    cudaGetLastError();   // clear, then run on single CTAs
+  }
+  if (!maps(false, &ma, &mb0, &mb1)) return false;
+  auto kern = q.c_e8 != nullptr ? tc_gemm_kernel<kEkCompact> : tc_gemm_kernel<kEkStore>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return false;

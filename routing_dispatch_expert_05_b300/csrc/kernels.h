@@ -8,8 +8,8 @@
 
 namespace moe {
 
-// Tokens whose selection statistics one router partial covers (one warp of
-// the routing epilogue, or of the selection kernel).
+// Tokens whose selection statistics one router partial covers (one CTA of
+// the selection kernel).
 constexpr int kRouteTokensPerPartial = 32;
 // Tokens per dispatch chunk (the unit of the per-chunk histogram).
 constexpr int kDispatchTokensPerChunk = 256;
@@ -37,6 +37,8 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* row_of_slot, int32_t* token_of_row,
                      int32_t* counts, int32_t* kept, int32_t* dropped,
                      int32_t* err, cudaStream_t st);
+// x_perm[r] = x[token_of_row[r]] for r < offsets[E] (16-byte vectors on the
+// load/store units; a TMA bulk-copy version measured 1.5x slower)
 void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
                         const int32_t* offsets, int n_experts, int64_t max_rows,
                         void* x_perm, int num_sms, cudaStream_t st);
@@ -74,22 +76,14 @@ struct GemmProblem {
   const int32_t* a_row_map;
 };
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st);
+// router logits [N, E] fp32 for a few tokens (CUDA cores, one thread per
+// expert); x [N, d], w [E, d], b [E] or null, in the layer dtype
+void launch_router_small(const void* x, const void* w, const void* b, float* logits,
+                         int64_t n_tokens, int n_experts, int d, int is_bf16, cudaStream_t st);
+// below this many tokens the router GEMM runs on the CUDA cores
+constexpr int64_t kRouterSmallTokens = 512;
 
 // ---- tcgen05 grouped GEMM (bf16 storage, fp32 accumulation in TMEM) -------
-// Routing epilogue of the router GEMM (one group, n_out = E <= 256): instead
-// of (or as well as, if C != null) storing the logits, the epilogue selects
-// each token's k experts, writes idx / w and one statistics partial per 32
-// tokens (same layout and meaning as launch_route_from_logits).
-constexpr int kRouteMaxK = 8;
-struct RouteEpilogue {
-  int32_t* idx;              // [N, k]; null: no routing epilogue
-  float* w;                  // [N, k]
-  float* psum_part;          // [ceil(N/32), E]
-  int32_t* cnt_part;         // [ceil(N/32), E]
-  const float* sel_bias;     // [E] (mode 2)
-  int mode;                  // MOE_ROUTE_*
-  int top_k;                 // 1..kRouteMaxK
-};
 struct TcProblem {
   const void* A;             // [a_rows, K] bf16 row-major
   int64_t a_rows;
@@ -121,7 +115,9 @@ struct TcProblem {
   // is row a_row_map[r] of A ([a_rows, K], e.g. the token rows x), for
   // r < offsets[n_groups].  null: A is already in grouped row order.
   const int32_t* a_row_map;
-  RouteEpilogue route;
+  // 1: run on CTA pairs (tcgen05 cta_group::2, 256-row tiles) where the
+  // problem allows it (plain or compact output, A not gathered)
+  int use_pairs;
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);

@@ -8,8 +8,9 @@
 //
 // One warp handles one token: lane l holds experts l, l+32, ... (EPL per
 // lane).  Each of the k rounds takes every lane's best remaining candidate
-// and reduces them across the warp with the total order (key desc, index
-// asc); lane 0's winner is authoritative.  Probabilities for the balance
+// and reduces them across the warp in the total order (key desc, index asc)
+// with two warp reductions (redux.sync): the largest key, then the lowest
+// index holding it.  Probabilities for the balance
 // statistic are accumulated per warp in registers and reduced across warps
 // in a fixed order, so the per-partial sums are deterministic.
 #include <climits>
@@ -45,33 +46,38 @@ __device__ __forceinline__ float sigmoid_f32_via_f64(float l) {
 __device__ __forceinline__ float sigmoid_fast(float l) { return 1.0f / (1.0f + expf(-l)); }
 constexpr float kSlack = 1.0f / 65536.0f;
 
-// One selection round: the lane holding the best remaining candidate (key
-// desc, index asc) among all lanes; returns its expert index (INT_MAX if
-// none is left).
+// Keys as unsigned integers in the same order (x < y  <=>  u(x) < u(y) for
+// non-NaN floats); -0 is folded onto +0 first, so the two tie as floats do.
+__device__ __forceinline__ uint32_t ordered(float k) {
+  const uint32_t b = __float_as_uint(k + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unordered(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// One selection round: the best remaining candidate of the warp in the total
+// order (key desc, index asc) -- a warp max of the keys, then a warp min of
+// the indices of the lanes holding that key (two redux.sync).  Returns the
+// expert index (INT_MAX if none is left) and its key.
 template <int EPL>
-__device__ __forceinline__ int warp_best(const float (&key)[EPL], const int (&slot)[EPL],
+__device__ __forceinline__ int warp_best(const uint32_t (&ok)[EPL], const int (&slot)[EPL],
                                          int lane, int E, float* best_key) {
-  float bk = -INFINITY;
+  uint32_t bk = 0u;
   int bi = INT_MAX;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    if (e < E && slot[i] < 0 && (bi == INT_MAX || key[i] > bk)) {
-      bk = key[i];
+    if (e < E && slot[i] < 0 && (bi == INT_MAX || ok[i] > bk)) {
+      bk = ok[i];
       bi = e;
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ok = __shfl_xor_sync(kFull, bk, off);
-    const int oi = __shfl_xor_sync(kFull, bi, off);
-    if (oi != INT_MAX && (bi == INT_MAX || ok > bk || (ok == bk && oi < bi))) {
-      bk = ok;
-      bi = oi;
-    }
-  }
-  *best_key = __shfl_sync(kFull, bk, 0);
-  return __shfl_sync(kFull, bi, 0);
+  const uint32_t kmax = __reduce_max_sync(kFull, bi == INT_MAX ? 0u : bk);
+  const uint32_t mine = (bi != INT_MAX && bk == kmax) ? (uint32_t)bi : 0xFFFFFFFFu;
+  const uint32_t emin = __reduce_min_sync(kFull, mine);
+  *best_key = unordered(kmax);
+  return emin == 0xFFFFFFFFu ? INT_MAX : (int)emin;
 }
 
 template <int EPL>
@@ -121,9 +127,12 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
         part += sa[i];
       }
       const float ssum = warp_sum_bcast(part);
+      uint32_t ok[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) ok[i] = ordered(key[i]);
       float kth = -INFINITY;
       for (int j = 0; j < top_k; ++j) {
-        const int bi = warp_best<EPL>(key, slot, lane, E, &kth);
+        const int bi = warp_best<EPL>(ok, slot, lane, E, &kth);
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
           if (lane + 32 * i == bi) slot[i] = j;
@@ -161,9 +170,12 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
 #pragma unroll
     for (int i = 0; i < EPL; ++i) ps[i] += (lane + 32 * i < E) ? p[i] : 0.f;
 
+    uint32_t ok[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) ok[i] = ordered(key[i]);
     for (int j = 0; j < top_k; ++j) {
       float bk;
-      const int bi = warp_best<EPL>(key, slot, lane, E, &bk);
+      const int bi = warp_best<EPL>(ok, slot, lane, E, &bk);
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
         if (lane + 32 * i == bi) slot[i] = j;
@@ -235,12 +247,19 @@ balance_finalize_kernel(const float* __restrict__ psum_part,
     s_last = atomicAdd(ticket, 1u) == (unsigned)(n_experts - 1);
   }
   __syncthreads();
-  if (s_last && tid == 0) {
+  if (s_last) {
+    // every block's term is visible (fence + ticket); load them all at
+    // once, then sum in expert order
     __threadfence();
-    double acc = 0.0;
-    for (int q = 0; q < n_experts; ++q) acc += ((volatile double*)terms)[q];
-    if (balance) balance[0] = n_tokens > 0 ? (float)((double)coef * acc) : 0.f;
-    *ticket = 0u;
+    for (int q = tid; q < n_experts; q += kFinThreads)
+      s_ps[q] = ((volatile double*)terms)[q];
+    __syncthreads();
+    if (tid == 0) {
+      double acc = 0.0;
+      for (int q = 0; q < n_experts; ++q) acc += s_ps[q];
+      if (balance) balance[0] = n_tokens > 0 ? (float)((double)coef * acc) : 0.f;
+      *ticket = 0u;
+    }
   }
 }
 
