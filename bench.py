@@ -140,6 +140,25 @@ def oracle_sample(shape, inputs, target_s=12.0, max_tokens=None):
     return n, elapsed
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings (ms) over all ranks of the default
+    process group (the slowest rank sets the job's time); identity when no
+    group is initialised.  Works on any backend (nccl on GPUs, gloo on CPU)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_rank, n_ranks, ms_step_max):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time
+    (independent replicas, weak scaling)."""
+    return tokens_per_rank * n_ranks / (ms_step_max * 1e-3)
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -230,11 +249,7 @@ def run_ours(args, shape, peaks, peaks_kind):
 
     stage_ms = {name: statistics.median(stage_times(name)) for name in stages}
     stage_mean = {name: sum(stage_times(name)) / args.steps for name in stages}
-    ms_step = total_ms / args.steps
-    if ws_n > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks([total_ms / args.steps], device=dev)[0]
 
     # the plain moe_forward call, eager and replayed from a CUDA graph
     barrier()
@@ -280,11 +295,7 @@ def run_ours(args, shape, peaks, peaks_kind):
         M.moe_forward_host(cfg, xh, weights, oh, fstats, ws)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if ws_n > 1:
-        tt = torch.tensor([e2e_ms, fwd_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms, fwd_ms = float(tt[0].item()), float(tt[1].item())
+    e2e_ms, fwd_ms = max_over_ranks([e0.elapsed_time(e1) / args.steps, fwd_ms], device=dev)
     err = M.moe_read_device_error(ws)
     if err != M.MOE_OK:
         raise RuntimeError(f"device error word set: {M.STATUS_NAMES.get(err, err)}")
@@ -337,7 +348,7 @@ def run_ours(args, shape, peaks, peaks_kind):
 
     res = {
         "metric": METRIC,
-        "value": round(N * ws_n / (ms_step * 1e-3), 1),
+        "value": round(job_tokens_per_s(N, ws_n, ms_step), 1),
         "unit": "tokens/s",
         "n_gpus": ws_n,
         "steps": args.steps,
@@ -363,7 +374,7 @@ def run_ours(args, shape, peaks, peaks_kind):
                        grouped_flop / (grouped_ms * 1e-3) / 1e12 / peak_tf, 4),
                    "stages": stage_report},
         "roofline": roofline,
-        "e2e": {"value": round(N * ws_n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(N, ws_n, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": N * d * es, "d2h_bytes_per_step": N * d * es,
                 "ms_per_step": round(e2e_ms, 4), "api": "moe_forward_host"},
         "gpu_launches": kernel_launches_per_step(shape) * args.steps,

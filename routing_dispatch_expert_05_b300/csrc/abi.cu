@@ -194,7 +194,7 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
   float* lg = logits ? logits : at<float>(ws, L.logits);
   float* psum = at<float>(ws, L.route_psum);
   int32_t* cnt = at<int32_t>(ws, L.route_cnt);
-  if (gemm && c.n_tokens < kRouterSmallTokens && c.d_model * elem_size(c) * 2 <= 48 * 1024) {
+  if (gemm && c.n_tokens < kRouterSmallTokens && c.d_model * elem_size(c) * 4 <= 48 * 1024) {
     // a few tokens: every expert's dot product at once on the CUDA cores
     launch_router_small(x, w.w_router, w.b_router, lg, c.n_tokens, c.n_experts, c.d_model,
                         c.dtype == MOE_BF16, st);

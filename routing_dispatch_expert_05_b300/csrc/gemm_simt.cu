@@ -173,13 +173,15 @@ void launch_typed(const GemmProblem& p, cudaStream_t st) {
 }
 
 // Router logits for a few tokens: logits[t, e] = sum_i x[t, i] W[e, i] (+ b[e]),
-// fp32 accumulation.  One CTA per kSmallTok tokens (staged in shared memory),
-// one thread per expert; each thread streams its router row in 16-byte
-// pieces.  With few tokens the tensor-core router runs one tile whose k-loop
-// is a serial chain; here every expert's dot product runs at once.
-constexpr int kSmallTok = 2;
+// fp32 accumulation.  A CTA takes kSmallTok tokens (staged in shared memory);
+// its warps walk the experts, lanes splitting d so that each router row is
+// read as whole 512-byte warp loads, and a warp reduction finishes each
+// (token, expert) sum.  With few tokens the tensor-core router is one tile
+// whose k-loop is a serial chain; here all experts proceed at once.
+constexpr int kSmallTok = 4;
+constexpr int kSmallWarps = 8;
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kSmallWarps * 32)
 router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* __restrict__ b,
                     float* __restrict__ logits, int64_t n_tokens, int n_experts, int d) {
   extern __shared__ __align__(16) uint8_t sx_raw[];
@@ -188,31 +190,39 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* _
   const int nt = (int)min((int64_t)kSmallTok, n_tokens - t0);
   constexpr int V = 16 / sizeof(T);                  // elements per 16 bytes
   const int nv = d / V;
-  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) {
+  for (int i = threadIdx.x; i < kSmallTok * nv; i += blockDim.x) {
     const int tt = i / nv, v = i - tt * nv;
-    reinterpret_cast<uint4*>(sx + (int64_t)tt * d)[v] =
-        reinterpret_cast<const uint4*>(x + (t0 + tt) * d)[v];
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (tt < nt) val = reinterpret_cast<const uint4*>(x + (t0 + tt) * d)[v];
+    reinterpret_cast<uint4*>(sx + (int64_t)tt * d)[v] = val;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < n_experts; e += kSmallWarps) {
     const uint4* wr = reinterpret_cast<const uint4*>(W + (int64_t)e * d);
     float acc[kSmallTok];
 #pragma unroll
     for (int tt = 0; tt < kSmallTok; ++tt) acc[tt] = 0.f;
-    for (int v = 0; v < nv; ++v) {
+    for (int v = lane; v < nv; v += 32) {
       const uint4 wv = __ldg(wr + v);
       const T* wp = reinterpret_cast<const T*>(&wv);
 #pragma unroll
       for (int tt = 0; tt < kSmallTok; ++tt) {
-        if (tt >= nt) break;
         const uint4 xv = reinterpret_cast<const uint4*>(sx + (int64_t)tt * d)[v];
         const T* xp = reinterpret_cast<const T*>(&xv);
 #pragma unroll
         for (int j = 0; j < V; ++j) acc[tt] = fmaf(to_f32(xp[j]), to_f32(wp[j]), acc[tt]);
       }
     }
-    const float bias = b ? to_f32(b[e]) : 0.f;
-    for (int tt = 0; tt < nt; ++tt) logits[(t0 + tt) * n_experts + e] = acc[tt] + bias;
+#pragma unroll
+    for (int tt = 0; tt < kSmallTok; ++tt)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
+    if (lane == 0) {
+      const float bias = b ? to_f32(b[e]) : 0.f;
+      for (int tt = 0; tt < nt; ++tt) logits[(t0 + tt) * n_experts + e] = acc[tt] + bias;
+    }
   }
 }
 
@@ -222,7 +232,7 @@ void launch_router_small(const void* x, const void* w, const void* b, float* log
                          int64_t n_tokens, int n_experts, int d, int is_bf16, cudaStream_t st) {
   if (n_tokens <= 0) return;
   const int blocks = (int)ceil_div64(n_tokens, kSmallTok);
-  const int threads = std::min(256, (n_experts + 31) / 32 * 32);
+  const int threads = kSmallWarps * 32;
   const size_t smem = (size_t)kSmallTok * d * (is_bf16 ? 2 : 4);
   if (is_bf16)
     router_small_kernel<bf16><<<blocks, threads, smem, st>>>(

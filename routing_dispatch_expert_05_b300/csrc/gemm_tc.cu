@@ -226,9 +226,19 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
         "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),            \
         "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
       : "r"(taddr))
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+// tcgen05.wait::ld, with the 32 destination registers of an outstanding load as
+// in/out operands: no use of them can be scheduled before the wait.
+#define MOE_TMEM_WAIT32(r)                                                          \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                     \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]),        \
+                 "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]),        \
+                 "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),   \
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),   \
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),   \
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),   \
+                 "+r"(r[30]), "+r"(r[31])                                           \
+               :                                                                    \
+               : "memory")
 
 // ---------------------------------------------------------------- tiles
 struct Tile {
@@ -292,50 +302,70 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The epilogues below read the accumulator in 32-column chunks; the load of
+// chunk c+1 is issued before chunk c is converted and stored, so its TMEM
+// latency overlaps that work (tcgen05.wait::ld then finds it complete).
+
 // Compact output of one tile, one pass over the accumulator: for each 32
 // columns of a row, the largest |v| picks a power of two 2^s that brings it
 // into [2^14, 2^15); v * 2^s (exact) is rounded once to fp16, and the biased
 // exponent of 2^-s (one byte, an E8 shared exponent) is stored beside it.
 // The warp takes half `half` of the tile's 256 columns (4 exponents).
+__device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, int lane,
+                                              int row_base, const bf16* bp, int ci, int c0,
+                                              const uint32_t (&r)[32], uint32_t* stg,
+                                              uint32_t& e8w) {
+  float v[32];
+  float mx = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = __uint_as_float(r[j]);
+    if (bp != nullptr && c0 + j < p.n_out) v[j] += __bfloat162float(bp[c0 + j]);
+    mx = fmaxf(mx, fabsf(v[j]));                   // columns past n_out hold 0
+  }
+  int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+  e = min(max(e, -100), 127);                      // zero / tiny blocks: bounded scale
+  const float scale = __uint_as_float((uint32_t)(127 + 14 - e) << 23);   // 2^(14-e)
+  e8w |= (uint32_t)(e + 113) << (8 * ci);                                // 2^(e-14)
+  uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgB16Stride);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    dst[j] = make_uint4(pack_half2(v[8 * j] * scale, v[8 * j + 1] * scale),
+                        pack_half2(v[8 * j + 2] * scale, v[8 * j + 3] * scale),
+                        pack_half2(v[8 * j + 4] * scale, v[8 * j + 5] * scale),
+                        pack_half2(v[8 * j + 6] * scale, v[8 * j + 7] * scale));
+  __syncwarp();
+  store_staged_b16(stg, lane, row_base, tl.row_end, c0, p.n_out, p.C);
+  __syncwarp();
+}
+
 __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, int lane, int half,
                                              int row_base, uint32_t tb, uint32_t* stg) {
+  constexpr int kCh = BN / 32 / 2;                 // chunks per half
   const int row = row_base + lane;
   const bf16* bp = p.bias ? p.bias + (int64_t)tl.g * p.bias_stride : nullptr;
+  const int ch0 = half * kCh;
   uint32_t e8w = 0u;                               // this row's 4 exponents
-#pragma unroll 1
-  for (int ci = 0; ci < BN / 32 / 2; ++ci) {
-    const int ch = half * (BN / 32 / 2) + ci;
-    const int c0 = tl.n * BN + ch * 32;
-    if (c0 >= p.n_out) break;                      // warp-uniform
-    uint32_t r[32];
-    MOE_TMEM_LD32(tb + ch * 32, r);
-    tmem_ld_wait();
-    float v[32];
-    float mx = 0.f;
+  uint32_t ra[32], rb[32];
+  MOE_TMEM_LD32(tb + ch0 * 32, ra);
+  MOE_TMEM_WAIT32(ra);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = __uint_as_float(r[j]);
-      if (bp != nullptr && c0 + j < p.n_out) v[j] += __bfloat162float(bp[c0 + j]);
-      mx = fmaxf(mx, fabsf(v[j]));                 // columns past n_out hold 0
+  for (int ci = 0; ci < kCh; ++ci) {
+    const int c0 = tl.n * BN + (ch0 + ci) * 32;
+    // chunk ci is in ra (even ci) or rb (odd ci); load the next one first
+    if (ci % 2 == 0) {
+      if (ci + 1 < kCh) MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, rb);
+      if (c0 < p.n_out) compact_chunk(p, tl, lane, row_base, bp, ci, c0, ra, stg, e8w);
+      if (ci + 1 < kCh) MOE_TMEM_WAIT32(rb);
+    } else {
+      if (ci + 1 < kCh) MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, ra);
+      if (c0 < p.n_out) compact_chunk(p, tl, lane, row_base, bp, ci, c0, rb, stg, e8w);
+      if (ci + 1 < kCh) MOE_TMEM_WAIT32(ra);
     }
-    int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
-    e = min(max(e, -100), 127);                    // zero / tiny blocks: bounded scale
-    const float scale = __uint_as_float((uint32_t)(127 + 14 - e) << 23);   // 2^(14-e)
-    e8w |= (uint32_t)(e + 113) << (8 * ci);                                // 2^(e-14)
-    uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgB16Stride);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      dst[j] = make_uint4(pack_half2(v[8 * j] * scale, v[8 * j + 1] * scale),
-                          pack_half2(v[8 * j + 2] * scale, v[8 * j + 3] * scale),
-                          pack_half2(v[8 * j + 4] * scale, v[8 * j + 5] * scale),
-                          pack_half2(v[8 * j + 6] * scale, v[8 * j + 7] * scale));
-    __syncwarp();
-    store_staged_b16(stg, lane, row_base, tl.row_end, c0, p.n_out, p.C);
-    __syncwarp();
   }
   if (row < tl.row_end) {
-    const int b0 = tl.n * (BN / 32) + half * (BN / 32 / 2);   // first exponent index
-    const int n4 = min(BN / 32 / 2, p.e8_cols - b0);
+    const int b0 = tl.n * (BN / 32) + half * kCh;  // first exponent index
+    const int n4 = min(kCh, p.e8_cols - b0);
     uint8_t* ep = p.c_e8 + (int64_t)row * p.e8_cols + b0;
     if (n4 == 4 && (reinterpret_cast<uintptr_t>(ep) & 3u) == 0) {
       *reinterpret_cast<uint32_t*>(ep) = e8w;
@@ -345,32 +375,102 @@ __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, in
   }
 }
 
+// One 32-column chunk of the plain output: v holds the values (activation
+// applied); stage them and write whole row segments.
+__device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int lane,
+                                            int row_base, int col0, const float (&v)[32],
+                                            float* stg_f, uint32_t* stg_w) {
+  if (p.c_is_f32) {
+    // two 16-column halves through the staging rows
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float4* dst = reinterpret_cast<float4*>(stg_f + lane * kStgF32Stride);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[j] = make_float4(v[16 * hh + 4 * j], v[16 * hh + 4 * j + 1],
+                             v[16 * hh + 4 * j + 2], v[16 * hh + 4 * j + 3]);
+      __syncwarp();
+      store_staged_f32(stg_f, lane, row_base, tl.row_end, col0 + 16 * hh, p.n_out,
+                       static_cast<float*>(p.C));
+      __syncwarp();
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(stg_w + lane * kStgB16Stride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                          pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                          pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                          pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    __syncwarp();
+    store_staged_b16(stg_w, lane, row_base, tl.row_end, col0, p.n_out, p.C);
+    __syncwarp();
+  }
+}
+
 // Plain output of one tile (bf16, or fp32 if c_is_f32): SwiGLU / SiLU+bias /
-// identity epilogue, staged per 32-row chunk for row-contiguous stores.  The
-// warp takes half `half` of the tile's output columns.
+// identity epilogue.  The warp takes half `half` of the tile's output columns.
 __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int lane, int half,
                                            int row_base, uint32_t tb, float* stg_f,
                                            uint32_t* stg_w) {
-  const int cols_tile = p.swiglu ? BN / 2 : BN;   // output columns per tile
-  const int nch = cols_tile / 32 / 2;              // chunks per half
-#pragma unroll 1
-  for (int ci = 0; ci < nch; ++ci) {
-    const int ch = half * nch + ci;
-    const int col0 = tl.n * cols_tile + ch * 32;
-    if (col0 >= p.n_out) break;                  // warp-uniform
-    float v[32];
-    if (p.swiglu) {
-      uint32_t g[32], u[32];
-      MOE_TMEM_LD32(tb + ch * 32, g);
-      MOE_TMEM_LD32(tb + BN / 2 + ch * 32, u);
-      tmem_ld_wait();
+  if (p.swiglu) {
+    // 128 output columns per tile: gate in accumulator columns 0..127, up in
+    // 128..255; two chunks per half
+    constexpr int kCh = BN / 2 / 32 / 2;
+    const int ch0 = half * kCh;
+    uint32_t ga[32], ua[32], gb[32], ub[32];
+    MOE_TMEM_LD32(tb + ch0 * 32, ga);
+    MOE_TMEM_LD32(tb + BN / 2 + ch0 * 32, ua);
+    MOE_TMEM_WAIT32(ga);
+    MOE_TMEM_WAIT32(ua);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-    } else {
-      uint32_t r[32];
-      MOE_TMEM_LD32(tb + ch * 32, r);
-      tmem_ld_wait();
+    for (int ci = 0; ci < kCh; ++ci) {
+      const int col0 = tl.n * (BN / 2) + (ch0 + ci) * 32;
+      const uint32_t(&g)[32] = ci % 2 == 0 ? ga : gb;
+      const uint32_t(&u)[32] = ci % 2 == 0 ? ua : ub;
+      if (ci + 1 < kCh) {
+        if (ci % 2 == 0) {
+          MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, gb);
+          MOE_TMEM_LD32(tb + BN / 2 + (ch0 + ci + 1) * 32, ub);
+        } else {
+          MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, ga);
+          MOE_TMEM_LD32(tb + BN / 2 + (ch0 + ci + 1) * 32, ua);
+        }
+      }
+      if (col0 < p.n_out) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+        store_chunk(p, tl, lane, row_base, col0, v, stg_f, stg_w);
+      }
+      if (ci + 1 < kCh) {
+        if (ci % 2 == 0) {
+          MOE_TMEM_WAIT32(gb);
+          MOE_TMEM_WAIT32(ub);
+        } else {
+          MOE_TMEM_WAIT32(ga);
+          MOE_TMEM_WAIT32(ua);
+        }
+      }
+    }
+    return;
+  }
+  constexpr int kCh = BN / 32 / 2;
+  const int ch0 = half * kCh;
+  uint32_t ra[32], rb[32];
+  MOE_TMEM_LD32(tb + ch0 * 32, ra);
+  MOE_TMEM_WAIT32(ra);
+#pragma unroll
+  for (int ci = 0; ci < kCh; ++ci) {
+    const int col0 = tl.n * BN + (ch0 + ci) * 32;
+    const uint32_t(&r)[32] = ci % 2 == 0 ? ra : rb;
+    if (ci + 1 < kCh) {
+      if (ci % 2 == 0) MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, rb);
+      else MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, ra);
+    }
+    if (col0 < p.n_out) {
+      float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
       if (p.bias) {
@@ -383,32 +483,11 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int 
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
       }
+      store_chunk(p, tl, lane, row_base, col0, v, stg_f, stg_w);
     }
-    if (p.c_is_f32) {
-      // two 16-column halves through the staging rows
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float4* dst = reinterpret_cast<float4*>(stg_f + lane * kStgF32Stride);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dst[j] = make_float4(v[16 * hh + 4 * j], v[16 * hh + 4 * j + 1],
-                               v[16 * hh + 4 * j + 2], v[16 * hh + 4 * j + 3]);
-        __syncwarp();
-        store_staged_f32(stg_f, lane, row_base, tl.row_end, col0 + 16 * hh, p.n_out,
-                         static_cast<float*>(p.C));
-        __syncwarp();
-      }
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(stg_w + lane * kStgB16Stride);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                            pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                            pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                            pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-      __syncwarp();
-      store_staged_b16(stg_w, lane, row_base, tl.row_end, col0, p.n_out, p.C);
-      __syncwarp();
+    if (ci + 1 < kCh) {
+      if (ci % 2 == 0) MOE_TMEM_WAIT32(rb);
+      else MOE_TMEM_WAIT32(ra);
     }
   }
 }

@@ -1,0 +1,57 @@
+"""The multi-GPU bookkeeping of bench.py on CPU ranks (gloo, world size 2).
+
+With several GPUs the layer runs as independent replicas (tokens are
+independent without a global capacity): the job's time is the slowest
+rank's and its throughput counts every rank's tokens.  These checks run the
+same helpers bench.py uses, over two gloo processes on this host.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank r reports step times (10 + r, 3 - r) ms
+    got = bench.max_over_ranks([10.0 + rank, 3.0 - rank])
+    dist.barrier()
+    out[rank] = got
+    dist.destroy_process_group()
+
+
+def test_slowest_rank_sets_the_time_over_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    assert res[0] == res[1] == [11.0, 3.0]
+
+
+def test_job_throughput_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.job_tokens_per_s(16384, 4, 2.0) == pytest.approx(16384 * 4 / 2e-3)
+    assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]     # no process group: identity
