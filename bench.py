@@ -46,6 +46,11 @@ if ROOT not in sys.path:
 from routing_dispatch_expert_05_b300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; grouped-GEMM % bf16 peak; routing % HBM BW"
+# DRAM bytes (read + write) of one launch of the up projection at full size,
+# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (one pass)
+# on the current kernel: 1.340 GB read + 0.196 GB written on the Qwen3-style
+# layer.  Reset to None whenever that kernel changes.
+UP_TRAFFIC_BYTES = {"qwen3_moe": 1.340e9 + 0.196e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
                   "bf16_tflops_sustained": 1400.0}
 
@@ -310,6 +315,8 @@ def run_ours(args, shape, peaks, peaks_kind):
     peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     achieved = up_flop / (up_ms * 1e-3) / 1e12
     traffic = args.up_traffic_bytes
+    if traffic is None:
+        traffic = UP_TRAFFIC_BYTES.get(shape.name)
     roofline = {"bound": "tensor", "kernel": "grouped expert up-projection (tcgen05)",
                 "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(achieved / peak_tf, 4),

@@ -313,8 +313,16 @@ MOE_API moe_status_t moe_forward_timed(const moe_config_t *cfg, const void *x,
 
 /* moe_forward for callers whose activations live in host memory: copies
  * x_host [N, d] into the workspace, runs the layer and copies the result to
- * out_host [N, d], all enqueued on `stream` (use page-locked host memory
- * for asynchronous copies).  Weights and stats are device memory. */
+ * out_host [N, d] (use page-locked host memory for asynchronous copies).
+ * Weights and stats are device memory.  The results equal moe_forward's.
+ *   - Without a capacity limit and with N >= 8192, the tokens are split into
+ *     up to four chunks (whole 32-token statistics groups) and the copies of
+ *     one chunk overlap the compute of another: the copies run on two
+ *     streams that the library creates, with some events, on the first such
+ *     call on each device (kept until exit); the compute runs on `stream`;
+ *     the statistics are reduced once over all chunks.  When the call
+ *     returns, all of it is ordered before later work on `stream`.
+ *   - Otherwise everything is enqueued on `stream` in order. */
 MOE_API moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_host,
                               const moe_weights_t *weights, void *out_host,
                               moe_stats_t *stats, void *ws, size_t ws_bytes,

@@ -3,6 +3,8 @@
 // moe_read_device_error, which waits to read one word back).
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <algorithm>
 
 #include "../../include/moe.h"
 #include "common.cuh"
@@ -70,6 +72,34 @@ Layout layout_of(const moe_config_t& c) {
   L.out_stage = take((size_t)N * d * es);
   L.total = o;
   return L;
+}
+
+// The scratch areas of a workspace laid out for config `c`.
+struct Scratch {
+  int32_t* err;
+  double* fin_terms;
+  unsigned* fin_ticket;
+  float* psum;         // router partials [route_parts, E]
+  int32_t* cnt;
+  int32_t* chunk_cnt;  // dispatch per-chunk histogram and bases
+  int32_t* chunk_base;
+  float* logits;
+  int route_parts;
+};
+
+Scratch scratch_of(const Layout& L, void* ws) {
+  char* b = static_cast<char*>(ws);
+  Scratch sc;
+  sc.err = reinterpret_cast<int32_t*>(b + L.err);
+  sc.fin_terms = reinterpret_cast<double*>(b + L.fin_terms);
+  sc.fin_ticket = reinterpret_cast<unsigned*>(b + L.fin_ticket);
+  sc.psum = reinterpret_cast<float*>(b + L.route_psum);
+  sc.cnt = reinterpret_cast<int32_t*>(b + L.route_cnt);
+  sc.chunk_cnt = reinterpret_cast<int32_t*>(b + L.chunk_cnt);
+  sc.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
+  sc.logits = reinterpret_cast<float*>(b + L.logits);
+  sc.route_parts = L.route_parts;
+  return sc;
 }
 
 moe_status_t check_config(const moe_config_t* c) {
@@ -187,13 +217,16 @@ moe_status_t zero_stats(const moe_config_t& c, moe_stats_t* s, cudaStream_t st) 
 }
 
 // ---- stage bodies (arguments already checked) -----------------------------
+// The router and the selection of c.n_tokens tokens.  Their statistics
+// partials go to partials part0.. of the scratch; with `finalize` the
+// counts and the balance statistic of those tokens are reduced into stats.
 void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
                  float* logits, int32_t* idx, float* wts, moe_stats_t* stats,
-                 void* ws, cudaStream_t st, bool gemm) {
-  const Layout L = layout_of(c);
-  float* lg = logits ? logits : at<float>(ws, L.logits);
-  float* psum = at<float>(ws, L.route_psum);
-  int32_t* cnt = at<int32_t>(ws, L.route_cnt);
+                 const Scratch& sc, cudaStream_t st, bool gemm, int64_t part0 = 0,
+                 bool finalize = true) {
+  float* lg = logits ? logits : sc.logits;
+  float* psum = sc.psum + part0 * c.n_experts;
+  int32_t* cnt = sc.cnt + part0 * c.n_experts;
   if (gemm && c.n_tokens < kRouterSmallTokens && c.d_model * elem_size(c) * 4 <= 48 * 1024) {
     // a few tokens: every expert's dot product at once on the CUDA cores
     launch_router_small(x, w.w_router, w.b_router, lg, c.n_tokens, c.n_experts, c.d_model,
@@ -222,7 +255,7 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     q.bias_stride = 0;
     q.C = lg;
     q.c_is_f32 = 1;
-    q.err = err_word(ws);
+    q.err = sc.err;
     if (tc_gemm_supported(q) && launch_tc_gemm(q, num_sms(), st)) gemm = false;
   }
   if (gemm) {
@@ -245,21 +278,19 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
   }
   launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route, w.sel_bias, idx,
                            wts, psum, cnt, st);
-  launch_balance_finalize(psum, cnt, L.route_parts, c.n_experts, c.n_tokens,
-                          c.balance_coef, stats ? stats->counts : nullptr,
-                          stats ? stats->balance : nullptr, at<double>(ws, L.fin_terms),
-                          at<unsigned>(ws, L.fin_ticket), st);
+  if (finalize)
+    launch_balance_finalize(psum, cnt, (int)ceil_div64(c.n_tokens, kRouteTokensPerPartial),
+                            c.n_experts, c.n_tokens, c.balance_coef,
+                            stats ? stats->counts : nullptr, stats ? stats->balance : nullptr,
+                            sc.fin_terms, sc.fin_ticket, st);
 }
 
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                    int32_t* offsets, int32_t* ros, int32_t* tor, void* x_perm,
-                   moe_stats_t* stats, void* ws, cudaStream_t st) {
-  const Layout L = layout_of(c);
-  launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c),
-                  at<int32_t>(ws, L.chunk_cnt), at<int32_t>(ws, L.chunk_base),
-                  offsets, ros, tor, stats ? stats->counts : nullptr,
-                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr,
-                  at<int32_t>(ws, L.err), st);
+                   moe_stats_t* stats, const Scratch& sc, cudaStream_t st) {
+  launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c), sc.chunk_cnt,
+                  sc.chunk_base, offsets, ros, tor, stats ? stats->counts : nullptr,
+                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st);
   if (x_perm != nullptr)
     launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
                        c.n_tokens * c.top_k, x_perm, num_sms(), st);
@@ -483,7 +514,7 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x,
   if (c.n_tokens == 0) return zero_stats(c, stats, st);
   MOE_TRY(need({x, idx, w}));
   MOE_TRY(maybe({logits}));
-  router_body(c, x, *weights, logits, idx, w, stats, ws, st, true);
+  router_body(c, x, *weights, logits, idx, w, stats, scratch_of(layout_of(c), ws), st, true);
   return last_cuda();
 }
 
@@ -501,7 +532,8 @@ moe_status_t moe_route_logits(const moe_config_t* cfg, const float* logits,
   MOE_TRY(need({logits, idx, w}));
   moe_weights_t wt{};
   wt.sel_bias = sel_bias;
-  router_body(c, nullptr, wt, const_cast<float*>(logits), idx, w, stats, ws, st, false);
+  router_body(c, nullptr, wt, const_cast<float*>(logits), idx, w, stats,
+              scratch_of(layout_of(c), ws), st, false);
   return last_cuda();
 }
 
@@ -525,7 +557,8 @@ moe_status_t moe_dispatch_permute(const moe_config_t* cfg, const int32_t* idx,
   // x and x_perm: both present (rows are gathered) or both NULL (no gather)
   if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(maybe({x, x_perm}));
-  dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats, ws, st);
+  dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats,
+                scratch_of(layout_of(c), ws), st);
   return last_cuda();
 }
 
@@ -626,21 +659,15 @@ namespace {
 // The whole layer; ev (if not null) receives kForwardEvents events: the
 // start, then one after each stage (router, dispatch, up, down, shared,
 // combine -- "shared" coincides with "down" when there is none).
-moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
-                          const moe_weights_t* weights, void* out, moe_stats_t* stats,
-                          void* ws, size_t ws_bytes, void* stream, cudaEvent_t const* ev) {
-  MOE_TRY(check_config(cfg));
-  const moe_config_t& c = *cfg;
-  MOE_TRY(check_router_weights(c, weights));
-  MOE_TRY(check_up_weights(c, weights));
-  MOE_TRY(check_down_weights(c, weights));
-  MOE_TRY(check_shared_weights(c, weights));
-  MOE_TRY(check_stats(stats));
-  const Layout L = layout_of(c);
-  MOE_TRY(check_ws(ws, ws_bytes, L.total));
-  auto st = static_cast<cudaStream_t>(stream);
-  if (c.n_tokens == 0) return zero_stats(c, stats, st);
-  MOE_TRY(need({x, out}));
+// The whole layer for the n_tokens of `c`, on stream st, with buffers from
+// the workspace layout L (laid out for at least c.n_tokens tokens) and its
+// scratch sc.  Router partials go to part0..; with `finalize` the counts and
+// balance statistic are reduced into stats (else only kept/dropped are set).
+// ev (if not null) receives MOE_FORWARD_EVENTS events around the stages.
+moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch& sc,
+                          int64_t part0, bool finalize, const void* x,
+                          const moe_weights_t& w, void* out, moe_stats_t* stats, void* ws,
+                          cudaStream_t st, cudaEvent_t const* ev) {
   int32_t* idx = at<int32_t>(ws, L.idx);
   float* wts = at<float>(ws, L.w);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
@@ -661,7 +688,7 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
     if (ev != nullptr) cudaEventRecord(ev[i], st);
   };
   mark(0);
-  router_body(c, x, *weights, nullptr, idx, wts, &rs, ws, st, true);
+  router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true, part0, finalize);
   mark(1);
   moe_stats_t ds{};
   if (stats) {
@@ -671,23 +698,20 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
   // the expert-sorted copy of the token rows is written once and read by
   // the up projection as whole 128-row TMA boxes (a per-row gather inside
   // the GEMM -- moe_expert_up_gather -- saves that memory, not time)
-  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, ws, st);
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, sc, st);
   mark(2);
-  MOE_TRY(up_body(c, x_perm, nullptr, offsets, *weights, h, err_word(ws), st));
+  MOE_TRY(up_body(c, x_perm, nullptr, offsets, w, h, sc.err, st));
   mark(3);
   // bf16 layers keep the expert outputs compact (half the bytes of fp32)
   uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
-  moe_status_t ds_ = c.dtype == MOE_BF16
-                         ? down_body(c, h, offsets, *weights, y, y_e8, err_word(ws), st)
-                         : MOE_ERR_UNSUPPORTED;
+  moe_status_t ds_ = c.dtype == MOE_BF16 ? down_body(c, h, offsets, w, y, y_e8, sc.err, st)
+                                         : MOE_ERR_UNSUPPORTED;
   const bool compact = ds_ == MOE_OK;
-  if (ds_ == MOE_ERR_UNSUPPORTED)
-    ds_ = down_body(c, h, offsets, *weights, y, nullptr, err_word(ws), st);
+  if (ds_ == MOE_ERR_UNSUPPORTED) ds_ = down_body(c, h, offsets, w, y, nullptr, sc.err, st);
   MOE_TRY(ds_);
   mark(4);
   if (c.n_shared > 0)
-    MOE_TRY(shared_body(c, x, *weights, at<char>(ws, L.h_shared), shared_out,
-                        err_word(ws), st));
+    MOE_TRY(shared_body(c, x, w, at<char>(ws, L.h_shared), shared_out, sc.err, st));
   mark(5);
   if (compact)
     launch_combine_compact(y, y_e8, ros, wts, shared_out, out, c.n_tokens, c.top_k,
@@ -698,6 +722,124 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
   mark(6);
   return last_cuda();
 }
+
+moe_status_t check_forward_args(const moe_config_t* cfg, const moe_weights_t* weights,
+                                moe_stats_t* stats, void* ws, size_t ws_bytes) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_router_weights(c, weights));
+  MOE_TRY(check_up_weights(c, weights));
+  MOE_TRY(check_down_weights(c, weights));
+  MOE_TRY(check_shared_weights(c, weights));
+  MOE_TRY(check_stats(stats));
+  return check_ws(ws, ws_bytes, layout_of(c).total);
+}
+
+moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
+                          const moe_weights_t* weights, void* out, moe_stats_t* stats,
+                          void* ws, size_t ws_bytes, void* stream, cudaEvent_t const* ev) {
+  MOE_TRY(check_forward_args(cfg, weights, stats, ws, ws_bytes));
+  const moe_config_t& c = *cfg;
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) return zero_stats(c, stats, st);
+  MOE_TRY(need({x, out}));
+  const Layout L = layout_of(c);
+  return forward_core(c, L, scratch_of(L, ws), 0, true, x, *weights, out, stats, ws, st, ev);
+}
+
+// ---- the host-buffer forward, pipelined over token chunks ------------------
+// Without a capacity limit every token's output depends on that token alone,
+// so moe_forward_host can split the tokens into chunks and overlap the copy
+// of chunk i+1 to the device and of chunk i-1 back with the compute of chunk
+// i.  The copies run on two streams of the library's own (created once per
+// device); the compute runs on the caller's stream, in chunk order, and the
+// statistics are reduced once over all chunks' partials -- the same results,
+// bit for bit, as one moe_forward over all tokens.
+constexpr int kHostChunks = 4;
+constexpr int64_t kHostChunkMin = 4096;     // smaller chunks re-stream the weights too often
+constexpr int kMaxDevices = 64;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, in[kHostChunks] = {}, done[kHostChunks] = {}, out_done = nullptr;
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+// the current device's pipeline objects, created on its first use (lock held)
+HostPipe* host_pipe() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostPipe& hp = g_pipe[dev];
+  if (hp.ready) return &hp;
+  bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.out_done, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kHostChunks; ++i)
+    ok = cudaEventCreateWithFlags(&hp.in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  hp.ready = true;
+  return &hp;
+}
+
+moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
+                                    const moe_weights_t& w, char* oh, moe_stats_t* stats,
+                                    void* ws, cudaStream_t st, HostPipe& hp) {
+  const Layout L = layout_of(c);
+  const Scratch sc = scratch_of(L, ws);
+  const size_t row = (size_t)c.d_model * elem_size(c);
+  char* xd = at<char>(ws, L.x_stage);
+  char* od = at<char>(ws, L.out_stage);
+  const int nch = (int)std::min<int64_t>(kHostChunks, c.n_tokens / kHostChunkMin);
+  // chunk starts on a statistics-partial boundary
+  const int64_t chunk =
+      ceil_div64(ceil_div64(c.n_tokens, nch), kRouteTokensPerPartial) * kRouteTokensPerPartial;
+  bool ok = cudaEventRecord(hp.start, st) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess;
+  moe_stats_t none{};
+  for (int i = 0; ok && i < nch; ++i) {
+    const int64_t s0 = (int64_t)i * chunk;
+    const int64_t n = std::min(chunk, c.n_tokens - s0);
+    if (n <= 0) break;
+    ok = cudaMemcpyAsync(xd + s0 * row, xh + s0 * row, n * row, cudaMemcpyHostToDevice,
+                         hp.h2d) == cudaSuccess &&
+         cudaEventRecord(hp.in[i], hp.h2d) == cudaSuccess &&
+         cudaStreamWaitEvent(st, hp.in[i], 0) == cudaSuccess;
+    if (!ok) break;
+    moe_config_t ci = c;
+    ci.n_tokens = n;
+    MOE_TRY(forward_core(ci, L, sc, s0 / kRouteTokensPerPartial, false, xd + s0 * row, w,
+                         od + s0 * row, &none, ws, st, nullptr));
+    ok = cudaEventRecord(hp.done[i], st) == cudaSuccess &&
+         cudaStreamWaitEvent(hp.d2h, hp.done[i], 0) == cudaSuccess &&
+         cudaMemcpyAsync(oh + s0 * row, od + s0 * row, n * row, cudaMemcpyDeviceToHost,
+                         hp.d2h) == cudaSuccess;
+  }
+  if (ok && stats != nullptr) {
+    // all chunks' partials at once: counts and the balance statistic; no
+    // capacity, so every selection is kept
+    int32_t* counts = stats->counts ? stats->counts : stats->kept;
+    launch_balance_finalize(sc.psum, sc.cnt, sc.route_parts, c.n_experts, c.n_tokens,
+                            c.balance_coef, counts, stats->balance, sc.fin_terms,
+                            sc.fin_ticket, st);
+    const size_t eb = (size_t)c.n_experts * 4;
+    if (stats->kept && counts != stats->kept)
+      ok = cudaMemcpyAsync(stats->kept, counts, eb, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+    if (ok && stats->dropped) ok = cudaMemsetAsync(stats->dropped, 0, eb, st) == cudaSuccess;
+  }
+  // the caller's stream completes with the last copy back
+  ok = ok && cudaEventRecord(hp.out_done, hp.d2h) == cudaSuccess &&
+       cudaStreamWaitEvent(st, hp.out_done, 0) == cudaSuccess;
+  return ok ? last_cuda() : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -725,13 +867,19 @@ moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host,
                               const moe_weights_t* weights, void* out_host,
                               moe_stats_t* stats, void* ws, size_t ws_bytes,
                               void* stream) {
-  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_forward_args(cfg, weights, stats, ws, ws_bytes));
   const moe_config_t& c = *cfg;
   const Layout L = layout_of(c);
-  MOE_TRY(check_ws(ws, ws_bytes, L.total));
   if (c.n_tokens > 0 && (x_host == nullptr || out_host == nullptr))
     return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);
+  if (capacity_of(c) < 0 && c.n_tokens >= 2 * kHostChunkMin) {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* hp = host_pipe();
+    if (hp != nullptr)
+      return forward_host_pipelined(c, static_cast<const char*>(x_host), *weights,
+                                    static_cast<char*>(out_host), stats, ws, st, *hp);
+  }
   const size_t bytes = (size_t)c.n_tokens * c.d_model * elem_size(c);
   void* xd = at<char>(ws, L.x_stage);
   void* od = at<char>(ws, L.out_stage);

@@ -66,6 +66,22 @@ __device__ __forceinline__ uint4 ld_vec16_nc(const void* p) {
                : "l"(p));
   return r;
 }
+// 32-byte vectors (256-bit global loads / stores)
+struct Vec32 {
+  uint32_t v[8];
+};
+__device__ __forceinline__ void ld_vec32_nc(const void* p, Vec32& r) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]),
+                 "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_vec32(void* p, const Vec32& r) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r.v[0]),
+               "r"(r.v[1]), "r"(r.v[2]), "r"(r.v[3]), "r"(r.v[4]), "r"(r.v[5]), "r"(r.v[6]),
+               "r"(r.v[7])
+               : "memory");
+}
 __device__ __forceinline__ void st_vec16(void* p, uint4 v) {
   *reinterpret_cast<uint4*>(p) = v;
 }

@@ -444,6 +444,26 @@ def test_forward_host_matches_forward():
     assert torch.equal(oh, out.cpu())
 
 
+def test_forward_host_pipelined_matches_forward():
+    """Without a capacity, moe_forward_host splits the tokens into chunks and
+    overlaps the host copies with the compute; the output and every
+    statistic equal one moe_forward over all tokens, bit for bit."""
+    inp = inputs_for("qwen3_moe", 12288 + 96)        # three chunks, ragged tail
+    D = Device(inp)
+    shape = inp.shape
+    out, st = _forward(D)
+    xh = D.t["x"].cpu().pin_memory()
+    oh = torch.full((shape.n_tokens, shape.d_model), 7.0, dtype=D.tdtype).pin_memory()
+    st2, sts2 = D.stats()
+    for _ in range(2):                                  # twice: the pipeline is reused
+        M.moe_forward_host(D.cfg, xh, D.weights, oh, sts2, D.ws)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, out.cpu())
+        for name in ("counts", "kept", "dropped", "balance"):
+            assert torch.equal(st2[name], st[name]), name
+    assert D.device_error() == M.MOE_OK
+
+
 def test_forward_timed_matches_forward():
     """The instrumented entry point makes the same launches: identical output
     and statistics, and its events bracket every stage in order."""
