@@ -328,6 +328,24 @@ MOE_API moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_hos
                               moe_stats_t *stats, void *ws, size_t ws_bytes,
                               void *stream);
 
+/* ---- between steps ------------------------------------------------------ */
+
+/* Balancing-bias update and load diagnostic ("DeepSeek 5.7", section 2: a
+ * non-gradient balancing bias added to the selection keys; its study lab
+ * plots expert load before and after bias updates, and its implementation
+ * plan asks for a coefficient-of-variation diagnostic).  The pages do not
+ * state the update; this is the plainest rule they admit:
+ *   sel_bias[e] <- sel_bias[e] + gamma * sign(mean load - counts[e])
+ * (one fp32 add per expert; the sign compares E * counts[e] with the total
+ * on integers, so an expert exactly at the mean keeps its bias), and
+ *   *load_cv = population std(counts) / mean(counts)   (0 if all are 0).
+ * counts [E] int32 (device, e.g. stats.counts of a forward); sel_bias [E]
+ * fp32 updated in place (device, nullable); load_cv [1] fp32 (device,
+ * nullable, not both NULL).  Enqueued on `stream`. */
+MOE_API moe_status_t moe_update_selection_bias(const moe_config_t *cfg,
+                                       const int32_t *counts, float *sel_bias,
+                                       float gamma, float *load_cv, void *stream);
+
 /* ---- diagnostics -------------------------------------------------------- */
 
 /* Waits for `stream`, then reads and clears the device error word at the

@@ -354,6 +354,39 @@ def balance_statistic(counts, p, n_tokens: int, coef: float) -> float:
 
 
 # --------------------------------------------------------------------------
+# between steps: the selection-bias update and the load diagnostic
+# --------------------------------------------------------------------------
+def selection_bias_update(sel_bias, counts, gamma: float) -> np.ndarray:
+    """b_e <- b_e + gamma * sign(mean load - load_e), in fp32.
+
+    DSEEK s.2 adds a non-gradient balancing bias to the selection keys, and
+    its study lab shows the per-expert load changing as that bias is
+    updated; the pages do not state the update.  This is the plainest rule consistent
+    with them (a reading, not a page's formula): an expert above the mean
+    load is made less attractive by gamma, one below it more, one exactly
+    at the mean is left alone.  The sign is decided on integers
+    (E * load_e against the total) and the add is one fp32 add.
+    """
+    counts = np.asarray(counts, np.int64)
+    b = np.asarray(sel_bias, np.float32)
+    total = int(counts.sum())
+    e = counts.shape[0]
+    sign = np.sign(total - e * counts).astype(np.float32)   # +1 below the mean
+    return (b + np.float32(gamma) * sign).astype(np.float32)
+
+
+def load_cv(counts) -> float:
+    """Coefficient of variation of the per-expert load: population standard
+    deviation over the mean (DSEEK implementation plan, which asks for this
+    statistic as a diagnostic of the load); 0 when nothing was routed."""
+    c = np.asarray(counts, np.float64)
+    m = c.mean() if c.size else 0.0
+    if m == 0.0:
+        return 0.0
+    return float(np.sqrt(np.mean((c - m) ** 2)) / m)
+
+
+# --------------------------------------------------------------------------
 # the whole layer
 # --------------------------------------------------------------------------
 def forward(shape, values: dict) -> dict:

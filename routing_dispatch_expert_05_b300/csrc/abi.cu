@@ -891,6 +891,21 @@ moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host,
   return MOE_OK;
 }
 
+moe_status_t moe_update_selection_bias(const moe_config_t* cfg, const int32_t* counts,
+                                       float* sel_bias, float gamma, float* load_cv,
+                                       void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (!std::isfinite(gamma)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need({counts}));
+  if (sel_bias == nullptr && load_cv == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((sel_bias != nullptr && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) ||
+      (load_cv != nullptr && (reinterpret_cast<uintptr_t>(load_cv) & 3u)))
+    return MOE_ERR_INVALID_ARG;
+  launch_bias_update(counts, cfg->n_experts, gamma, sel_bias, load_cv,
+                     static_cast<cudaStream_t>(stream));
+  return last_cuda();
+}
+
 moe_status_t moe_read_device_error(void* ws, int32_t* code, void* stream) {
   if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);

@@ -92,6 +92,9 @@ struct Params {
   int c_is_f32;
   uint8_t* c_e8;              // compact fp16 output: per (row, 32 columns) exponent
   int e8_cols;                // ceil(n_out / 32)
+  int mma_n;                  // MMA N / B rows per tile (single CTA, no SwiGLU):
+                              // 256, or n_out rounded up to 16 when a single n-tile
+                              // is narrower (the router: N = E)
   int32_t* err;
   const int32_t* a_row_map;   // null: A rows are the tile rows; else A row r
                               // is row a_row_map[r] of the A tensor
@@ -603,7 +606,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (!good) { ok = false; break; }
           uint8_t* a = sA + stage * kTileA;
           if (lane == 0) {
-            mbar_expect_tx(&full[stage], kStageBytes);
+            mbar_expect_tx(&full[stage], kTileA + (uint32_t)p.mma_n * BK * 2);
             uint8_t* b = sB + stage * kTileB;
             if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
             if (p.swiglu) {
@@ -645,7 +648,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      const uint32_t idesc = idesc_bf16(BM, p.mma_n);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -1085,6 +1088,8 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.c_is_f32 = q.c_is_f32;
   p.c_e8 = q.c_e8;
   p.e8_cols = q.e8_cols;
+  // a single n-tile narrower than 256 columns multiplies only its own width
+  p.mma_n = (!q.swiglu && q.n_out < BN) ? (q.n_out + 15) / 16 * 16 : BN;
   p.err = q.err;
   p.a_row_map = q.a_row_map;
   const int ksub = p.k_sub;
@@ -1099,7 +1104,7 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
       return make_map(mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2) &&
              make_map(mb1, q.B1, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2);
     if (!make_map(mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2,
-                  pair_tiles ? BN / 2 : BN))
+                  pair_tiles ? BN / 2 : (uint32_t)p.mma_n))
       return false;
     *mb1 = *mb0;
     return true;

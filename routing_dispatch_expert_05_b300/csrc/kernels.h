@@ -30,6 +30,11 @@ void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
                              float coef, int32_t* counts, float* balance,
                              double* terms, unsigned* ticket, cudaStream_t st);
 
+// between steps: selection-bias update from the per-expert counts and the
+// load's coefficient of variation (either output nullable)
+void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float* sel_bias,
+                        float* load_cv, cudaStream_t st);
+
 // ---- dispatch -------------------------------------------------------------
 void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int n_experts, int64_t capacity /* <0: none */,

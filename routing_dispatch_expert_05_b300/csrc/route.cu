@@ -81,7 +81,7 @@ __device__ __forceinline__ int warp_best(const uint32_t (&ok)[EPL], const int (&
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 4 : 2)
 route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
              int top_k, int mode, const float* __restrict__ sel_bias,
              int32_t* __restrict__ idx, float* __restrict__ w,
@@ -263,7 +263,46 @@ balance_finalize_kernel(const float* __restrict__ psum_part,
   }
 }
 
+// Between steps: b_e <- b_e + gamma * sign(mean load - load_e) (one fp32
+// add; the sign compares E * load_e with the total on integers) and the
+// load's coefficient of variation (population std / mean, 0 if nothing was
+// routed).  One block, thread e = expert e; the sums run in a fixed order.
+__global__ void __launch_bounds__(kMaxExperts)
+bias_update_kernel(const int32_t* __restrict__ counts, int n_experts, float gamma,
+                   float* __restrict__ sel_bias, float* __restrict__ load_cv) {
+  __shared__ long long s_total;
+  __shared__ double s_dev[kMaxExperts];
+  const int e = threadIdx.x;
+  if (e == 0) {
+    long long t = 0;
+    for (int q = 0; q < n_experts; ++q) t += counts[q];
+    s_total = t;
+  }
+  __syncthreads();
+  const long long total = s_total;
+  const double mean = (double)total / n_experts;
+  if (e < n_experts) {
+    const long long c = counts[e];
+    const long long diff = total - (long long)n_experts * c;
+    const float sgn = diff > 0 ? 1.f : (diff < 0 ? -1.f : 0.f);
+    if (sel_bias != nullptr) sel_bias[e] = __fadd_rn(sel_bias[e], gamma * sgn);
+    const double dv = (double)c - mean;
+    s_dev[e] = dv * dv;
+  }
+  __syncthreads();
+  if (e == 0 && load_cv != nullptr) {
+    double acc = 0.0;
+    for (int q = 0; q < n_experts; ++q) acc += s_dev[q];
+    load_cv[0] = total > 0 ? (float)(sqrt(acc / n_experts) / mean) : 0.f;
+  }
+}
+
 }  // namespace
+
+void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float* sel_bias,
+                        float* load_cv, cudaStream_t st) {
+  bias_update_kernel<<<1, kMaxExperts, 0, st>>>(counts, n_experts, gamma, sel_bias, load_cv);
+}
 
 void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_experts,
                               int top_k, int mode, const float* sel_bias,

@@ -32,7 +32,7 @@ EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_dispatch_permute_noalloc", "moe_expert_up",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_timed", "moe_forward_host",
-            "moe_read_device_error",
+            "moe_update_selection_bias", "moe_read_device_error",
             "moe_status_string", "moe_version")
 
 
@@ -95,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_host": [cfgp, vp, wp, vp, sp, vp, sz, vp],
         "moe_forward_timed": [cfgp, vp, wp, vp, sp, vp, sz, vp, P(vp), ctypes.c_int32],
         "moe_read_device_error": [vp, P(ctypes.c_int32), vp],
+        "moe_update_selection_bias": [cfgp, vp, vp, ctypes.c_float, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -297,6 +298,15 @@ def moe_forward_host(cfg, x_host, weights: MoEWeights, out_host, stats, ws,
         ctypes.byref(cfg), ptr(x_host), ctypes.byref(weights), ptr(out_host),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_forward_host")
+
+
+def moe_update_selection_bias(cfg, counts, sel_bias, gamma, load_cv=None, stream=None):
+    """sel_bias += gamma * sign(mean load - counts) (in place) and the load's
+    coefficient of variation into load_cv; both tensors may be None (not
+    both)."""
+    _check(load_library().moe_update_selection_bias(
+        ctypes.byref(cfg), ptr(counts), ptr(sel_bias), float(gamma), ptr(load_cv),
+        _stream(stream)), "moe_update_selection_bias")
 
 
 def moe_read_device_error(ws, stream=None) -> int:

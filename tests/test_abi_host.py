@@ -139,3 +139,16 @@ def test_forward_timed_rejects_a_wrong_event_count(lib):
     st = lib.moe_forward_timed(ctypes.byref(cfg), None, ctypes.byref(w), None, None,
                                None, 0, None, None, M.MOE_FORWARD_EVENTS)
     assert st == M.MOE_ERR_INVALID_ARG
+
+
+def test_bias_update_rejects_bad_arguments(lib):
+    cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
+    buf = ctypes.create_string_buffer(4096)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    f = lib.moe_update_selection_bias
+    assert f(ctypes.byref(cfg), None, addr, 1e-3, addr, None) == M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(cfg), addr, None, 1e-3, None, None) == M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(cfg), addr, addr, float("nan"), addr, None) == M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(cfg), addr, addr + 2, 1e-3, None, None) == M.MOE_ERR_INVALID_ARG
+    bad = _bad(n_experts=0)
+    assert f(ctypes.byref(bad), addr, addr, 1e-3, addr, None) == M.MOE_ERR_INVALID_ARG

@@ -532,3 +532,68 @@ def test_forward_full_size_sampled(name):
     cnt = to_np(st["counts"])
     assert cnt.sum() == shape.n_tokens * shape.top_k
     assert D.device_error() == M.MOE_OK
+
+
+# ------------------------------------------- between steps: bias update
+@pytest.mark.parametrize("E", [1, 3, 8, 64, 128, 256])
+@pytest.mark.parametrize("gamma", [1e-3, 0.37])
+def test_selection_bias_update_bit_exact(E, gamma):
+    rng = np.random.default_rng(1000 + E)
+    counts = rng.integers(0, 50, E).astype(np.int32)
+    if E >= 3:
+        counts[:3] = 0                     # idle experts
+        counts[-1] = counts.sum() // E     # may sit exactly at the mean
+    bias = rng.standard_normal(E).astype(np.float32)
+    bias[0] = -0.0
+    shape = _cfg(n_experts=E, top_k=1)
+    cfg = M.make_config(shape)
+    dc = torch.from_numpy(counts).cuda()
+    db = torch.from_numpy(bias.copy()).cuda()
+    cv = torch.full((1,), -1.0, device="cuda")
+    for step in range(2):                  # two updates in a row
+        M.moe_update_selection_bias(cfg, dc, db, gamma, cv)
+        bias = O.selection_bias_update(bias, counts, gamma)
+        torch.cuda.synchronize()
+        got = db.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), bias.view(np.uint32)), step
+        ref_cv = O.load_cv(counts)
+        assert abs(float(to_np(cv)[0]) - ref_cv) <= 1e-6 * max(ref_cv, 1e-30)
+
+
+def test_selection_bias_update_degenerate_loads():
+    E = 16
+    cfg = M.make_config(_cfg(n_experts=E, top_k=1))
+    bias = torch.linspace(-1, 1, E, device="cuda")
+    before = bias.clone()
+    cv = torch.full((1,), -1.0, device="cuda")
+    # nothing routed: every expert sits at the mean, CV 0
+    M.moe_update_selection_bias(cfg, torch.zeros(E, dtype=torch.int32, device="cuda"),
+                                bias, 0.5, cv)
+    torch.cuda.synchronize()
+    assert torch.equal(bias, before) and float(cv[0]) == 0.0
+    # perfectly balanced: same
+    M.moe_update_selection_bias(cfg, torch.full((E,), 7, dtype=torch.int32, device="cuda"),
+                                bias, 0.5, cv)
+    torch.cuda.synchronize()
+    assert torch.equal(bias, before) and float(cv[0]) == 0.0
+    # everything on one expert: CV = sqrt(E - 1); only load_cv requested
+    c = torch.zeros(E, dtype=torch.int32, device="cuda")
+    c[5] = 1000
+    M.moe_update_selection_bias(cfg, c, None, 0.5, cv)
+    torch.cuda.synchronize()
+    assert abs(float(cv[0]) - (E - 1) ** 0.5) <= 1e-6 * (E - 1) ** 0.5
+
+
+def test_selection_bias_update_from_forward_counts():
+    """The counts a sigmoid-bias forward reports feed the update directly."""
+    inp = inputs_for("deepseek_v3_block", 256)
+    D = Device(inp)
+    _, st = _forward(D)
+    shape = inp.shape
+    cfg = M.make_config(shape)
+    bias0 = inp.values["sel_bias"].astype(np.float32)
+    db = torch.from_numpy(bias0.copy()).cuda()
+    M.moe_update_selection_bias(cfg, st["counts"], db, 1e-3, None)
+    torch.cuda.synchronize()
+    ref = O.selection_bias_update(bias0, to_np(st["counts"]), 1e-3)
+    assert np.array_equal(db.cpu().numpy().view(np.uint32), ref.view(np.uint32))

@@ -449,3 +449,38 @@ def test_forward_tokens_matches_forward():
     part = O.forward_tokens(shape, v, [0, 5, 11])
     assert np.array_equal(part["idx"], full["idx"][[0, 5, 11]])
     assert np.allclose(part["out"], full["out"][[0, 5, 11]], rtol=0, atol=1e-2)
+
+
+# ---------------------------------------------- selection-bias update, CV
+def test_bias_update_moves_against_the_load():
+    """Over-loaded experts lose gamma, under-loaded gain it, one at the mean
+    keeps its bias (mean of (6, 2, 4, 4) is 4)."""
+    b = np.array([0.5, -0.25, 0.0, 0.125], np.float32)
+    got = O.selection_bias_update(b, [6, 2, 4, 4], 0.01)
+    g = np.float32(0.01)
+    assert got.dtype == np.float32
+    assert got[0] == np.float32(0.5) - g and got[1] == np.float32(-0.25) + g
+    assert got[2] == np.float32(0.0) and got[3] == np.float32(0.125)
+
+
+def test_bias_update_fixed_points():
+    b = np.random.default_rng(0).uniform(-0.1, 0.1, 16).astype(np.float32)
+    assert np.array_equal(O.selection_bias_update(b, np.full(16, 7), 0.5), b)   # balanced
+    assert np.array_equal(O.selection_bias_update(b, np.zeros(16, int), 0.5), b)  # nothing routed
+    assert np.array_equal(O.selection_bias_update(b, [3] * 16, 0.0), b)
+
+
+def test_bias_update_sign_decided_exactly():
+    # mean load 10/3 is not a float; the sign compares E * load with the
+    # total on integers: 9 < 10 (below), 12 > 10 (above)
+    got = O.selection_bias_update(np.zeros(3, np.float32), [3, 3, 4], 1.0)
+    assert list(got) == [1.0, 1.0, -1.0]
+
+
+def test_load_cv_closed_forms():
+    assert O.load_cv([5, 5, 5, 5]) == 0.0
+    assert O.load_cv([0, 0, 0]) == 0.0
+    # (1, 2, 3, 4): mean 2.5, population variance 1.25
+    assert abs(O.load_cv([1, 2, 3, 4]) - np.sqrt(1.25) / 2.5) < 1e-15
+    # everything on one of E experts: cv = sqrt(E - 1)
+    assert abs(O.load_cv([0, 0, 0, 0, 0, 0, 0, 80]) - np.sqrt(7.0)) < 1e-12
