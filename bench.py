@@ -175,8 +175,8 @@ def blas_threads():
 
 def kernel_launches_per_step(shape):
     """Kernels the library launches for one moe_forward of this layer."""
-    router = 3          # logits GEMM, selection kernel, statistic finalize
-    dispatch = 4        # count, scan, rank, row gather
+    router = 2          # logits GEMM, selection (+ statistic, last CTA)
+    dispatch = 4        # count, scan, rank, row copy
     experts = 2         # grouped up (with activation), grouped down
     shared = 2 if shape.n_shared > 0 else 0
     combine = 1

@@ -51,8 +51,10 @@
  *     out) set a sticky error word at the start of the workspace instead;
  *     read it with moe_read_device_error.
  *   - The workspace `ws` must be zero-filled once when it is allocated (its
- *     first word is the device error word); after that no call needs it
- *     cleared.  Calls that share a workspace must be ordered on one stream.
+ *     first word is the device error word; the selection totals live there
+ *     too and every call leaves them zero); after that no call needs it
+ *     cleared, except after a call that returned MOE_ERR_CUDA.  Calls that
+ *     share a workspace must be ordered on one stream.
  *   - n_tokens == 0 is legal: outputs are empty, counts/kept/dropped are
  *     zero-filled, balance is 0.
  */
@@ -160,9 +162,10 @@ typedef struct moe_stats {
 
 /* ---- sizes ------------------------------------------------------------ */
 
-/* Bytes of scratch the stage calls below need in `ws` (error word, router
- * and dispatch partial sums, a logits buffer).  Never fails for a valid
- * config; returns MOE_ERR_INVALID_ARG otherwise. */
+/* Bytes of scratch the stage calls below need in `ws` (error word, the
+ * running per-expert selection totals of the balance statistic, dispatch
+ * per-chunk counts, a logits buffer).  Never fails for a valid config;
+ * returns MOE_ERR_INVALID_ARG otherwise. */
 MOE_API moe_status_t moe_scratch_size(const moe_config_t *cfg, size_t *bytes);
 
 /* Bytes of workspace moe_forward / moe_forward_host need: the scratch plus

@@ -23,12 +23,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   // scratch (shared by all stage calls)
-  size_t err, fin_ticket, fin_terms, route_psum, route_cnt, chunk_cnt, chunk_base, logits,
+  size_t err, fin_ticket, route_psum, route_cnt, chunk_cnt, chunk_base, logits,
       scratch_end;
   // intermediates of moe_forward
   size_t idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, y_e8, h_shared,
       shared_out, x_stage, out_stage, total;
-  int route_parts, chunks;
+  int chunks;
 };
 
 Layout layout_of(const moe_config_t& c) {
@@ -42,13 +42,12 @@ Layout layout_of(const moe_config_t& c) {
   const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model,
                 F = c.d_ff;
   const size_t es = elem_size(c);
-  L.route_parts = (int)ceil_div64(N, kRouteTokensPerPartial);
   L.chunks = (int)ceil_div64(N, kDispatchTokensPerChunk);
   L.err = take(kAlign);
   L.fin_ticket = L.err + 64;   // inside the first (zero-filled) block
-  L.fin_terms = take((size_t)E * 8);
-  L.route_psum = take((size_t)L.route_parts * E * 4);
-  L.route_cnt = take((size_t)L.route_parts * E * 4);
+  // running selection totals (zero between forwards, like the ticket)
+  L.route_psum = take((size_t)E * 8);
+  L.route_cnt = take((size_t)E * 4);
   L.chunk_cnt = take((size_t)L.chunks * E * 4);
   L.chunk_base = take((size_t)L.chunks * E * 4);
   L.logits = take((size_t)N * E * 4);
@@ -77,28 +76,22 @@ Layout layout_of(const moe_config_t& c) {
 // The scratch areas of a workspace laid out for config `c`.
 struct Scratch {
   int32_t* err;
-  double* fin_terms;
-  unsigned* fin_ticket;
-  float* psum;         // router partials [route_parts, E]
-  int32_t* cnt;
+  RouteTotals totals;  // running selection statistics
   int32_t* chunk_cnt;  // dispatch per-chunk histogram and bases
   int32_t* chunk_base;
   float* logits;
-  int route_parts;
 };
 
 Scratch scratch_of(const Layout& L, void* ws) {
   char* b = static_cast<char*>(ws);
   Scratch sc;
   sc.err = reinterpret_cast<int32_t*>(b + L.err);
-  sc.fin_terms = reinterpret_cast<double*>(b + L.fin_terms);
-  sc.fin_ticket = reinterpret_cast<unsigned*>(b + L.fin_ticket);
-  sc.psum = reinterpret_cast<float*>(b + L.route_psum);
-  sc.cnt = reinterpret_cast<int32_t*>(b + L.route_cnt);
+  sc.totals.ticket = reinterpret_cast<unsigned*>(b + L.fin_ticket);
+  sc.totals.psum_fx = reinterpret_cast<unsigned long long*>(b + L.route_psum);
+  sc.totals.cnt = reinterpret_cast<unsigned*>(b + L.route_cnt);
   sc.chunk_cnt = reinterpret_cast<int32_t*>(b + L.chunk_cnt);
   sc.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
   sc.logits = reinterpret_cast<float*>(b + L.logits);
-  sc.route_parts = L.route_parts;
   return sc;
 }
 
@@ -217,17 +210,16 @@ moe_status_t zero_stats(const moe_config_t& c, moe_stats_t* s, cudaStream_t st) 
 }
 
 // ---- stage bodies (arguments already checked) -----------------------------
-// The router and the selection of c.n_tokens tokens.  Their statistics
-// partials go to partials part0.. of the scratch; with `finalize` the
-// counts and the balance statistic of those tokens are reduced into stats.
+// The router and the selection of c.n_tokens tokens.  Their statistics join
+// the running totals of the scratch; with `finalize` the totals (over
+// n_total tokens, all launches since the last finalize) become the counts
+// and the balance statistic in stats, and are cleared.
 void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
                  float* logits, int32_t* idx, float* wts, moe_stats_t* stats,
-                 const Scratch& sc, cudaStream_t st, bool gemm, int64_t part0 = 0,
-                 bool finalize = true) {
+                 const Scratch& sc, cudaStream_t st, bool gemm, bool finalize = true,
+                 int64_t n_total = -1) {
   float* lg = logits ? logits : sc.logits;
-  float* psum = sc.psum + part0 * c.n_experts;
-  int32_t* cnt = sc.cnt + part0 * c.n_experts;
-  if (gemm && c.n_tokens < kRouterSmallTokens && c.d_model * elem_size(c) * 4 <= 48 * 1024) {
+  if (gemm && c.n_tokens < kRouterSmallTokens) {
     // a few tokens: every expert's dot product at once on the CUDA cores
     launch_router_small(x, w.w_router, w.b_router, lg, c.n_tokens, c.n_experts, c.d_model,
                         c.dtype == MOE_BF16, st);
@@ -276,13 +268,14 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
     p.is_bf16 = c.dtype == MOE_BF16;
     launch_simt_gemm(p, st);
   }
+  RouteFinal fin{};
+  fin.finalize = finalize;
+  fin.n_total = n_total < 0 ? c.n_tokens : n_total;
+  fin.coef = c.balance_coef;
+  fin.counts = stats ? stats->counts : nullptr;
+  fin.balance = stats ? stats->balance : nullptr;
   launch_route_from_logits(lg, c.n_tokens, c.n_experts, c.top_k, c.route, w.sel_bias, idx,
-                           wts, psum, cnt, st);
-  if (finalize)
-    launch_balance_finalize(psum, cnt, (int)ceil_div64(c.n_tokens, kRouteTokensPerPartial),
-                            c.n_experts, c.n_tokens, c.balance_coef,
-                            stats ? stats->counts : nullptr, stats ? stats->balance : nullptr,
-                            sc.fin_terms, sc.fin_ticket, st);
+                           wts, sc.totals, fin, st);
 }
 
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
@@ -292,8 +285,8 @@ void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                   sc.chunk_base, offsets, ros, tor, stats ? stats->counts : nullptr,
                   stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st);
   if (x_perm != nullptr)
-    launch_gather_rows(x, (int64_t)c.d_model * elem_size(c), tor, offsets, c.n_experts,
-                       c.n_tokens * c.top_k, x_perm, num_sms(), st);
+    launch_scatter_rows(x, (int64_t)c.d_model * elem_size(c), ros, c.n_tokens, c.top_k,
+                        x_perm, num_sms(), st);
 }
 
 // CTA pairs (256-row tiles) pay off when experts hold enough rows; with a
@@ -661,11 +654,12 @@ namespace {
 // combine -- "shared" coincides with "down" when there is none).
 // The whole layer for the n_tokens of `c`, on stream st, with buffers from
 // the workspace layout L (laid out for at least c.n_tokens tokens) and its
-// scratch sc.  Router partials go to part0..; with `finalize` the counts and
-// balance statistic are reduced into stats (else only kept/dropped are set).
+// scratch sc.  The selection statistics join the scratch's running totals;
+// with `finalize` they become (over n_total tokens) the counts and balance
+// statistic in stats (else only kept/dropped are set).
 // ev (if not null) receives MOE_FORWARD_EVENTS events around the stages.
 moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch& sc,
-                          int64_t part0, bool finalize, const void* x,
+                          bool finalize, int64_t n_total, const void* x,
                           const moe_weights_t& w, void* out, moe_stats_t* stats, void* ws,
                           cudaStream_t st, cudaEvent_t const* ev) {
   int32_t* idx = at<int32_t>(ws, L.idx);
@@ -688,7 +682,7 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
     if (ev != nullptr) cudaEventRecord(ev[i], st);
   };
   mark(0);
-  router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true, part0, finalize);
+  router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true, finalize, n_total);
   mark(1);
   moe_stats_t ds{};
   if (stats) {
@@ -696,8 +690,10 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
     ds.dropped = stats->dropped;
   }
   // the expert-sorted copy of the token rows is written once and read by
-  // the up projection as whole 128-row TMA boxes (a per-row gather inside
-  // the GEMM -- moe_expert_up_gather -- saves that memory, not time)
+  // the up projection as whole 128-row TMA boxes.  Gathering the rows inside
+  // the GEMM instead (moe_expert_up_gather: tile::gather4, one 128-byte row
+  // piece per row and k-block) saves that memory but measured 3.3x slower
+  // on the Qwen3-style layer.
   dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, sc, st);
   mark(2);
   MOE_TRY(up_body(c, x_perm, nullptr, offsets, w, h, sc.err, st));
@@ -744,7 +740,8 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x,
   if (c.n_tokens == 0) return zero_stats(c, stats, st);
   MOE_TRY(need({x, out}));
   const Layout L = layout_of(c);
-  return forward_core(c, L, scratch_of(L, ws), 0, true, x, *weights, out, stats, ws, st, ev);
+  return forward_core(c, L, scratch_of(L, ws), true, c.n_tokens, x, *weights, out, stats, ws,
+                      st, ev);
 }
 
 // ---- the host-buffer forward, pipelined over token chunks ------------------
@@ -797,17 +794,25 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
   char* xd = at<char>(ws, L.x_stage);
   char* od = at<char>(ws, L.out_stage);
   const int nch = (int)std::min<int64_t>(kHostChunks, c.n_tokens / kHostChunkMin);
-  // chunk starts on a statistics-partial boundary
+  // chunks start on selection-CTA boundaries (the same per-CTA sums as one
+  // launch over all tokens)
   const int64_t chunk =
-      ceil_div64(ceil_div64(c.n_tokens, nch), kRouteTokensPerPartial) * kRouteTokensPerPartial;
+      ceil_div64(ceil_div64(c.n_tokens, nch), kRouteTokensPerCta) * kRouteTokensPerCta;
+  const int nrun = (int)ceil_div64(c.n_tokens, chunk);   // chunks holding tokens
   bool ok = cudaEventRecord(hp.start, st) == cudaSuccess &&
             cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess;
-  moe_stats_t none{};
-  for (int i = 0; ok && i < nch; ++i) {
+  // the last chunk's selection turns the running totals of all chunks into
+  // the counts and the balance statistic; no capacity, so every selection
+  // is kept
+  moe_stats_t none{}, last{};
+  if (stats != nullptr) {
+    last.counts = stats->counts ? stats->counts : stats->kept;
+    last.balance = stats->balance;
+  }
+  for (int i = 0; ok && i < nrun; ++i) {
     const int64_t s0 = (int64_t)i * chunk;
     const int64_t n = std::min(chunk, c.n_tokens - s0);
-    if (n <= 0) break;
     ok = cudaMemcpyAsync(xd + s0 * row, xh + s0 * row, n * row, cudaMemcpyHostToDevice,
                          hp.h2d) == cudaSuccess &&
          cudaEventRecord(hp.in[i], hp.h2d) == cudaSuccess &&
@@ -815,20 +820,16 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
     if (!ok) break;
     moe_config_t ci = c;
     ci.n_tokens = n;
-    MOE_TRY(forward_core(ci, L, sc, s0 / kRouteTokensPerPartial, false, xd + s0 * row, w,
-                         od + s0 * row, &none, ws, st, nullptr));
+    const bool fin = i == nrun - 1;
+    MOE_TRY(forward_core(ci, L, sc, fin, c.n_tokens, xd + s0 * row, w, od + s0 * row,
+                         fin ? &last : &none, ws, st, nullptr));
     ok = cudaEventRecord(hp.done[i], st) == cudaSuccess &&
          cudaStreamWaitEvent(hp.d2h, hp.done[i], 0) == cudaSuccess &&
          cudaMemcpyAsync(oh + s0 * row, od + s0 * row, n * row, cudaMemcpyDeviceToHost,
                          hp.d2h) == cudaSuccess;
   }
   if (ok && stats != nullptr) {
-    // all chunks' partials at once: counts and the balance statistic; no
-    // capacity, so every selection is kept
-    int32_t* counts = stats->counts ? stats->counts : stats->kept;
-    launch_balance_finalize(sc.psum, sc.cnt, sc.route_parts, c.n_experts, c.n_tokens,
-                            c.balance_coef, counts, stats->balance, sc.fin_terms,
-                            sc.fin_ticket, st);
+    int32_t* counts = last.counts;
     const size_t eb = (size_t)c.n_experts * 4;
     if (stats->kept && counts != stats->kept)
       ok = cudaMemcpyAsync(stats->kept, counts, eb, cudaMemcpyDeviceToDevice, st) == cudaSuccess;

@@ -19,7 +19,8 @@
 //              inside a 32-slot step come from __match_any_sync (lanes with
 //              the same expert) and a running per-(warp, expert) counter;
 //              warp bases are an exclusive scan over the chunk's warps.
-// A fourth kernel copies x rows into x_perm (16-byte vectors).
+// A fourth kernel copies x rows into x_perm (32- or 16-byte vectors), either
+// row by row of x_perm (gather) or token by token of x (scatter).
 #include <algorithm>
 
 #include "common.cuh"
@@ -203,7 +204,72 @@ gather_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
   }
 }
 
+// The same copy driven from the token side: x_perm[row_of_slot[t*k + j]] =
+// x[t] for every kept slot.  One warp per token reads its row once (1 KB or
+// 4 KB per pass, 32-byte or 16-byte vectors) and writes it to each of its
+// rows, so x is read from memory once instead of once per assignment.
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
+                    const int32_t* __restrict__ row_of_slot, int64_t n_tokens, int top_k,
+                    uint8_t* __restrict__ x_perm, bool wide) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int shift = wide ? 5 : 4;
+  const int64_t nvec = row_bytes >> shift;
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < n_tokens; t += warps_total) {
+    const uint8_t* src = x + t * row_bytes;
+    for (int64_t u0 = 0; u0 < nvec; u0 += 128) {
+      Vec32 a[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t u = u0 + lane + 32 * q;
+        if (u < nvec) {
+          if (wide) {
+            ld_vec32_nc(src + (u << 5), a[q]);
+          } else {
+            const uint4 v = ld_vec16_nc(src + (u << 4));
+            a[q].v[0] = v.x; a[q].v[1] = v.y; a[q].v[2] = v.z; a[q].v[3] = v.w;
+          }
+        }
+      }
+      for (int j0 = 0; j0 < top_k; j0 += 32) {
+        const int32_t mine = j0 + lane < top_k ? row_of_slot[t * top_k + j0 + lane] : -1;
+        const int nj = min(32, top_k - j0);
+        for (int j = 0; j < nj; ++j) {
+          const int32_t r = __shfl_sync(kFull, mine, j);
+          if (r < 0) continue;                       // dropped
+          uint8_t* dst = x_perm + (int64_t)r * row_bytes;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t u = u0 + lane + 32 * q;
+            if (u >= nvec) continue;
+            if (wide) {
+              st_vec32(dst + (u << 5), a[q]);
+            } else {
+              st_vec16(dst + (u << 4), make_uint4(a[q].v[0], a[q].v[1], a[q].v[2], a[q].v[3]));
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,
+                         int64_t n_tokens, int top_k, void* x_perm, int num_sms,
+                         cudaStream_t st) {
+  if (n_tokens <= 0) return;
+  const int64_t blocks_needed = ceil_div64(n_tokens, 8);
+  const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)num_sms * 8);
+  const bool wide = row_bytes % 32 == 0 && (reinterpret_cast<uintptr_t>(x) & 31u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(x_perm) & 31u) == 0;
+  scatter_rows_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(x), row_bytes,
+                                              row_of_slot, n_tokens, top_k,
+                                              static_cast<uint8_t*>(x_perm), wide);
+}
 
 void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int n_experts, int64_t capacity, int32_t* chunk_cnt,

@@ -173,57 +173,84 @@ void launch_typed(const GemmProblem& p, cudaStream_t st) {
 }
 
 // Router logits for a few tokens: logits[t, e] = sum_i x[t, i] W[e, i] (+ b[e]),
-// fp32 accumulation.  A CTA takes kSmallTok tokens (staged in shared memory);
-// its warps walk the experts, lanes splitting d so that each router row is
-// read as whole 512-byte warp loads, and a warp reduction finishes each
-// (token, expert) sum.  With few tokens the tensor-core router is one tile
-// whose k-loop is a serial chain; here all experts proceed at once.
-constexpr int kSmallTok = 4;
-constexpr int kSmallWarps = 8;
-template <typename T>
-__global__ void __launch_bounds__(kSmallWarps * 32)
+// fp32 accumulation.  A CTA takes EB experts and 8 * TPW tokens; each lane
+// holds its slice of the EB router rows in registers (16-byte pieces
+// lane, lane + 32, ...; MAXV of them per pass over d), each warp walks TPW
+// tokens reading their x rows from L2, and a warp reduction finishes each
+// (token, expert) sum.  With few tokens the weights are read once per CTA
+// column and the work spreads over E / EB x N / (8 TPW) CTAs.
+template <typename T, int EB, int TPW, int MAXV>
+__global__ void __launch_bounds__(256)
 router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* __restrict__ b,
                     float* __restrict__ logits, int64_t n_tokens, int n_experts, int d) {
-  extern __shared__ __align__(16) uint8_t sx_raw[];
-  T* sx = reinterpret_cast<T*>(sx_raw);              // [kSmallTok][d]
-  const int64_t t0 = (int64_t)blockIdx.x * kSmallTok;
-  const int nt = (int)min((int64_t)kSmallTok, n_tokens - t0);
   constexpr int V = 16 / sizeof(T);                  // elements per 16 bytes
-  const int nv = d / V;
-  for (int i = threadIdx.x; i < kSmallTok * nv; i += blockDim.x) {
-    const int tt = i / nv, v = i - tt * nv;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (tt < nt) val = reinterpret_cast<const uint4*>(x + (t0 + tt) * d)[v];
-    reinterpret_cast<uint4*>(sx + (int64_t)tt * d)[v] = val;
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < n_experts; e += kSmallWarps) {
-    const uint4* wr = reinterpret_cast<const uint4*>(W + (int64_t)e * d);
-    float acc[kSmallTok];
+  const int e0 = blockIdx.x * EB;
+  const int64_t tw = ((int64_t)blockIdx.y * 8 + warp) * TPW;   // this warp's first token
+  const int nv = d / V;
+  float acc[EB][TPW];
 #pragma unroll
-    for (int tt = 0; tt < kSmallTok; ++tt) acc[tt] = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-      const uint4 wv = __ldg(wr + v);
-      const T* wp = reinterpret_cast<const T*>(&wv);
+  for (int eb = 0; eb < EB; ++eb)
 #pragma unroll
-      for (int tt = 0; tt < kSmallTok; ++tt) {
-        const uint4 xv = reinterpret_cast<const uint4*>(sx + (int64_t)tt * d)[v];
+    for (int tt = 0; tt < TPW; ++tt) acc[eb][tt] = 0.f;
+  for (int c0 = 0; c0 < nv; c0 += 32 * MAXV) {
+    uint4 wv[EB][MAXV];
+#pragma unroll
+    for (int eb = 0; eb < EB; ++eb)
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        const int v = c0 + lane + 32 * i;
+        wv[eb][i] = (v < nv && e0 + eb < n_experts)
+                        ? __ldg(reinterpret_cast<const uint4*>(W + (int64_t)(e0 + eb) * d) + v)
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) {
+      const int64_t t = tw + tt;
+      if (t >= n_tokens) break;
+      const uint4* xr = reinterpret_cast<const uint4*>(x + t * d);
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        const int v = c0 + lane + 32 * i;
+        if (v >= nv) break;
+        const uint4 xv = __ldg(xr + v);
         const T* xp = reinterpret_cast<const T*>(&xv);
 #pragma unroll
-        for (int j = 0; j < V; ++j) acc[tt] = fmaf(to_f32(xp[j]), to_f32(wp[j]), acc[tt]);
+        for (int eb = 0; eb < EB; ++eb) {
+          const T* wp = reinterpret_cast<const T*>(&wv[eb][i]);
+#pragma unroll
+          for (int j = 0; j < V; ++j) acc[eb][tt] = fmaf(to_f32(xp[j]), to_f32(wp[j]), acc[eb][tt]);
+        }
       }
     }
+  }
 #pragma unroll
-    for (int tt = 0; tt < kSmallTok; ++tt)
+  for (int eb = 0; eb < EB; ++eb)
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
-        acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
-    if (lane == 0) {
+        acc[eb][tt] += __shfl_xor_sync(kFull, acc[eb][tt], off);
+  if (lane == 0) {
+#pragma unroll
+    for (int eb = 0; eb < EB; ++eb) {
+      const int e = e0 + eb;
+      if (e >= n_experts) break;
       const float bias = b ? to_f32(b[e]) : 0.f;
-      for (int tt = 0; tt < nt; ++tt) logits[(t0 + tt) * n_experts + e] = acc[tt] + bias;
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
+        if (tw + tt < n_tokens) logits[(tw + tt) * n_experts + e] = acc[eb][tt] + bias;
     }
   }
+}
+
+template <typename T, int EB, int TPW, int MAXV>
+void launch_router_small_t(const void* x, const void* w, const void* b, float* logits,
+                           int64_t n_tokens, int n_experts, int d, cudaStream_t st) {
+  const dim3 grid((unsigned)ceil_div64(n_experts, EB), (unsigned)ceil_div64(n_tokens, 8 * TPW));
+  router_small_kernel<T, EB, TPW, MAXV><<<grid, 256, 0, st>>>(
+      static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(b), logits,
+      n_tokens, n_experts, d);
 }
 
 }  // namespace
@@ -231,17 +258,16 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* _
 void launch_router_small(const void* x, const void* w, const void* b, float* logits,
                          int64_t n_tokens, int n_experts, int d, int is_bf16, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const int blocks = (int)ceil_div64(n_tokens, kSmallTok);
-  const int threads = kSmallWarps * 32;
-  const size_t smem = (size_t)kSmallTok * d * (is_bf16 ? 2 : 4);
-  if (is_bf16)
-    router_small_kernel<bf16><<<blocks, threads, smem, st>>>(
-        static_cast<const bf16*>(x), static_cast<const bf16*>(w), static_cast<const bf16*>(b),
-        logits, n_tokens, n_experts, d);
-  else
-    router_small_kernel<float><<<blocks, threads, smem, st>>>(
-        static_cast<const float*>(x), static_cast<const float*>(w),
-        static_cast<const float*>(b), logits, n_tokens, n_experts, d);
+  // up to 128 tokens: 2 experts x 32 tokens per CTA (more CTAs); beyond, 4 x
+  // 64 (fewer re-reads of x)
+  const bool few = n_tokens <= 128;
+  if (is_bf16) {
+    if (few) launch_router_small_t<bf16, 2, 4, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
+    else launch_router_small_t<bf16, 4, 8, 4>(x, w, b, logits, n_tokens, n_experts, d, st);
+  } else {
+    if (few) launch_router_small_t<float, 2, 4, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
+    else launch_router_small_t<float, 4, 8, 4>(x, w, b, logits, n_tokens, n_experts, d, st);
+  }
 }
 
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st) {

@@ -771,6 +771,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+// gather4 (four rows of one box each) completing on either CTA's barrier
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map, uint32_t bar,
+                                                 int c0, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar),
+        "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
 __device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -884,38 +894,62 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // Lane 0 waits for free stages and loads B (and a plain A tile).  With a
+    // row map, this CTA's 128 A rows are gathered: lane l loads rows
+    // 4l..4l+3 of them (tokens row_map[row]) with one gather4 per k-block.
+    const bool gather = p.a_row_map != nullptr;
+    const int m_total = s_off[G];
+    if (gather || lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_phases = 0;
       for (int t = pair; t < total; t += n_pairs) {
         const Tile tl = tile_of(t, s_tile_start, s_off, G, nt, BM2);
+        int src[4] = {0, 0, 0, 0};
+        if (gather) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // rows past the last kept row read token 0; they are never stored
+            const int row = tl.row0 + (int)rank * 128 + lane * 4 + i;
+            src[i] = row < m_total ? __ldg(p.a_row_map + row) : 0;
+          }
+        }
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
+          int good = 1;
+          if (lane == 0) good = wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err);
+          if (gather) good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) { ok = false; break; }
           const uint32_t bar = map_to_rank(&full[stage], 0);
-          if (leader) mbar_expect_tx(&full[stage], 2 * kStageBytes2);
           uint8_t* a = sA + stage * kTileA2;
-          uint8_t* b = sB + stage * kTileB2;
-          tma_load_2d_pair(a, &tmA, bar, kb * BK, tl.row0 + (int)rank * 128);
-          if (p.swiglu) {
-            const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
-            tma_load_2d_pair(b, rank ? &tmB1 : &tmB0, bar, kb * BK, brow);
-          } else {
-            const int sub = kb / kb_per_sub;
-            const int kk = (kb - sub * kb_per_sub) * BK;
-            const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN + (int)rank * 128;
-            tma_load_2d_pair(b, &tmB0, bar, kk, brow);
+          if (lane == 0) {
+            if (leader) mbar_expect_tx(&full[stage], 2 * kStageBytes2);
+            uint8_t* b = sB + stage * kTileB2;
+            if (!gather) tma_load_2d_pair(a, &tmA, bar, kb * BK, tl.row0 + (int)rank * 128);
+            if (p.swiglu) {
+              const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
+              tma_load_2d_pair(b, rank ? &tmB1 : &tmB0, bar, kb * BK, brow);
+            } else {
+              const int sub = kb / kb_per_sub;
+              const int kk = (kb - sub * kb_per_sub) * BK;
+              const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN + (int)rank * 128;
+              tma_load_2d_pair(b, &tmB0, bar, kk, brow);
+            }
+            used |= 1u << stage;
+            last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
           }
-          used |= 1u << stage;
-          last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
+          if (gather) {
+            __syncwarp();
+            tma_gather4_pair(a + lane * 4 * (BK * 2), &tmA, bar, kb * BK, src[0], src[1],
+                             src[2], src[3]);
+          }
           if (++stage == kStages2) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
       }
       // the leader's full barriers count both CTAs' copies: every issued
       // copy of the pair has landed once they complete
-      if (leader) {
+      if (leader && lane == 0) {
         for (int s = 0; s < kStages2; ++s) {
           if (!(used >> s & 1u)) continue;
           const uint64_t t0 = globaltimer();
@@ -1110,9 +1144,8 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
     return true;
   };
   CUtensorMap ma, mb0, mb1;
-  // CTA pairs for grouped row order (not a gathered A); the single-CTA
-  // kernel runs if pairs cannot be launched here
-  if (q.use_pairs && q.a_row_map == nullptr) {
+  // CTA pairs; the single-CTA kernel runs if pairs cannot be launched here
+  if (q.use_pairs) {
     auto kern2 = q.c_e8 != nullptr ? tc2_gemm_kernel<kEkCompact> : tc2_gemm_kernel<kEkStore>;
     int n_pairs = 0;
     if (cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -8,27 +8,38 @@
 
 namespace moe {
 
-// Tokens whose selection statistics one router partial covers (one CTA of
-// the selection kernel).
-constexpr int kRouteTokensPerPartial = 32;
+// Tokens per CTA of the selection kernel.  The host pipeline starts its
+// chunks on multiples of it, so every CTA sums the same tokens either way.
+constexpr int kRouteTokensPerCta = 32;
 // Tokens per dispatch chunk (the unit of the per-chunk histogram).
 constexpr int kDispatchTokensPerChunk = 256;
 constexpr int kMaxExperts = 256;
 
 // ---- router ---------------------------------------------------------------
-// logits[N, E] (fp32) -> idx, w, per-partial selection counts and
-// probability sums ([P][E], P = ceil(N / kRouteTokensPerPartial)).
+// Running per-expert totals of one forward's selection statistics, in the
+// workspace: probability sums in units of 2^-32 (integers, so the totals do
+// not depend on the order in which CTAs add them), selection counts, and a
+// ticket.  All three are zero between forwards.
+struct RouteTotals {
+  unsigned long long* psum_fx;   // [E]
+  unsigned* cnt;                 // [E]
+  unsigned* ticket;
+};
+// With `finalize`, the last CTA of the launch turns the totals (of every
+// launch since they were last cleared) into counts[E] and the balance
+// statistic over n_total tokens (either output nullable) and clears them.
+struct RouteFinal {
+  bool finalize;
+  int64_t n_total;
+  float coef;
+  int32_t* counts;
+  float* balance;
+};
+// logits[N, E] (fp32) -> idx, w; adds this launch's statistics to `tot`.
 void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_experts,
                               int top_k, int mode, const float* sel_bias,
-                              int32_t* idx, float* w, float* psum_part,
-                              int32_t* cnt_part, cudaStream_t st);
-// sums the partials in a fixed order: counts[E] (optional) and the balance
-// statistic (optional).  terms: [E] doubles of scratch; ticket: one counter
-// that is zero on entry (and is left zero).
-void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
-                             int n_parts, int n_experts, int64_t n_tokens,
-                             float coef, int32_t* counts, float* balance,
-                             double* terms, unsigned* ticket, cudaStream_t st);
+                              int32_t* idx, float* w, const RouteTotals& tot,
+                              const RouteFinal& fin, cudaStream_t st);
 
 // between steps: selection-bias update from the per-expert counts and the
 // load's coefficient of variation (either output nullable)
@@ -47,6 +58,10 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
 void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
                         const int32_t* offsets, int n_experts, int64_t max_rows,
                         void* x_perm, int num_sms, cudaStream_t st);
+
+void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,
+                         int64_t n_tokens, int top_k, void* x_perm, int num_sms,
+                         cudaStream_t st);
 
 // ---- SIMT GEMM (fp32 and bf16 storage, fp32 accumulation) ----------------
 enum Epilogue : int {

@@ -10,9 +10,14 @@
 // lane).  Each of the k rounds takes every lane's best remaining candidate
 // and reduces them across the warp in the total order (key desc, index asc)
 // with two warp reductions (redux.sync): the largest key, then the lowest
-// index holding it.  Probabilities for the balance
-// statistic are accumulated per warp in registers and reduced across warps
-// in a fixed order, so the per-partial sums are deterministic.
+// index holding it.
+//
+// The balance statistic ("Tutorial -- MoE SER Expert Routing", section 4):
+// per-expert probability sums are accumulated per warp
+// in registers, reduced across the CTA's warps in a fixed order, and added
+// to running totals in the workspace as integers (fixed point), so the
+// totals are the same whatever order the CTAs finish in.  The last CTA of
+// the forward turns them into the selection counts and the statistic.
 #include <climits>
 #include <math.h>
 
@@ -84,10 +89,11 @@ template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 4 : 2)
 route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
              int top_k, int mode, const float* __restrict__ sel_bias,
-             int32_t* __restrict__ idx, float* __restrict__ w,
-             float* __restrict__ psum_part, int32_t* __restrict__ cnt_part) {
+             int32_t* __restrict__ idx, float* __restrict__ w, const RouteTotals tot,
+             const RouteFinal fin) {
   __shared__ float s_ps[kRouteWarps][EPL * 32];
   __shared__ int s_cnt[EPL * 32];
+  __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = n_experts;
   for (int e = threadIdx.x; e < EPL * 32; e += blockDim.x) s_cnt[e] = 0;
@@ -101,18 +107,28 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
     bias[i] = (mode == 2 && e < E) ? sel_bias[e] : 0.f;
   }
 
-  const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerPartial;
-  const int64_t t1 = min(n_tokens, t0 + kRouteTokensPerPartial);
-  for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
-    float l[EPL], key[EPL], num[EPL], p[EPL];
-    int slot[EPL];
+  const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerCta;
+  const int64_t t1 = min(n_tokens, t0 + kRouteTokensPerCta);
+  // the next token's logits are loaded while this one is ranked
+  float l_next[EPL];
+  auto load_row = [&](int64_t t) {
     const float* row = logits + t * E;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      l[i] = e < E ? row[e] : -INFINITY;
+      l_next[i] = (t < t1 && e < E) ? __ldcs(row + e) : -INFINITY;
+    }
+  };
+  load_row(t0 + warp);
+  for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
+    float l[EPL], key[EPL], num[EPL], p[EPL];
+    int slot[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      l[i] = l_next[i];
       slot[i] = -1;
     }
+    load_row(t + kRouteWarps);
     if (mode == 2) {
       // Rank fp32 keys first (within kSlack of the exact ones); the exact top
       // k lies among the experts whose fp32 key is within 2 kSlack of the
@@ -199,66 +215,42 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
 #pragma unroll
   for (int i = 0; i < EPL; ++i) s_ps[warp][lane + 32 * i] = ps[i];
   __syncthreads();
+  // this CTA's sums join the running totals: the probability sum (at most
+  // 32) in fixed point, 2^-32 units (N * 2^32 stays below 2^63)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float acc = 0.f;
 #pragma unroll
     for (int q = 0; q < kRouteWarps; ++q) acc += s_ps[q][e];
-    psum_part[(int64_t)blockIdx.x * E + e] = acc;
-    cnt_part[(int64_t)blockIdx.x * E + e] = s_cnt[e];
+    const unsigned long long fx = __float2ull_rn(acc * 4294967296.0f);
+    if (fx != 0ull) atomicAdd(tot.psum_fx + e, fx);
+    if (s_cnt[e] != 0) atomicAdd(tot.cnt + e, (unsigned)s_cnt[e]);
   }
-}
-
-// Per-expert totals of the partials (block e, fixed-order tree), then the
-// last block to finish sums the per-expert terms in expert order: the
-// statistic is the same on every run.  `ticket` (zero when the workspace
-// was allocated) is reset by that last block.
-constexpr int kFinThreads = 256;
-__global__ void __launch_bounds__(kFinThreads)
-balance_finalize_kernel(const float* __restrict__ psum_part,
-                        const int32_t* __restrict__ cnt_part, int n_parts,
-                        int n_experts, int64_t n_tokens, float coef,
-                        int32_t* __restrict__ counts, float* __restrict__ balance,
-                        double* __restrict__ terms, unsigned* __restrict__ ticket) {
-  __shared__ double s_ps[kFinThreads];
-  __shared__ long long s_cnt[kFinThreads];
-  __shared__ bool s_last;
-  const int e = blockIdx.x, tid = threadIdx.x;
-  double ps = 0.0;
-  long long cnt = 0;
-  for (int q = tid; q < n_parts; q += kFinThreads) {
-    ps += (double)psum_part[(int64_t)q * n_experts + e];
-    cnt += cnt_part[(int64_t)q * n_experts + e];
-  }
-  s_ps[tid] = ps;
-  s_cnt[tid] = cnt;
+  if (!fin.finalize) return;
+  // the last CTA to finish (ticket) reads and clears the totals
+  __threadfence();
   __syncthreads();
-  for (int h = kFinThreads / 2; h > 0; h >>= 1) {
-    if (tid < h) {
-      s_ps[tid] += s_ps[tid + h];
-      s_cnt[tid] += s_cnt[tid + h];
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    if (counts) counts[e] = (int32_t)s_cnt[0];
-    const double n = n_tokens > 0 ? (double)n_tokens : 1.0;
-    terms[e] = ((double)s_cnt[0] / n) * (s_ps[0] / n);
-    __threadfence();
-    s_last = atomicAdd(ticket, 1u) == (unsigned)(n_experts - 1);
+  if (threadIdx.x == 0) s_last = atomicAdd(tot.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float* s_term = &s_ps[0][0];                  // kRouteWarps * EPL * 32 >= E
+  const float n = (float)fin.n_total;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const unsigned long long fx = atomicExch(tot.psum_fx + e, 0ull);
+    const unsigned c = atomicExch(tot.cnt + e, 0u);
+    if (fin.counts != nullptr) fin.counts[e] = (int32_t)c;
+    // frac_e * mean p_e = (count_e / N) * (sum_t p / N)
+    s_term[e] = ((float)c / n) * ((float)fx * 2.3283064365386963e-10f / n);
   }
   __syncthreads();
-  if (s_last) {
-    // every block's term is visible (fence + ticket); load them all at
-    // once, then sum in expert order
-    __threadfence();
-    for (int q = tid; q < n_experts; q += kFinThreads)
-      s_ps[q] = ((volatile double*)terms)[q];
-    __syncthreads();
-    if (tid == 0) {
-      double acc = 0.0;
-      for (int q = 0; q < n_experts; ++q) acc += s_ps[q];
-      if (balance) balance[0] = n_tokens > 0 ? (float)((double)coef * acc) : 0.f;
-      *ticket = 0u;
+  if (warp == 0) {
+    float acc = 0.f;
+    for (int e = lane; e < E; e += 32) acc += s_term[e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    if (lane == 0) {
+      if (fin.balance != nullptr) fin.balance[0] = fin.coef * acc;
+      *tot.ticket = 0u;
     }
   }
 }
@@ -306,33 +298,22 @@ void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float
 
 void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_experts,
                               int top_k, int mode, const float* sel_bias,
-                              int32_t* idx, float* w, float* psum_part,
-                              int32_t* cnt_part, cudaStream_t st) {
+                              int32_t* idx, float* w, const RouteTotals& tot,
+                              const RouteFinal& fin, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const int parts = (int)ceil_div64(n_tokens, kRouteTokensPerPartial);
-  const dim3 grid(parts), block(kRouteWarps * 32);
+  const dim3 grid((unsigned)ceil_div64(n_tokens, kRouteTokensPerCta)), block(kRouteWarps * 32);
   if (n_experts <= 32)
     route_kernel<1><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, psum_part, cnt_part);
+                                            sel_bias, idx, w, tot, fin);
   else if (n_experts <= 64)
     route_kernel<2><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, psum_part, cnt_part);
+                                            sel_bias, idx, w, tot, fin);
   else if (n_experts <= 128)
     route_kernel<4><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, psum_part, cnt_part);
+                                            sel_bias, idx, w, tot, fin);
   else
     route_kernel<8><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, psum_part, cnt_part);
-}
-
-void launch_balance_finalize(const float* psum_part, const int32_t* cnt_part,
-                             int n_parts, int n_experts, int64_t n_tokens,
-                             float coef, int32_t* counts, float* balance,
-                             double* terms, unsigned* ticket, cudaStream_t st) {
-  if (!counts && !balance) return;
-  balance_finalize_kernel<<<n_experts, kFinThreads, 0, st>>>(
-      psum_part, cnt_part, n_parts, n_experts, n_tokens, coef, counts, balance, terms,
-      ticket);
+                                            sel_bias, idx, w, tot, fin);
 }
 
 }  // namespace moe

@@ -245,6 +245,31 @@ def test_expert_up_gather_matches_materialised_rows(name, N):
     assert D.device_error() == M.MOE_OK
 
 
+@pytest.mark.parametrize("name,N", [("qwen3_moe", 4096), ("deepseek_v3_block", 2048)])
+def test_expert_up_gather_on_pairs(name, N):
+    """Enough rows per expert for 256-row CTA-pair tiles: the gathered up
+    projection still equals the one over x_perm bit for bit."""
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    idx, disp, _ = _oracle_dispatch_inputs(shape, inp)
+    rows = shape.n_tokens * shape.top_k
+    m = int(disp["offsets"][-1])
+    off = torch.zeros(shape.n_experts + 1, dtype=torch.int32, device="cuda")
+    ros = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    tor = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    xp = D.empty(rows, shape.d_model)
+    M.moe_dispatch_permute(D.cfg, dev(idx), D.t["x"], off, ros, tor, xp, None, D.ws)
+    h_ref = D.empty(rows, shape.d_ff)
+    M.moe_expert_up(D.cfg, xp, off, D.weights, h_ref, D.ws)
+    h = D.empty(rows, shape.d_ff)
+    M.moe_expert_up_gather(D.cfg, D.t["x"], tor, off, D.weights, h, D.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(tor)[:m], disp["token_of_row"])
+    assert torch.equal(h[:m], h_ref[:m])
+    assert D.device_error() == M.MOE_OK
+
+
 def test_shared_ffn_parity():
     inp = inputs_for("deepseek_v3_block", 300)
     shape = inp.shape
@@ -290,7 +315,11 @@ def test_combine_parity(dtype, shared, cf):
 # ------------------------------------------- router GEMM + selection
 ROUTER_CASES = [("toy_top2_fp32", None), ("capacity_top2_fp32", None),
                 ("capacity_top2_bf16", None), ("deepseek_v3_block", 1000),
-                ("qwen3_moe", 1000), ("decode_stream", None)]
+                ("qwen3_moe", 1000), ("decode_stream", None),
+                # the CUDA-core router below 512 tokens: both CTA shapes,
+                # ragged token counts
+                ("toy_top2_fp32", 5), ("deepseek_v3_block", 37), ("qwen3_moe", 200),
+                ("capacity_top2_fp32", 300), ("qwen3_moe", 511)]
 
 
 @pytest.mark.parametrize("name,N", ROUTER_CASES)
