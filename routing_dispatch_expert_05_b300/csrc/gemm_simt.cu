@@ -258,14 +258,14 @@ void launch_router_small_t(const void* x, const void* w, const void* b, float* l
 void launch_router_small(const void* x, const void* w, const void* b, float* logits,
                          int64_t n_tokens, int n_experts, int d, int is_bf16, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  // up to 128 tokens: 2 experts x 32 tokens per CTA (more CTAs); beyond, 4 x
+  // up to 128 tokens: 2 experts x 8 tokens per CTA (more CTAs); beyond, 4 x
   // 64 (fewer re-reads of x)
   const bool few = n_tokens <= 128;
   if (is_bf16) {
-    if (few) launch_router_small_t<bf16, 2, 4, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
+    if (few) launch_router_small_t<bf16, 2, 1, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
     else launch_router_small_t<bf16, 4, 8, 4>(x, w, b, logits, n_tokens, n_experts, d, st);
   } else {
-    if (few) launch_router_small_t<float, 2, 4, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
+    if (few) launch_router_small_t<float, 2, 1, 8>(x, w, b, logits, n_tokens, n_experts, d, st);
     else launch_router_small_t<float, 4, 8, 4>(x, w, b, logits, n_tokens, n_experts, d, st);
   }
 }

@@ -8,8 +8,9 @@
 
 namespace moe {
 
-// Tokens per CTA of the selection kernel.  The host pipeline starts its
-// chunks on multiples of it, so every CTA sums the same tokens either way.
+// Tokens per CTA of the selection kernel from 4096 tokens on (8 below).  The
+// host pipeline starts its chunks on multiples of it, so every CTA sums the
+// same tokens either way.
 constexpr int kRouteTokensPerCta = 32;
 // Tokens per dispatch chunk (the unit of the per-chunk histogram).
 constexpr int kDispatchTokensPerChunk = 256;

@@ -89,8 +89,8 @@ template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 4 : 2)
 route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
              int top_k, int mode, const float* __restrict__ sel_bias,
-             int32_t* __restrict__ idx, float* __restrict__ w, const RouteTotals tot,
-             const RouteFinal fin) {
+             int32_t* __restrict__ idx, float* __restrict__ w, int tokens_per_cta,
+             const RouteTotals tot, const RouteFinal fin) {
   __shared__ float s_ps[kRouteWarps][EPL * 32];
   __shared__ int s_cnt[EPL * 32];
   __shared__ bool s_last;
@@ -107,8 +107,8 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
     bias[i] = (mode == 2 && e < E) ? sel_bias[e] : 0.f;
   }
 
-  const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerCta;
-  const int64_t t1 = min(n_tokens, t0 + kRouteTokensPerCta);
+  const int64_t t0 = (int64_t)blockIdx.x * tokens_per_cta;
+  const int64_t t1 = min(n_tokens, t0 + tokens_per_cta);
   // the next token's logits are loaded while this one is ranked
   float l_next[EPL];
   auto load_row = [&](int64_t t) {
@@ -301,19 +301,24 @@ void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_exper
                               int32_t* idx, float* w, const RouteTotals& tot,
                               const RouteFinal& fin, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const dim3 grid((unsigned)ceil_div64(n_tokens, kRouteTokensPerCta)), block(kRouteWarps * 32);
+  // a token per warp for small layers (more CTAs); otherwise four per warp,
+  // kRouteTokensPerCta per CTA.  Chosen by the whole forward's token count,
+  // so the chunks of the host pipeline split tokens into CTAs as one launch
+  // over all of them would.
+  const int tpc = fin.n_total < 4096 ? kRouteWarps : kRouteTokensPerCta;
+  const dim3 grid((unsigned)ceil_div64(n_tokens, tpc)), block(kRouteWarps * 32);
   if (n_experts <= 32)
     route_kernel<1><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tot, fin);
+                                            sel_bias, idx, w, tpc, tot, fin);
   else if (n_experts <= 64)
     route_kernel<2><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tot, fin);
+                                            sel_bias, idx, w, tpc, tot, fin);
   else if (n_experts <= 128)
     route_kernel<4><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tot, fin);
+                                            sel_bias, idx, w, tpc, tot, fin);
   else
     route_kernel<8><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tot, fin);
+                                            sel_bias, idx, w, tpc, tot, fin);
 }
 
 }  // namespace moe

@@ -473,11 +473,13 @@ def test_forward_host_matches_forward():
     assert torch.equal(oh, out.cpu())
 
 
-def test_forward_host_pipelined_matches_forward():
+@pytest.mark.parametrize("N", [12288 + 96, 8200])
+def test_forward_host_pipelined_matches_forward(N):
     """Without a capacity, moe_forward_host splits the tokens into chunks and
     overlaps the host copies with the compute; the output and every
-    statistic equal one moe_forward over all tokens, bit for bit."""
-    inp = inputs_for("qwen3_moe", 12288 + 96)        # three chunks, ragged tail
+    statistic equal one moe_forward over all tokens, bit for bit (three
+    chunks with a ragged tail; two chunks, the last under 4096 tokens)."""
+    inp = inputs_for("qwen3_moe", N)
     D = Device(inp)
     shape = inp.shape
     out, st = _forward(D)
@@ -540,6 +542,20 @@ def test_forward_special_cases(E, k):
     out, _ = _forward(D)
     ref = O.forward(shape, inp.values)
     assert_output_close(to_np(out), ref["out_exact"], shape.dtype, "special")
+
+
+@pytest.mark.parametrize("d", [48, 40, 272])
+def test_forward_bf16_row_widths(d):
+    """bf16 layers whose rows are not a multiple of the combine's 32-byte
+    pieces (40: 16-byte path) or hold only a few of them (48, 272: several
+    tokens per CTA) still match the oracle."""
+    shape = _cfg(n_tokens=300, n_experts=8, top_k=2, d_model=d, d_ff=64,
+                 dtype=W.DTYPE_BF16)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, _ = _forward(D)
+    ref = O.forward(shape, inp.values)
+    assert_output_close(to_np(out), ref["out_exact"], shape.dtype, "row widths")
 
 
 # -------------------------------------------- full-size sampled checks
