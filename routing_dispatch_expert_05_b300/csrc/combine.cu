@@ -110,52 +110,84 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_s
 // The same gather-reduce over compact expert outputs: y16 [N*k, d] fp16 and
 // one exponent byte per (row, 32 columns), value = y16 * 2^(e8 - 127).  The
 // power of two folds into the weight (an exact product), so the fp32 sum is
-// sum_j (w_j * 2^(e8_j - 127)) * y16_j in slot order, as for fp32 y.  The
-// k rows of a token (up to 8 at a time) are loaded before their FMAs.
+// sum_j (w_j * 2^(e8_j - 127)) * y16_j in slot order, as for fp32 y.
+// The kernel is bound by the latency of its row loads, so it keeps them
+// back to back: the next token's slot rows and weights (up to 8) are loaded
+// while this token's expert rows are in flight and handed over through
+// shared memory, so each token costs one round trip to memory, not two.
+constexpr int kPrefetchSlots = 8;
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 combine_compact_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
                        const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
                        const float* __restrict__ shared, T* __restrict__ out,
                        int64_t n_tokens, int top_k, int d_model) {
   constexpr int C = 8;                       // columns per thread step (16 B of fp16)
-  constexpr int KB = 8;                      // slots in flight
+  constexpr int KB = kPrefetchSlots;
+  __shared__ int s_r[2][KB];
+  __shared__ float s_w[2][KB];
   const int nvec = d_model / C;
   const int e8_cols = (d_model + kYScaleBlock - 1) / kYScaleBlock;
-  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
-    const int32_t* rows = row_of_slot + t * top_k;
-    const float* wt = w + t * top_k;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+  const int tid = threadIdx.x;
+  const int kp = min(top_k, KB);             // slots handed over through shared memory
+  int64_t t = blockIdx.x;
+  if (tid < kp && t < n_tokens) {
+    s_r[0][tid] = row_of_slot[t * top_k + tid];
+    s_w[0][tid] = w[t * top_k + tid];
+  }
+  __syncthreads();
+  int buf = 0;
+  for (; t < n_tokens; t += gridDim.x) {
+    const int64_t tn = t + gridDim.x;
+    int r_next = -1;
+    float w_next = 0.f;
+    if (tid < kp && tn < n_tokens) {
+      r_next = row_of_slot[tn * top_k + tid];
+      w_next = w[tn * top_k + tid];
+    }
+    for (int v = tid; v < nvec; v += blockDim.x) {
       const int64_t col = (int64_t)v * C;
       const int blk = (int)(col / kYScaleBlock);
       float acc[C];
 #pragma unroll
       for (int i = 0; i < C; ++i) acc[i] = 0.f;
-      for (int j0 = 0; j0 < top_k; j0 += KB) {
-        uint4 val[KB];
-        float cj[KB];
+      uint4 val[KB];
+      float cj[KB];
 #pragma unroll
-        for (int q = 0; q < KB; ++q) {
-          const int j = j0 + q;
-          const int r = j < top_k ? rows[j] : -1;
-          cj[q] = 0.f;
-          val[q] = make_uint4(0u, 0u, 0u, 0u);
-          if (r >= 0) {
-            val[q] = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
-            const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
-            cj[q] = wt[j] * __uint_as_float(e8 << 23);
-          }
+      for (int q = 0; q < KB; ++q) {
+        const int r = q < kp ? s_r[buf][q] : -1;
+        cj[q] = 0.f;
+        val[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (r >= 0) {
+          val[q] = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
+          const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
+          cj[q] = s_w[buf][q] * __uint_as_float(e8 << 23);
         }
+      }
 #pragma unroll
-        for (int q = 0; q < KB; ++q) {
-          if (j0 + q >= top_k || cj[q] == 0.f && rows[j0 + q] < 0) continue;
-          const __half2* h2 = reinterpret_cast<const __half2*>(&val[q]);
+      for (int q = 0; q < KB; ++q) {
+        if (q >= kp || s_r[buf][q] < 0) continue;       // absent or dropped
+        const __half2* h2 = reinterpret_cast<const __half2*>(&val[q]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(h2[i]);
-            acc[2 * i] = fmaf(cj[q], f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(cj[q], f.y, acc[2 * i + 1]);
-          }
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(h2[i]);
+          acc[2 * i] = fmaf(cj[q], f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(cj[q], f.y, acc[2 * i + 1]);
+        }
+      }
+      // slots past the first KB (top_k > 8), in order, straight from memory
+      for (int j = KB; j < top_k; ++j) {
+        const int r = row_of_slot[t * top_k + j];
+        if (r < 0) continue;
+        const uint4 vj = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
+        const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
+        const float c = w[t * top_k + j] * __uint_as_float(e8 << 23);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&vj);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(h2[i]);
+          acc[2 * i] = fmaf(c, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(c, f.y, acc[2 * i + 1]);
         }
       }
       if (shared != nullptr) {
@@ -177,87 +209,13 @@ combine_compact_kernel(const __half* __restrict__ y, const uint8_t* __restrict__
         st_vec16(op, o);
       }
     }
-  }
-}
-
-// The compact combine with 32-byte pieces: a thread owns 16 consecutive
-// columns (one 256-bit load per slot, within one exponent block), the same
-// products and the same slot order as above.
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-combine_compact32_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
-                         const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
-                         const float* __restrict__ shared, T* __restrict__ out,
-                         int64_t n_tokens, int top_k, int d_model) {
-  constexpr int C = 16;                      // columns per thread step (32 B of fp16)
-  constexpr int KB = 8;                      // slots in flight
-  const int nvec = d_model / C;
-  const int e8_cols = (d_model + kYScaleBlock - 1) / kYScaleBlock;
-  // short rows: several tokens per CTA at once, whole warps per token
-  const int tpt = nvec >= kThreads ? kThreads : (nvec + 31) / 32 * 32;
-  const int tpb = kThreads / tpt;
-  const int sub = threadIdx.x / tpt, lt = threadIdx.x - sub * tpt;
-  if (sub >= tpb) return;
-  for (int64_t t = (int64_t)blockIdx.x * tpb + sub; t < n_tokens; t += (int64_t)gridDim.x * tpb) {
-    const int32_t* rows = row_of_slot + t * top_k;
-    const float* wt = w + t * top_k;
-    for (int v = lt; v < nvec; v += tpt) {
-      const int64_t col = (int64_t)v * C;
-      const int blk = (int)(col / kYScaleBlock);
-      float acc[C];
-#pragma unroll
-      for (int i = 0; i < C; ++i) acc[i] = 0.f;
-      for (int j0 = 0; j0 < top_k; j0 += KB) {
-        Vec32 val[KB];
-        float cj[KB];
-#pragma unroll
-        for (int q = 0; q < KB; ++q) {
-          const int j = j0 + q;
-          const int r = j < top_k ? rows[j] : -1;
-          cj[q] = 0.f;
-          if (r >= 0) {
-            ld_vec32_nc(y + (int64_t)r * d_model + col, val[q]);
-            const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
-            cj[q] = wt[j] * __uint_as_float(e8 << 23);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) val[q].v[i] = 0u;
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < KB; ++q) {
-          if (j0 + q >= top_k || cj[q] == 0.f && rows[j0 + q] < 0) continue;
-          const __half2* h2 = reinterpret_cast<const __half2*>(val[q].v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 f = __half22float2(h2[i]);
-            acc[2 * i] = fmaf(cj[q], f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(cj[q], f.y, acc[2 * i + 1]);
-          }
-        }
-      }
-      if (shared != nullptr) {
-        const float4* sp = reinterpret_cast<const float4*>(shared + t * d_model + col);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 s4 = __ldcs(sp + i);
-          acc[4 * i] += s4.x; acc[4 * i + 1] += s4.y; acc[4 * i + 2] += s4.z;
-          acc[4 * i + 3] += s4.w;
-        }
-      }
-      T* op = out + t * d_model + col;
-      if constexpr (sizeof(T) == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<float4*>(op)[i] =
-              make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-      } else {
-        Vec32 o;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o.v[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
-        st_vec32(op, o);
-      }
+    // hand the next token's slots over (every thread is done with buf's)
+    if (tid < kp) {
+      s_r[buf ^ 1][tid] = r_next;
+      s_w[buf ^ 1][tid] = w_next;
     }
+    __syncthreads();
+    buf ^= 1;
   }
 }
 
@@ -268,26 +226,9 @@ void launch_combine_compact(const void* y16, const uint8_t* y_e8, const int32_t*
                             int top_k, int d_model, int is_bf16, int num_sms,
                             cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 16);
+  // three CTAs per SM are resident (register bound); a CTA walks its tokens
+  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 3);
   const __half* y = static_cast<const __half*>(y16);
-  // 32-byte pieces where every row start is 32-byte aligned
-  const bool wide = d_model % 16 == 0 && (reinterpret_cast<uintptr_t>(y16) & 31u) == 0 &&
-                    (reinterpret_cast<uintptr_t>(out) & 31u) == 0 &&
-                    (shared == nullptr || (reinterpret_cast<uintptr_t>(shared) & 31u) == 0);
-  if (wide) {
-    const int64_t nvec = d_model / 16;
-    const int64_t tpb = nvec >= kThreads ? 1 : kThreads / ((nvec + 31) / 32 * 32);
-    const int blocks32 =
-        (int)std::min<int64_t>(ceil_div64(n_tokens, tpb), (int64_t)num_sms * 16);
-    if (is_bf16)
-      combine_compact32_kernel<bf16><<<blocks32, kThreads, 0, st>>>(
-          y, y_e8, row_of_slot, w, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
-    else
-      combine_compact32_kernel<float><<<blocks32, kThreads, 0, st>>>(
-          y, y_e8, row_of_slot, w, shared, static_cast<float*>(out), n_tokens, top_k,
-          d_model);
-    return;
-  }
   if (is_bf16)
     combine_compact_kernel<bf16><<<blocks, kThreads, 0, st>>>(
         y, y_e8, row_of_slot, w, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);

@@ -7,10 +7,11 @@
 // order, ties to the lower expert index, and the first k are taken.
 //
 // One warp handles one token: lane l holds experts l, l+32, ... (EPL per
-// lane).  Each of the k rounds takes every lane's best remaining candidate
-// and reduces them across the warp in the total order (key desc, index asc)
-// with two warp reductions (redux.sync): the largest key, then the lowest
-// index holding it.
+// lane), sorted best first.  Each of the k rounds reduces the lanes' heads
+// across the warp in the total order (key desc, index asc) with two warp
+// reductions (redux.sync): the largest key, then the lowest index holding
+// it; the winning lane drops its head.  The weights divide each chosen
+// numerator by their sum taken in slot order.
 //
 // The balance statistic ("Tutorial -- MoE SER Expert Routing", section 4):
 // per-expert probability sums are accumulated per warp
@@ -18,7 +19,6 @@
 // to running totals in the workspace as integers (fixed point), so the
 // totals are the same whatever order the CTAs finish in.  The last CTA of
 // the forward turns them into the selection counts and the statistic.
-#include <climits>
 #include <math.h>
 
 #include "common.cuh"
@@ -34,11 +34,6 @@ __device__ __forceinline__ float warp_sum_bcast(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
   return __shfl_sync(kFull, v, 0);
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
-  return v;
 }
 
 // sigmoid evaluated in double, rounded once to fp32 (the selection key's
@@ -61,28 +56,43 @@ __device__ __forceinline__ float unordered(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// One selection round: the best remaining candidate of the warp in the total
-// order (key desc, index asc) -- a warp max of the keys, then a warp min of
-// the indices of the lanes holding that key (two redux.sync).  Returns the
-// expert index (INT_MAX if none is left) and its key.
+// Selection keeps, per lane, its candidates sorted best first as 64-bit
+// words (ordered key << 32 | ~expert): a larger word is a larger key, or the
+// same key and a lower expert index -- the total order of the selection.
+// Word 0 marks "none" (every finite key orders above 0).
+__device__ __forceinline__ uint64_t cand_word(uint32_t okey, int e) {
+  return ((uint64_t)okey << 32) | (uint32_t)~(uint32_t)e;
+}
 template <int EPL>
-__device__ __forceinline__ int warp_best(const uint32_t (&ok)[EPL], const int (&slot)[EPL],
-                                         int lane, int E, float* best_key) {
-  uint32_t bk = 0u;
-  int bi = INT_MAX;
+__device__ __forceinline__ void sort_desc(uint64_t (&c)[EPL]) {
+  // odd-even transposition: EPL rounds of compare-exchange
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E && slot[i] < 0 && (bi == INT_MAX || ok[i] > bk)) {
-      bk = ok[i];
-      bi = e;
+  for (int r = 0; r < EPL; ++r)
+#pragma unroll
+    for (int i = r & 1; i + 1 < EPL; i += 2) {
+      const uint64_t hi = c[i] > c[i + 1] ? c[i] : c[i + 1];
+      const uint64_t lo = c[i] > c[i + 1] ? c[i + 1] : c[i];
+      c[i] = hi;
+      c[i + 1] = lo;
     }
-  }
-  const uint32_t kmax = __reduce_max_sync(kFull, bi == INT_MAX ? 0u : bk);
-  const uint32_t mine = (bi != INT_MAX && bk == kmax) ? (uint32_t)bi : 0xFFFFFFFFu;
+}
+// One round: the warp's best remaining candidate -- the largest head key
+// (redux.sync max), then the lowest expert index among the heads holding it
+// (redux.sync min) -- which its lane then drops from its queue.  Returns the
+// expert; *okey_out is its ordered key.
+template <int EPL>
+__device__ __forceinline__ uint32_t take_best(uint64_t (&c)[EPL], int lane, uint32_t* okey_out) {
+  const uint32_t hk = (uint32_t)(c[0] >> 32);
+  const uint32_t kmax = __reduce_max_sync(kFull, hk);
+  const uint32_t mine = hk == kmax ? ~(uint32_t)c[0] : 0xFFFFFFFFu;
   const uint32_t emin = __reduce_min_sync(kFull, mine);
-  *best_key = unordered(kmax);
-  return emin == 0xFFFFFFFFu ? INT_MAX : (int)emin;
+  if (lane == (int)(emin & 31u)) {
+#pragma unroll
+    for (int i = 0; i + 1 < EPL; ++i) c[i] = c[i + 1];
+    c[EPL - 1] = 0ull;
+  }
+  *okey_out = kmax;
+  return emin;
 }
 
 template <int EPL>
@@ -92,6 +102,8 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
              int32_t* __restrict__ idx, float* __restrict__ w, int tokens_per_cta,
              const RouteTotals tot, const RouteFinal fin) {
   __shared__ float s_ps[kRouteWarps][EPL * 32];
+  __shared__ float s_num[kRouteWarps][EPL * 32];   // this token's numerators, by expert
+  __shared__ int s_sel[kRouteWarps][EPL * 32];     // its selected experts, by slot
   __shared__ int s_cnt[EPL * 32];
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,95 +133,85 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
   };
   load_row(t0 + warp);
   for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
-    float l[EPL], key[EPL], num[EPL], p[EPL];
-    int slot[EPL];
+    float l[EPL], num[EPL], p[EPL];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      l[i] = l_next[i];
-      slot[i] = -1;
-    }
+    for (int i = 0; i < EPL; ++i) l[i] = l_next[i];
     load_row(t + kRouteWarps);
+    uint64_t c[EPL];
     if (mode == 2) {
       // Rank fp32 keys first (within kSlack of the exact ones); the exact top
       // k lies among the experts whose fp32 key is within 2 kSlack of the
       // k-th fp32 key, so only those get the double-precision sigmoid.
-      float sa[EPL];
+      float sa[EPL], ka[EPL];
       float part = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const bool v = lane + 32 * i < E;
-        sa[i] = v ? sigmoid_fast(l[i]) : 0.f;
-        key[i] = __fadd_rn(sa[i], bias[i]);
+        const int e = lane + 32 * i;
+        sa[i] = e < E ? sigmoid_fast(l[i]) : 0.f;
+        ka[i] = __fadd_rn(sa[i], bias[i]);
         part += sa[i];
+        c[i] = e < E ? cand_word(ordered(ka[i]), e) : 0ull;
       }
-      const float ssum = warp_sum_bcast(part);
-      uint32_t ok[EPL];
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) ok[i] = ordered(key[i]);
-      float kth = -INFINITY;
-      for (int j = 0; j < top_k; ++j) {
-        const int bi = warp_best<EPL>(ok, slot, lane, E, &kth);
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-          if (lane + 32 * i == bi) slot[i] = j;
-      }
-      const float thr = kth - 4.f * kSlack;
+      const float rs = 1.f / warp_sum_bcast(part);
+      sort_desc<EPL>(c);
+      uint32_t kth = 0u;
+      for (int j = 0; j < top_k; ++j) take_best<EPL>(c, lane, &kth);
+      const float thr = unordered(kth) - 4.f * kSlack;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const bool cand = lane + 32 * i < E && key[i] >= thr;
-        const float s = cand ? sigmoid_f32_via_f64(l[i]) : 0.f;
-        num[i] = s;
-        key[i] = cand ? __fadd_rn(s, bias[i]) : -INFINITY;
-        slot[i] = cand ? -1 : 0x7fff;      // non-candidates never selected
-        p[i] = sa[i] / ssum;
+        const int e = lane + 32 * i;
+        const bool cand = e < E && ka[i] >= thr;
+        const float sx = cand ? sigmoid_f32_via_f64(l[i]) : 0.f;
+        num[i] = sx;
+        c[i] = cand ? cand_word(ordered(__fadd_rn(sx, bias[i])), e) : 0ull;
+        p[i] = sa[i] * rs;
       }
     } else {
-      float m = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) m = fmaxf(m, l[i]);
-      m = warp_max(m);
-      float ex[EPL], part = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const bool v = lane + 32 * i < E;
-        ex[i] = v ? expf(l[i] - m) : 0.f;
-        part += ex[i];
-      }
-      const float z = warp_sum_bcast(part);
+      // key = logit; the numerators are exp(l - max) in both modes: the
+      // renormalised top-k of the softmax and the softmax of the top k are
+      // the same weights
+      uint32_t lmax = 0u;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        p[i] = ex[i] / z;
-        key[i] = l[i];
-        num[i] = mode == 0 ? p[i] : ex[i];
+        const int e = lane + 32 * i;
+        const uint32_t ok = ordered(l[i]);
+        c[i] = e < E ? cand_word(ok, e) : 0ull;
+        lmax = (e < E && ok > lmax) ? ok : lmax;
       }
+      const float m = unordered(__reduce_max_sync(kFull, lmax));
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        num[i] = lane + 32 * i < E ? expf(l[i] - m) : 0.f;
+        part += num[i];
+      }
+      const float rz = 1.f / warp_sum_bcast(part);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) p[i] = num[i] * rz;
     }
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) ps[i] += (lane + 32 * i < E) ? p[i] : 0.f;
-
-    uint32_t ok[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) ok[i] = ordered(key[i]);
-    for (int j = 0; j < top_k; ++j) {
-      float bk;
-      const int bi = warp_best<EPL>(ok, slot, lane, E, &bk);
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i == bi) slot[i] = j;
-    }
-
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) part += (slot[i] >= 0 && slot[i] < top_k) ? num[i] : 0.f;
-    const float zsel = warp_sum_bcast(part);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      if (slot[i] >= 0 && slot[i] < top_k) {
-        const int e = lane + 32 * i;
-        idx[t * top_k + slot[i]] = e;
-        w[t * top_k + slot[i]] = num[i] / zsel;
-        atomicAdd(&s_cnt[e], 1);
-      }
+      ps[i] += p[i];
+      s_num[warp][lane + 32 * i] = num[i];
     }
+    sort_desc<EPL>(c);
+    // k rounds; every lane sums the chosen numerators in slot order
+    float zsel = 0.f;
+    __syncwarp();
+    for (int j = 0; j < top_k; ++j) {
+      uint32_t kj;
+      const uint32_t e = take_best<EPL>(c, lane, &kj);
+      zsel += s_num[warp][e];
+      if (lane == 0) s_sel[warp][j] = (int)e;
+    }
+    __syncwarp();
+    for (int j = lane; j < top_k; j += 32) {
+      const int e = s_sel[warp][j];
+      idx[t * top_k + j] = e;
+      w[t * top_k + j] = s_num[warp][e] / zsel;
+      atomicAdd(&s_cnt[e], 1);
+    }
+    __syncwarp();
   }
 
 #pragma unroll
