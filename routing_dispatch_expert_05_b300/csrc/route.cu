@@ -157,13 +157,48 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
       uint32_t kth = 0u;
       for (int j = 0; j < top_k; ++j) take_best<EPL>(c, lane, &kth);
       const float thr = unordered(kth) - 4.f * kSlack;
+      // The candidates (usually about k of them, spread over the lanes'
+      // EPL slots) are packed into consecutive lanes, so that one warp-wide
+      // double-precision evaluation serves up to 32 of them, and the results
+      // are shuffled back.
+      const unsigned lt_mask = (1u << lane) - 1u;
+      unsigned cm[EPL];
+      int cbase[EPL];
+      int nc = 0;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        cm[i] = __ballot_sync(kFull, lane + 32 * i < E && ka[i] >= thr);
+        cbase[i] = nc;
+        nc += __popc(cm[i]);
+      }
+      float sx[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) sx[i] = 0.f;
+      for (int b0 = 0; b0 < nc; b0 += 32) {
+        const int o = b0 + lane;                      // the candidate this lane evaluates
+        float lo = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int n = o - cbase[i];
+          const bool here = n >= 0 && n < __popc(cm[i]);
+          const int src = here ? (int)__fns(cm[i], 0, n + 1) : 0;
+          const float v = __shfl_sync(kFull, l[i], src);
+          if (here) lo = v;
+        }
+        const float so = o < nc ? sigmoid_f32_via_f64(lo) : 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int myo = cbase[i] + __popc(cm[i] & lt_mask);
+          const float v = __shfl_sync(kFull, so, (myo - b0) & 31);
+          if (((cm[i] >> lane) & 1u) && myo >= b0 && myo < b0 + 32) sx[i] = v;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        const bool cand = e < E && ka[i] >= thr;
-        const float sx = cand ? sigmoid_f32_via_f64(l[i]) : 0.f;
-        num[i] = sx;
-        c[i] = cand ? cand_word(ordered(__fadd_rn(sx, bias[i])), e) : 0ull;
+        const bool cand = (cm[i] >> lane) & 1u;
+        num[i] = sx[i];
+        c[i] = cand ? cand_word(ordered(__fadd_rn(sx[i], bias[i])), e) : 0ull;
         p[i] = sa[i] * rs;
       }
     } else {

@@ -164,7 +164,10 @@ def test_dispatch_flags_bad_expert_index():
 # ---------------------------------------------------------- expert FFNs
 FFN_CASES = [("toy_top2_fp32", 64), ("capacity_top2_fp32", 700),
              ("capacity_top2_bf16", 700), ("deepseek_v3_block", 300),
-             ("qwen3_moe", 200)]
+             ("qwen3_moe", 200),
+             # enough rows per expert for CTA pairs, with short group tails
+             # left to the single-CTA pass
+             ("deepseek_v3_block", 1536)]
 
 
 def _oracle_dispatch_inputs(shape, inp, zipf=1.1, seed=77):
