@@ -331,6 +331,46 @@ MOE_API moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_hos
                               moe_stats_t *stats, void *ws, size_t ws_bytes,
                               void *stream);
 
+/* ---- backward ------------------------------------------------------------ */
+
+/* Gradients of L = <dout, out> + d_balance * B with the routing held fixed
+ * ("DeepSeek 5.7: MoE from scratch", Worked example and study lab: the router
+ * receives gradients through the contribution weights, the top-k choice is
+ * not differentiable, an expert no token chose receives none).  The reading
+ * (the pages give no formulas): the selected experts and the kept
+ * assignments are those of the forward; the contribution weights (softmax
+ * over the selected logits, or s_sel / sum s_sel in the sigmoid mode) and
+ * the balance statistic (through p; the counts are constant) are
+ * differentiated through the logits; dropped assignments pass nothing to
+ * their expert.  All outputs fp32, device memory, overwritten:
+ *   dx [N, d], d_w_router [E, d], d_b_router [E] (nullable; only with a
+ *   router bias), d_w1 / d_w3 [E, F, d], d_w2 [E, d, F]. */
+typedef struct {
+  float *dx;
+  float *d_w_router;
+  float *d_b_router;
+  float *d_w1;
+  float *d_w3;
+  float *d_w2;
+} moe_grads_t;
+
+/* Bytes of workspace moe_backward needs (the forward's plus the gradient
+ * intermediates: recomputed activations, transposed operands). */
+MOE_API moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes);
+
+/* The backward pass: recomputes the forward's routing, grouping and expert
+ * activations from x, then runs the gradients back through the combine, the
+ * experts (data and weight gradients on the tensor cores) and the router.
+ * x [N, d] and dout [N, d] are bf16 device arrays.  Supported: bf16 SwiGLU
+ * experts without expert biases or shared experts, d and F multiples of 64,
+ * E a multiple of 8, N > 0 (else MOE_ERR_UNSUPPORTED, nothing enqueued).
+ * With a capacity the drops are those of the forward.  Enqueued on
+ * `stream`; ws as for moe_forward, moe_backward_workspace_size bytes. */
+MOE_API moe_status_t moe_backward(const moe_config_t *cfg, const void *x,
+                                  const moe_weights_t *weights, const void *dout,
+                                  float d_balance, moe_grads_t *grads, void *ws,
+                                  size_t ws_bytes, void *stream);
+
 /* ---- between steps ------------------------------------------------------ */
 
 /* Balancing-bias update and load diagnostic ("DeepSeek 5.7", section 2: a

@@ -26,7 +26,8 @@ struct Layout {
   size_t err, fin_ticket, route_psum, route_cnt, chunk_cnt, chunk_base, logits,
       scratch_end;
   // intermediates of moe_forward
-  size_t idx, w, offsets, row_of_slot, token_of_row, x_perm, h, y, y_e8, h_shared,
+  size_t idx, w, offsets, row_of_slot, token_of_row, slot_of_row, x_perm, h, y, y_e8,
+      h_shared,
       shared_out, x_stage, out_stage, total;
   int chunks;
 };
@@ -57,6 +58,7 @@ Layout layout_of(const moe_config_t& c) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.row_of_slot = take((size_t)N * k * 4);
   L.token_of_row = take((size_t)N * k * 4);
+  L.slot_of_row = take((size_t)N * k * 4);
   L.x_perm = take((size_t)N * k * d * es);
   L.h = take((size_t)N * k * F * es);
   // expert outputs: fp32, or (bf16 layers on the tensor cores) fp16 with an
@@ -280,10 +282,12 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
 
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                    int32_t* offsets, int32_t* ros, int32_t* tor, void* x_perm,
-                   moe_stats_t* stats, const Scratch& sc, cudaStream_t st) {
+                   moe_stats_t* stats, const Scratch& sc, cudaStream_t st,
+                   int32_t* slot_of_row = nullptr) {
   launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c), sc.chunk_cnt,
                   sc.chunk_base, offsets, ros, tor, stats ? stats->counts : nullptr,
-                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st);
+                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st,
+                  slot_of_row);
   if (x_perm != nullptr)
     launch_scatter_rows(x, (int64_t)c.d_model * elem_size(c), ros, c.n_tokens, c.top_k,
                         x_perm, num_sms(), st);
@@ -356,9 +360,13 @@ moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_ma
 
 // y_e8 != null asks for the compact expert outputs (fp16 + exponents); it
 // returns MOE_ERR_UNSUPPORTED (nothing launched) where only fp32 y is made.
+// With slot_of_row and wts (compact output only) row r is written, scaled by
+// its routing weight, to row slot_of_row[r] = t*k + j: the weighted expert
+// outputs in slot order, for launch_combine_slots.
 moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offsets,
                        const moe_weights_t& w, void* y, uint8_t* y_e8, int32_t* err,
-                       cudaStream_t st) {
+                       cudaStream_t st, const int32_t* slot_of_row = nullptr,
+                       const float* wts = nullptr) {
   GemmProblem p{};
   p.A = h;
   p.B0 = w.w2;
@@ -399,6 +407,8 @@ moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offs
     q.c_is_f32 = 0;
     q.c_e8 = y_e8;
     q.e8_cols = (int)ceil_div64(c.d_model, kYScaleBlock);
+    q.c_row_map = slot_of_row;
+    q.c_row_scale = wts;
     if (c.dtype != MOE_BF16 || !tc_gemm_supported(q)) return MOE_ERR_UNSUPPORTED;
     return launch_tc_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
   }
@@ -694,14 +704,17 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
   // the GEMM instead (moe_expert_up_gather: tile::gather4, one 128-byte row
   // piece per row and k-block) saves that memory but measured 3.3x slower
   // on the Qwen3-style layer.
-  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, sc, st);
+  int32_t* sor = at<int32_t>(ws, L.slot_of_row);
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, &ds, sc, st, sor);
   mark(2);
   MOE_TRY(up_body(c, x_perm, nullptr, offsets, w, h, sc.err, st));
   mark(3);
   // bf16 layers keep the expert outputs compact (half the bytes of fp32)
   uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
-  moe_status_t ds_ = c.dtype == MOE_BF16 ? down_body(c, h, offsets, w, y, y_e8, sc.err, st)
-                                         : MOE_ERR_UNSUPPORTED;
+  // (weighted and in slot order, so that the combine streams a token's rows)
+  moe_status_t ds_ = c.dtype == MOE_BF16
+                         ? down_body(c, h, offsets, w, y, y_e8, sc.err, st, sor, wts)
+                         : MOE_ERR_UNSUPPORTED;
   const bool compact = ds_ == MOE_OK;
   if (ds_ == MOE_ERR_UNSUPPORTED) ds_ = down_body(c, h, offsets, w, y, nullptr, sc.err, st);
   MOE_TRY(ds_);
@@ -710,8 +723,8 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
     MOE_TRY(shared_body(c, x, w, at<char>(ws, L.h_shared), shared_out, sc.err, st));
   mark(5);
   if (compact)
-    launch_combine_compact(y, y_e8, ros, wts, shared_out, out, c.n_tokens, c.top_k,
-                           c.d_model, c.dtype == MOE_BF16, num_sms(), st);
+    launch_combine_slots(y, y_e8, ros, shared_out, out, c.n_tokens, c.top_k, c.d_model,
+                         c.dtype == MOE_BF16, num_sms(), st);
   else
     launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
                    c.dtype == MOE_BF16, num_sms(), st);
@@ -841,6 +854,215 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
   return ok ? last_cuda() : MOE_ERR_CUDA;
 }
 
+// ---- backward -------------------------------------------------------------
+// Buffers of moe_backward after the forward's own layout (which holds the
+// recomputed routing, grouping, x_perm, h and compact y).
+struct BwLayout {
+  Layout fw;
+  int64_t kt, nt;        // columns of the transposed grouped / token operands
+  size_t counts, koff, koff_n, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, xpT, dyT, hT,
+      dguT, dzT, xT, w2T, w13T, wrT, total;
+};
+
+BwLayout bw_layout_of(const moe_config_t& c) {
+  BwLayout B{};
+  B.fw = layout_of(c);
+  size_t o = B.fw.total;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
+  const int64_t M = N * k;
+  B.kt = (M + 64 * E + 63) / 64 * 64;                 // every group padded to 64
+  B.nt = (N + 63) / 64 * 64 + 64;
+  B.counts = take((size_t)E * 4);
+  B.koff = take((size_t)(E + 1) * 4);
+  B.koff_n = take(2 * 4);
+  B.g = take((size_t)M * F * 2);
+  B.u = take((size_t)M * F * 2);
+  B.dy = take((size_t)M * d * 2);
+  B.dh = take((size_t)M * F * 2);
+  B.dgu = take((size_t)M * 2 * F * 2);
+  B.dxp = take((size_t)M * d * 2);
+  B.dz = take((size_t)N * E * 4);
+  B.dz16 = take((size_t)N * E * 2);
+  B.dxr = take((size_t)N * d * 4);
+  B.dw = take((size_t)N * k * 4);
+  B.xpT = take((size_t)d * B.kt * 2);
+  B.dyT = take((size_t)d * B.kt * 2);
+  B.hT = take((size_t)F * B.kt * 2);
+  B.dguT = take((size_t)2 * F * B.kt * 2);
+  B.dzT = take((size_t)E * B.nt * 2);
+  B.xT = take((size_t)d * B.nt * 2);
+  B.w2T = take((size_t)E * F * d * 2);
+  B.w13T = take((size_t)E * 2 * d * F * 2);
+  B.wrT = take((size_t)d * E * 2);
+  B.total = o;
+  return B;
+}
+
+moe_status_t check_backward_args(const moe_config_t* cfg, const moe_weights_t* w) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  // the tensor-core path: bf16 SwiGLU experts without biases or shared
+  // experts, feature widths in whole k-blocks, E a multiple of 8 (the
+  // router's gradient GEMMs read E-wide rows)
+  if (c.dtype != MOE_BF16 || c.expert != MOE_EXPERT_SWIGLU || c.has_bias || c.n_shared > 0 ||
+      c.d_ff % 64 != 0 || c.d_model % 64 != 0 || c.n_experts % 8 != 0)
+    return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_router_weights(c, w));
+  MOE_TRY(check_up_weights(c, w));
+  return check_down_weights(c, w);
+}
+
+TcProblem plain_problem(const void* A, int64_t a_rows, int K, const void* B0, int b_groups,
+                        int b_rows, const int32_t* offsets, int n_groups, int64_t rows,
+                        int n_out, void* C, int c_is_f32, int32_t* err) {
+  TcProblem q{};
+  q.A = A;
+  q.a_rows = a_rows;
+  q.K = K;
+  q.B0 = B0;
+  q.b_groups = b_groups;
+  q.b_rows = b_rows;
+  q.k_sub = K;
+  q.n_sub = 1;
+  q.offsets = offsets;
+  q.n_groups = n_groups;
+  q.rows = rows;
+  q.n_out = n_out;
+  q.epilogue = kEpiNone;
+  q.C = C;
+  q.c_is_f32 = c_is_f32;
+  q.err = err;
+  return q;
+}
+
+moe_status_t tc_run(const TcProblem& q, cudaStream_t st) {
+  if (!tc_gemm_supported(q)) return MOE_ERR_UNSUPPORTED;
+  return launch_tc_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t wgrad_run(const void* A, int rows_a, const void* B, int rows_b, int64_t k_total,
+                       const int32_t* koff, int groups, float* C, int32_t* err,
+                       cudaStream_t st) {
+  WgradProblem q{};
+  q.A = A;
+  q.B = B;
+  q.rows_a = rows_a;
+  q.rows_b = rows_b;
+  q.k_total = k_total;
+  q.k_offsets = koff;
+  q.n_groups = groups;
+  q.C = C;
+  q.err = err;
+  return launch_tc_wgrad(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The backward pass (routing held fixed): the forward's routing, grouping
+// and expert activations are recomputed, then the gradients run back
+// through the combine, the experts and the router.
+moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weights_t& w,
+                           const void* dout, float d_balance, moe_grads_t& gr, void* ws,
+                           cudaStream_t st) {
+  const BwLayout B = bw_layout_of(c);
+  const Layout& L = B.fw;
+  const Scratch sc = scratch_of(L, ws);
+  const int64_t N = c.n_tokens, M = N * c.top_k;
+  const int E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* wts = at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* ros = at<int32_t>(ws, L.row_of_slot);
+  int32_t* tor = at<int32_t>(ws, L.token_of_row);
+  void* x_perm = at<char>(ws, L.x_perm);
+  void* h = at<char>(ws, L.h);
+  void* y = at<char>(ws, L.y);
+  uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
+  int32_t* counts = at<int32_t>(ws, B.counts);
+  int32_t* koff = at<int32_t>(ws, B.koff);
+  int32_t* koff_n = at<int32_t>(ws, B.koff_n);
+  void* g = at<char>(ws, B.g);
+  void* u = at<char>(ws, B.u);
+  void* dy = at<char>(ws, B.dy);
+  void* dh = at<char>(ws, B.dh);
+  void* dgu = at<char>(ws, B.dgu);
+  void* dxp = at<char>(ws, B.dxp);
+  float* dz = at<float>(ws, B.dz);
+  void* dz16 = at<char>(ws, B.dz16);
+  float* dxr = at<float>(ws, B.dxr);
+  float* dw = at<float>(ws, B.dw);
+  char* xpT = at<char>(ws, B.xpT);
+  char* dyT = at<char>(ws, B.dyT);
+  char* hT = at<char>(ws, B.hT);
+  char* dguT = at<char>(ws, B.dguT);
+  char* dzT = at<char>(ws, B.dzT);
+  char* xT = at<char>(ws, B.xT);
+  char* w2T = at<char>(ws, B.w2T);
+  char* w13T = at<char>(ws, B.w13T);
+  char* wrT = at<char>(ws, B.wrT);
+  const int ns = num_sms();
+
+  // 1. recompute: routing (counts for the balance term), grouping, x_perm,
+  //    g = x W1^T, u = x W3^T, h = silu(g) u, y = h W2^T (compact, row order)
+  moe_stats_t rs{};
+  rs.counts = counts;
+  router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true);
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, nullptr, sc, st);
+  TcProblem q = plain_problem(x_perm, M, d, w.w1, E, F, offsets, E, M, F, g, 0, sc.err);
+  q.use_pairs = pairs_pay(c);
+  MOE_TRY(tc_run(q, st));
+  q.B0 = w.w3;
+  q.C = u;
+  MOE_TRY(tc_run(q, st));
+  launch_silu_mul(g, u, h, offsets, E, F, ns, st);
+  MOE_TRY(down_body(c, h, offsets, w, y, y_e8, sc.err, st));
+
+  // 2. combine and router: dw, dy = w dout, dlogits
+  launch_combine_backward(y, y_e8, ros, wts, dout, N, k, d, dw, dy, ns, st);
+  launch_router_backward(sc.logits, idx, wts, dw, counts, N, E, k, c.route, c.balance_coef,
+                         d_balance, dz, dz16, st);
+
+  // 3. data gradients: dh = dy W2, [dg | du] = SwiGLU', dx_perm = dg W1 + du W3,
+  //    dx = sum over slots + dlogits Wr
+  launch_transpose_batched(w.w2, E, d, F, w2T, (int64_t)F * d, st);
+  launch_transpose_batched(w.w1, E, F, d, w13T, (int64_t)2 * d * F, st);
+  launch_transpose_batched(w.w3, E, F, d, w13T + (size_t)d * F * 2, (int64_t)2 * d * F, st);
+  launch_transpose_batched(w.w_router, 1, E, d, wrT, (int64_t)d * E, st);
+  q = plain_problem(dy, M, d, w2T, E, F, offsets, E, M, F, dh, 0, sc.err);
+  q.use_pairs = pairs_pay(c);
+  MOE_TRY(tc_run(q, st));
+  launch_swiglu_backward(dh, g, u, dgu, offsets, E, F, ns, st);
+  q = plain_problem(dgu, M, 2 * F, w13T, E, d, offsets, E, M, d, dxp, 0, sc.err);
+  q.k_sub = F;
+  q.n_sub = 2;
+  q.use_pairs = pairs_pay(c);
+  MOE_TRY(tc_run(q, st));
+  q = plain_problem(dz16, N, E, wrT, 1, d, nullptr, 1, N, d, dxr, 1, sc.err);
+  MOE_TRY(tc_run(q, st));
+  launch_dx_reduce(dxp, ros, dxr, N, k, d, gr.dx, ns, st);
+
+  // 4. weight gradients over each expert's rows (transposed, zero-padded)
+  launch_pad_offsets(offsets, M, E, koff, st);
+  launch_transpose_grouped(x_perm, false, d, offsets, M, E, koff, B.kt, xpT, st);
+  launch_transpose_grouped(dy, false, d, offsets, M, E, koff, B.kt, dyT, st);
+  launch_transpose_grouped(h, false, F, offsets, M, E, koff, B.kt, hT, st);
+  launch_transpose_grouped(dgu, false, 2 * F, offsets, M, E, koff, B.kt, dguT, st);
+  MOE_TRY(wgrad_run(dyT, d, hT, F, B.kt, koff, E, gr.d_w2, sc.err, st));
+  MOE_TRY(wgrad_run(dguT, F, xpT, d, B.kt, koff, E, gr.d_w1, sc.err, st));
+  MOE_TRY(wgrad_run(dguT + (size_t)F * B.kt * 2, F, xpT, d, B.kt, koff, E, gr.d_w3, sc.err,
+                    st));
+  // router: d_w_router = dlogits^T x over all tokens (one group)
+  launch_pad_offsets(nullptr, N, 1, koff_n, st);
+  launch_transpose_grouped(dz16, false, E, nullptr, N, 1, koff_n, B.nt, dzT, st);
+  launch_transpose_grouped(x, false, d, nullptr, N, 1, koff_n, B.nt, xT, st);
+  MOE_TRY(wgrad_run(dzT, E, xT, d, B.nt, koff_n, 1, gr.d_w_router, sc.err, st));
+  if (gr.d_b_router != nullptr) launch_column_sums(dz, N, E, gr.d_b_router, st);
+  return last_cuda();
+}
+
 }  // namespace
 
 extern "C" {
@@ -905,6 +1127,29 @@ moe_status_t moe_update_selection_bias(const moe_config_t* cfg, const int32_t* c
   launch_bias_update(counts, cfg->n_experts, gamma, sel_bias, load_cv,
                      static_cast<cudaStream_t>(stream));
   return last_cuda();
+}
+
+moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = bw_layout_of(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* weights,
+                          const void* dout, float d_balance, moe_grads_t* grads, void* ws,
+                          size_t ws_bytes, void* stream) {
+  MOE_TRY(check_backward_args(cfg, weights));
+  const moe_config_t& c = *cfg;
+  if (grads == nullptr || !std::isfinite(d_balance)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(ws, ws_bytes, bw_layout_of(c).total));
+  if (c.n_tokens == 0) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(need({x, dout, grads->dx, grads->d_w_router, grads->d_w1, grads->d_w3,
+                grads->d_w2}));
+  MOE_TRY(maybe({grads->d_b_router}));
+  if (grads->d_b_router != nullptr && weights->b_router == nullptr) return MOE_ERR_INVALID_ARG;
+  return backward_impl(c, x, *weights, dout, d_balance, *grads, ws,
+                       static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_read_device_error(void* ws, int32_t* code, void* stream) {

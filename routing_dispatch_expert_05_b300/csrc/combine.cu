@@ -107,87 +107,55 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_s
   }
 }
 
-// The same gather-reduce over compact expert outputs: y16 [N*k, d] fp16 and
-// one exponent byte per (row, 32 columns), value = y16 * 2^(e8 - 127).  The
-// power of two folds into the weight (an exact product), so the fp32 sum is
-// sum_j (w_j * 2^(e8_j - 127)) * y16_j in slot order, as for fp32 y.
-// The kernel is bound by the latency of its row loads, so it keeps them
-// back to back: the next token's slot rows and weights (up to 8) are loaded
-// while this token's expert rows are in flight and handed over through
-// shared memory, so each token costs one round trip to memory, not two.
-constexpr int kPrefetchSlots = 8;
+// The combine when the down projection has already weighted and placed the
+// expert outputs (compact) in slot order: row t*k + j holds w[t,j] * y of
+// slot j, so of the weighted sum ("DeepSeek 5.7", s.3) only the sum is left
+// here.  out[t] = sum over kept slots j of those rows, in slot order, + S[t].  A token's k rows are contiguous, so the kernel streams
+// them; their addresses need no index load.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 3)
-combine_compact_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
-                       const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
-                       const float* __restrict__ shared, T* __restrict__ out,
-                       int64_t n_tokens, int top_k, int d_model) {
+__global__ void __launch_bounds__(kThreads, 4)
+combine_slots_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
+                     const int32_t* __restrict__ row_of_slot,
+                     const float* __restrict__ shared, T* __restrict__ out,
+                     int64_t n_tokens, int top_k, int d_model) {
   constexpr int C = 8;                       // columns per thread step (16 B of fp16)
-  constexpr int KB = kPrefetchSlots;
-  __shared__ int s_r[2][KB];
-  __shared__ float s_w[2][KB];
+  constexpr int KB = 8;                      // slots in flight
   const int nvec = d_model / C;
   const int e8_cols = (d_model + kYScaleBlock - 1) / kYScaleBlock;
-  const int tid = threadIdx.x;
-  const int kp = min(top_k, KB);             // slots handed over through shared memory
-  int64_t t = blockIdx.x;
-  if (tid < kp && t < n_tokens) {
-    s_r[0][tid] = row_of_slot[t * top_k + tid];
-    s_w[0][tid] = w[t * top_k + tid];
-  }
-  __syncthreads();
-  int buf = 0;
-  for (; t < n_tokens; t += gridDim.x) {
-    const int64_t tn = t + gridDim.x;
-    int r_next = -1;
-    float w_next = 0.f;
-    if (tid < kp && tn < n_tokens) {
-      r_next = row_of_slot[tn * top_k + tid];
-      w_next = w[tn * top_k + tid];
-    }
-    for (int v = tid; v < nvec; v += blockDim.x) {
+  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
       const int64_t col = (int64_t)v * C;
       const int blk = (int)(col / kYScaleBlock);
       float acc[C];
 #pragma unroll
       for (int i = 0; i < C; ++i) acc[i] = 0.f;
-      uint4 val[KB];
-      float cj[KB];
+      for (int j0 = 0; j0 < top_k; j0 += KB) {
+        uint4 val[KB];
+        float sc[KB];
+        bool keep[KB];
 #pragma unroll
-      for (int q = 0; q < KB; ++q) {
-        const int r = q < kp ? s_r[buf][q] : -1;
-        cj[q] = 0.f;
-        val[q] = make_uint4(0u, 0u, 0u, 0u);
-        if (r >= 0) {
-          val[q] = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
-          const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
-          cj[q] = s_w[buf][q] * __uint_as_float(e8 << 23);
+        for (int q = 0; q < KB; ++q) {
+          const int j = j0 + q;
+          const int64_t slot = t * top_k + j;
+          keep[q] = false;
+          sc[q] = 0.f;
+          val[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (j < top_k) {
+            keep[q] = row_of_slot[slot] >= 0;       // dropped slots hold no row
+            val[q] = __ldcs(reinterpret_cast<const uint4*>(y + slot * d_model + col));
+            sc[q] = __uint_as_float((uint32_t)y_e8[slot * e8_cols + blk] << 23);
+          }
         }
-      }
 #pragma unroll
-      for (int q = 0; q < KB; ++q) {
-        if (q >= kp || s_r[buf][q] < 0) continue;       // absent or dropped
-        const __half2* h2 = reinterpret_cast<const __half2*>(&val[q]);
+        for (int q = 0; q < KB; ++q) {
+          if (!keep[q]) continue;
+          const __half2* h2 = reinterpret_cast<const __half2*>(&val[q]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(h2[i]);
-          acc[2 * i] = fmaf(cj[q], f.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(cj[q], f.y, acc[2 * i + 1]);
-        }
-      }
-      // slots past the first KB (top_k > 8), in order, straight from memory
-      for (int j = KB; j < top_k; ++j) {
-        const int r = row_of_slot[t * top_k + j];
-        if (r < 0) continue;
-        const uint4 vj = __ldcs(reinterpret_cast<const uint4*>(y + (int64_t)r * d_model + col));
-        const uint32_t e8 = y_e8[(int64_t)r * e8_cols + blk];
-        const float c = w[t * top_k + j] * __uint_as_float(e8 << 23);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&vj);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(h2[i]);
-          acc[2 * i] = fmaf(c, f.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(c, f.y, acc[2 * i + 1]);
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(h2[i]);
+            acc[2 * i] = fmaf(sc[q], f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(sc[q], f.y, acc[2 * i + 1]);
+          }
         }
       }
       if (shared != nullptr) {
@@ -209,33 +177,23 @@ combine_compact_kernel(const __half* __restrict__ y, const uint8_t* __restrict__
         st_vec16(op, o);
       }
     }
-    // hand the next token's slots over (every thread is done with buf's)
-    if (tid < kp) {
-      s_r[buf ^ 1][tid] = r_next;
-      s_w[buf ^ 1][tid] = w_next;
-    }
-    __syncthreads();
-    buf ^= 1;
   }
 }
 
 }  // namespace
 
-void launch_combine_compact(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
-                            const float* w, const float* shared, void* out, int64_t n_tokens,
-                            int top_k, int d_model, int is_bf16, int num_sms,
-                            cudaStream_t st) {
+void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
+                          const float* shared, void* out, int64_t n_tokens, int top_k,
+                          int d_model, int is_bf16, int num_sms, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  // three CTAs per SM are resident (register bound); a CTA walks its tokens
-  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 3);
+  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 4);
   const __half* y = static_cast<const __half*>(y16);
   if (is_bf16)
-    combine_compact_kernel<bf16><<<blocks, kThreads, 0, st>>>(
-        y, y_e8, row_of_slot, w, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
+    combine_slots_kernel<bf16><<<blocks, kThreads, 0, st>>>(
+        y, y_e8, row_of_slot, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
   else
-    combine_compact_kernel<float><<<blocks, kThreads, 0, st>>>(
-        y, y_e8, row_of_slot, w, shared, static_cast<float*>(out), n_tokens, top_k,
-        d_model);
+    combine_slots_kernel<float><<<blocks, kThreads, 0, st>>>(
+        y, y_e8, row_of_slot, shared, static_cast<float*>(out), n_tokens, top_k, d_model);
 }
 
 void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,

@@ -93,7 +93,8 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
                      const int32_t* __restrict__ chunk_base,
                      const int32_t* __restrict__ offsets,
                      int32_t* __restrict__ row_of_slot,
-                     int32_t* __restrict__ token_of_row) {
+                     int32_t* __restrict__ token_of_row,
+                     int32_t* __restrict__ slot_of_row) {
   __shared__ int s_w[kRankWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kRankWarps * kMaxExperts; i += blockDim.x)
@@ -145,6 +146,7 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
       if (e >= 0 && (capacity < 0 || rank < capacity)) {
         row = offsets[e] + rank;
         token_of_row[row] = (int32_t)(s / top_k);
+        if (slot_of_row != nullptr) slot_of_row[row] = (int32_t)s;
       }
       row_of_slot[s] = row;
     }
@@ -275,7 +277,8 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int n_experts, int64_t capacity, int32_t* chunk_cnt,
                      int32_t* chunk_base, int32_t* offsets, int32_t* row_of_slot,
                      int32_t* token_of_row, int32_t* counts, int32_t* kept,
-                     int32_t* dropped, int32_t* err, cudaStream_t st) {
+                     int32_t* dropped, int32_t* err, cudaStream_t st,
+                     int32_t* slot_of_row) {
   const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
   if (chunks > 0)
     dispatch_count_kernel<<<chunks, 256, 0, st>>>(idx, n_tokens, top_k, n_experts,
@@ -286,7 +289,7 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
   if (chunks > 0)
     dispatch_rank_kernel<<<chunks, kRankWarps * 32, 0, st>>>(
         idx, n_tokens, top_k, n_experts, capacity, chunk_base, offsets,
-        row_of_slot, token_of_row);
+        row_of_slot, token_of_row, slot_of_row);
 }
 
 void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,

@@ -98,6 +98,15 @@ struct Params {
   int32_t* err;
   const int32_t* a_row_map;   // null: A rows are the tile rows; else A row r
                               // is row a_row_map[r] of the A tensor
+  const int32_t* c_row_map;   // compact output only: row r goes to output row
+                              // c_row_map[r] (null: row r)
+  const float* c_row_scale;   // compact output only: output row o is scaled by
+                              // c_row_scale[o] before compacting (null: 1)
+  // weight-gradient kernel: group g contracts columns k_offsets[g] ..
+  // k_offsets[g+1] (non-zero multiples of BK) of A [wg_rows, *] and B
+  // [n_out, *] into rows g * wg_rows .. of C
+  const int32_t* k_offsets;
+  int wg_rows;
 };
 
 // ---------------------------------------------------------------- PTX
@@ -300,6 +309,23 @@ __device__ __forceinline__ void store_staged_b16(const uint32_t* stg, int lane, 
   }
 }
 
+// The same 64-byte row segments to output rows given per lane: lane r holds
+// the output row of staged row r (negative: not stored).
+__device__ __forceinline__ void store_staged_b16_rows(const uint32_t* stg, int lane, int orow,
+                                                      int col0, int n_out, void* C) {
+  const int c8 = lane & 3;
+  const bool col_ok = col0 + c8 * 8 < n_out;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2);
+    const int o = __shfl_sync(0xffffffffu, orow, r);
+    if (col_ok && o >= 0) {
+      const uint4 val = *reinterpret_cast<const uint4*>(stg + r * kStgB16Stride + c8 * 4);
+      st_vec16(static_cast<uint16_t*>(C) + (int64_t)o * n_out + col0 + c8 * 8, val);
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -314,8 +340,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // into [2^14, 2^15); v * 2^s (exact) is rounded once to fp16, and the biased
 // exponent of 2^-s (one byte, an E8 shared exponent) is stored beside it.
 // The warp takes half `half` of the tile's 256 columns (4 exponents).
-__device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, int lane,
-                                              int row_base, const bf16* bp, int ci, int c0,
+__device__ __forceinline__ void compact_chunk(const Params& p, int lane, int orow, float rscale,
+                                              const bf16* bp, int ci, int c0,
                                               const uint32_t (&r)[32], uint32_t* stg,
                                               uint32_t& e8w) {
   float v[32];
@@ -324,6 +350,7 @@ __device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, i
   for (int j = 0; j < 32; ++j) {
     v[j] = __uint_as_float(r[j]);
     if (bp != nullptr && c0 + j < p.n_out) v[j] += __bfloat162float(bp[c0 + j]);
+    v[j] *= rscale;
     mx = fmaxf(mx, fabsf(v[j]));                   // columns past n_out hold 0
   }
   int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
@@ -338,7 +365,7 @@ __device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, i
                         pack_half2(v[8 * j + 4] * scale, v[8 * j + 5] * scale),
                         pack_half2(v[8 * j + 6] * scale, v[8 * j + 7] * scale));
   __syncwarp();
-  store_staged_b16(stg, lane, row_base, tl.row_end, c0, p.n_out, p.C);
+  store_staged_b16_rows(stg, lane, orow, c0, p.n_out, p.C);
   __syncwarp();
 }
 
@@ -346,6 +373,13 @@ __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, in
                                              int row_base, uint32_t tb, uint32_t* stg) {
   constexpr int kCh = BN / 32 / 2;                 // chunks per half
   const int row = row_base + lane;
+  // this lane's output row (rows past the group are not stored) and scale
+  int orow = -1;
+  float rscale = 1.f;
+  if (row < tl.row_end) {
+    orow = p.c_row_map != nullptr ? __ldg(p.c_row_map + row) : row;
+    if (p.c_row_scale != nullptr) rscale = __ldg(p.c_row_scale + orow);
+  }
   const bf16* bp = p.bias ? p.bias + (int64_t)tl.g * p.bias_stride : nullptr;
   const int ch0 = half * kCh;
   uint32_t e8w = 0u;                               // this row's 4 exponents
@@ -358,18 +392,18 @@ __device__ __forceinline__ void compact_tile(const Params& p, const Tile& tl, in
     // chunk ci is in ra (even ci) or rb (odd ci); load the next one first
     if (ci % 2 == 0) {
       if (ci + 1 < kCh) MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, rb);
-      if (c0 < p.n_out) compact_chunk(p, tl, lane, row_base, bp, ci, c0, ra, stg, e8w);
+      if (c0 < p.n_out) compact_chunk(p, lane, orow, rscale, bp, ci, c0, ra, stg, e8w);
       if (ci + 1 < kCh) MOE_TMEM_WAIT32(rb);
     } else {
       if (ci + 1 < kCh) MOE_TMEM_LD32(tb + (ch0 + ci + 1) * 32, ra);
-      if (c0 < p.n_out) compact_chunk(p, tl, lane, row_base, bp, ci, c0, rb, stg, e8w);
+      if (c0 < p.n_out) compact_chunk(p, lane, orow, rscale, bp, ci, c0, rb, stg, e8w);
       if (ci + 1 < kCh) MOE_TMEM_WAIT32(ra);
     }
   }
-  if (row < tl.row_end) {
+  if (orow >= 0) {
     const int b0 = tl.n * (BN / 32) + half * kCh;  // first exponent index
     const int n4 = min(kCh, p.e8_cols - b0);
-    uint8_t* ep = p.c_e8 + (int64_t)row * p.e8_cols + b0;
+    uint8_t* ep = p.c_e8 + (int64_t)orow * p.e8_cols + b0;
     if (n4 == 4 && (reinterpret_cast<uintptr_t>(ep) & 3u) == 0) {
       *reinterpret_cast<uint32_t*>(ep) = e8w;
     } else {
@@ -614,7 +648,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
               tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
             } else {
-              const int sub = kb / kb_per_sub;
+              // K split into n_sub blocks of B (whole k-blocks each); with
+              // one block, K itself (of any length)
+              const int sub = p.n_sub > 1 ? kb / kb_per_sub : 0;
               const int kk = (kb - sub * kb_per_sub) * BK;
               const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN;
               tma_load_2d(b, &tmB0, &full[stage], kk, brow);
@@ -704,6 +740,169 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       } else {
         store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------- weight gradients
+// Per group g: C[g*R + i, j] = sum over c in [k_offsets[g], k_offsets[g+1])
+// of A[i, c] * B[j, c], fp32 out (R = wg_rows rows of A, n_out rows of B).
+// A and B are the grouped activations transposed (feature-major, the tokens'
+// rows as columns, each group's span zero-padded to whole k-blocks), so the
+// contraction over a group's rows is an ordinary K-major MMA loop whose
+// length differs per group.  The pipeline is the single-CTA kernel's: one
+// CTA per SM walks the (g, m, n) tiles; TMA producer, one MMA thread, eight
+// epilogue warps, two TMEM accumulators, bounded waits.
+__global__ void __launch_bounds__(kThreads, 1)
+tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kTileA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = p.wg_rows;
+  const int mt = (R + BM - 1) / BM;
+  const int nt = (p.n_out + BN - 1) / BN;
+  const int per_g = mt * nt;
+  const int total = p.n_groups * per_g;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&tmA);
+    prefetch_map(&tmB);
+  }
+  if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_phases = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const int g = t / per_g, l = t - g * per_g;
+        const int m = l / nt, n = l - m * nt;
+        const int k0 = p.k_offsets[g];
+        const int nkb = (p.k_offsets[g + 1] - k0) / BK;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
+          mbar_expect_tx(&full[stage], kTileA + (uint32_t)BN * BK * 2);
+          tma_load_2d(sA + stage * kTileA, &tmA, &full[stage], k0 + kb * BK, m * BM);
+          tma_load_2d(sB + stage * kTileB, &tmB, &full[stage], k0 + kb * BK, n * BN);
+          used |= 1u << stage;
+          last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      for (int s = 0; s < kStages; ++s) {
+        if (!(used >> s & 1u)) continue;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&full[s], last_phases >> s & 1u)) {
+          if (globaltimer() - t0 > kTimeoutNs) {
+            set_device_error(p.err, kDevTimeout);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const int g = t / per_g;
+        const int nkb = (p.k_offsets[g + 1] - p.k_offsets[g]) / BK;
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&full[stage], phase, s_abort, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kTileA);
+          const uint32_t b0 = smem_u32(sB + stage * kTileB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
+                 (kb | kk) != 0);
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      umma_commit(drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+          set_device_error(p.err, kDevTimeout);
+          break;
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    float* stg_f = reinterpret_cast<float*>(s_stage + (warp - 2) * kStgWarpBytes);
+    uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg_f);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int g = t / per_g, l = t - g * per_g;
+      const int m = l / nt;
+      Tile tl;
+      tl.g = g;
+      tl.row0 = g * R + m * BM;
+      tl.row_end = (g + 1) * R;
+      tl.n = l - m * nt;
+      if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
+      tc_fence_after();
+      const int row_base = tl.row0 + q * 32;
+      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -930,7 +1129,9 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
               tma_load_2d_pair(b, rank ? &tmB1 : &tmB0, bar, kb * BK, brow);
             } else {
-              const int sub = kb / kb_per_sub;
+              // K split into n_sub blocks of B (whole k-blocks each); with
+              // one block, K itself (of any length)
+              const int sub = p.n_sub > 1 ? kb / kb_per_sub : 0;
               const int kk = (kb - sub * kb_per_sub) * BK;
               const int brow = (tl.g * p.n_sub + sub) * p.b_rows + tl.n * BN + (int)rank * 128;
               tma_load_2d_pair(b, &tmB0, bar, kk, brow);
@@ -1071,12 +1272,39 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 }  // namespace tc
 
+bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
+  using namespace tc;
+  if (q.rows_a < 1 || q.rows_b < 8 || q.rows_b % 8 != 0 || q.k_total % BK != 0 ||
+      q.n_groups < 1 || encode_fn() == nullptr)
+    return false;
+  Params p{};
+  p.n_out = q.rows_b;
+  p.wg_rows = q.rows_a;
+  p.n_groups = q.n_groups;
+  p.k_offsets = q.k_offsets;
+  p.epilogue = kEpiNone;
+  p.C = q.C;
+  p.c_is_f32 = 1;
+  p.mma_n = BN;
+  p.err = q.err;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, q.A, (uint64_t)q.k_total, (uint64_t)q.rows_a, (uint64_t)q.k_total * 2, BM) ||
+      !make_map(&mb, q.B, (uint64_t)q.k_total, (uint64_t)q.rows_b, (uint64_t)q.k_total * 2, BN))
+    return false;
+  if (cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return false;
+  tc_wgrad_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess;
+}
+
 bool tc_gemm_supported(const TcProblem& q) {
   if (q.K < 1 || q.n_out < 8 || q.n_out % 8 != 0) return false;
   if (q.k_sub % tc::BK != 0 && q.n_sub > 1) return false;
   if (q.n_groups > kMaxExperts) return false;
   // compact output: one exponent per 32 columns, no SwiGLU pairing
   if (q.c_e8 != nullptr && (q.swiglu || q.e8_cols != (q.n_out + 31) / 32)) return false;
+  if (q.c_e8 == nullptr && (q.c_row_map != nullptr || q.c_row_scale != nullptr)) return false;
   return tc::encode_fn() != nullptr;
 }
 
@@ -1126,6 +1354,8 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.mma_n = (!q.swiglu && q.n_out < BN) ? (q.n_out + 15) / 16 * 16 : BN;
   p.err = q.err;
   p.a_row_map = q.a_row_map;
+  p.c_row_map = q.c_row_map;
+  p.c_row_scale = q.c_row_scale;
   const int ksub = p.k_sub;
   const uint64_t brows_total = (uint64_t)q.b_groups * q.n_sub * q.b_rows;
   // A [a_rows, K] (a gathered A is read one row per box, four per gather4);

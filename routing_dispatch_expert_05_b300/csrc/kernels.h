@@ -53,7 +53,7 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* chunk_cnt, int32_t* chunk_base, int32_t* offsets,
                      int32_t* row_of_slot, int32_t* token_of_row,
                      int32_t* counts, int32_t* kept, int32_t* dropped,
-                     int32_t* err, cudaStream_t st);
+                     int32_t* err, cudaStream_t st, int32_t* slot_of_row = nullptr);
 // x_perm[r] = x[token_of_row[r]] for r < offsets[E] (16-byte vectors on the
 // load/store units; a TMA bulk-copy version measured 1.5x slower)
 void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
@@ -137,11 +137,33 @@ struct TcProblem {
   // r < offsets[n_groups].  null: A is already in grouped row order.
   const int32_t* a_row_map;
   // 1: run on CTA pairs (tcgen05 cta_group::2, 256-row tiles) where the
-  // problem allows it (plain or compact output, A not gathered)
+  // problem allows it
   int use_pairs;
+  // Compact output only: row r of the grouped problem is written to output
+  // row c_row_map[r] (e.g. its assignment slot t*k + j), scaled by
+  // c_row_scale[output row] (e.g. the routing weight) before compacting.
+  const int32_t* c_row_map;
+  const float* c_row_scale;
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
+
+// Weight gradients on the tensor cores: for each group g,
+//   C[g*rows_a + i, j] = sum_{c in [k_offsets[g], k_offsets[g+1])} A[i, c] B[j, c]
+// A [rows_a, k_total] and B [rows_b, k_total] bf16 row-major (the grouped
+// activations transposed, every group's column span a non-zero multiple of
+// 64, zero-padded); C fp32 [n_groups * rows_a, rows_b].
+struct WgradProblem {
+  const void* A;
+  const void* B;
+  int rows_a, rows_b;
+  int64_t k_total;            // columns of A and B (multiple of 64)
+  const int32_t* k_offsets;   // [n_groups + 1], device
+  int n_groups;
+  float* C;
+  int32_t* err;
+};
+bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st);
 
 // ---- combine ----------------------------------------------------------------
 // y: fp32 expert outputs [N*k, d]; out: layer dtype [N, d]
@@ -150,10 +172,41 @@ void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
                     int d_model, int is_bf16, int num_sms, cudaStream_t st);
 // the same with compact expert outputs: y16 [N*k, d] fp16 and
 // y_e8 [N*k, ceil(d/32)] (value = y16 * 2^(y_e8 - 127) for its 32 columns)
-void launch_combine_compact(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
-                            const float* w, const float* shared, void* out, int64_t n_tokens,
-                            int top_k, int d_model, int is_bf16, int num_sms,
-                            cudaStream_t st);
+// compact expert outputs already weighted and in slot order (row t*k + j)
+void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
+                          const float* shared, void* out, int64_t n_tokens, int top_k,
+                          int d_model, int is_bf16, int num_sms, cudaStream_t st);
 constexpr int kYScaleBlock = 32;    // columns per compact-output exponent
+
+// ---- backward (backward.cu) -----------------------------------------------
+// koff[g+1] = koff[g] + max(64, 64 * ceil(m_g / 64)), m_g from offsets (or
+// one group of `rows` rows when offsets is null)
+void launch_pad_offsets(const int32_t* offsets, int64_t rows, int G, int32_t* koff,
+                        cudaStream_t st);
+// out [C, k_total] bf16: column koff[g] + l = row offsets[g] + l of in [*, C]
+// (bf16, or fp32 when in_f32), zeros on each group's padding
+void launch_transpose_grouped(const void* in, bool in_f32, int C, const int32_t* offsets,
+                              int64_t rows, int G, const int32_t* koff, int64_t k_total,
+                              void* out, cudaStream_t st);
+// out[b][c][r] = in[b][r][c] (bf16), batch b of the output at out + b * out_stride
+void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
+                              int64_t out_stride, cudaStream_t st);
+void launch_silu_mul(const void* g, const void* u, void* h, const int32_t* offsets,
+                     int n_experts, int F, int num_sms, cudaStream_t st);
+void launch_swiglu_backward(const void* dh, const void* g, const void* u, void* dgu,
+                            const int32_t* offsets, int n_experts, int F, int num_sms,
+                            cudaStream_t st);
+void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
+                             const float* w, const void* dout, int64_t n_tokens, int top_k,
+                             int d, float* dw, void* dy, int num_sms, cudaStream_t st);
+void launch_router_backward(const float* logits, const int32_t* idx, const float* w,
+                            const float* dw, const int32_t* counts, int64_t n_tokens, int E,
+                            int k, int mode, float coef, float d_balance, float* dz,
+                            void* dz16 /* nullable bf16 copy */, cudaStream_t st);
+void launch_dx_reduce(const void* dxp, const int32_t* row_of_slot, const float* dxr,
+                      int64_t n_tokens, int top_k, int d, float* dx, int num_sms,
+                      cudaStream_t st);
+// d_b_router[e] = sum_t dz[t, e] (fixed-order tree per expert)
+void launch_column_sums(const float* dz, int64_t n_tokens, int E, float* out, cudaStream_t st);
 
 }  // namespace moe

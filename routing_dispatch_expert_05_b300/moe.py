@@ -32,7 +32,8 @@ EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_dispatch_permute_noalloc", "moe_expert_up",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_timed", "moe_forward_host",
-            "moe_update_selection_bias", "moe_read_device_error",
+            "moe_update_selection_bias", "moe_backward_workspace_size", "moe_backward",
+            "moe_read_device_error",
             "moe_status_string", "moe_version")
 
 
@@ -60,6 +61,11 @@ class MoEWeights(ctypes.Structure):
 
 class MoEStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("counts", "kept", "dropped", "balance")]
+
+
+class MoEGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dx", "d_w_router", "d_b_router", "d_w1",
+                                               "d_w3", "d_w2")]
 
 
 _lib = None
@@ -96,6 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_timed": [cfgp, vp, wp, vp, sp, vp, sz, vp, P(vp), ctypes.c_int32],
         "moe_read_device_error": [vp, P(ctypes.c_int32), vp],
         "moe_update_selection_bias": [cfgp, vp, vp, ctypes.c_float, vp, vp],
+        "moe_backward_workspace_size": [cfgp, P(sz)],
+        "moe_backward": [cfgp, vp, wp, vp, ctypes.c_float, P(MoEGrads), vp, sz, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -300,6 +308,28 @@ def moe_forward_host(cfg, x_host, weights: MoEWeights, out_host, stats, ws,
         _stream(stream)), "moe_forward_host")
 
 
+def backward_workspace_size(cfg: MoEConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return n.value
+
+
+def make_grads(dx, d_w_router, d_w1, d_w3, d_w2, d_b_router=None) -> MoEGrads:
+    return MoEGrads(ptr(dx), ptr(d_w_router), ptr(d_b_router), ptr(d_w1), ptr(d_w3),
+                    ptr(d_w2))
+
+
+def moe_backward(cfg, x, weights: MoEWeights, dout, d_balance, grads: MoEGrads, ws,
+                 stream=None):
+    """Gradients of <dout, out> + d_balance * balance (routing held fixed)
+    into the fp32 arrays of `grads`; ws holds backward_workspace_size bytes."""
+    wp, wb = _ws(ws)
+    _check(load_library().moe_backward(ctypes.byref(cfg), ptr(x), ctypes.byref(weights),
+                                       ptr(dout), float(d_balance), ctypes.byref(grads), wp,
+                                       wb, _stream(stream)), "moe_backward")
+
+
 def moe_update_selection_bias(cfg, counts, sel_bias, gamma, load_cv=None, stream=None):
     """sel_bias += gamma * sign(mean load - counts) (in place) and the load's
     coefficient of variation into load_cv; both tensors may be None (not
@@ -344,8 +374,10 @@ def upload(inputs, device="cuda") -> Dict[str, torch.Tensor]:
 class MoEWorkspace:
     """A zero-filled workspace for moe_forward of one configuration."""
 
-    def __init__(self, cfg: MoEConfig, device="cuda", forward: bool = True):
-        n = workspace_size(cfg) if forward else scratch_size(cfg)
+    def __init__(self, cfg: MoEConfig, device="cuda", forward: bool = True,
+                 backward: bool = False):
+        n = backward_workspace_size(cfg) if backward else (
+            workspace_size(cfg) if forward else scratch_size(cfg))
         self.tensor = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
     @property

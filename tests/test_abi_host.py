@@ -152,3 +152,28 @@ def test_bias_update_rejects_bad_arguments(lib):
     assert f(ctypes.byref(cfg), addr, addr + 2, 1e-3, None, None) == M.MOE_ERR_INVALID_ARG
     bad = _bad(n_experts=0)
     assert f(ctypes.byref(bad), addr, addr, 1e-3, addr, None) == M.MOE_ERR_INVALID_ARG
+
+
+def test_backward_rejects_unsupported_layers(lib):
+    """fp32 layers, SiLU-MLP experts and shared experts get
+    MOE_ERR_UNSUPPORTED before anything is enqueued (no GPU needed)."""
+    buf = ctypes.create_string_buffer(4096)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    w = M.MoEWeights()
+    g = M.MoEGrads()
+    for name in ("toy_top2_fp32", "capacity_top2_bf16", "deepseek_v3_block"):
+        cfg = M.make_config(W.WORKLOADS[name])
+        st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(w), addr, 0.0,
+                              ctypes.byref(g), addr, 1 << 20, None)
+        assert st == M.MOE_ERR_UNSUPPORTED, name
+    cfg = M.make_config(W.WORKLOADS["qwen3_moe"])
+    n = ctypes.c_size_t()
+    assert lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0
+    fw = ctypes.c_size_t()
+    lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(fw))
+    assert n.value > fw.value
+    # missing gradient outputs
+    w.w_router = w.w1 = w.w3 = w.w2 = addr
+    st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(w), addr, 0.0,
+                          ctypes.byref(g), addr, n.value, None)
+    assert st == M.MOE_ERR_INVALID_ARG

@@ -1,0 +1,139 @@
+"""GPU parity of the backward pass (moe_backward) against the backward
+oracle.
+
+The oracle differentiates in float64 without storage roundings; the GPU
+path keeps its intermediates (g, u, h, dy, dh, [dg|du], dx_perm, the
+transposed operands) in bf16 with fp32 accumulation.  A gradient passes
+through about five such roundings, each within 2^-9 relative, so each
+tensor is compared as ||gpu - oracle|| / ||oracle|| <= BWD_NORM (2e-2, a
+few times the compounded rounding) and max |gpu - oracle| <= BWD_MAX *
+max |oracle| (2e-2: no element far off; the products of Gaussian factors
+these gradients are made of are heavy-tailed, so the bound scales with the
+largest element, not the RMS).  The
+routing the gradients are taken at is the GPU's own (read back with
+moe_router_topk, the same kernels the backward recomputes it with), given
+to the oracle, so a near-tie in the router cannot pick different experts on
+the two sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_backward as OB
+from oracle import moe_oracle as O
+from routing_dispatch_expert_05_b300 import build as B
+from routing_dispatch_expert_05_b300 import moe as M
+from routing_dispatch_expert_05_b300 import workloads as W
+from tests.parity_util import to_np
+
+pytestmark = pytest.mark.gpu
+
+BWD_NORM = 2e-2
+BWD_MAX = 2e-2
+
+
+def assert_grad_close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, what
+    assert np.isfinite(got).all(), what
+    nrm = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(got - ref)) / max(nrm, 1e-30)
+    assert rel <= BWD_NORM, f"{what}: relative norm error {rel:.3e}"
+    big = float(np.abs(ref).max())
+    err = float(np.abs(got - ref).max())
+    assert err <= BWD_MAX * big, f"{what}: max error {err:.3e} > {BWD_MAX} * {big:.3e}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    M.load_library()
+    torch.cuda.init()
+
+
+def _shape(route, N=256, E=16, k=4, d=256, F=128, cf=0.0, router_bias="normal", seed=21):
+    return W.MoEShape(name="bwd", n_tokens=N, d_model=d, n_experts=E, top_k=k, d_ff=F,
+                      expert=W.EXPERT_SWIGLU, route=route, dtype=W.DTYPE_BF16,
+                      router_bias=router_bias, sel_bias_range=0.1, capacity_factor=cf,
+                      balance_coef=0.01, seed=seed)
+
+
+def _run(shape, d_balance, dout_seed=3):
+    inp = W.make_inputs(shape)
+    t = M.upload(inp)
+    cfg = M.make_config(shape)
+    weights = M.make_weights(t)
+    N, d, E, k, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.top_k, shape.d_ff
+    dout = np.random.default_rng(dout_seed).standard_normal((N, d)).astype(np.float32)
+    dout = W.bits_to_f32(W.bf16_bits(dout))              # exactly representable in bf16
+    dout_t = torch.from_numpy(dout).to(torch.bfloat16).cuda()
+    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
+    g = dict(dx=z(N, d), d_w_router=z(E, d), d_w1=z(E, F, d), d_w3=z(E, F, d), d_w2=z(E, d, F))
+    if "b_router" in inp.values:
+        g["d_b_router"] = z(E)
+    grads = M.make_grads(**g)
+    ws = M.MoEWorkspace(cfg, backward=True)
+    M.moe_backward(cfg, t["x"], weights, dout_t, d_balance, grads, ws)
+    # the routing the GPU recomputes, read back through the router entry point
+    fws = M.MoEWorkspace(cfg)
+    idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(N, k, dtype=torch.float32, device="cuda")
+    M.moe_router_topk(cfg, t["x"], weights, None, idx, w, None, fws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+    idx_np = to_np(idx).astype(np.int64)
+    disp = O.dispatch(idx_np, E, shape.capacity_factor)
+    kept = (disp["row_of_slot"] >= 0).reshape(idx_np.shape)
+    ref = OB.layer_backward(shape, inp.values, dout, d_balance,
+                            route_fixed=(idx_np, kept, disp["counts"]))
+    return g, ref, ws, (cfg, t, weights, dout_t, grads)
+
+
+CASES = [(W.ROUTE_SOFTMAX_TOPK, {}), (W.ROUTE_TOPK_SOFTMAX, dict(E=64, k=6)),
+         (W.ROUTE_SIGMOID_BIAS, dict(E=32, k=3, router_bias="none")),
+         (W.ROUTE_SOFTMAX_TOPK, dict(E=8, k=2, cf=1.0, N=320)),
+         # enough rows per expert for the CTA-pair GEMMs
+         (W.ROUTE_TOPK_SOFTMAX, dict(N=2048))]
+
+
+@pytest.mark.parametrize("d_balance", [0.0, 0.7])
+@pytest.mark.parametrize("route,kw", CASES)
+def test_backward_matches_oracle(route, kw, d_balance):
+    shape = _shape(route, **kw)
+    g, ref, _, _ = _run(shape, d_balance)
+    for name in ("dx", "d_w_router", "d_w1", "d_w3", "d_w2", "d_b_router"):
+        if name not in g:
+            continue
+        assert_grad_close(to_np(g[name]), ref[name], name)
+
+
+def test_backward_unused_expert_gets_zero():
+    shape = _shape(W.ROUTE_SOFTMAX_TOPK, N=128, E=16, k=2)
+    inp = W.make_inputs(shape)
+    assert "b_router" in inp.values
+    inp.values["b_router"][5] = -60.0                     # nobody selects expert 5
+    inp.bits["b_router"] = W.bf16_bits(inp.values["b_router"])
+    t = M.upload(inp)
+    cfg = M.make_config(shape)
+    weights = M.make_weights(t)
+    N, d, E, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.d_ff
+    dout = torch.randn(N, d, device="cuda").to(torch.bfloat16)
+    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
+    g = dict(dx=z(N, d), d_w_router=z(E, d), d_w1=z(E, F, d), d_w3=z(E, F, d), d_w2=z(E, d, F))
+    ws = M.MoEWorkspace(cfg, backward=True)
+    M.moe_backward(cfg, t["x"], weights, dout, 0.0, M.make_grads(**g), ws)
+    torch.cuda.synchronize()
+    for name in ("d_w1", "d_w3", "d_w2"):
+        assert torch.count_nonzero(g[name][5]) == 0, name
+        assert torch.isfinite(g[name]).all(), name
+
+
+def test_backward_is_deterministic():
+    shape = _shape(W.ROUTE_TOPK_SOFTMAX, E=64, k=6)
+    g, _, ws, (cfg, t, weights, dout_t, grads) = _run(shape, 0.5)
+    first = {k_: v.clone() for k_, v in g.items()}
+    M.moe_backward(cfg, t["x"], weights, dout_t, 0.5, grads, ws)
+    torch.cuda.synchronize()
+    for name, v in g.items():
+        assert torch.equal(v, first[name]), name

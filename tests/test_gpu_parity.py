@@ -561,6 +561,25 @@ def test_forward_bf16_row_widths(d):
     assert_output_close(to_np(out), ref["out_exact"], shape.dtype, "row widths")
 
 
+@pytest.mark.parametrize("expert,N,d,F", [(W.EXPERT_SILU_MLP, 300, 64, 72),
+                                          (W.EXPERT_SWIGLU, 600, 72, 64)])
+def test_forward_bf16_k_not_whole_blocks(expert, N, d, F):
+    """Tensor-core GEMMs whose reduction length is not a whole number of
+    64-wide k-blocks: the down projection (K = F = 72) and the router GEMM
+    (K = d = 72, 600 tokens) read the right B columns in their last block."""
+    shape = _cfg(n_tokens=N, n_experts=8, top_k=2, d_model=d, d_ff=F, expert=expert,
+                 has_bias=expert == W.EXPERT_SILU_MLP, dtype=W.DTYPE_BF16)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, _ = _forward(D)
+    ref = O.forward(shape, inp.values)
+    keys = O.selection_keys(ref["logits"], shape.route, None)
+    amb, _ = set_ambiguous_tokens(keys, shape.top_k, _router_margin(D, ref["logits"]))
+    keep = ~amb
+    assert keep.mean() > 0.9
+    assert_output_close(to_np(out)[keep], ref["out_exact"][keep], shape.dtype, "k tail")
+
+
 # -------------------------------------------- full-size sampled checks
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["qwen3_moe", "deepseek_v3_block"])
