@@ -438,6 +438,57 @@ def run_reference(args, shape):
     return res, rank
 
 
+def run_backward(args, shape, peaks, peaks_kind):
+    """Time moe_backward (one GPU): recompute + data and weight gradients.
+
+    Algorithmic FLOPs per step, SwiGLU experts: the recomputed g, u (2 d F)
+    and y (d F) per kept assignment, the data gradients dh (d F) and dx_perm
+    (2 d F), the weight gradients dW2 (d F) and dW1, dW3 (2 d F) -- 18 d F
+    FLOP per assignment -- plus the router's three N x E x d products.
+    """
+    import torch
+    from routing_dispatch_expert_05_b300 import moe as M
+
+    inputs = W.make_inputs(shape)
+    t = M.upload(inputs)
+    cfg = M.make_config(shape)
+    weights = M.make_weights(t)
+    N, d, E, k, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.top_k, shape.d_ff
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    dout = torch.randn(N, d, device="cuda", generator=gen).to(torch.bfloat16)
+    f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device="cuda")
+    g = dict(dx=f32(N, d), d_w_router=f32(E, d), d_w1=f32(E, F, d), d_w3=f32(E, F, d),
+             d_w2=f32(E, d, F))
+    if "b_router" in inputs.values:
+        g["d_b_router"] = f32(E)
+    grads = M.make_grads(**g)
+    ws = M.MoEWorkspace(cfg, backward=True)
+    for _ in range(args.warmup):
+        M.moe_backward(cfg, t["x"], weights, dout, 1.0, grads, ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        M.moe_backward(cfg, t["x"], weights, dout, 1.0, grads, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flop = 18.0 * d * F * N * k + 3 * 2.0 * N * E * d
+    tflops = flop / (ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+    return {"metric": "MoE-layer bwd tokens/s on 1 B300 (routing held fixed)",
+            "value": round(N / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": shape.name, "n_tokens": N, "d_model": d, "n_experts": E,
+                       "top_k": k, "d_ff": F},
+            "gemm_tflops_effective": round(tflops, 1),
+            "frac_of_sustained_bf16": round(tflops / peak, 4),
+            "peak_kind": f"{peaks_kind} sustained bf16"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,6 +503,8 @@ def main(argv=None):
                     help="DRAM bytes per launch of the up projection from an ncu capture")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiler captures)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time moe_backward instead of the forward (one GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -464,7 +517,10 @@ def main(argv=None):
         from routing_dispatch_expert_05_b300 import build as B
         B.build()
         peaks, kind = load_peaks()
-        res, rank = run_ours(args, shape, peaks, kind)
+        if args.backward:
+            res, rank = run_backward(args, shape, peaks, kind), 0
+        else:
+            res, rank = run_ours(args, shape, peaks, kind)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
 

@@ -361,7 +361,8 @@ MOE_API moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t
 /* The backward pass: recomputes the forward's routing, grouping and expert
  * activations from x, then runs the gradients back through the combine, the
  * experts (data and weight gradients on the tensor cores) and the router.
- * x [N, d] and dout [N, d] are bf16 device arrays.  Supported: bf16 SwiGLU
+ * x [N, d] and dout [N, d] are bf16 device arrays; x, dout and the
+ * gradient arrays 16-byte aligned (else MOE_ERR_INVALID_ARG).  Supported: bf16 SwiGLU
  * experts without expert biases or shared experts, d and F multiples of 64,
  * E a multiple of 8, N > 0 (else MOE_ERR_UNSUPPORTED, nothing enqueued).
  * With a capacity the drops are those of the forward.  Enqueued on

@@ -1046,18 +1046,18 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
 
   // 4. weight gradients over each expert's rows (transposed, zero-padded)
   launch_pad_offsets(offsets, M, E, koff, st);
-  launch_transpose_grouped(x_perm, false, d, offsets, M, E, koff, B.kt, xpT, st);
-  launch_transpose_grouped(dy, false, d, offsets, M, E, koff, B.kt, dyT, st);
-  launch_transpose_grouped(h, false, F, offsets, M, E, koff, B.kt, hT, st);
-  launch_transpose_grouped(dgu, false, 2 * F, offsets, M, E, koff, B.kt, dguT, st);
+  launch_transpose_grouped(x_perm, d, offsets, M, E, koff, B.kt, xpT, st);
+  launch_transpose_grouped(dy, d, offsets, M, E, koff, B.kt, dyT, st);
+  launch_transpose_grouped(h, F, offsets, M, E, koff, B.kt, hT, st);
+  launch_transpose_grouped(dgu, 2 * F, offsets, M, E, koff, B.kt, dguT, st);
   MOE_TRY(wgrad_run(dyT, d, hT, F, B.kt, koff, E, gr.d_w2, sc.err, st));
   MOE_TRY(wgrad_run(dguT, F, xpT, d, B.kt, koff, E, gr.d_w1, sc.err, st));
   MOE_TRY(wgrad_run(dguT + (size_t)F * B.kt * 2, F, xpT, d, B.kt, koff, E, gr.d_w3, sc.err,
                     st));
   // router: d_w_router = dlogits^T x over all tokens (one group)
   launch_pad_offsets(nullptr, N, 1, koff_n, st);
-  launch_transpose_grouped(dz16, false, E, nullptr, N, 1, koff_n, B.nt, dzT, st);
-  launch_transpose_grouped(x, false, d, nullptr, N, 1, koff_n, B.nt, xT, st);
+  launch_transpose_grouped(dz16, E, nullptr, N, 1, koff_n, B.nt, dzT, st);
+  launch_transpose_grouped(x, d, nullptr, N, 1, koff_n, B.nt, xT, st);
   MOE_TRY(wgrad_run(dzT, E, xT, d, B.nt, koff_n, 1, gr.d_w_router, sc.err, st));
   if (gr.d_b_router != nullptr) launch_column_sums(dz, N, E, gr.d_b_router, st);
   return last_cuda();
@@ -1147,6 +1147,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   MOE_TRY(need({x, dout, grads->dx, grads->d_w_router, grads->d_w1, grads->d_w3,
                 grads->d_w2}));
   MOE_TRY(maybe({grads->d_b_router}));
+  for (const void* q : {x, dout, (const void*)grads->dx, (const void*)grads->d_w_router,
+                        (const void*)grads->d_w1, (const void*)grads->d_w3,
+                        (const void*)grads->d_w2})
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (grads->d_b_router != nullptr && weights->b_router == nullptr) return MOE_ERR_INVALID_ARG;
   return backward_impl(c, x, *weights, dout, d_balance, *grads, ws,
                        static_cast<cudaStream_t>(stream));

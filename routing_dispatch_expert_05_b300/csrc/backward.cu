@@ -41,15 +41,32 @@ __global__ void pad_offsets_kernel(const int32_t* __restrict__ offsets, int64_t 
   }
 }
 
-// out[c, koff[g] + l] = in[off[g] + l, c] for l < m_g, 0 on the padding;
-// 64 x 64 tiles through shared memory.  TIn is bf16 or float (then
-// rounded to bf16).
-template <typename TIn>
+// 64 x 64 bf16 tiles through shared memory, 16-byte accesses on both sides:
+// a thread loads 8 consecutive elements of a source row and, after the
+// barrier, gathers 8 of a column into one 16-byte store; 8 threads cover one
+// 128-byte row segment either way.  Rows and columns are multiples of 8.
+constexpr int kTp = 64 + 8;                        // padded tile row (elements)
+
+__device__ __forceinline__ void tile_store_t(const bf16 (*tile)[kTp], int i, bf16* dst_row0,
+                                             int64_t ld, bool ok) {
+  const int c = i >> 3, r8 = (i & 7) * 8;          // output row c, source rows r8..r8+7
+  if (!ok) return;
+  uint4 v;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bf16 lo = tile[r8 + 2 * j][c], hi = tile[r8 + 2 * j + 1][c];
+    w[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+  }
+  st_vec16(dst_row0 + (int64_t)c * ld + r8, v);
+}
+
+// out[c, koff[g] + l] = in[off[g] + l, c] for l < m_g, 0 on the padding
 __global__ void __launch_bounds__(256)
-transpose_grouped_kernel(const TIn* __restrict__ in, int C, const int32_t* __restrict__ offsets,
+transpose_grouped_kernel(const bf16* __restrict__ in, int C, const int32_t* __restrict__ offsets,
                          int64_t rows, int G, const int32_t* __restrict__ koff,
                          int64_t k_total, bf16* __restrict__ out) {
-  __shared__ bf16 tile[64][72];
+  __shared__ __align__(16) bf16 tile[64][kTp];
   __shared__ int64_t s_src[64];
   const int64_t pc0 = (int64_t)blockIdx.x * 64;
   const int c0 = blockIdx.y * 64;
@@ -67,18 +84,16 @@ transpose_grouped_kernel(const TIn* __restrict__ in, int C, const int32_t* __res
     s_src[threadIdx.x] = (pc < koff[G] && l < m) ? o0 + l : -1;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int r = i >> 6, c = i & 63;
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int r = i >> 3, c8 = (i & 7) * 8;
     const int64_t src = s_src[r];
-    float v = 0.f;
-    if (src >= 0 && c0 + c < C) v = to_f32(in[src * C + c0 + c]);
-    tile[r][c] = __float2bfloat16_rn(v);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (src >= 0 && c0 + c8 < C) v = ld_vec16_nc(in + src * C + c0 + c8);
+    *reinterpret_cast<uint4*>(&tile[r][c8]) = v;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int c = i >> 6, r = i & 63;
-    if (c0 + c < C && pc0 + r < k_total) out[(int64_t)(c0 + c) * k_total + pc0 + r] = tile[r][c];
-  }
+  for (int i = threadIdx.x; i < 64 * 8; i += 256)
+    tile_store_t(tile, i, out + (int64_t)c0 * k_total + pc0, k_total, c0 + (i >> 3) < C);
 }
 
 // out[b][c][r] = in[b][r][c]: batched [rows, cols] -> [cols, rows], output
@@ -86,92 +101,124 @@ transpose_grouped_kernel(const TIn* __restrict__ in, int C, const int32_t* __res
 __global__ void __launch_bounds__(256)
 transpose_batched_kernel(const bf16* __restrict__ in, int rows, int cols,
                          bf16* __restrict__ out, int64_t out_stride) {
-  __shared__ bf16 tile[64][72];
+  __shared__ __align__(16) bf16 tile[64][kTp];
   const int b = blockIdx.z;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
   const bf16* src = in + (int64_t)b * rows * cols;
   bf16* dst = out + (int64_t)b * out_stride;
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int r = i >> 6, c = i & 63;
-    tile[r][c] = (r0 + r < rows && c0 + c < cols) ? src[(int64_t)(r0 + r) * cols + c0 + c]
-                                                  : __float2bfloat16_rn(0.f);
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int r = i >> 3, c8 = (i & 7) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < rows && c0 + c8 < cols) v = ld_vec16_nc(src + (int64_t)(r0 + r) * cols + c0 + c8);
+    *reinterpret_cast<uint4*>(&tile[r][c8]) = v;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int c = i >> 6, r = i & 63;
-    if (r0 + r < rows && c0 + c < cols) dst[(int64_t)(c0 + c) * rows + r0 + r] = tile[r][c];
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int c = i >> 3, r8 = (i & 7) * 8;
+    tile_store_t(tile, i, dst + (int64_t)c0 * rows + r0, rows, c0 + c < cols && r0 + r8 < rows);
   }
 }
 
 // ---------------------------------------------------------------- SwiGLU
-// h = silu(g) * u for the kept rows (n_rows = offsets[E] rows of F)
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 t = __bfloat1622float2(p[j]);
+    f[2 * j] = t.x;
+    f[2 * j + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// h = silu(g) * u for the kept rows (offsets[E] rows of F), 8 per thread
 __global__ void silu_mul_kernel(const bf16* __restrict__ g, const bf16* __restrict__ u,
                                 bf16* __restrict__ h, const int32_t* __restrict__ offsets,
                                 int n_experts, int F) {
-  const int64_t n = (int64_t)offsets[n_experts] * F;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+  const int64_t n8 = (int64_t)offsets[n_experts] * F / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const float gv = __bfloat162float(g[i]), uv = __bfloat162float(u[i]);
-    h[i] = __float2bfloat16_rn(gv * sigmoid_fast(gv) * uv);
+    float gv[8], uv[8], hv[8];
+    unpack8(ld_vec16_nc(g + 8 * i), gv);
+    unpack8(ld_vec16_nc(u + 8 * i), uv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hv[j] = gv[j] * sigmoid_fast(gv[j]) * uv[j];
+    st_vec16(h + 8 * i, pack8(hv));
   }
 }
 
-// dgu[r] = [dg | du]: dg = dh u silu'(g), du = dh silu(g)
+// dgu[r] = [dg | du]: dg = dh u silu'(g), du = dh silu(g); 8 per thread
 __global__ void swiglu_backward_kernel(const bf16* __restrict__ dh, const bf16* __restrict__ g,
                                        const bf16* __restrict__ u, bf16* __restrict__ dgu,
                                        const int32_t* __restrict__ offsets, int n_experts,
                                        int F) {
-  const int64_t n = (int64_t)offsets[n_experts] * F;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+  const int64_t n8 = (int64_t)offsets[n_experts] * F / 8;
+  const int f8 = F / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / F;
-    const int f = (int)(i - r * F);
-    const float gv = __bfloat162float(g[i]), uv = __bfloat162float(u[i]);
-    const float dv = __bfloat162float(dh[i]);
-    const float sg = sigmoid_fast(gv);
-    const float silu = gv * sg;
-    const float dsilu = sg * (1.f + gv * (1.f - sg));
-    dgu[r * 2 * F + f] = __float2bfloat16_rn(dv * uv * dsilu);
-    dgu[r * 2 * F + F + f] = __float2bfloat16_rn(dv * silu);
+    const int64_t r = i / f8;
+    const int f = (int)(i - r * f8) * 8;
+    float gv[8], uv[8], dv[8], dg[8], du[8];
+    unpack8(ld_vec16_nc(g + 8 * i), gv);
+    unpack8(ld_vec16_nc(u + 8 * i), uv);
+    unpack8(ld_vec16_nc(dh + 8 * i), dv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float sg = sigmoid_fast(gv[j]);
+      dg[j] = dv[j] * uv[j] * sg * (1.f + gv[j] * (1.f - sg));
+      du[j] = dv[j] * gv[j] * sg;
+    }
+    st_vec16(dgu + r * 2 * F + f, pack8(dg));
+    st_vec16(dgu + r * 2 * F + F + f, pack8(du));
   }
 }
 
 // ---------------------------------------------------------------- combine
-// Per token (one CTA): dw[t,j] = <dout[t], y[row]> with y compact (fp16 and
-// an exponent per 32 columns, row order), dy[row] = w[t,j] dout[t] (bf16).
-constexpr int kCbThreads = 256;
-__global__ void __launch_bounds__(kCbThreads)
+// One warp per assignment (t, j): dw[t,j] = <dout[t], y[row]> with y compact
+// (fp16 and an exponent per 32 columns, row order), dy[row] = w[t,j] dout[t]
+// (bf16); lanes take 8 columns at a time (16-byte loads and stores).
+__global__ void __launch_bounds__(256)
 combine_backward_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
                         const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
                         const bf16* __restrict__ dout, int64_t n_tokens, int top_k, int d,
                         float* __restrict__ dw, bf16* __restrict__ dy) {
-  __shared__ float s_red[kCbThreads / 32];
+  const int lane = threadIdx.x & 31;
   const int e8_cols = (d + kYScaleBlock - 1) / kYScaleBlock;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
-    for (int j = 0; j < top_k; ++j) {
-      const int r = row_of_slot[t * top_k + j];
-      const float wj = w[t * top_k + j];
-      float part = 0.f;
-      if (r >= 0) {
-        for (int c = threadIdx.x; c < d; c += blockDim.x) {
-          const float dv = __bfloat162float(dout[t * d + c]);
-          const float sc = __uint_as_float((uint32_t)y_e8[(int64_t)r * e8_cols + c / kYScaleBlock] << 23);
-          part = fmaf(dv, __half2float(y[(int64_t)r * d + c]) * sc, part);
-          dy[(int64_t)r * d + c] = __float2bfloat16_rn(wj * dv);
-        }
+  const int64_t n_slots = n_tokens * top_k;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < n_slots;
+       s += warps) {
+    const int r = row_of_slot[s];
+    if (r < 0) {                                   // dropped: no output, no gradient
+      if (lane == 0) dw[s] = 0.f;
+      continue;
+    }
+    const int64_t t = s / top_k;
+    const float ws = w[s];
+    float part = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+      float dv[8];
+      unpack8(ld_vec16_nc(dout + t * d + c), dv);
+      const uint4 yv = ld_vec16_nc(y + (int64_t)r * d + c);
+      const float sc = __uint_as_float((uint32_t)y_e8[(int64_t)r * e8_cols + c / kYScaleBlock] << 23);
+      const __half2* yh = reinterpret_cast<const __half2*>(&yv);
+      float dyv[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(yh[j]);
+        part = fmaf(dv[2 * j], f.x * sc, part);
+        part = fmaf(dv[2 * j + 1], f.y * sc, part);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-      if (lane == 0) s_red[warp] = part;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float acc = 0.f;
-        for (int q = 0; q < kCbThreads / 32; ++q) acc += s_red[q];
-        dw[t * top_k + j] = r >= 0 ? acc : 0.f;
-      }
-      __syncthreads();
+      for (int j = 0; j < 8; ++j) dyv[j] = ws * dv[j];
+      st_vec16(dy + (int64_t)r * d + c, pack8(dyv));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+    if (lane == 0) dw[s] = part;
   }
 }
 
@@ -265,19 +312,30 @@ router_backward_kernel(const float* __restrict__ logits, const int32_t* __restri
 }
 
 // ---------------------------------------------------------------- dx
-// dx[t] = dxr[t] + sum over kept slots of dxp[row] (fp32 out)
+// dx[t] = dxr[t] + sum over kept slots of dxp[row] (fp32 out), 8 columns per
+// thread
 __global__ void __launch_bounds__(256)
 dx_reduce_kernel(const bf16* __restrict__ dxp, const int32_t* __restrict__ row_of_slot,
                  const float* __restrict__ dxr, int64_t n_tokens, int top_k, int d,
                  float* __restrict__ dx) {
   for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      float acc = dxr ? dxr[t * d + c] : 0.f;
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float acc[8];
+      const float4* xr = reinterpret_cast<const float4*>(dxr + t * d + c);
+      const float4 a0 = xr[0], a1 = xr[1];
+      acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
+      acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
       for (int j = 0; j < top_k; ++j) {
         const int r = row_of_slot[t * top_k + j];
-        if (r >= 0) acc += __bfloat162float(dxp[(int64_t)r * d + c]);
+        if (r < 0) continue;
+        float v[8];
+        unpack8(ld_vec16_nc(dxp + (int64_t)r * d + c), v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] += v[q];
       }
-      dx[t * d + c] = acc;
+      float4* o = reinterpret_cast<float4*>(dx + t * d + c);
+      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -308,17 +366,14 @@ void launch_pad_offsets(const int32_t* offsets, int64_t rows, int G, int32_t* ko
   pad_offsets_kernel<<<1, 32, 0, st>>>(offsets, rows, G, koff);
 }
 
-void launch_transpose_grouped(const void* in, bool in_f32, int C, const int32_t* offsets,
-                              int64_t rows, int G, const int32_t* koff, int64_t k_total,
-                              void* out, cudaStream_t st) {
+void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int64_t rows,
+                              int G, const int32_t* koff, int64_t k_total, void* out,
+                              cudaStream_t st) {
   if (k_total <= 0 || C <= 0) return;
   const dim3 grid((unsigned)(k_total / 64), (unsigned)((C + 63) / 64));
-  if (in_f32)
-    transpose_grouped_kernel<float><<<grid, 256, 0, st>>>(
-        static_cast<const float*>(in), C, offsets, rows, G, koff, k_total, static_cast<bf16*>(out));
-  else
-    transpose_grouped_kernel<bf16><<<grid, 256, 0, st>>>(
-        static_cast<const bf16*>(in), C, offsets, rows, G, koff, k_total, static_cast<bf16*>(out));
+  transpose_grouped_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), C, offsets,
+                                                 rows, G, koff, k_total,
+                                                 static_cast<bf16*>(out));
 }
 
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
@@ -348,8 +403,8 @@ void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t
                              const float* w, const void* dout, int64_t n_tokens, int top_k,
                              int d, float* dw, void* dy, int num_sms, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 8);
-  combine_backward_kernel<<<blocks, kCbThreads, 0, st>>>(
+  const int blocks = (int)std::min<int64_t>(ceil_div64(n_tokens * top_k, 8), (int64_t)num_sms * 8);
+  combine_backward_kernel<<<blocks, 256, 0, st>>>(
       static_cast<const __half*>(y16), y_e8, row_of_slot, w, static_cast<const bf16*>(dout),
       n_tokens, top_k, d, dw, static_cast<bf16*>(dy));
 }

@@ -184,10 +184,10 @@ constexpr int kYScaleBlock = 32;    // columns per compact-output exponent
 void launch_pad_offsets(const int32_t* offsets, int64_t rows, int G, int32_t* koff,
                         cudaStream_t st);
 // out [C, k_total] bf16: column koff[g] + l = row offsets[g] + l of in [*, C]
-// (bf16, or fp32 when in_f32), zeros on each group's padding
-void launch_transpose_grouped(const void* in, bool in_f32, int C, const int32_t* offsets,
-                              int64_t rows, int G, const int32_t* koff, int64_t k_total,
-                              void* out, cudaStream_t st);
+// (bf16; C and k_total multiples of 8), zeros on each group's padding
+void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int64_t rows,
+                              int G, const int32_t* koff, int64_t k_total, void* out,
+                              cudaStream_t st);
 // out[b][c][r] = in[b][r][c] (bf16), batch b of the output at out + b * out_stride
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
                               int64_t out_stride, cudaStream_t st);
