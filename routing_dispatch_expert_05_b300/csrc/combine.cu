@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot,
                const float* __restrict__ w, const float* __restrict__ shared,
                T* __restrict__ out, int64_t n_tokens, int top_k, int d_model) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int C = sizeof(T) == 2 ? 8 : 4;  // columns per thread step
   constexpr int NV = C / 4;                  // float4 per row segment
   const int nvec = d_model / C;
@@ -118,6 +120,8 @@ combine_slots_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y
                      const int32_t* __restrict__ row_of_slot,
                      const float* __restrict__ shared, T* __restrict__ out,
                      int64_t n_tokens, int top_k, int d_model) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int C = 8;                       // columns per thread step (16 B of fp16)
   constexpr int KB = 8;                      // slots in flight
   const int nvec = d_model / C;
@@ -189,11 +193,11 @@ void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* r
   const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 4);
   const __half* y = static_cast<const __half*>(y16);
   if (is_bf16)
-    combine_slots_kernel<bf16><<<blocks, kThreads, 0, st>>>(
-        y, y_e8, row_of_slot, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
+    launch_pdl(combine_slots_kernel<bf16>, dim3(blocks), dim3(kThreads), 0, st, y, y_e8,
+               row_of_slot, shared, static_cast<bf16*>(out), n_tokens, top_k, d_model);
   else
-    combine_slots_kernel<float><<<blocks, kThreads, 0, st>>>(
-        y, y_e8, row_of_slot, shared, static_cast<float*>(out), n_tokens, top_k, d_model);
+    launch_pdl(combine_slots_kernel<float>, dim3(blocks), dim3(kThreads), 0, st, y, y_e8,
+               row_of_slot, shared, static_cast<float*>(out), n_tokens, top_k, d_model);
 }
 
 void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,

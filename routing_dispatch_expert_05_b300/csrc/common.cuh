@@ -100,4 +100,39 @@ __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) {
   return (a + b - 1) / b;
 }
 
+// Programmatic dependent launch.  The layer's kernels are launched with
+// programmatic stream serialization, so a kernel's CTAs may start while its
+// predecessor's last CTAs still run; pdl_wait() (griddepcontrol.wait) blocks
+// until the predecessor grid has completed and its memory is visible, and
+// every such kernel calls it before reading anything a predecessor wrote.
+// pdl_launch_dependents() lets the next kernel's CTAs be scheduled as soon
+// as resources free up (their own pdl_wait keeps them correct).  Launched
+// without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+#ifndef __CUDACC_RTC__
+// kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization (the kernel must call pdl_wait before reading its inputs)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+#endif
+
 }  // namespace moe

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256)
 dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
                       int n_experts, int32_t* __restrict__ chunk_cnt,
                       int32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int s_cnt[kMaxExperts];
   for (int e = threadIdx.x; e < n_experts; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -60,6 +62,8 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                      int32_t* __restrict__ dropped) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int s_kept[kMaxExperts];
   const int e = threadIdx.x;
   if (e < n_experts) {
@@ -95,6 +99,8 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
                      int32_t* __restrict__ row_of_slot,
                      int32_t* __restrict__ token_of_row,
                      int32_t* __restrict__ slot_of_row) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int s_w[kRankWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kRankWarps * kMaxExperts; i += blockDim.x)
@@ -160,6 +166,8 @@ gather_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
                    const int32_t* __restrict__ token_of_row,
                    const int32_t* __restrict__ offsets, int n_experts,
                    uint8_t* __restrict__ x_perm, bool wide) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t rows = offsets[n_experts];
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -214,6 +222,8 @@ __global__ void __launch_bounds__(256)
 scatter_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
                     const int32_t* __restrict__ row_of_slot, int64_t n_tokens, int top_k,
                     uint8_t* __restrict__ x_perm, bool wide) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int shift = wide ? 5 : 4;
@@ -268,7 +278,7 @@ void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of
   const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)num_sms * 8);
   const bool wide = row_bytes % 32 == 0 && (reinterpret_cast<uintptr_t>(x) & 31u) == 0 &&
                     (reinterpret_cast<uintptr_t>(x_perm) & 31u) == 0;
-  scatter_rows_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(x), row_bytes,
+  launch_pdl(scatter_rows_kernel, dim3(blocks), dim3(256), 0, st, static_cast<const uint8_t*>(x), row_bytes,
                                               row_of_slot, n_tokens, top_k,
                                               static_cast<uint8_t*>(x_perm), wide);
 }
@@ -281,13 +291,13 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* slot_of_row) {
   const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
   if (chunks > 0)
-    dispatch_count_kernel<<<chunks, 256, 0, st>>>(idx, n_tokens, top_k, n_experts,
-                                                  chunk_cnt, err);
-  dispatch_scan_kernel<<<1, kMaxExperts, 0, st>>>(chunk_cnt, chunks, n_experts,
+    launch_pdl(dispatch_count_kernel, dim3(chunks), dim3(256), 0, st, idx, n_tokens, top_k,
+               n_experts, chunk_cnt, err);
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, chunk_cnt, chunks, n_experts,
                                                   capacity, chunk_base, offsets,
                                                   counts, kept, dropped);
   if (chunks > 0)
-    dispatch_rank_kernel<<<chunks, kRankWarps * 32, 0, st>>>(
+    launch_pdl(dispatch_rank_kernel, dim3(chunks), dim3(kRankWarps * 32), 0, st, 
         idx, n_tokens, top_k, n_experts, capacity, chunk_base, offsets,
         row_of_slot, token_of_row, slot_of_row);
 }

@@ -26,6 +26,8 @@ __device__ __forceinline__ float ld_elem(const void* base, int64_t i) {
 
 template <typename T, int EPI>
 __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmProblem p) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int NB = EPI == kEpiSwiglu ? 2 : 1;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[NB][BK][BN + 4];
@@ -183,6 +185,8 @@ template <typename T, int EB, int TPW, int MAXV>
 __global__ void __launch_bounds__(256)
 router_small_kernel(const T* __restrict__ x, const T* __restrict__ W, const T* __restrict__ b,
                     float* __restrict__ logits, int64_t n_tokens, int n_experts, int d) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int V = 16 / sizeof(T);                  // elements per 16 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.x * EB;
@@ -248,9 +252,9 @@ template <typename T, int EB, int TPW, int MAXV>
 void launch_router_small_t(const void* x, const void* w, const void* b, float* logits,
                            int64_t n_tokens, int n_experts, int d, cudaStream_t st) {
   const dim3 grid((unsigned)ceil_div64(n_experts, EB), (unsigned)ceil_div64(n_tokens, 8 * TPW));
-  router_small_kernel<T, EB, TPW, MAXV><<<grid, 256, 0, st>>>(
-      static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(b), logits,
-      n_tokens, n_experts, d);
+  launch_pdl(router_small_kernel<T, EB, TPW, MAXV>, grid, dim3(256), 0, st,
+             static_cast<const T*>(x), static_cast<const T*>(w), static_cast<const T*>(b), logits,
+             n_tokens, n_experts, d);
 }
 
 }  // namespace

@@ -578,6 +578,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (p.swiglu) prefetch_map(&tmB1);
   }
   if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
+  pdl_wait();                 // the grouping (offsets) and A come from predecessors
+  pdl_launch_dependents();
   if (warp == 2) {
     int carry = 0;
     for (int base = 0; base < G; base += 32) {
@@ -1058,6 +1060,8 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (p.swiglu) prefetch_map(&tmB1);
   }
   if (warp == 1) tmem_alloc_pair(s_tmem, kTmemCols);
+  pdl_wait();
+  pdl_launch_dependents();
   if (warp == 2) {
     int carry = 0;
     for (int base = 0; base < G; base += 32) {
@@ -1387,13 +1391,15 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
       cfg.blockDim = dim3(kThreads);
       cfg.dynamicSmemBytes = kSmemBytes2;
       cfg.stream = st;
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = 2;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cfg.numAttrs = 2;
       if (cudaLaunchKernelEx(&cfg, kern2, ma, mb0, mb1, p) == cudaSuccess) return true;
     }
     cudaGetLastError();   // clear, then run on single CTAs
@@ -1403,8 +1409,8 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return false;
-  kern<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb0, mb1, p);
-  return cudaGetLastError() == cudaSuccess;
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), kSmemBytes, st, ma, mb0, mb1, p) ==
+         cudaSuccess;
 }
 
 }  // namespace moe

@@ -106,6 +106,8 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
   __shared__ int s_sel[kRouteWarps][EPL * 32];     // its selected experts, by slot
   __shared__ int s_cnt[EPL * 32];
   __shared__ bool s_last;
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = n_experts;
   for (int e = threadIdx.x; e < EPL * 32; e += blockDim.x) s_cnt[e] = 0;
@@ -345,17 +347,17 @@ void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_exper
   const int tpc = fin.n_total < 4096 ? kRouteWarps : kRouteTokensPerCta;
   const dim3 grid((unsigned)ceil_div64(n_tokens, tpc)), block(kRouteWarps * 32);
   if (n_experts <= 32)
-    route_kernel<1><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tpc, tot, fin);
+    launch_pdl(route_kernel<1>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
   else if (n_experts <= 64)
-    route_kernel<2><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tpc, tot, fin);
+    launch_pdl(route_kernel<2>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
   else if (n_experts <= 128)
-    route_kernel<4><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tpc, tot, fin);
+    launch_pdl(route_kernel<4>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
   else
-    route_kernel<8><<<grid, block, 0, st>>>(logits, n_tokens, n_experts, top_k, mode,
-                                            sel_bias, idx, w, tpc, tot, fin);
+    launch_pdl(route_kernel<8>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
 }
 
 }  // namespace moe
