@@ -113,7 +113,7 @@ typedef int32_t moe_status_t;
 #define MOE_EXPERT_SILU_MLP  0
 #define MOE_EXPERT_SWIGLU    1
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define MOE_MAX_EXPERTS  256
 
 /* Layer description.  All fields are read, none is written. */
