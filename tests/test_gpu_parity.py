@@ -535,6 +535,48 @@ def test_forward_zero_tokens():
     assert (to_np(st["counts"]) == 0).all() and float(to_np(st["balance"])[0]) == 0.0
 
 
+def _forward_vs_oracle(shape, what):
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, st = _forward(D)
+    ref = O.forward(shape, inp.values)
+    keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
+    amb, _ = set_ambiguous_tokens(keys, shape.top_k, _router_margin(D, ref["logits"]))
+    keep = ~amb
+    assert keep.mean() > 0.9
+    assert_output_close(to_np(out)[keep], ref["out_exact"][keep], shape.dtype, what)
+    assert D.device_error() == M.MOE_OK
+    return out, st, ref
+
+
+def test_forward_256_experts():
+    """The largest expert count: 256 SwiGLU experts, top-8 (selection with 8
+    candidates per lane, 256 groups in the grouped GEMMs)."""
+    shape = _cfg(n_tokens=700, n_experts=256, top_k=8, d_model=128, d_ff=64,
+                 route=W.ROUTE_TOPK_SOFTMAX, dtype=W.DTYPE_BF16)
+    _forward_vs_oracle(shape, "E=256")
+
+
+@pytest.mark.parametrize("route", [0, 1, 2])
+def test_forward_single_token(route):
+    shape = _cfg(n_tokens=1, n_experts=16, top_k=4, d_model=128, d_ff=64, route=route,
+                 dtype=W.DTYPE_BF16)
+    if route == W.ROUTE_SIGMOID_BIAS:
+        shape = shape.replace(sel_bias_range=0.1)
+    _forward_vs_oracle(shape, "N=1")
+
+
+def test_forward_capacity_drops_everything():
+    """cf small enough that the capacity int(cf * (N // E)) is 0: every
+    assignment is dropped and the layer output is exactly zero."""
+    shape = _cfg(n_tokens=64, n_experts=8, top_k=2, d_model=64, d_ff=64,
+                 dtype=W.DTYPE_BF16, capacity_factor=0.01)
+    out, st, ref = _forward_vs_oracle(shape, "cap 0")
+    assert torch.count_nonzero(out) == 0
+    assert int(to_np(st["kept"]).sum()) == 0
+    assert int(to_np(st["dropped"]).sum()) == 64 * 2
+
+
 @pytest.mark.parametrize("E,k", [(1, 1), (4, 4)])
 def test_forward_special_cases(E, k):
     """E = 1, k = 1 is the dense FFN; k = E with no capacity is the dense
