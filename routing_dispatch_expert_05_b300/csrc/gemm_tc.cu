@@ -345,17 +345,26 @@ __device__ __forceinline__ void compact_chunk(const Params& p, int lane, int oro
                                               const uint32_t (&r)[32], uint32_t* stg,
                                               uint32_t& e8w) {
   float v[32];
-  float mx = 0.f;
+  float mx0 = 0.f, mx1 = 0.f, mx2 = 0.f, mx3 = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    v[j] = __uint_as_float(r[j]);
-    if (bp != nullptr && c0 + j < p.n_out) v[j] += __bfloat162float(bp[c0 + j]);
-    v[j] *= rscale;
-    mx = fmaxf(mx, fabsf(v[j]));                   // columns past n_out hold 0
+  for (int j = 0; j < 32; j += 4) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[j + q] = __uint_as_float(r[j + q]);
+      if (bp != nullptr && c0 + j + q < p.n_out) v[j + q] += __bfloat162float(bp[c0 + j + q]);
+    }
+    // four independent max chains (columns past n_out hold 0)
+    mx0 = fmaxf(mx0, fabsf(v[j]));
+    mx1 = fmaxf(mx1, fabsf(v[j + 1]));
+    mx2 = fmaxf(mx2, fabsf(v[j + 2]));
+    mx3 = fmaxf(mx3, fabsf(v[j + 3]));
   }
+  // the block's largest |v * rscale| is |rscale| * max |v| (rounding is
+  // monotone); rscale * 2^(14-e) is exact, so v * it rounds as (v * rscale) * 2^(14-e)
+  const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * fabsf(rscale);
   int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
   e = min(max(e, -100), 127);                      // zero / tiny blocks: bounded scale
-  const float scale = __uint_as_float((uint32_t)(127 + 14 - e) << 23);   // 2^(14-e)
+  const float scale = rscale * __uint_as_float((uint32_t)(127 + 14 - e) << 23);
   e8w |= (uint32_t)(e + 113) << (8 * ci);                                // 2^(e-14)
   uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgB16Stride);
 #pragma unroll
