@@ -329,9 +329,15 @@ def run_ours(args, shape, peaks, peaks_kind):
     router_bytes = N * d * es + E * d * es + N * k * 8
     # idx read twice, row_of_slot and token_of_row written, rows copied
     dispatch_bytes = N * k * 4 * 4 + N * d * es + m_kept * d * es
-    # expert outputs: fp16 + one fp32 scale per 256 columns (bf16 layers) or fp32
-    y_row_bytes = d * 2 + 4 * ((d + 255) // 256) if shape.dtype == W.DTYPE_BF16 else d * 4
-    combine_bytes = m_kept * y_row_bytes + N * d * es + N * k * 8 + \
+    # expert outputs: fp16 + one exponent byte per 32 columns (bf16 layers,
+    # already weighted, in slot order) or fp32 with the weights read separately
+    if shape.dtype == W.DTYPE_BF16:
+        y_row_bytes = d * 2 + (d + 31) // 32
+        slot_bytes = N * k * 4                     # row_of_slot (drop flags)
+    else:
+        y_row_bytes = d * 4
+        slot_bytes = N * k * 8                     # row_of_slot and w
+    combine_bytes = m_kept * y_row_bytes + N * d * es + slot_bytes + \
         (N * d * 4 if shape.n_shared > 0 else 0)
     stage_report = {}
     for name in stages:
