@@ -392,6 +392,17 @@ MOE_API moe_status_t moe_update_selection_bias(const moe_config_t *cfg,
 
 /* ---- diagnostics -------------------------------------------------------- */
 
+/* Failure-path self-check: runs the expert GEMMs' bounded mbarrier wait on
+ * barriers nothing completes, with a limit of limit_ns (1 us .. 1 s) instead
+ * of the kernels' 2 s.  The wait gives up, records MOE_ERR_TIMEOUT in the
+ * device error word of ws (read it with moe_read_device_error) and the
+ * kernel returns; the context stays usable.  The error word is sticky:
+ * zero the workspace's first 256 bytes before using ws for the layer again.
+ * ws: at least 256 bytes, 16-byte aligned.  No counterpart on the pages. */
+MOE_API moe_status_t moe_check_wait_timeout(void *ws, size_t ws_bytes, int64_t limit_ns,
+                                            void *stream);
+
+
 /* Waits for `stream`, then reads and clears the device error word at the
  * start of `ws`: *code = MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT. */
 MOE_API moe_status_t moe_read_device_error(void *ws, int32_t *code, void *stream);

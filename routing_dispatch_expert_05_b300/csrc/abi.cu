@@ -1156,6 +1156,17 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
                        static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,
+                                    void* stream) {
+  if (ws == nullptr || ws_bytes < kAlign || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (limit_ns < 1000 || limit_ns > 1000000000) return MOE_ERR_INVALID_ARG;
+  int32_t* err = static_cast<int32_t*>(ws);
+  int32_t* flags = err + 32;                       // bytes 128..135 of the first block
+  return launch_wait_check(err, (uint64_t)limit_ns, flags, static_cast<cudaStream_t>(stream))
+             ? last_cuda()
+             : MOE_ERR_CUDA;
+}
+
 moe_status_t moe_read_device_error(void* ws, int32_t* code, void* stream) {
   if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);

@@ -142,14 +142,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // Wait for the phase of `bar` with parity `parity` to complete, giving up
 // when another role aborted or after kTimeoutNs (then abort everyone).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag, int32_t* err) {
+                                             volatile int* abort_flag, int32_t* err,
+                                             uint64_t limit_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         set_device_error(err, kDevTimeout);
         return false;
@@ -1254,6 +1255,32 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// ------------------------------------------------------- wait self-check
+// The bounded-wait path of the GEMM kernels, made to run out on purpose: two
+// roles wait on mbarriers nothing will ever complete; the first gives up
+// after limit_ns, records kDevTimeout and raises the CTA's abort flag; the
+// second (with a 4x longer limit of its own) leaves on that flag.  flags[r]
+// = 1 if role r's wait succeeded (it never should).  No trap, no endless
+// loop: the kernel returns and the context stays usable.
+__global__ void __launch_bounds__(64)
+wait_check_kernel(int32_t* err, uint64_t limit_ns, int32_t* flags) {
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  volatile int* ab = &s_abort;
+  if (lane == 0 && warp < 2) {
+    const bool ok = wait_bounded(&bar[warp], 0, ab, err, warp == 0 ? limit_ns : 4 * limit_ns);
+    flags[warp] = ok ? 1 : 0;
+  }
+}
+
 // ---------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
@@ -1308,6 +1335,11 @@ bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
                            kSmemBytes) != cudaSuccess)
     return false;
   tc_wgrad_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess;
+}
+
+bool launch_wait_check(int32_t* err, uint64_t limit_ns, int32_t* flags, cudaStream_t st) {
+  tc::wait_check_kernel<<<1, 64, 0, st>>>(err, limit_ns, flags);
   return cudaGetLastError() == cudaSuccess;
 }
 

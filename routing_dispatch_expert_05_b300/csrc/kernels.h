@@ -164,6 +164,8 @@ struct WgradProblem {
   int32_t* err;
 };
 bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st);
+// the GEMM kernels' bounded mbarrier wait, run out on purpose (see moe.h)
+bool launch_wait_check(int32_t* err, uint64_t limit_ns, int32_t* flags, cudaStream_t st);
 
 // ---- combine ----------------------------------------------------------------
 // y: fp32 expert outputs [N*k, d]; out: layer dtype [N, d]

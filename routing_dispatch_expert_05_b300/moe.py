@@ -33,7 +33,7 @@ EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_timed", "moe_forward_host",
             "moe_update_selection_bias", "moe_backward_workspace_size", "moe_backward",
-            "moe_read_device_error",
+            "moe_check_wait_timeout", "moe_read_device_error",
             "moe_status_string", "moe_version")
 
 
@@ -103,6 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_read_device_error": [vp, P(ctypes.c_int32), vp],
         "moe_update_selection_bias": [cfgp, vp, vp, ctypes.c_float, vp, vp],
         "moe_backward_workspace_size": [cfgp, P(sz)],
+        "moe_check_wait_timeout": [vp, sz, ctypes.c_int64, vp],
         "moe_backward": [cfgp, vp, wp, vp, ctypes.c_float, P(MoEGrads), vp, sz, vp],
     }
     for name, args in sig.items():
@@ -337,6 +338,13 @@ def moe_update_selection_bias(cfg, counts, sel_bias, gamma, load_cv=None, stream
     _check(load_library().moe_update_selection_bias(
         ctypes.byref(cfg), ptr(counts), ptr(sel_bias), float(gamma), ptr(load_cv),
         _stream(stream)), "moe_update_selection_bias")
+
+
+def moe_check_wait_timeout(ws, limit_ns: int, stream=None):
+    """Run the GEMMs' bounded wait out on purpose (see moe.h)."""
+    wp, wb = _ws(ws)
+    _check(load_library().moe_check_wait_timeout(wp, wb, int(limit_ns), _stream(stream)),
+           "moe_check_wait_timeout")
 
 
 def moe_read_device_error(ws, stream=None) -> int:

@@ -177,3 +177,13 @@ def test_backward_rejects_unsupported_layers(lib):
     st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(w), addr, 0.0,
                           ctypes.byref(g), addr, n.value, None)
     assert st == M.MOE_ERR_INVALID_ARG
+
+
+def test_wait_check_rejects_bad_arguments(lib):
+    buf = ctypes.create_string_buffer(4096)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    f = lib.moe_check_wait_timeout
+    assert f(None, 4096, 1_000_000, None) == M.MOE_ERR_INVALID_ARG
+    assert f(addr, 128, 1_000_000, None) == M.MOE_ERR_INVALID_ARG       # below 256 bytes
+    assert f(addr, 4096, 10, None) == M.MOE_ERR_INVALID_ARG             # limit below 1 us
+    assert f(addr, 4096, 5_000_000_000, None) == M.MOE_ERR_INVALID_ARG  # above 1 s
