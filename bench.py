@@ -74,10 +74,19 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+    """nvidia-smi clock / throttle-reason samples while the timed region runs.
+
+    Samples are taken every 50 ms and carry nvidia-smi's own timestamp;
+    `stop(region)` keeps those taken between the host times (time.time())
+    that bracket the timed region, so an idle sample from before or after it
+    does not enter the median.  If the region is shorter than one interval
+    and no sample falls inside it, the nearest samples are reported with
+    "in_region": 0."""
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, uuid=None):
         self.uuid = uuid
@@ -88,11 +97,12 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.INTERVAL_MS)], stdout=open(self.out, "w"),
+                stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, region=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -100,32 +110,63 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         try:
             with open(self.out) as f:
-                for line in f:
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) < 10:
-                        continue
-                    if self.uuid and parts[1] != self.uuid:
-                        continue
-                    rows.append(parts)
+                text = f.read()
             os.unlink(self.out)
         except OSError:
             return None
+        return self.summarise(text, self.uuid, region)
+
+    @staticmethod
+    def summarise(text, uuid=None, region=None):
+        """Median SM clock, max clock and the throttle reasons seen, from
+        nvidia-smi's CSV rows (the FIELDS order)."""
+        import datetime
+        rows = []
+        for line in text.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 11:
+                continue
+            if uuid and parts[2] != uuid:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            rows.append((ts, parts))
         if not rows:
             return None
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        chosen = rows
+        in_region = None
+        if region is not None:
+            t0, t1 = region
+            inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+            in_region = len(inside)
+            if inside:
+                chosen = inside
+            else:
+                # the region fell between two samples: the one before it and
+                # the one after it
+                timed = [r for r in rows if r[0] is not None]
+                before = [r for r in timed if r[0] < t0][-1:]
+                after = [r for r in timed if r[0] > t1][:1]
+                chosen = before + after or rows
+        num = lambda v: v.replace(".", "", 1).isdigit()
+        sm = [float(p[3]) for _, p in chosen if num(p[3])]
+        mx = [float(p[4]) for _, p in chosen if num(p[4])]
         reasons = set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in rows:
-            for name, v in zip(names, r[6:10]):
+        for _, p in chosen:
+            for name, v in zip(names, p[7:11]):
                 if v.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None,
+               "reasons": sorted(reasons), "samples": len(chosen)}
+        if in_region is not None:
+            out["in_region"] = in_region
+        return out
 
 
 def oracle_sample(shape, inputs, target_s=12.0, max_tokens=None):
@@ -239,12 +280,14 @@ def run_ours(args, shape, peaks, peaks_kind):
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    h_start = time.time()
     t_start.record(stream)
     for s_ in range(args.steps):
         M.moe_forward_timed(cfg, x, weights, out, fstats, ws, evs[s_])
     t_end.record(stream)
     barrier()
-    clocks = sampler.stop()
+    h_end = time.time()
+    clocks = sampler.stop(region=(h_start, h_end))
     total_ms = t_start.elapsed_time(t_end)
     names = list(M.FORWARD_STAGES)
 
@@ -412,7 +455,10 @@ def run_reference(args, shape):
         return None, rank
     inputs = W.make_inputs(shape)
     from oracle import moe_oracle as O
-    n_s, el = oracle_sample(shape, inputs, target_s=max(1.0, args.cpu_seconds / 2),
+    # each step's sample shrinks with the step count, so that the whole run
+    # stays near a minute and a half of CPU time
+    per_step = min(args.cpu_seconds / 2, 90.0 / (args.steps + args.warmup))
+    n_s, el = oracle_sample(shape, inputs, target_s=max(0.05, per_step),
                             max_tokens=args.ref_tokens)
     sub = inputs.first_tokens(n_s)
     for _ in range(args.warmup):
@@ -498,7 +544,7 @@ def run_backward(args, shape, peaks, peaks_kind):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="qwen3_moe", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -55,3 +55,43 @@ def test_job_throughput_counts_every_rank():
     import bench
     assert bench.job_tokens_per_s(16384, 4, 2.0) == pytest.approx(16384 * 4 / 2e-3)
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]     # no process group: identity
+
+
+def _clock_rows(rows):
+    """nvidia-smi CSV rows in the sampler's field order: (time, sm MHz,
+    reasons active?) per row, the same GPU."""
+    lines = []
+    for t, sm, slow in rows:
+        act = "Active" if slow else "Not Active"
+        lines.append(f"2026/01/02 03:04:{t:06.3f}, 0, GPU-x, {sm}, 2032, 900.00 W, 0x0, "
+                     f"Not Active, Not Active, {act}, Not Active")
+    return "\n".join(lines)
+
+
+def test_clock_summary_keeps_only_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import datetime
+    import bench
+    base = datetime.datetime(2026, 1, 2, 3, 4, 0).timestamp()
+    # idle samples (345 MHz) before and after; loaded ones inside [10, 10.3]
+    text = _clock_rows([(9.90, 345, False), (10.05, 2032, False), (10.10, 2017, False),
+                        (10.25, 2032, False), (10.40, 345, True)])
+    got = bench.ClockSampler.summarise(text, "GPU-x", (base + 10.0, base + 10.3))
+    assert got["in_region"] == 3 and got["samples"] == 3
+    assert got["sm_mhz"] == 2032 and got["sm_max_mhz"] == 2032
+    assert got["reasons"] == []                    # the slowdown came after the region
+    # another GPU's rows are ignored
+    assert bench.ClockSampler.summarise(text, "GPU-y", None) is None
+
+
+def test_clock_summary_of_a_region_between_two_samples():
+    sys.path.insert(0, ROOT)
+    import datetime
+    import bench
+    base = datetime.datetime(2026, 1, 2, 3, 4, 0).timestamp()
+    text = _clock_rows([(9.0, 345, False), (10.00, 2032, False), (10.05, 2010, True),
+                        (11.0, 345, False)])
+    got = bench.ClockSampler.summarise(text, None, (base + 10.01, base + 10.04))
+    assert got["in_region"] == 0 and got["samples"] == 2
+    assert got["sm_mhz"] == (2032 + 2010) / 2
+    assert got["reasons"] == ["sw_thermal_slowdown"]
