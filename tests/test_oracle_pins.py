@@ -304,6 +304,78 @@ def test_expert_ffn_matches_torch(kind, dtype):
     assert np.all(np.abs(got - ref) <= 2 * 2.0 ** -23 * np.abs(ref) + 1e-300)
 
 
+# Closed forms of the expert FFN.  The weights are scaled permutation
+# matrices, so every output is one or two values of silu(z) = z * sigma(z) at
+# z in {1, 2, -1}, written out below as decimal literals from the logistic
+# function's values (sigma(1) = e / (1 + e), sigma(2) = e^2 / (1 + e^2),
+# sigma(-1) = 1 - sigma(1)).  A swapped gate and up matrix, a transposed
+# operand, a bias in the wrong place, a missing activation, a wrong rounding
+# point or a wrong expert index each changes at least one of them.
+SILU_1 = 0.7310585786300049          # silu(1) = sigma(1)
+SILU_2 = 1.7615941559557646          # silu(2) = 2 sigma(2)
+SILU_M1 = -0.2689414213699951        # silu(-1) = -(1 - sigma(1))
+
+
+def _swiglu_closed_form_weights():
+    # W1 x = (x1, x2, x0); W3 x = 0.5 (x2, x0, x1); y = (1.25 h2, 2 h0, 3 h1)
+    w1 = np.array([[0, 1, 0], [0, 0, 1], [1, 0, 0]], np.float64)
+    w3 = 0.5 * np.array([[0, 0, 1], [1, 0, 0], [0, 1, 0]], np.float64)
+    w2 = np.array([[0, 0, 1.25], [2, 0, 0], [0, 3, 0]], np.float64)
+    return w1, w3, w2
+
+
+def test_swiglu_expert_closed_form_fp32():
+    """QWEN expert forward pass / DSEEK s.1: h = silu(W1 x) * (W3 x), y = W2 h."""
+    w1, w3, w2 = _swiglu_closed_form_weights()
+    x = np.array([[1.0, 2.0, -1.0]])
+    # W1 x = (2, -1, 1), W3 x = (-0.5, 0.5, 1)
+    want_h = [-0.5 * SILU_2, 0.5 * SILU_M1, SILU_1]
+    want_y = [1.25 * SILU_1, -SILU_2, 1.5 * SILU_M1]
+    h, y = O.expert_ffn(x, w1, w2, O.SWIGLU, O.F32, w3=w3)
+    assert np.allclose(h[0], want_h, rtol=1.2e-7, atol=0)
+    assert np.allclose(y[0], want_y, rtol=2.5e-7, atol=0)
+
+
+def test_swiglu_expert_closed_form_bf16_rounds_h_only():
+    """bf16 layers store h in bf16 and accumulate y in fp32: h = bf16 of
+    (-0.88080, -0.13447, 0.73106) = (-225/256, -138/1024, 187/256); y = W2 h
+    is then exact in fp32 (1.25 * 187/256 = 233.75/256 is not a bf16 value,
+    so rounding y to bf16 as well would show)."""
+    w1, w3, w2 = _swiglu_closed_form_weights()
+    x = np.array([[1.0, 2.0, -1.0]])
+    h, y = O.expert_ffn(x, w1, w2, O.SWIGLU, O.BF16, w3=w3)
+    assert h[0].tolist() == [-0.87890625, -0.134765625, 0.73046875]
+    assert y[0].tolist() == [0.9130859375, -1.7578125, -0.404296875]
+
+
+def test_silu_mlp_expert_closed_form_with_biases():
+    """EXPERT In[7]: h = silu(W1 x + b1), y = W2 h + b2."""
+    x = np.array([[0.5, -1.0]])
+    w1 = np.array([[2.0, 0.0], [0.0, -1.0], [1.0, 1.0]])     # W1 x = (1, 1, -0.5)
+    b1 = np.array([0.0, 1.0, 0.5])                           # pre-activation (1, 2, 0)
+    w2 = np.array([[1.0, -1.0, 4.0], [0.0, 0.5, 0.0]])
+    b2 = np.array([0.25, -1.0])
+    h, y = O.expert_ffn(x, w1, w2, O.SILU_MLP, O.F32, b1=b1, b2=b2)
+    assert np.allclose(h[0], [SILU_1, SILU_2, 0.0], rtol=1.2e-7, atol=0)
+    assert np.allclose(y[0], [SILU_1 - SILU_2 + 0.25, 0.5 * SILU_2 - 1.0], rtol=2.5e-7, atol=0)
+    # bf16: h = (187/256, 225/128, 0), y exact in fp32
+    h, y = O.expert_ffn(x, w1, w2, O.SILU_MLP, O.BF16, b1=b1, b2=b2)
+    assert h[0].tolist() == [0.73046875, 1.7578125, 0.0]
+    assert y[0].tolist() == [-0.77734375, -0.12109375]
+
+
+def test_grouped_ffn_applies_each_expert_to_its_own_rows():
+    """d = F = 1: expert 0 is (w1, w3, w2) = (1, 1, 1), expert 1 is empty,
+    expert 2 is (2, -1, 0.5); rows 0 | - | 1, 2 by the offsets."""
+    p = {"w1": np.array([1.0, 9.0, 2.0]).reshape(3, 1, 1),
+         "w3": np.array([1.0, 9.0, -1.0]).reshape(3, 1, 1),
+         "w2": np.array([1.0, 9.0, 0.5]).reshape(3, 1, 1)}
+    x = np.array([[1.0], [1.0], [-0.5]])
+    _, y = O.grouped_ffn(x, [0, 1, 1, 3], p, O.SWIGLU, O.F32)
+    # row 0: silu(1); row 1: 0.5 * silu(2) * (-1); row 2: 0.5 * silu(-1) * 0.5
+    assert np.allclose(y[:, 0], [SILU_1, -0.5 * SILU_2, 0.25 * SILU_M1], rtol=2.5e-7, atol=0)
+
+
 def test_combine_matches_index_add():
     rng = np.random.default_rng(8)
     n, k, d, e = 6, 3, 4, 5
@@ -343,6 +415,20 @@ def test_shared_experts_concatenation_identity():
                                      TF.linear(T(x), T(ws3[s])), O.F32),
                         T(ws2[s])) for s in range(2))
     assert np.allclose(two, ref.numpy(), rtol=1e-6, atol=1e-9)
+
+
+def test_shared_experts_closed_form():
+    """DSEEK s.4: the shared experts are always on, each with weight 1, and
+    their outputs add.  d = F_s = 1: expert 0 is (1, 1, 1), expert 1 is
+    (2, -1, 0.5); x = 1 gives silu(1) + 0.5 * silu(2) * (-1)."""
+    ws1 = np.array([1.0, 2.0]).reshape(2, 1, 1)
+    ws3 = np.array([1.0, -1.0]).reshape(2, 1, 1)
+    ws2 = np.array([1.0, 0.5]).reshape(2, 1, 1)
+    x = np.array([[1.0]])
+    got = O.shared_ffn(x, ws1, ws3, ws2, O.F32)
+    assert np.allclose(got[0], [SILU_1 - 0.5 * SILU_2], rtol=1e-6, atol=0)
+    # bf16: each expert's h is rounded (187/256 and -225/128), the sum is not
+    assert O.shared_ffn(x, ws1, ws3, ws2, O.BF16)[0].tolist() == [0.73046875 - 0.87890625]
 
 
 # ------------------------------------------------------ balance statistic
