@@ -256,6 +256,45 @@ def test_bf16_rounding_avoids_double_rounding():
 
 
 # --------------------------------------------------------------- pieces
+def test_router_logits_of_unit_inputs_are_weight_columns():
+    """BUILD step 2: the gate is Linear(d, E), logits = x W^T + b; a unit
+    input picks one column of W (a transposed W would pick a row)."""
+    w = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]])
+    b = np.array([0.5, -1.0])
+    x = np.array([[0.0, 1.0, 0.0], [0.0, 0.0, 2.0]])
+    assert O.router_logits(x, w, b).tolist() == [[2.5, 4.0], [6.5, 11.0]]
+    assert O.router_logits(x, w).tolist() == [[2.0, 5.0], [6.0, 12.0]]
+
+
+@pytest.mark.parametrize("mode", [O.SOFTMAX_TOPK, O.TOPK_SOFTMAX])
+def test_softmax_mode_weights_closed_form(mode):
+    """Logits ln(1, 2, 5, 1/2): top-2 is experts 2 and 1 with weights 5/7 and
+    2/7 in both softmax modes (BUILD step 2; QWEN routing probabilities); the
+    statistic's p is the full softmax, (1, 2, 5, 1/2) / 8.5."""
+    lg = np.log(np.array([[1.0, 2.0, 5.0, 0.5]])).astype(np.float32)
+    idx, w, p = O.route(lg, mode, 2)
+    assert idx.tolist() == [[2, 1]]
+    assert np.allclose(w, [[5 / 7, 2 / 7]], rtol=1e-6, atol=0)
+    assert np.allclose(p, [[1 / 8.5, 2 / 8.5, 5 / 8.5, 0.5 / 8.5]], rtol=1e-6, atol=0)
+
+
+def test_sigmoid_mode_weights_closed_form():
+    """DSEEK s.2: logits ln(1, 3, 1/3, 7) give s = (1/2, 3/4, 1/4, 7/8).
+    Without a bias, top-2 is experts 3 and 1 with weights 7/13 and 6/13; a
+    bias of 0.7 on expert 2 selects experts 2 and 3, whose weights use s
+    alone: 2/9 and 7/9.  p = s / sum(s) either way."""
+    lg = np.log(np.array([[1.0, 3.0, 1 / 3, 7.0]])).astype(np.float32)
+    p_want = [[0.5 / 2.375, 0.75 / 2.375, 0.25 / 2.375, 0.875 / 2.375]]
+    idx, w, p = O.route(lg, O.SIGMOID_BIAS, 2, np.zeros(4, np.float32))
+    assert idx.tolist() == [[3, 1]]
+    assert np.allclose(w, [[7 / 13, 6 / 13]], rtol=1e-6, atol=0)
+    assert np.allclose(p, p_want, rtol=1e-6, atol=0)
+    idx, w, p = O.route(lg, O.SIGMOID_BIAS, 2, np.array([0, 0, 0.7, 0], np.float32))
+    assert idx.tolist() == [[2, 3]]
+    assert np.allclose(w, [[2 / 9, 7 / 9]], rtol=1e-6, atol=0)
+    assert np.allclose(p, p_want, rtol=1e-6, atol=0)
+
+
 def test_router_logits_match_torch_linear():
     rng = np.random.default_rng(2)
     x = rng.standard_normal((7, 5))
