@@ -55,6 +55,18 @@ def _table_assignments(seed=7):
     return g, counts, idx.reshape(-1, 1).astype(np.int32)
 
 
+def test_capacity_truncates_tokens_per_expert_first():
+    """EXPERT In[10] (reading R1): capacity = int(cf * (N // E)).  The
+    tokens per expert are an integer division before the factor applies, so
+    a ragged N gives a smaller capacity than int(cf * N / E) would."""
+    assert O.capacity(2.0, 11, 4) == 4          # int(2.0 * 2), not int(5.5) = 5
+    assert O.capacity(1.25, 7, 2) == 3          # int(1.25 * 3), not int(4.375) = 4
+    assert O.capacity(0.5, 3, 4) == 0           # fewer tokens than experts: nothing kept
+    assert O.capacity(0.0, 100, 4) is None and O.capacity(-1.0, 100, 4) is None
+    d = O.dispatch(np.array([[0], [0], [0], [0], [0], [1], [1]]), 2, 1.25)
+    assert d["kept"].tolist() == [3, 2] and d["dropped"].tolist() == [2, 0]
+
+
 def test_capacity_table_out12():
     g, counts, idx = _table_assignments()
     n_tok = int(g["num_tokens"][0][0])
