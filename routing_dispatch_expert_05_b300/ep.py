@@ -30,8 +30,11 @@ the scan of counts over ranks before step 1's ranking and is not done here.
 
 This module is the host side: the plan (pure index arithmetic) and the
 orchestration over torch.distributed.  The per-rank stages are passed in as
-callables -- on a GPU the library's own kernels (moe_router_topk,
-moe_dispatch_permute, moe_grouped_ffn, moe_combine) and NCCL all-to-all.
+callables -- on a GPU the library's own entry points (moe_router_topk,
+moe_dispatch_permute, moe_grouped_ffn on the rank's slice of the expert
+stacks, moe_combine) -- and the exchange is whatever backend the process
+group has: NCCL between GPUs, or gloo through the host (whose all-to-all has
+no 16-bit types, so bf16 rows travel as int32 pairs).
 """
 from __future__ import annotations
 
