@@ -112,3 +112,48 @@ def test_ep_forward_equals_single_process_layer(world):
     got = np.concatenate([np.asarray(res[r]) for r in range(world)])
     assert got.shape == ref.shape
     assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_receive_plan_properties_over_random_counts():
+    """For any counts: the plan is a permutation of the arrival rows that
+    visits experts in order, sources in order inside an expert, and each
+    source's rows in arrival order; the group offsets are the per-expert
+    totals."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = hypothesis.strategies
+
+    @hypothesis.settings(max_examples=200, deadline=None)
+    @hypothesis.given(st.integers(1, 4).flatmap(
+        lambda r: st.integers(1, 5).flatmap(
+            lambda l: st.lists(st.lists(st.integers(0, 6), min_size=l, max_size=l),
+                               min_size=r, max_size=r))))
+    def check(rows):
+        rc = np.array(rows, np.int64)
+        p = ep.receive_plan(rc)
+        total = int(rc.sum())
+        assert sorted(p.to_expert_major.tolist()) == list(range(total))
+        assert p.local_offsets.tolist() == [0] + np.cumsum(rc.sum(axis=0)).tolist()
+        assert p.rows_from.tolist() == rc.sum(axis=1).tolist()
+        # label every arrival row with (expert, source, index within the block)
+        labels = []
+        for s in range(rc.shape[0]):
+            for e in range(rc.shape[1]):
+                labels += [(e, s, i) for i in range(rc[s, e])]
+        ordered = [labels[a] for a in p.to_expert_major.tolist()]
+        assert ordered == sorted(labels)
+
+    check()
+
+
+def test_send_counts_cover_the_grouped_buffer():
+    rng = np.random.default_rng(12)
+    for world in (1, 2, 4, 8):
+        per_expert = rng.integers(0, 9, 16)
+        offsets = np.concatenate([[0], np.cumsum(per_expert)])
+        c = ep.send_counts(offsets, world)
+        assert c.shape == (world, 16 // world)
+        assert c.sum() == offsets[-1]
+        # rank r's block is one contiguous slice of the grouped buffer
+        starts = offsets[::16 // world][:world]
+        assert (starts + c.sum(axis=1)).tolist() == offsets[16 // world::16 // world].tolist()
+    assert list(ep.experts_of_rank(16, 4, 2)) == [8, 9, 10, 11]
