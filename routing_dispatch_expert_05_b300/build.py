@@ -2,7 +2,7 @@
 
 Each ``csrc/*.cu`` is compiled to an object under ``_build/`` (in parallel),
 then linked with ``nvcc -shared``.  The CUDA runtime is linked statically;
-the driver API (tensor-map encoding) is reached at run time through
+the CUDA driver API (tensor-map encoding) is reached at run time through
 ``cudaGetDriverEntryPoint``, so the library loads on a machine without a
 GPU (nothing in it runs there).
 
