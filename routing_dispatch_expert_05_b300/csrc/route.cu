@@ -95,7 +95,10 @@ __device__ __forceinline__ uint32_t take_best(uint64_t (&c)[EPL], int lane, uint
   return emin;
 }
 
-template <int EPL>
+// SIG: the sigmoid mode (its candidate packing keeps the most arrays live),
+// compiled apart from the two softmax modes so that each gets its own
+// register allocation under the launch bound.
+template <int EPL, bool SIG>
 __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 4 : 2)
 route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
              int top_k, int mode, const float* __restrict__ sel_bias,
@@ -118,7 +121,7 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     ps[i] = 0.f;
-    bias[i] = (mode == 2 && e < E) ? sel_bias[e] : 0.f;
+    bias[i] = (SIG && e < E) ? sel_bias[e] : 0.f;
   }
 
   const int64_t t0 = (int64_t)blockIdx.x * tokens_per_cta;
@@ -140,7 +143,7 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
     for (int i = 0; i < EPL; ++i) l[i] = l_next[i];
     load_row(t + kRouteWarps);
     uint64_t c[EPL];
-    if (mode == 2) {
+    if constexpr (SIG) {
       // Rank fp32 keys first (within kSlack of the exact ones); the exact top
       // k lies among the experts whose fp32 key is within 2 kSlack of the
       // k-th fp32 key, so only those get the double-precision sigmoid.
@@ -328,6 +331,25 @@ bias_update_kernel(const int32_t* __restrict__ counts, int n_experts, float gamm
   }
 }
 
+template <bool SIG>
+void launch_route_epl(dim3 grid, dim3 block, cudaStream_t st, const float* logits,
+                      int64_t n_tokens, int n_experts, int top_k, int mode,
+                      const float* sel_bias, int32_t* idx, float* w, int tpc,
+                      const RouteTotals& tot, const RouteFinal& fin) {
+  if (n_experts <= 32)
+    launch_pdl(route_kernel<1, SIG>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
+  else if (n_experts <= 64)
+    launch_pdl(route_kernel<2, SIG>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
+  else if (n_experts <= 128)
+    launch_pdl(route_kernel<4, SIG>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
+  else
+    launch_pdl(route_kernel<8, SIG>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
+               mode, sel_bias, idx, w, tpc, tot, fin);
+}
+
 }  // namespace
 
 void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float* sel_bias,
@@ -346,18 +368,12 @@ void launch_route_from_logits(const float* logits, int64_t n_tokens, int n_exper
   // over all of them would.
   const int tpc = fin.n_total < 4096 ? kRouteWarps : kRouteTokensPerCta;
   const dim3 grid((unsigned)ceil_div64(n_tokens, tpc)), block(kRouteWarps * 32);
-  if (n_experts <= 32)
-    launch_pdl(route_kernel<1>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
-               mode, sel_bias, idx, w, tpc, tot, fin);
-  else if (n_experts <= 64)
-    launch_pdl(route_kernel<2>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
-               mode, sel_bias, idx, w, tpc, tot, fin);
-  else if (n_experts <= 128)
-    launch_pdl(route_kernel<4>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
-               mode, sel_bias, idx, w, tpc, tot, fin);
+  if (mode == 2)
+    launch_route_epl<true>(grid, block, st, logits, n_tokens, n_experts, top_k, mode, sel_bias,
+                           idx, w, tpc, tot, fin);
   else
-    launch_pdl(route_kernel<8>, grid, block, 0, st, logits, n_tokens, n_experts, top_k,
-               mode, sel_bias, idx, w, tpc, tot, fin);
+    launch_route_epl<false>(grid, block, st, logits, n_tokens, n_experts, top_k, mode, sel_bias,
+                            idx, w, tpc, tot, fin);
 }
 
 }  // namespace moe
