@@ -20,7 +20,6 @@ import functools
 import numpy as np
 import torch
 
-from oracle import moe_oracle as O
 from routing_dispatch_expert_05_b300 import moe as M
 from routing_dispatch_expert_05_b300 import workloads as W
 

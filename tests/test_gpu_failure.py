@@ -5,7 +5,6 @@ the other waiting role leaves on the CTA's abort flag, the kernel returns,
 and the same context then runs the layer normally."""
 import time
 
-import numpy as np
 import pytest
 import torch
 

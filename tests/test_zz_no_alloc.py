@@ -14,7 +14,6 @@ it runs the same alone in a fresh process or after every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
