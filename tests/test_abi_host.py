@@ -187,3 +187,60 @@ def test_wait_check_rejects_bad_arguments(lib):
     assert f(addr, 128, 1_000_000, None) == M.MOE_ERR_INVALID_ARG       # below 256 bytes
     assert f(addr, 4096, 10, None) == M.MOE_ERR_INVALID_ARG             # limit below 1 us
     assert f(addr, 4096, 5_000_000_000, None) == M.MOE_ERR_INVALID_ARG  # above 1 s
+
+
+def test_grouping_expert_and_combine_calls_reject_bad_arguments(lib):
+    """Every stage entry point checks its pointers, weights and workspace
+    before it enqueues anything: the addresses here are host memory and each
+    call must return at a check (the toy layer: fp32 SiLU-MLP with biases,
+    64 tokens)."""
+    cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
+    c = ctypes.byref(cfg)
+    buf = ctypes.create_string_buffer(1 << 20)
+    a = (ctypes.addressof(buf) + 255) // 256 * 256
+    big = 1 << 40                       # claimed workspace size; never touched
+    full = M.MoEWeights(w_router=a, b_router=a, w1=a, b1=a, w2=a, b2=a)
+    # grouping: (cfg, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats, ws, bytes, stream)
+    disp = lib.moe_dispatch_permute
+    assert disp(c, a, a, None, a, a, a, None, a, big, None) == -1          # no offsets
+    assert disp(c, a, a, a, a, a, None, None, a, big, None) == -1          # x without x_perm
+    assert disp(c, a, a, a, a + 4, a, a, None, a, big, None) == -1         # misaligned row_of_slot
+    assert disp(c, None, a, a, a, a, a, None, a, big, None) == -1          # no idx
+    assert disp(c, a, a, a, a, a, a, None, a, 16, None) == -3              # short workspace
+    assert disp(c, a, a, a, a, a, a, None, None, big, None) == -1          # no workspace
+    bad_stats = M.MoEStats(counts=a + 4)
+    assert disp(c, a, a, a, a, a, a, ctypes.byref(bad_stats), a, big, None) == -1
+    noalloc = lib.moe_dispatch_permute_noalloc
+    assert noalloc(c, a, a, None, a, a, a, None, None) == -1               # no offsets
+    assert noalloc(c, None, a, a, a, a, a, None, None) == -1               # no idx
+    assert noalloc(c, a, None, a, a, a, a, None, None) == -1               # x_perm without x
+    big_n = _bad(n_tokens=70000)                                           # beyond its fixed scratch
+    assert noalloc(ctypes.byref(big_n), a, a, a, a, a, a, None, None) == -2
+    # expert GEMMs
+    no_b1 = M.MoEWeights(w1=a, w2=a, b2=a)
+    assert lib.moe_expert_up(c, a, a, ctypes.byref(no_b1), a, a, big, None) == -1
+    assert lib.moe_expert_up(c, a, a, None, a, a, big, None) == -1         # no weights
+    assert lib.moe_expert_up(c, a, a, ctypes.byref(full), None, a, big, None) == -1   # no h
+    assert lib.moe_expert_up(c, a, a, ctypes.byref(full), a, a, 16, None) == -3
+    assert lib.moe_expert_up_gather(c, a, None, a, ctypes.byref(full), a, a, big, None) == -1
+    no_b2 = M.MoEWeights(w1=a, b1=a, w2=a)
+    assert lib.moe_expert_down(c, a, a, ctypes.byref(no_b2), a, a, big, None) == -1
+    assert lib.moe_expert_down(c, a, a, ctypes.byref(full), a + 8, a, big, None) == -1  # misaligned y
+    no_w2 = M.MoEWeights(w1=a, b1=a, b2=a)
+    assert lib.moe_grouped_ffn(c, a, a, ctypes.byref(no_w2), a, a, a, big, None) == -1
+    assert lib.moe_grouped_ffn(c, a, None, ctypes.byref(full), a, a, a, big, None) == -1
+    swiglu = _bad(expert=W.EXPERT_SWIGLU, has_bias=False, dtype=W.DTYPE_BF16)
+    no_w3 = M.MoEWeights(w1=a, w2=a)
+    assert lib.moe_expert_up(ctypes.byref(swiglu), a, a, ctypes.byref(no_w3), a, a, big,
+                             None) == -1
+    # combine: (cfg, y, row_of_slot, w, shared_out, out, ws, bytes, stream)
+    assert lib.moe_combine(c, a, a, None, None, a, a, big, None) == -1     # no weights
+    assert lib.moe_combine(c, a, a, a, a + 4, a, a, big, None) == -1       # misaligned shared_out
+    assert lib.moe_combine(c, a, a, a, None, a, None, big, None) == -1     # no workspace
+    # the host-buffer forward and the error read-back
+    assert lib.moe_forward_host(c, None, ctypes.byref(full), a, None, a, big, None) == -1
+    assert lib.moe_forward_host(c, a, ctypes.byref(full), a, None, a, 16, None) == -3
+    code = ctypes.c_int32(7)
+    assert lib.moe_read_device_error(None, ctypes.byref(code), None) == -1
+    assert lib.moe_read_device_error(a, None, None) == -1
+    assert code.value == 7
