@@ -214,7 +214,7 @@ def capacity(capacity_factor: float, n_tokens: int, n_experts: int):
     return int(capacity_factor * (n_tokens // n_experts))
 
 
-def dispatch(idx, n_experts: int, capacity_factor: float = 0.0):
+def dispatch(idx, n_experts: int, capacity_factor: float = 0.0, expert_capacity=None):
     """Group assignments by expert with a per-expert capacity [EXPERT In[10]].
 
     Assignments are visited in token order (and slot order within a token).
@@ -224,12 +224,22 @@ def dispatch(idx, n_experts: int, capacity_factor: float = 0.0):
     expert-sorted buffer in arrival order (a stable grouping) [DSEEK s.3;
     QWEN group tokens by expert].
 
+    ``expert_capacity`` ([E] integers), if given, replaces the one capacity
+    derived from ``capacity_factor`` by one per expert: what a shard of a
+    larger batch may still keep once the assignments of the tokens before it
+    are counted (the same token-order rule applied to the whole batch).
+
     Returns a dict with counts (selections per expert), kept, dropped,
     offsets [E+1], row_of_slot [N*k] (-1 = dropped) and token_of_row [M].
     """
     idx = np.asarray(idx, np.int64)
     n_tokens, k = idx.shape
-    cap = capacity(capacity_factor, n_tokens, n_experts)
+    if expert_capacity is not None:
+        caps = np.asarray(expert_capacity, np.int64)
+        cap = None
+    else:
+        cap = capacity(capacity_factor, n_tokens, n_experts)
+        caps = None
     counts = np.zeros(n_experts, np.int64)
     processed = np.zeros(n_experts, np.int64)
     dropped = np.zeros(n_experts, np.int64)
@@ -237,7 +247,8 @@ def dispatch(idx, n_experts: int, capacity_factor: float = 0.0):
     flat = idx.reshape(-1).tolist()
     for s, e in enumerate(flat):
         counts[e] += 1
-        if cap is None or processed[e] < cap:
+        limit = caps[e] if caps is not None else cap
+        if limit is None or processed[e] < limit:
             local[s] = processed[e]
             processed[e] += 1
         else:
@@ -249,7 +260,8 @@ def dispatch(idx, n_experts: int, capacity_factor: float = 0.0):
     token_of_row = np.full(m, -1, np.int64)
     kept_slots = np.nonzero(row_of_slot >= 0)[0]
     token_of_row[row_of_slot[kept_slots]] = kept_slots // k
-    return dict(capacity=cap, counts=counts, kept=processed, dropped=dropped,
+    return dict(capacity=caps if caps is not None else cap, counts=counts, kept=processed,
+                dropped=dropped,
                 offsets=offsets, row_of_slot=row_of_slot,
                 token_of_row=token_of_row)
 

@@ -67,6 +67,26 @@ def test_capacity_truncates_tokens_per_expert_first():
     assert d["kept"].tolist() == [3, 2] and d["dropped"].tolist() == [2, 0]
 
 
+def test_dispatch_with_per_expert_capacities():
+    """EXPERT In[10]'s token-order rule with one capacity per expert (a
+    shard's remaining room): caps (1, 2) keep the first assignment to
+    expert 0 and the first two to expert 1."""
+    idx = np.array([[0], [0], [1], [0], [1], [1]])
+    d = O.dispatch(idx, 2, expert_capacity=[1, 2])
+    assert d["kept"].tolist() == [1, 2] and d["dropped"].tolist() == [2, 1]
+    assert d["row_of_slot"].tolist() == [0, -1, 1, -1, 2, -1]
+    assert d["token_of_row"].tolist() == [0, 2, 4]
+    # zero room drops everything; the scalar rule is the broadcast case
+    assert O.dispatch(idx, 2, expert_capacity=[0, 0])["kept"].tolist() == [0, 0]
+    rng = np.random.default_rng(3)
+    for cf in (0.5, 1.0, 1.25):
+        idx = np.stack([rng.permutation(6)[:2] for _ in range(40)])
+        a = O.dispatch(idx, 6, cf)
+        b = O.dispatch(idx, 6, expert_capacity=[a["capacity"]] * 6)
+        for key in ("kept", "dropped", "offsets", "row_of_slot", "token_of_row"):
+            assert np.array_equal(a[key], b[key]), key
+
+
 def test_capacity_table_out12():
     g, counts, idx = _table_assignments()
     n_tok = int(g["num_tokens"][0][0])
