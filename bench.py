@@ -212,6 +212,23 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
+def host_description():
+    """The host the CPU baseline ran on: logical CPUs, CPU model and the
+    thread-count settings in the environment."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    env = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+           if k in os.environ}
+    return {"nproc": os.cpu_count(), "cpu_model": model, "thread_env": env}
+
+
 def kernel_launches_per_step(shape):
     """Kernels the library launches for one moe_forward of this layer."""
     router = 2          # logits GEMM, selection (+ statistic, last CTA)
@@ -438,6 +455,7 @@ def run_ours(args, shape, peaks, peaks_kind):
         n_s, el = oracle_sample(shape, inputs, target_s=args.cpu_seconds)
         res["cpu_baseline"] = {"value": round(n_s / el, 2), "unit": "tokens/s",
                                "cores": blas_threads(), "kind": "oracle",
+                               "host": host_description(),
                                "sample": f"first {n_s} tokens of the workload, one "
                                          f"forward, {el:.2f} s"}
     if ws_n > 1:
@@ -480,7 +498,7 @@ def run_reference(args, shape):
         "config": {"workload": shape.name, "n_tokens": shape.n_tokens,
                    "sample_tokens": n_s},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
-                         "kind": "oracle",
+                         "kind": "oracle", "host": host_description(),
                          "sample": f"first {n_s} tokens of the workload per step"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
