@@ -212,6 +212,27 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
+SMALL_WORKLOADS = ("toy_top2_fp32", "capacity_top2_fp32", "capacity_top2_bf16")
+
+
+def single_thread_rate(shape, inputs, n_tokens):
+    """The oracle's tokens/s on one thread (BLAS limited to one thread) for
+    the first n_tokens; reported beside the all-core figure for the small
+    workloads, where the threads have little to share."""
+    from oracle import moe_oracle as O
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        return None
+    sub = inputs.first_tokens(n_tokens)
+    with threadpool_limits(limits=1):
+        O.forward(sub.shape, sub.values)
+        t0 = time.perf_counter()
+        O.forward(sub.shape, sub.values)
+        el = time.perf_counter() - t0
+    return round(n_tokens / el, 2)
+
+
 def host_description():
     """The host the CPU baseline ran on: logical CPUs, CPU model and the
     thread-count settings in the environment."""
@@ -458,6 +479,8 @@ def run_ours(args, shape, peaks, peaks_kind):
                                "host": host_description(),
                                "sample": f"first {n_s} tokens of the workload, one "
                                          f"forward, {el:.2f} s"}
+        if shape.name in SMALL_WORKLOADS:
+            res["cpu_baseline"]["single_thread_value"] = single_thread_rate(shape, inputs, n_s)
     if ws_n > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -503,6 +526,8 @@ def run_reference(args, shape):
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    if shape.name in SMALL_WORKLOADS:
+        res["cpu_baseline"]["single_thread_value"] = single_thread_rate(shape, inputs, n_s)
     return res, rank
 
 
