@@ -16,7 +16,11 @@ dominant kernel).  `e2e` is the same metric through moe_forward_host: the
 timed region includes the copy of x from page-locked host memory and the
 copy of the output back.  The layer's working set (x, 1.2 GB of expert
 weights, the 1.3 GB of grouped intermediates) is far larger than the 126 MB
-L2, so no flush is needed between steps.
+L2, so no flush is needed between steps.  The decode workload (64 tokens)
+reads 1.2 GB of expert weights per step, of which the L2 could keep the last
+126 MB for the next step: there 512 MB are written between timed steps
+(`--flush-l2` does the same for any workload) and each step is timed between
+its own events.
 
 Several GPUs run independent replicas (the layer has no exchange step
 without a global capacity): one process per GPU under torchrun, a barrier
@@ -310,6 +314,11 @@ def run_ours(args, shape, peaks, peaks_kind):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
+    flush = None
+    if args.flush_l2 or shape.name == "decode_stream":
+        # written between the timed steps: 512 MB is four times the L2, so no
+        # weight one step reads is still cached for the next
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
@@ -319,12 +328,17 @@ def run_ours(args, shape, peaks, peaks_kind):
     h_start = time.time()
     t_start.record(stream)
     for s_ in range(args.steps):
+        if flush is not None:
+            flush.fill_(s_ & 0xFF)
         M.moe_forward_timed(cfg, x, weights, out, fstats, ws, evs[s_])
     t_end.record(stream)
     barrier()
     h_end = time.time()
     clocks = sampler.stop(region=(h_start, h_end))
     total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        # the flushes lie between the steps' own first and last events
+        total_ms = sum(evs[s_][0].elapsed_time(evs[s_][-1]) for s_ in range(args.steps))
     names = list(M.FORWARD_STAGES)
 
     def stage_times(name):
@@ -456,7 +470,9 @@ def run_ours(args, shape, peaks, peaks_kind):
                    "n_shared": shape.n_shared, "route": shape.route,
                    "capacity_factor": shape.capacity_factor,
                    "parallelism": f"replicas x{ws_n}",
-                   "l2": "working set > 126 MB L2 (no flush needed)",
+                   "l2": ("flushed between timed steps (512 MB written), steps timed "
+                          "between their own events" if flush is not None else
+                          "working set > 126 MB L2 (no flush needed)"),
                    "forward_api_ms_per_step": round(fwd_ms, 4),
                    "forward_graph_ms_per_step": (round(graph_ms, 4)
                                                  if isinstance(graph_ms, float) else graph_ms),
@@ -596,6 +612,8 @@ def main(argv=None):
                     help="DRAM bytes per launch of the up projection from an ncu capture")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (smaller cases for profiler captures)")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write 512 MB between timed steps (always on for decode_stream)")
     ap.add_argument("--backward", action="store_true",
                     help="time moe_backward instead of the forward (one GPU)")
     args = ap.parse_args(argv)
