@@ -527,6 +527,34 @@ def test_forward_is_deterministic():
     assert torch.equal(sa["balance"], sb["balance"])
 
 
+@pytest.mark.parametrize("name,N", [("deepseek_v3_block", 256), ("qwen3_moe", 4096)])
+def test_forward_captures_into_a_cuda_graph(name, N):
+    """No host synchronisation inside moe_forward (DSEEK failure modes): the
+    whole layer is captured into a CUDA graph, and each replay gives the
+    eager result bit for bit, outputs and statistics (4096 Qwen3-style
+    tokens put the expert GEMMs on CTA pairs)."""
+    inp = inputs_for(name, N)
+    D = Device(inp)
+    eager, se = _forward(D)
+    out = D.empty(inp.shape.n_tokens, inp.shape.d_model)
+    st, sts = D.stats()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            M.moe_forward(D.cfg, D.t["x"], D.weights, out, sts, D.ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+        for key in ("counts", "kept", "dropped", "balance"):
+            assert torch.equal(st[key], se[key]), key
+    assert D.device_error() == M.MOE_OK
+
+
 def test_forward_zero_tokens():
     inp = inputs_for("toy_top2_fp32", 0)
     D = Device(inp)
