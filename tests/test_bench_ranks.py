@@ -95,3 +95,35 @@ def test_clock_summary_of_a_region_between_two_samples():
     assert got["in_region"] == 0 and got["samples"] == 2
     assert got["sm_mhz"] == (2032 + 2010) / 2
     assert got["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """bench.py --impl reference (the oracle on this host) prints one JSON
+    line with the keys of the measurement contract."""
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--workload", "toy_top2_fp32", "--steps", "2",
+                "--warmup", "3", "--cpu-seconds", "0.5"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "toy_top2_fp32"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["single_thread_value"] > 0 and cb["host"]["nproc"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_bench_rejects_too_few_warmup_steps():
+    sys.path.insert(0, ROOT)
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--impl", "reference", "--warmup", "2"])
