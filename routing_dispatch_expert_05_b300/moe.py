@@ -391,3 +391,10 @@ class MoEWorkspace:
     @property
     def nbytes(self) -> int:
         return self.tensor.numel()
+
+    def reset(self) -> None:
+        """Zero the workspace again, on the current stream.  Needed only after
+        a call returned MOE_ERR_CUDA, which can leave the running selection
+        totals or the device error word set; every other call leaves the
+        workspace ready for the next."""
+        self.tensor.zero_()

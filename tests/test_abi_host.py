@@ -244,3 +244,13 @@ def test_grouping_expert_and_combine_calls_reject_bad_arguments(lib):
     assert lib.moe_read_device_error(None, ctypes.byref(code), None) == -1
     assert lib.moe_read_device_error(a, None, None) == -1
     assert code.value == 7
+
+
+def test_workspace_sizes_and_reset_on_the_host(lib):
+    cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
+    ws = M.MoEWorkspace(cfg, device="cpu")
+    assert ws.nbytes == M.workspace_size(cfg)
+    assert M.MoEWorkspace(cfg, device="cpu", forward=False).nbytes == M.scratch_size(cfg)
+    ws.tensor[:8] = 7
+    ws.reset()
+    assert int(ws.tensor.sum()) == 0
