@@ -31,12 +31,12 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _shape(n_tokens=256):
+def _shape(n_tokens=256, cf=1.25):
     from routing_dispatch_expert_05_b300 import workloads as W
     # the capacity workload's layer (SiLU-MLP with biases, skewed routing,
     # cf 1.25), smaller: capacity int(1.25 * (256 // 8)) = 40 per expert
     return W.WORKLOADS["capacity_top2_fp32"].replace(name="dp", n_tokens=n_tokens, d_model=32,
-                                                     d_ff=48)
+                                                     d_ff=48, capacity_factor=cf)
 
 
 def test_shard_room_is_what_the_batch_rule_leaves():
@@ -80,13 +80,13 @@ def _shard(n_tokens, world, rank):
     return bounds[rank], bounds[rank + 1]
 
 
-def _rank_main(rank, world, port, out):
+def _rank_main(rank, world, port, cf, out):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     from oracle import moe_oracle as O
     from routing_dispatch_expert_05_b300 import workloads as W
-    shape = _shape()
+    shape = _shape(cf=cf)
     v = W.make_inputs(shape).values
     lo, hi = _shard(shape.n_tokens, world, rank)
     xs = v["x"][lo:hi]
@@ -115,13 +115,14 @@ def _rank_main(rank, world, port, out):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3, 4])
-def test_dp_forward_with_batch_capacity_equals_the_whole_batch(world):
+@pytest.mark.parametrize("world,cf", [(2, 1.25), (3, 1.25), (4, 1.25), (2, 0.0)])
+def test_dp_forward_with_batch_capacity_equals_the_whole_batch(world, cf):
+    """cf 0: no capacity, the ranks are plain replicas and nothing drops."""
     port = _free_port()
     ctx = mp.get_context("spawn")
     with ctx.Manager() as mgr:
         out = mgr.dict()
-        procs = [ctx.Process(target=_rank_main, args=(r, world, port, out))
+        procs = [ctx.Process(target=_rank_main, args=(r, world, port, cf, out))
                  for r in range(world)]
         for p in procs:
             p.start()
@@ -131,9 +132,9 @@ def test_dp_forward_with_batch_capacity_equals_the_whole_batch(world):
         res = dict(out)
     from oracle import moe_oracle as O
     from routing_dispatch_expert_05_b300 import workloads as W
-    shape = _shape()
+    shape = _shape(cf=cf)
     ref = O.forward(shape, W.make_inputs(shape).values)
-    assert ref["dropped"].sum() > 0                       # the capacity binds
+    assert (ref["dropped"].sum() > 0) == (cf > 0)         # the capacity binds
     got = np.concatenate([np.asarray(res[r][0]) for r in range(world)])
     assert np.allclose(got, ref["out_exact"], rtol=1e-12, atol=1e-12)
     for r in range(world):
@@ -144,6 +145,8 @@ def test_dp_forward_with_batch_capacity_equals_the_whole_batch(world):
         assert stats["balance"] == pytest.approx(ref["balance"], rel=1e-12)
     # each shard on its own capacity int(cf * (n // E)) would keep another set
     # of assignments (the exchange is needed)
-    local = [O.dispatch(ref["idx"][slice(*_shard(shape.n_tokens, world, r))], shape.n_experts,
-                        shape.capacity_factor)["row_of_slot"] >= 0 for r in range(world)]
-    assert not np.array_equal(np.concatenate(local), ref["row_of_slot"] >= 0)
+    if cf > 0:
+        local = [O.dispatch(ref["idx"][slice(*_shard(shape.n_tokens, world, r))],
+                            shape.n_experts, shape.capacity_factor)["row_of_slot"] >= 0
+                 for r in range(world)]
+        assert not np.array_equal(np.concatenate(local), ref["row_of_slot"] >= 0)
