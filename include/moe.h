@@ -47,9 +47,11 @@
  *   - A status other than MOE_OK is returned before anything is enqueued
  *     when arguments are invalid (MOE_ERR_INVALID_ARG / _UNSUPPORTED /
  *     _WORKSPACE); MOE_ERR_CUDA reports a failed launch.  Problems found on
- *     the device (an expert index outside [0, E), a bounded wait that ran
- *     out) set a sticky error word at the start of the workspace instead;
- *     read it with moe_read_device_error.
+ *     the device (an expert index outside [0, E), group offsets that
+ *     decrease or overrun the grouped buffer, a bounded wait that ran out)
+ *     set a sticky error word at the start of the workspace instead; read it
+ *     with moe_read_device_error.  A GEMM given inconsistent offsets computes
+ *     nothing.
  *   - The workspace `ws` must be zero-filled once when it is allocated (its
  *     first word is the device error word; the selection totals live there
  *     too and every call leaves them zero); after that no call needs it
@@ -213,6 +215,24 @@ MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t
                                   void *x_perm, moe_stats_t *stats, void *ws,
                                   size_t ws_bytes, void *stream);
 
+/* moe_dispatch_permute with one capacity per expert: room [E] int32
+ * (device, 16-byte aligned; negative entries count as 0) replaces the
+ * capacity derived from cfg->capacity_factor, which is ignored.  The r-th
+ * assignment of expert e (in token order) is kept iff r < room[e].  This is
+ * the grouping of one contiguous shard of a larger batch whose capacity is
+ * int(cf * (N_batch // E)) over the whole batch ("Expert Networks > Code
+ * Implementation", In[10], drops in token order across the batch): with
+ * prior[e] the selections of expert e by the tokens before the shard,
+ * room[e] = clamp(capacity - prior[e], 0, capacity) keeps exactly the
+ * shard's part of the batch's kept set.  Outputs and errors as
+ * moe_dispatch_permute. */
+MOE_API moe_status_t moe_dispatch_permute_room(const moe_config_t *cfg, const int32_t *idx,
+                                  const void *x, const int32_t *room,
+                                  int32_t *offsets, int32_t *row_of_slot,
+                                  int32_t *token_of_row, void *x_perm,
+                                  moe_stats_t *stats, void *ws, size_t ws_bytes,
+                                  void *stream);
+
 /* moe_dispatch_permute for callers that cannot give the library any device
  * memory of its own: a serving engine that has already claimed the GPU's
  * memory for its own pool, or a hot loop that must not call cudaMalloc
@@ -223,8 +243,10 @@ MOE_API moe_status_t moe_dispatch_permute(const moe_config_t *cfg, const int32_t
  *     library (allocated on every GPU that loads it, kept until exit), so
  *     n_tokens is limited to 65536: larger layers get MOE_ERR_UNSUPPORTED.
  *   - The first call on each device looks up that array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *     (with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture.  Resetting the device
+ *     (cudaDeviceReset) after that first call is not supported: the kept
+ *     address would no longer be valid.
  *   - Calls share the array: calls whose GPU work may overlap (other
  *     streams, other host threads) race and must be ordered by the caller.
  *   - With no workspace there is no device error word: an expert index
@@ -402,6 +424,27 @@ MOE_API moe_status_t moe_update_selection_bias(const moe_config_t *cfg,
 MOE_API moe_status_t moe_check_wait_timeout(void *ws, size_t ws_bytes, int64_t limit_ns,
                                             void *stream);
 
+
+/* Consistency check of a grouping on the device ("DeepSeek 5.7", s.3 and
+ * Failure modes, where most implementation bugs are indexing bugs): for the
+ * selection idx [N, k] and the grouping written by moe_dispatch_permute
+ * (offsets [E+1], row_of_slot [N*k], token_of_row [N*k]; device), checks that
+ *   - offsets start at 0, never decrease, end at M <= N*k, and no group holds
+ *     more rows than the capacity;
+ *   - every idx is in [0, E) and a token's k experts are distinct;
+ *   - every kept slot s = t*k + j lies in its expert's rows,
+ *     offsets[idx[s]] <= row_of_slot[s] < offsets[idx[s]+1], with
+ *     token_of_row[row_of_slot[s]] == t, and exactly M slots are kept, so
+ *     row_of_slot is a bijection of the kept slots onto [0, M);
+ *   - rows of one group hold ascending tokens (arrival order).
+ * A failure sets MOE_ERR_DEVICE_CHECK in the device error word of ws (read
+ * it with moe_read_device_error); nothing else is written.  ws: scratch of
+ * moe_scratch_size bytes (two words of its first 256 bytes are used and left
+ * zero).  A debugging aid, not part of moe_forward. */
+MOE_API moe_status_t moe_check_grouping(const moe_config_t *cfg, const int32_t *idx,
+                                        const int32_t *offsets, const int32_t *row_of_slot,
+                                        const int32_t *token_of_row, void *ws,
+                                        size_t ws_bytes, void *stream);
 
 /* Waits for `stream`, then reads and clears the device error word at the
  * start of `ws`: *code = MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT. */

@@ -283,11 +283,11 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                    int32_t* offsets, int32_t* ros, int32_t* tor, void* x_perm,
                    moe_stats_t* stats, const Scratch& sc, cudaStream_t st,
-                   int32_t* slot_of_row = nullptr) {
+                   int32_t* slot_of_row = nullptr, const int32_t* room = nullptr) {
   launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c), sc.chunk_cnt,
                   sc.chunk_base, offsets, ros, tor, stats ? stats->counts : nullptr,
                   stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st,
-                  slot_of_row);
+                  slot_of_row, room);
   if (x_perm != nullptr)
     launch_scatter_rows(x, (int64_t)c.d_model * elem_size(c), ros, c.n_tokens, c.top_k,
                         x_perm, num_sms(), st);
@@ -299,12 +299,22 @@ bool pairs_pay(const moe_config_t& c) {
   return (double)c.n_tokens * c.top_k / c.n_experts >= 128.0;
 }
 
+// Experts of a few rows each (a decode-shaped layer): the swapped-operand
+// kernel, whose tiles are 128 weight rows by the expert's token rows rounded
+// up to 16, instead of 128- or 256-row token tiles that would be almost all
+// padding.
+bool swap_pays(const moe_config_t& c) {
+  return (double)c.n_tokens * c.top_k / c.n_experts <= 16.0;
+}
+
 // bf16 expert GEMMs run on the tensor cores; fp32 ones on the CUDA cores
 moe_status_t run_gemm(const moe_config_t& c, const TcProblem& tq, const GemmProblem& sq,
                       cudaStream_t st) {
   if (c.dtype == MOE_BF16 && tc_gemm_supported(tq))
     return launch_tc_gemm(tq, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
-  launch_simt_gemm(sq, st);
+  GemmProblem p = sq;
+  p.err = tq.err;
+  launch_simt_gemm(p, st);
   return MOE_OK;
 }
 
@@ -355,6 +365,8 @@ moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_ma
   q.C = h;
   q.err = err;
   q.use_pairs = pairs_pay(c);
+  if (c.dtype == MOE_BF16 && row_map == nullptr && swap_pays(c) && swap_gemm_supported(q))
+    return launch_swap_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
   return run_gemm(c, q, p, st);
 }
 
@@ -409,7 +421,10 @@ moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offs
     q.e8_cols = (int)ceil_div64(c.d_model, kYScaleBlock);
     q.c_row_map = slot_of_row;
     q.c_row_scale = wts;
-    if (c.dtype != MOE_BF16 || !tc_gemm_supported(q)) return MOE_ERR_UNSUPPORTED;
+    if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (swap_pays(c) && swap_gemm_supported(q))
+      return launch_swap_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+    if (!tc_gemm_supported(q)) return MOE_ERR_UNSUPPORTED;
     return launch_tc_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
   }
   return run_gemm(c, q, p, st);
@@ -562,6 +577,31 @@ moe_status_t moe_dispatch_permute(const moe_config_t* cfg, const int32_t* idx,
   MOE_TRY(maybe({x, x_perm}));
   dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats,
                 scratch_of(layout_of(c), ws), st);
+  return last_cuda();
+}
+
+moe_status_t moe_dispatch_permute_room(const moe_config_t* cfg, const int32_t* idx,
+                                       const void* x, const int32_t* room,
+                                       int32_t* offsets, int32_t* row_of_slot,
+                                       int32_t* token_of_row, void* x_perm,
+                                       moe_stats_t* stats, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_stats(stats));
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  MOE_TRY(need({offsets, room}));
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.n_tokens == 0) {
+    cudaMemsetAsync(offsets, 0, (size_t)(c.n_experts + 1) * 4, st);
+    MOE_TRY(last_cuda());
+    return zero_stats(c, stats, st);
+  }
+  MOE_TRY(need({idx, row_of_slot, token_of_row}));
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(maybe({x, x_perm}));
+  dispatch_body(c, idx, x, offsets, row_of_slot, token_of_row, x_perm, stats,
+                scratch_of(layout_of(c), ws), st, nullptr, room);
   return last_cuda();
 }
 
@@ -722,9 +762,10 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
   if (c.n_shared > 0)
     MOE_TRY(shared_body(c, x, w, at<char>(ws, L.h_shared), shared_out, sc.err, st));
   mark(5);
+  // without a capacity nothing is dropped: the combine need not read row_of_slot
   if (compact)
-    launch_combine_slots(y, y_e8, ros, shared_out, out, c.n_tokens, c.top_k, c.d_model,
-                         c.dtype == MOE_BF16, num_sms(), st);
+    launch_combine_slots(y, y_e8, capacity_of(c) < 0 ? nullptr : ros, shared_out, out,
+                         c.n_tokens, c.top_k, c.d_model, c.dtype == MOE_BF16, num_sms(), st);
   else
     launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
                    c.dtype == MOE_BF16, num_sms(), st);
@@ -1154,6 +1195,25 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (grads->d_b_router != nullptr && weights->b_router == nullptr) return MOE_ERR_INVALID_ARG;
   return backward_impl(c, x, *weights, dout, d_balance, *grads, ws,
                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_check_grouping(const moe_config_t* cfg, const int32_t* idx,
+                               const int32_t* offsets, const int32_t* row_of_slot,
+                               const int32_t* token_of_row, void* ws, size_t ws_bytes,
+                               void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_ws(ws, ws_bytes, layout_of(c).scratch_end));
+  MOE_TRY(need({offsets}));
+  if (c.n_tokens == 0) return MOE_OK;
+  MOE_TRY(need({idx, row_of_slot, token_of_row}));
+  // two words of the workspace's first (zero-filled) block: the kept-slot
+  // count and the last-CTA ticket, both left zero
+  unsigned* words = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 192);
+  launch_check_grouping(idx, offsets, row_of_slot, token_of_row, c.n_tokens, c.top_k,
+                        c.n_experts, capacity_of(c), words, words + 1, err_word(ws), num_sms(),
+                        static_cast<cudaStream_t>(stream));
+  return last_cuda();
 }
 
 moe_status_t moe_check_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns,

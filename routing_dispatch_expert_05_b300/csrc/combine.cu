@@ -114,6 +114,8 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_s
 // slot j, so of the weighted sum ("DeepSeek 5.7", s.3) only the sum is left
 // here.  out[t] = sum over kept slots j of those rows, in slot order, + S[t].  A token's k rows are contiguous, so the kernel streams
 // them; their addresses need no index load.
+// row_of_slot == null: the layer has no capacity, every slot is kept (its
+// rows are then read without waiting for an index load).
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 4)
 combine_slots_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
@@ -144,8 +146,9 @@ combine_slots_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y
           keep[q] = false;
           sc[q] = 0.f;
           val[q] = make_uint4(0u, 0u, 0u, 0u);
-          if (j < top_k) {
-            keep[q] = row_of_slot[slot] >= 0;       // dropped slots hold no row
+          // dropped slots hold no row: nothing of theirs is read
+          if (j < top_k && (row_of_slot == nullptr || row_of_slot[slot] >= 0)) {
+            keep[q] = true;
             val[q] = __ldcs(reinterpret_cast<const uint4*>(y + slot * d_model + col));
             sc[q] = __uint_as_float((uint32_t)y_e8[slot * e8_cols + blk] << 23);
           }

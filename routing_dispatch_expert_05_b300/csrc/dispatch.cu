@@ -19,8 +19,9 @@
 //              inside a 32-slot step come from __match_any_sync (lanes with
 //              the same expert) and a running per-(warp, expert) counter;
 //              warp bases are an exclusive scan over the chunk's warps.
-// A fourth kernel copies x rows into x_perm (32- or 16-byte vectors), either
-// row by row of x_perm (gather) or token by token of x (scatter).
+// A fourth kernel copies x rows into x_perm (32- or 16-byte vectors), token
+// by token of x: each token row is read once and written to its k rows (a
+// copy row by row of x_perm read each token row k times and was slower).
 #include <algorithm>
 
 #include "common.cuh"
@@ -56,9 +57,11 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top
     chunk_cnt[(int64_t)blockIdx.x * n_experts + e] = s_cnt[e];
 }
 
+// The capacity of expert e is `capacity` (< 0: none), or room[e] when a
+// per-expert room is given (what a shard of a larger batch may still keep).
 __global__ void __launch_bounds__(kMaxExperts)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
-                     int n_experts, int64_t capacity,
+                     int n_experts, int64_t capacity, const int32_t* __restrict__ room,
                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                      int32_t* __restrict__ dropped) {
@@ -74,7 +77,8 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
       chunk_base[o] = run;
       run += v;
     }
-    const int kp = capacity < 0 ? run : (int)min((int64_t)run, capacity);
+    const int64_t cap = room != nullptr ? (int64_t)max(room[e], 0) : capacity;
+    const int kp = cap < 0 ? run : (int)min((int64_t)run, cap);
     s_kept[e] = kp;
     if (counts) counts[e] = run;
     if (kept) kept[e] = kp;
@@ -91,9 +95,12 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
   }
 }
 
+// An assignment of rank r (arrival index among expert e's) is kept iff
+// r < kept_e = offsets[e+1] - offsets[e]: kept_e = min(total_e, capacity_e)
+// and r < total_e, so this is r < capacity_e, whichever capacity applied.
 __global__ void __launch_bounds__(kRankWarps * 32)
 dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
-                     int n_experts, int64_t capacity,
+                     int n_experts,
                      const int32_t* __restrict__ chunk_base,
                      const int32_t* __restrict__ offsets,
                      int32_t* __restrict__ row_of_slot,
@@ -149,7 +156,7 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
     __syncwarp();
     if (s < ws1) {
       int32_t row = -1;
-      if (e >= 0 && (capacity < 0 || rank < capacity)) {
+      if (e >= 0 && offsets[e] + rank < offsets[e + 1]) {
         row = offsets[e] + rank;
         token_of_row[row] = (int32_t)(s / top_k);
         if (slot_of_row != nullptr) slot_of_row[row] = (int32_t)s;
@@ -159,62 +166,7 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
   }
 }
 
-// x_perm[r] = x[token_of_row[r]] for r < offsets[E]; one warp per row,
-// 32-byte (or 16-byte) vectors, up to 4 in flight per lane.
-__global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
-                   const int32_t* __restrict__ token_of_row,
-                   const int32_t* __restrict__ offsets, int n_experts,
-                   uint8_t* __restrict__ x_perm, bool wide) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int64_t rows = offsets[n_experts];
-  const int lane = threadIdx.x & 31;
-  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t nvec = row_bytes >> 4;
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       r < rows; r += warps_total) {
-    const int64_t t = token_of_row[r];
-    const uint8_t* src = x + t * row_bytes;
-    uint8_t* dst = x_perm + r * row_bytes;
-    int64_t v = lane;
-    if (wide) {
-      // 32-byte pieces (256-bit loads and stores), four in flight per lane
-      const int64_t n32 = row_bytes >> 5;
-      int64_t u = lane;
-      for (; u + 96 < n32; u += 128) {
-        Vec32 a, b, c, d;
-        ld_vec32_nc(src + (u << 5), a);
-        ld_vec32_nc(src + ((u + 32) << 5), b);
-        ld_vec32_nc(src + ((u + 64) << 5), c);
-        ld_vec32_nc(src + ((u + 96) << 5), d);
-        st_vec32(dst + (u << 5), a);
-        st_vec32(dst + ((u + 32) << 5), b);
-        st_vec32(dst + ((u + 64) << 5), c);
-        st_vec32(dst + ((u + 96) << 5), d);
-      }
-      for (; u < n32; u += 32) {
-        Vec32 a;
-        ld_vec32_nc(src + (u << 5), a);
-        st_vec32(dst + (u << 5), a);
-      }
-      continue;
-    }
-    for (; v + 96 < nvec; v += 128) {
-      const uint4 a = ld_vec16_nc(src + (v << 4));
-      const uint4 b = ld_vec16_nc(src + ((v + 32) << 4));
-      const uint4 c = ld_vec16_nc(src + ((v + 64) << 4));
-      const uint4 d = ld_vec16_nc(src + ((v + 96) << 4));
-      st_vec16(dst + (v << 4), a);
-      st_vec16(dst + ((v + 32) << 4), b);
-      st_vec16(dst + ((v + 64) << 4), c);
-      st_vec16(dst + ((v + 96) << 4), d);
-    }
-    for (; v < nvec; v += 32) st_vec16(dst + (v << 4), ld_vec16_nc(src + (v << 4)));
-  }
-}
-
-// The same copy driven from the token side: x_perm[row_of_slot[t*k + j]] =
+// The row copy, driven from the token side: x_perm[row_of_slot[t*k + j]] =
 // x[t] for every kept slot.  One warp per token reads its row once (1 KB or
 // 4 KB per pass, 32-byte or 16-byte vectors) and writes it to each of its
 // rows, so x is read from memory once instead of once per assignment.
@@ -268,6 +220,82 @@ scatter_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
   }
 }
 
+// Consistency of a grouping ("DeepSeek 5.7", s.3 and Failure modes: most
+// implementation bugs are indexing bugs).  One thread per slot s = t*k + j,
+// with e = idx[s] and r = row_of_slot[s]:
+//   * e in [0, E), and e differs from the token's earlier slots;
+//   * r == -1 (dropped), or offsets[e] <= r < offsets[e+1] with
+//     token_of_row[r] == t;
+// one thread per row r < M = offsets[E]: token_of_row ascending within each
+// group (arrival order); block 0 checks offsets (start 0, never decreasing,
+// M <= N*k, no group above the capacity).  The kept slots are counted; the
+// last CTA (ticket) checks that they number M.  Kept slots map injectively
+// (two slots on one row would share both token and expert, which the
+// distinct-experts check excludes), so with M of them row_of_slot is a
+// bijection of the kept slots onto [0, M).  Any failure sets kDevBadRow.
+__global__ void __launch_bounds__(256)
+check_grouping_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+                      const int32_t* __restrict__ row_of_slot,
+                      const int32_t* __restrict__ token_of_row, int64_t n_tokens, int top_k,
+                      int n_experts, int64_t capacity, unsigned* __restrict__ kept_count,
+                      unsigned* __restrict__ ticket, int32_t* __restrict__ err) {
+  const int64_t n_slots = n_tokens * top_k;
+  const int64_t m = offsets[n_experts];
+  bool bad = false;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bad |= offsets[0] != 0 || m > n_slots;
+    for (int e = 0; e < n_experts; ++e) {
+      const int g = offsets[e + 1] - offsets[e];
+      bad |= g < 0 || (capacity >= 0 && g > capacity);
+    }
+  }
+  const bool m_ok = m >= 0 && m <= n_slots;
+  unsigned kept = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_slots; s += stride) {
+    const int64_t t = s / top_k;
+    const int e = idx[s];
+    if (e < 0 || e >= n_experts) { bad = true; continue; }
+    for (int64_t q = t * top_k; q < s; ++q) bad |= idx[q] == e;
+    const int r = row_of_slot[s];
+    if (r == -1) continue;
+    // (the row is compared with M first: token_of_row is read only inside it)
+    if (!m_ok || r < 0 || r >= m || r < offsets[e] || r >= offsets[e + 1] ||
+        token_of_row[r] != (int32_t)t) {
+      bad = true;
+      continue;
+    }
+    ++kept;
+  }
+  if (m_ok) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r + 1 < m; r += stride) {
+      // rows r and r+1 of one group hold strictly ascending tokens
+      const int32_t a = token_of_row[r], b = token_of_row[r + 1];
+      bad |= a < 0 || a >= n_tokens;
+      int lo = 0, hi = n_experts - 1;              // the group of row r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      if (r + 1 < offsets[lo + 1]) bad |= b <= a;
+    }
+  }
+  if (bad) set_device_error(err, kDevBadRow);
+  // kept slots: a warp sum, one atomic per warp
+  for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(kFull, kept, o);
+  if ((threadIdx.x & 31) == 0 && kept != 0) atomicAdd(kept_count, kept);
+  __threadfence();
+  __syncthreads();
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  const unsigned total = atomicExch(kept_count, 0u);
+  if (!m_ok || total != (unsigned)m) set_device_error(err, kDevBadRow);
+  *ticket = 0u;
+}
+
 }  // namespace
 
 void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,
@@ -288,33 +316,29 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* chunk_base, int32_t* offsets, int32_t* row_of_slot,
                      int32_t* token_of_row, int32_t* counts, int32_t* kept,
                      int32_t* dropped, int32_t* err, cudaStream_t st,
-                     int32_t* slot_of_row) {
+                     int32_t* slot_of_row, const int32_t* room) {
   const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
   if (chunks > 0)
     launch_pdl(dispatch_count_kernel, dim3(chunks), dim3(256), 0, st, idx, n_tokens, top_k,
                n_experts, chunk_cnt, err);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, chunk_cnt, chunks, n_experts,
-                                                  capacity, chunk_base, offsets,
-                                                  counts, kept, dropped);
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, chunk_cnt, chunks,
+             n_experts, capacity, room, chunk_base, offsets, counts, kept, dropped);
   if (chunks > 0)
-    launch_pdl(dispatch_rank_kernel, dim3(chunks), dim3(kRankWarps * 32), 0, st, 
-        idx, n_tokens, top_k, n_experts, capacity, chunk_base, offsets,
-        row_of_slot, token_of_row, slot_of_row);
+    launch_pdl(dispatch_rank_kernel, dim3(chunks), dim3(kRankWarps * 32), 0, st, idx, n_tokens,
+               top_k, n_experts, chunk_base, offsets, row_of_slot, token_of_row, slot_of_row);
 }
 
-void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
-                        const int32_t* offsets, int n_experts, int64_t max_rows,
-                        void* x_perm, int num_sms, cudaStream_t st) {
-  if (max_rows <= 0) return;
-  const int64_t blocks_needed = ceil_div64(max_rows, 8);
+void launch_check_grouping(const int32_t* idx, const int32_t* offsets,
+                           const int32_t* row_of_slot, const int32_t* token_of_row,
+                           int64_t n_tokens, int top_k, int n_experts, int64_t capacity,
+                           unsigned* kept_count, unsigned* ticket, int32_t* err, int num_sms,
+                           cudaStream_t st) {
+  if (n_tokens <= 0) return;
+  const int64_t blocks_needed = ceil_div64(n_tokens * top_k, 256);
   const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)num_sms * 8);
-  // rows of whole 32-byte pieces at 32-byte aligned bases move as 256-bit
-  // accesses (measured ~9% faster than 16-byte ones on 4 KB rows)
-  const bool wide = row_bytes % 32 == 0 && (reinterpret_cast<uintptr_t>(x) & 31u) == 0 &&
-                    (reinterpret_cast<uintptr_t>(x_perm) & 31u) == 0;
-  gather_rows_kernel<<<blocks, 256, 0, st>>>(
-      static_cast<const uint8_t*>(x), row_bytes, token_of_row, offsets, n_experts,
-      static_cast<uint8_t*>(x_perm), wide);
+  check_grouping_kernel<<<blocks, 256, 0, st>>>(idx, offsets, row_of_slot, token_of_row,
+                                                n_tokens, top_k, n_experts, capacity,
+                                                kept_count, ticket, err);
 }
 
 }  // namespace moe

@@ -43,11 +43,18 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmProblem p) {
   } else {
     const int G = p.n_groups;
     if (tid < 32) {
+      // the grouping must start at 0, never decrease and end within the
+      // buffer's rows; otherwise flag it and run no tile
       int carry = 0;
+      bool bad = false;
       for (int base = 0; base < G; base += 32) {
         const int gg = base + tid;
         int tiles = 0;
-        if (gg < G) tiles = (p.offsets[gg + 1] - p.offsets[gg] + BM - 1) / BM;
+        if (gg < G) {
+          const int m = p.offsets[gg + 1] - p.offsets[gg];
+          bad |= m < 0 || (gg == 0 && p.offsets[0] != 0);
+          tiles = m > 0 ? (m + BM - 1) / BM : 0;
+        }
         int incl = tiles;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -57,7 +64,11 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmProblem p) {
         if (gg < G) s_tile_start[gg] = carry + incl - tiles;
         carry += __shfl_sync(kFull, incl, 31);
       }
-      if (tid == 0) s_tile_start[G] = carry;
+      bad = __any_sync(kFull, bad) || p.offsets[G] > p.rows;
+      if (tid == 0) {
+        s_tile_start[G] = bad ? 0 : carry;
+        if (bad && blockIdx.x == 0 && blockIdx.y == 0) set_device_error(p.err, kDevBadRow);
+      }
     }
     __syncthreads();
     const int vt = blockIdx.x;

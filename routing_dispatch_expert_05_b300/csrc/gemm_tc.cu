@@ -29,20 +29,18 @@
 // Every wait on an mbarrier is bounded in time: on expiry the CTA records
 // kDevTimeout in the error word, the other roles leave their loops, in-flight
 // copies and MMAs are waited for (again bounded) and TMEM is freed.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 
 #include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
+constexpr int BM = 128, BN = 256, kStages = 4;
 // warp 0 TMA producer, warp 1 MMA issuer, warps 2.. epilogue: two epilogue
 // warps per TMEM lane quadrant (warp w may read lanes 32*(w%4)..), each
 // taking half of the tile's output columns
@@ -52,7 +50,6 @@ constexpr uint32_t kTileA = BM * BK * 2;            // 16 KB
 constexpr uint32_t kTileB = BN * BK * 2;            // 32 KB
 constexpr uint32_t kStageBytes = kTileA + kTileB;   // 48 KB
 constexpr uint32_t kTmemCols = 2 * BN;              // two accumulators
-constexpr uint64_t kTimeoutNs = 2000000000ull;      // 2 s
 constexpr int kBarBytes = 1024;
 // per-group tile starts and row offsets, padded so what follows stays
 // 128-byte aligned
@@ -74,6 +71,20 @@ static_assert(kStgWarpBytes % 16 == 0 && (kStgF32Stride * 4) % 16 == 0 &&
               "staged rows must keep 16-byte alignment and hold 64 bytes");
 static_assert(kEpiWarps == 8, "two epilogue warps per TMEM lane quadrant");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// Ring geometry of the single-CTA kernel.  The wide form holds a 256-row B
+// tile per stage (4 stages of 48 KB); the narrow form, for one n-tile of at
+// most 128 columns without SwiGLU (the router GEMM: N = E), holds a 128-row
+// B tile (6 stages of 32 KB): 50% more bytes of A in flight for a GEMM whose
+// time is the streaming of A from memory.
+template <bool NARROW> struct Ring {
+  static constexpr int kStages = NARROW ? 6 : 4;
+  static constexpr uint32_t kTileB = NARROW ? 128 * BK * 2 : BN * BK * 2;
+  static constexpr uint32_t kStageBytes = kTileA + kTileB;
+  static constexpr int kSmem = kStages * kStageBytes + kBarBytes + kTableBytes +
+                               kEpiWarps * kStgWarpBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  static_assert((kStages * kStageBytes + kBarBytes + kTableBytes) % 16 == 0, "staging alignment");
+};
 
 struct Params {
   const int32_t* offsets;     // [G+1] device or null (one group of `rows`)
@@ -108,150 +119,6 @@ struct Params {
   const int32_t* k_offsets;
   int wg_rows;
 };
-
-// ---------------------------------------------------------------- PTX
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase of `bar` with parity `parity` to complete, giving up
-// when another role aborted or after kTimeoutNs (then abort everyone).
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag, int32_t* err,
-                                             uint64_t limit_ns = kTimeoutNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort_flag = 1;
-        set_device_error(err, kDevTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
-                                            uint64_t* bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
-        "r"(c0), "r"(c1)
-      : "memory");
-}
-// Four rows r0..r3 (each one box of BK columns starting at column c0) into
-// consecutive 128-byte rows of shared memory; the map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
-        "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-               ::"r"(taddr), "r"(ncols) : "memory");
-}
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row core-matrix groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= (uint64_t)1 << 16;                             // leading byte offset (unused)
-  d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset
-  d |= (uint64_t)1 << 46;                             // descriptor version
-  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
-  return d;
-}
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                     uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-      ::"r"(smem_u32(bar)) : "memory");
-}
-#define MOE_TMEM_LD32(taddr, r)                                                     \
-  asm volatile(                                                                     \
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                     \
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"                     \
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"    \
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),     \
-        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),   \
-        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),            \
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),            \
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),            \
-        "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
-      : "r"(taddr))
-// tcgen05.wait::ld, with the 32 destination registers of an outstanding load as
-// in/out operands: no use of them can be scheduled before the wait.
-#define MOE_TMEM_WAIT32(r)                                                          \
-  asm volatile("tcgen05.wait::ld.sync.aligned;"                                     \
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]),        \
-                 "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]),        \
-                 "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),   \
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),   \
-                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),   \
-                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),   \
-                 "+r"(r[30]), "+r"(r[31])                                           \
-               :                                                                    \
-               : "memory")
 
 // ---------------------------------------------------------------- tiles
 struct Tile {
@@ -457,10 +324,11 @@ __device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int
 
 // Plain output of one tile (bf16, or fp32 if c_is_f32): SwiGLU / SiLU+bias /
 // identity epilogue.  The warp takes half `half` of the tile's output columns.
+template <bool WITH_SWIGLU = true>
 __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int lane, int half,
                                            int row_base, uint32_t tb, float* stg_f,
                                            uint32_t* stg_w) {
-  if (p.swiglu) {
+  if (WITH_SWIGLU && p.swiglu) {
     // 128 output columns per tile: gate in accumulator columns 0..127, up in
     // 128..255; two chunks per half
     constexpr int kCh = BN / 2 / 32 / 2;
@@ -539,15 +407,60 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int 
   }
 }
 
+// The tile table of a grouped problem, built by one warp: s_off[g] = first
+// row of group g (s_off[G] = rows in all), s_tile_start[g] = first tile of
+// group g (s_tile_start[G] = tiles in all), nt n-tiles per bm-row m-tile.
+// The grouping is checked on the way ("DeepSeek 5.7", Failure modes: most
+// bugs are indexing bugs): offsets must start at 0, never decrease and end
+// within the rows the buffers hold (p.rows).  A grouping that breaks this
+// sets kDevBadRow in the error word and gets no tiles, so nothing is read or
+// written through it.
+__device__ __forceinline__ void build_tile_table(const Params& p, int G, int nt, int bm, int lane,
+                                                 int* s_tile_start, int* s_off) {
+  int carry = 0;
+  bool bad = false;
+  for (int base = 0; base < G; base += 32) {
+    const int gg = base + lane;
+    int m = 0;
+    if (gg < G) {
+      const int o0 = p.offsets ? p.offsets[gg] : 0;
+      const int o1 = p.offsets ? p.offsets[gg + 1] : p.rows;
+      s_off[gg] = o0;
+      m = o1 - o0;
+      bad |= m < 0 || (gg == 0 && o0 != 0);
+    }
+    const int tiles = m > 0 ? (m + bm - 1) / bm * nt : 0;
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (gg < G) s_tile_start[gg] = carry + incl - tiles;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const int m_total = p.offsets ? p.offsets[G] : p.rows;
+  bad = __any_sync(0xffffffffu, bad) || m_total > p.rows;
+  if (lane == 0) {
+    s_tile_start[G] = bad ? 0 : carry;
+    s_off[G] = m_total;
+    if (bad) set_device_error(p.err, kDevBadRow);
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 // Epilogue kinds, one kernel instantiation each.
 enum : int { kEkStore = 0, kEkCompact = 1 };
 
-template <int EK>
+template <int EK, bool NARROW>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ Params p) {
+  using R = Ring<NARROW>;
+  constexpr int kStages = R::kStages;
+  constexpr uint32_t kTileB = R::kTileB;
+  constexpr uint32_t kStageBytes = R::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -590,32 +503,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
   pdl_wait();                 // the grouping (offsets) and A come from predecessors
   pdl_launch_dependents();
-  if (warp == 2) {
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int gg = base + lane;
-      int m = 0;
-      if (gg < G) {
-        const int o0 = p.offsets ? p.offsets[gg] : 0;
-        const int o1 = p.offsets ? p.offsets[gg + 1] : p.rows;
-        s_off[gg] = o0;
-        m = o1 - o0;
-      }
-      const int tiles = (m + BM - 1) / BM * nt;
-      int incl = tiles;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (gg < G) s_tile_start[gg] = carry + incl - tiles;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s_tile_start[G] = carry;
-      s_off[G] = p.offsets ? p.offsets[G] : p.rows;
-    }
-  }
+  if (warp == 2) build_tile_table(p, G, nt, BM, lane, s_tile_start, s_off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -655,7 +543,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_expect_tx(&full[stage], kTileA + (uint32_t)p.mma_n * BK * 2);
             uint8_t* b = sB + stage * kTileB;
             if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
-            if (p.swiglu) {
+            if (!NARROW && p.swiglu) {
               const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
               tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
               tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
@@ -750,7 +638,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if constexpr (EK == kEkCompact) {
         compact_tile(p, tl, lane, half, row_base, tb, stg_w);
       } else {
-        store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
+        store_tile<!NARROW>(p, tl, lane, half, row_base, tb, stg_f, stg_w);
       }
       tc_fence_before();
       __syncwarp();
@@ -1072,32 +960,7 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) tmem_alloc_pair(s_tmem, kTmemCols);
   pdl_wait();
   pdl_launch_dependents();
-  if (warp == 2) {
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int gg = base + lane;
-      int m = 0;
-      if (gg < G) {
-        const int o0 = p.offsets ? p.offsets[gg] : 0;
-        const int o1 = p.offsets ? p.offsets[gg + 1] : p.rows;
-        s_off[gg] = o0;
-        m = o1 - o0;
-      }
-      const int tiles = (m + BM2 - 1) / BM2 * nt;
-      int incl = tiles;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (gg < G) s_tile_start[gg] = carry + incl - tiles;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s_tile_start[G] = carry;
-      s_off[G] = p.offsets ? p.offsets[G] : p.rows;
-    }
-  }
+  if (warp == 2) build_tile_table(p, G, nt, BM2, lane, s_tile_start, s_off);
   tc_fence_before();
   __syncthreads();
   cluster_sync();                                  // both CTAs' barriers exist
@@ -1281,35 +1144,6 @@ wait_check_kernel(int32_t* err, uint64_t limit_ns, int32_t* flags) {
   }
 }
 
-// ---------------------------------------------------------------- host
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                         cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }();
-  return fn;
-}
-
-// 2-D bf16 map: `inner` contiguous elements per row, `outer` rows
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint64_t row_bytes, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace tc
 
 bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
@@ -1446,11 +1280,16 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
     cudaGetLastError();   // clear, then run on single CTAs
   }
   if (!maps(false, &ma, &mb0, &mb1)) return false;
-  auto kern = q.c_e8 != nullptr ? tc_gemm_kernel<kEkCompact> : tc_gemm_kernel<kEkStore>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+  // one n-tile of at most 128 columns (the router GEMM): the narrow ring
+  const bool narrow = !q.swiglu && p.mma_n <= 128;
+  auto kern = q.c_e8 != nullptr
+                  ? (narrow ? tc_gemm_kernel<kEkCompact, true> : tc_gemm_kernel<kEkCompact, false>)
+                  : (narrow ? tc_gemm_kernel<kEkStore, true> : tc_gemm_kernel<kEkStore, false>);
+  const int smem = narrow ? Ring<true>::kSmem : Ring<false>::kSmem;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return false;
-  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), kSmemBytes, st, ma, mb0, mb1, p) ==
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, st, ma, mb0, mb1, p) ==
          cudaSuccess;
 }
 

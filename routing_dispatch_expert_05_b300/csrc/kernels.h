@@ -48,21 +48,29 @@ void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float
                         float* load_cv, cudaStream_t st);
 
 // ---- dispatch -------------------------------------------------------------
+// capacity: one for every expert (< 0: none); room (device [E], nullable):
+// a capacity per expert instead
 void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int n_experts, int64_t capacity /* <0: none */,
                      int32_t* chunk_cnt, int32_t* chunk_base, int32_t* offsets,
                      int32_t* row_of_slot, int32_t* token_of_row,
                      int32_t* counts, int32_t* kept, int32_t* dropped,
-                     int32_t* err, cudaStream_t st, int32_t* slot_of_row = nullptr);
-// x_perm[r] = x[token_of_row[r]] for r < offsets[E] (16-byte vectors on the
-// load/store units; a TMA bulk-copy version measured 1.5x slower)
-void launch_gather_rows(const void* x, int64_t row_bytes, const int32_t* token_of_row,
-                        const int32_t* offsets, int n_experts, int64_t max_rows,
-                        void* x_perm, int num_sms, cudaStream_t st);
-
+                     int32_t* err, cudaStream_t st, int32_t* slot_of_row = nullptr,
+                     const int32_t* room = nullptr);
+// x_perm[row_of_slot[t*k + j]] = x[t] for every kept slot (one warp per token,
+// 32- or 16-byte vectors; a TMA bulk-copy version measured slower)
 void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,
                          int64_t n_tokens, int top_k, void* x_perm, int num_sms,
                          cudaStream_t st);
+// Device-side consistency check of a grouping (offsets monotone and within
+// the buffer, row_of_slot a bijection of the kept slots onto [0, M) that
+// agrees with idx and token_of_row, groups in arrival order); a failure sets
+// kDevBadRow.  kept_count and ticket: two zeroed words, left zero.
+void launch_check_grouping(const int32_t* idx, const int32_t* offsets,
+                           const int32_t* row_of_slot, const int32_t* token_of_row,
+                           int64_t n_tokens, int top_k, int n_experts, int64_t capacity,
+                           unsigned* kept_count, unsigned* ticket, int32_t* err, int num_sms,
+                           cudaStream_t st);
 
 // ---- SIMT GEMM (fp32 and bf16 storage, fp32 accumulation) ----------------
 enum Epilogue : int {
@@ -95,6 +103,7 @@ struct GemmProblem {
   // Optional row map (fused dispatch gather): row r of the grouped problem
   // reads row a_row_map[r] of A.  null: A is in grouped row order.
   const int32_t* a_row_map;
+  int32_t* err;              // device error word (nullable): a bad grouping
 };
 void launch_simt_gemm(const GemmProblem& p, cudaStream_t st);
 // router logits [N, E] fp32 for a few tokens (CUDA cores, one thread per
@@ -147,6 +156,13 @@ struct TcProblem {
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
+// The same grouped problem with the operands swapped (gemm_swap.cu), for
+// experts of a few rows each: weight rows on the MMA's M side, each expert's
+// token rows (A, up to 64 per tile) on N.  Supports the SwiGLU and SiLU+bias
+// up projections (bf16 C) and the compact down projection (c_e8 set, with
+// c_row_map / c_row_scale); n_out a multiple of 16 (32 when compact).
+bool swap_gemm_supported(const TcProblem& p);
+bool launch_swap_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
 
 // Weight gradients on the tensor cores: for each group g,
 //   C[g*rows_a + i, j] = sum_{c in [k_offsets[g], k_offsets[g+1])} A[i, c] B[j, c]
@@ -174,7 +190,8 @@ void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
                     int d_model, int is_bf16, int num_sms, cudaStream_t st);
 // the same with compact expert outputs: y16 [N*k, d] fp16 and
 // y_e8 [N*k, ceil(d/32)] (value = y16 * 2^(y_e8 - 127) for its 32 columns)
-// compact expert outputs already weighted and in slot order (row t*k + j)
+// compact expert outputs already weighted and in slot order (row t*k + j);
+// row_of_slot null: no slot was dropped (a layer without capacity)
 void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
                           const float* shared, void* out, int64_t n_tokens, int top_k,
                           int d_model, int is_bf16, int num_sms, cudaStream_t st);

@@ -109,11 +109,13 @@ extern "C" moe_status_t moe_dispatch_permute_noalloc(const moe_config_t* cfg,
                   stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr,
                   /*err=*/nullptr, st);
   if (x_perm != nullptr) {
+    // the row copy from the token side, as moe_dispatch_permute makes it:
+    // each token row is read once and written to each of its kept rows
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    launch_gather_rows(x, (int64_t)c.d_model * (c.dtype == MOE_BF16 ? 2 : 4), token_of_row,
-                       offsets, c.n_experts, c.n_tokens * c.top_k, x_perm, sms, st);
+    launch_scatter_rows(x, (int64_t)c.d_model * (c.dtype == MOE_BF16 ? 2 : 4), row_of_slot,
+                        c.n_tokens, c.top_k, x_perm, sms, st);
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

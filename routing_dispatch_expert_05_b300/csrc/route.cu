@@ -42,9 +42,19 @@ __device__ __forceinline__ float sigmoid_f32_via_f64(float l) {
   return (float)(1.0 / (1.0 + exp(-(double)l)));
 }
 // fp32 sigmoid: expf (<= 2 ulp), an add and a correctly rounded divide; its
-// distance to sigmoid_f32_via_f64 is far below kSlack
+// distance to sigmoid_f32_via_f64 is below 2^-22
 __device__ __forceinline__ float sigmoid_fast(float l) { return 1.0f / (1.0f + expf(-l)); }
+// Bound on |fl(sigmoid_fast(l) + b) - fl(sigmoid_f32_via_f64(l) + b)| for keys
+// of magnitude near |key|: the two sigmoids differ by < 2^-22, and the two
+// fp32 adds round at most one ulp of the key apart (one ulp <= |key| 2^-23).
+// The absolute floor covers keys near zero; the relative part covers large
+// selection biases, where one ulp of the key outgrows any absolute slack
+// (|key| ~ 10^3 has ulps of 2^-14..2^-13).  Both parts carry a factor of two
+// or more of margin.
 constexpr float kSlack = 1.0f / 65536.0f;
+__device__ __forceinline__ float key_slack(float key) {
+  return kSlack + fabsf(key) * (1.0f / 4194304.0f);   // 2^-16 + |key| 2^-22
+}
 
 // Keys as unsigned integers in the same order (x < y  <=>  u(x) < u(y) for
 // non-NaN floats); -0 is folded onto +0 first, so the two tie as floats do.
@@ -144,9 +154,9 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
     load_row(t + kRouteWarps);
     uint64_t c[EPL];
     if constexpr (SIG) {
-      // Rank fp32 keys first (within kSlack of the exact ones); the exact top
-      // k lies among the experts whose fp32 key is within 2 kSlack of the
-      // k-th fp32 key, so only those get the double-precision sigmoid.
+      // Rank fp32 keys first (within key_slack of the exact ones); the exact
+      // top k lies among the experts whose fp32 key is within 2 key_slack of
+      // the k-th fp32 key, so only those get the double-precision sigmoid.
       float sa[EPL], ka[EPL];
       float part = 0.f;
 #pragma unroll
@@ -161,7 +171,8 @@ route_kernel(const float* __restrict__ logits, int64_t n_tokens, int n_experts,
       sort_desc<EPL>(c);
       uint32_t kth = 0u;
       for (int j = 0; j < top_k; ++j) take_best<EPL>(c, lane, &kth);
-      const float thr = unordered(kth) - 4.f * kSlack;
+      const float kth_key = unordered(kth);
+      const float thr = kth_key - 4.f * key_slack(kth_key);
       // The candidates (usually about k of them, spread over the lanes'
       // EPL slots) are packed into consecutive lanes, so that one warp-wide
       // double-precision evaluation serves up to 32 of them, and the results

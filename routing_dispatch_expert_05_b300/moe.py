@@ -29,11 +29,11 @@ MOE_EXPERT_SILU_MLP, MOE_EXPERT_SWIGLU = 0, 1
 # every function include/moe.h declares (checked by the tests)
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_router_topk",
             "moe_route_logits", "moe_dispatch_permute",
-            "moe_dispatch_permute_noalloc", "moe_expert_up",
+            "moe_dispatch_permute_room", "moe_dispatch_permute_noalloc", "moe_expert_up",
             "moe_expert_up_gather", "moe_expert_down", "moe_grouped_ffn", "moe_shared_ffn", "moe_combine",
             "moe_forward", "moe_forward_timed", "moe_forward_host",
             "moe_update_selection_bias", "moe_backward_workspace_size", "moe_backward",
-            "moe_check_wait_timeout", "moe_read_device_error",
+            "moe_check_grouping", "moe_check_wait_timeout", "moe_read_device_error",
             "moe_status_string", "moe_version")
 
 
@@ -91,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route_logits": [cfgp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_dispatch_permute": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_dispatch_permute_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, sp, vp],
+        "moe_dispatch_permute_room": [cfgp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp],
         "moe_expert_up": [cfgp, vp, vp, wp, vp, vp, sz, vp],
         "moe_expert_up_gather": [cfgp, vp, vp, vp, wp, vp, vp, sz, vp],
         "moe_expert_down": [cfgp, vp, vp, wp, vp, vp, sz, vp],
@@ -104,6 +105,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_update_selection_bias": [cfgp, vp, vp, ctypes.c_float, vp, vp],
         "moe_backward_workspace_size": [cfgp, P(sz)],
         "moe_check_wait_timeout": [vp, sz, ctypes.c_int64, vp],
+        "moe_check_grouping": [cfgp, vp, vp, vp, vp, vp, sz, vp],
         "moe_backward": [cfgp, vp, wp, vp, ctypes.c_float, P(MoEGrads), vp, sz, vp],
     }
     for name, args in sig.items():
@@ -212,6 +214,17 @@ def moe_dispatch_permute(cfg, idx, x, offsets, row_of_slot, token_of_row, x_perm
         ptr(token_of_row), ptr(x_perm),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_dispatch_permute")
+
+
+def moe_dispatch_permute_room(cfg, idx, x, room, offsets, row_of_slot, token_of_row,
+                              x_perm, stats, ws, stream=None):
+    """moe_dispatch_permute with a per-expert capacity room [E] (int32)."""
+    wp, wb = _ws(ws)
+    _check(load_library().moe_dispatch_permute_room(
+        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(room), ptr(offsets), ptr(row_of_slot),
+        ptr(token_of_row), ptr(x_perm),
+        ctypes.byref(stats) if stats is not None else None, wp, wb,
+        _stream(stream)), "moe_dispatch_permute_room")
 
 
 def moe_dispatch_permute_noalloc(cfg, idx, x, offsets, row_of_slot, token_of_row,
@@ -338,6 +351,14 @@ def moe_update_selection_bias(cfg, counts, sel_bias, gamma, load_cv=None, stream
     _check(load_library().moe_update_selection_bias(
         ctypes.byref(cfg), ptr(counts), ptr(sel_bias), float(gamma), ptr(load_cv),
         _stream(stream)), "moe_update_selection_bias")
+
+
+def moe_check_grouping(cfg, idx, offsets, row_of_slot, token_of_row, ws, stream=None):
+    """Check a grouping on the device; a failure shows in the error word."""
+    wp, wb = _ws(ws)
+    _check(load_library().moe_check_grouping(
+        ctypes.byref(cfg), ptr(idx), ptr(offsets), ptr(row_of_slot), ptr(token_of_row),
+        wp, wb, _stream(stream)), "moe_check_grouping")
 
 
 def moe_check_wait_timeout(ws, limit_ns: int, stream=None):

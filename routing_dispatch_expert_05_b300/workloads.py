@@ -113,10 +113,16 @@ WORKLOADS: Dict[str, MoEShape] = {
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
-    """fp32 array -> uint16 bf16 bit patterns, round to nearest even."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    """fp32 array -> uint16 bf16 bit patterns, round to nearest even.
+
+    Finite values and infinities only (no NaN is ever drawn): the rounding
+    increment then never carries out of 32 bits, so the sum stays uint32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (u >> 16) & 1
+    r += 0x7FFF
+    r += u
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -210,6 +210,20 @@ def test_grouping_expert_and_combine_calls_reject_bad_arguments(lib):
     assert disp(c, a, a, a, a, a, a, None, None, big, None) == -1          # no workspace
     bad_stats = M.MoEStats(counts=a + 4)
     assert disp(c, a, a, a, a, a, a, ctypes.byref(bad_stats), a, big, None) == -1
+    # grouping with a per-expert room: (cfg, idx, x, room, offsets, ...)
+    room = lib.moe_dispatch_permute_room
+    assert room(c, a, a, None, a, a, a, a, None, a, big, None) == -1       # no room
+    assert room(c, a, a, a + 4, a, a, a, a, None, a, big, None) == -1      # misaligned room
+    assert room(c, a, a, a, None, a, a, a, None, a, big, None) == -1       # no offsets
+    assert room(c, a, a, a, a, a, a, None, None, a, big, None) == -1       # x without x_perm
+    assert room(c, a, a, a, a, a, a, a, None, a, 16, None) == -3           # short workspace
+    # the grouping check: (cfg, idx, offsets, row_of_slot, token_of_row, ws, bytes, stream)
+    chk = lib.moe_check_grouping
+    assert chk(c, a, None, a, a, a, big, None) == -1                       # no offsets
+    assert chk(c, None, a, a, a, a, big, None) == -1                       # no idx
+    assert chk(c, a, a, a + 4, a, a, big, None) == -1                      # misaligned rows
+    assert chk(c, a, a, a, a, a, 16, None) == -3                           # short workspace
+    assert chk(c, a, a, a, a, None, big, None) == -1                       # no workspace
     noalloc = lib.moe_dispatch_permute_noalloc
     assert noalloc(c, a, a, None, a, a, a, None, None) == -1               # no offsets
     assert noalloc(c, None, a, a, a, a, a, None, None) == -1               # no idx

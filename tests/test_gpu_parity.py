@@ -69,6 +69,50 @@ def test_route_logits_bit_exact(mode, E, k, kind):
     assert M.moe_read_device_error(ws) == M.MOE_OK
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 6), (128, 8), (256, 8)])
+@pytest.mark.parametrize("spread", [1e-3, 1.0])
+def test_route_sigmoid_large_bias_bit_exact(E, k, spread):
+    """Selection biases of magnitude ~10^3 ("DeepSeek 5.7", s.2 puts no bound
+    on the balancing bias): one ulp of a key s + b is then 2^-14..2^-13, far
+    above the error of the fast fp32 sigmoid, so the candidates that get the
+    exact (double) sigmoid must be chosen relative to the key's magnitude.
+    Biases sit on a few shared values, some straddling the binade boundary
+    at 1024, and narrow logits (spread 1e-3) put many keys within an ulp of
+    one another: exact ties to the lower index and one-ulp near-ties
+    everywhere.  idx must equal the all-double definition bit for bit."""
+    N = 1000
+    rng = np.random.default_rng(E * 10 + k + int(spread * 7))
+    levels = np.array([1023.75, 1023.9375, 1000.0, 1000.0, 2047.5, -999.0],
+                      np.float32)
+    bias = levels[rng.integers(0, len(levels), E)]
+    # k + 2 experts (all of them for small E) share the top level, whose keys
+    # s + 2047.5 straddle the binade boundary at 2048 (ulps 2^-12 / 2^-11)
+    bias[rng.permutation(E)[:min(E, k + 2)]] = np.float32(2047.5)
+    logits = (spread * rng.standard_normal((N, E))).astype(np.float32)
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, route=W.ROUTE_SIGMOID_BIAS)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    idx = torch.full((N, k), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((N, k), dtype=torch.float32, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    bal = torch.zeros(1, dtype=torch.float32, device="cuda")
+    M.moe_route_logits(cfg, dev(logits), dev(bias), idx, w,
+                       M.make_stats(counts=counts, balance=bal), ws)
+    torch.cuda.synchronize()
+    i_o, w_o, p_o = O.route(logits, W.ROUTE_SIGMOID_BIAS, k, bias)
+    keys = O.selection_keys(logits, W.ROUTE_SIGMOID_BIAS, bias)
+    # the case is what it claims: many exact ties at the k-th key
+    kth = -np.sort(-keys, axis=1)[:, k - 1]
+    assert ((keys == kth[:, None]).sum(axis=1) > 1).mean() > (0.2 if spread < 0.1 else 0.0)
+    assert np.array_equal(to_np(idx), i_o)
+    assert np.allclose(to_np(w), w_o, rtol=2e-6, atol=2e-7)
+    cnt_o = np.bincount(i_o.reshape(-1), minlength=E)
+    assert np.array_equal(to_np(counts), cnt_o)
+    b_o = O.balance_statistic(cnt_o, p_o, N, shape.balance_coef)
+    assert abs(float(to_np(bal)[0]) - b_o) <= BALANCE_REL * abs(b_o)
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+
+
 def test_route_logits_empty_and_tail():
     for N in (0, 1, 127, 129):
         shape = _cfg(n_tokens=N, n_experts=16, top_k=4)
@@ -161,13 +205,95 @@ def test_dispatch_flags_bad_expert_index():
     assert int(to_np(offsets)[-1]) == N * k - 2
 
 
+@pytest.mark.parametrize("N,E,k,cf,zipf", DISPATCH_CASES)
+def test_check_grouping_accepts_every_dispatch(N, E, k, cf, zipf):
+    """The device-side consistency check passes on every grouping the
+    dispatch writes (capacity drops, N < E, k = E, E = 1, many empty
+    experts)."""
+    idx = W.make_assignments(N, E, k, seed=N + 2 * E + k, zipf_s=zipf)
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, capacity_factor=cf)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    di = dev(idx)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    ros = torch.zeros(N * k, dtype=torch.int32, device="cuda")
+    tor = torch.zeros(N * k, dtype=torch.int32, device="cuda")
+    M.moe_dispatch_permute(cfg, di, None, offsets, ros, tor, None, None, ws)
+    for _ in range(2):                      # its counters are left zero: twice in a row
+        M.moe_check_grouping(cfg, di, offsets, ros, tor, ws)
+        assert M.moe_read_device_error(ws) == M.MOE_OK
+
+
+def _planted_groupings(idx, offsets, ros, tor, k):
+    """Inconsistent groupings, each one mistake away from a valid one, every
+    index still inside its buffer (so the check reads nothing out of range)."""
+    kept = np.nonzero(ros >= 0)[0]
+    a, b = kept[0], kept[len(kept) // 2]
+    out = []
+    r = ros.copy(); r[a], r[b] = r[b], r[a]
+    out.append(("rows swapped", idx, offsets, r, tor))
+    r = ros.copy(); r[b] = -1
+    out.append(("kept slot marked dropped", idx, offsets, r, tor))
+    t = tor.copy(); t[ros[b]] = (t[ros[b]] + 1) % (idx.shape[0])
+    out.append(("token_of_row wrong", idx, offsets, ros, t))
+    o = offsets.copy(); o[1], o[2] = o[2], o[1]
+    out.append(("offsets decrease", idx, o, ros, tor))
+    i = idx.copy(); i[0, 1] = i[0, 0]
+    out.append(("duplicate expert in a token", i, offsets, ros, tor))
+    return out
+
+
+def test_check_grouping_flags_planted_inconsistencies():
+    N, E, k = 1000, 16, 4
+    idx = W.make_assignments(N, E, k, seed=9, zipf_s=1.0)
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k)
+    cfg = M.make_config(shape)
+    ws = M.MoEWorkspace(cfg, forward=False)
+    disp = O.dispatch(idx, E, 0.0)
+    base = (idx.astype(np.int32), disp["offsets"].astype(np.int32),
+            disp["row_of_slot"].astype(np.int32), disp["token_of_row"].astype(np.int32))
+    M.moe_check_grouping(cfg, *(dev(a) for a in base), ws)
+    assert M.moe_read_device_error(ws) == M.MOE_OK       # the oracle's grouping passes
+    tor_full = np.zeros(N * k, np.int32)
+    tor_full[:len(base[3])] = base[3]
+    for what, i, o, r, t in _planted_groupings(base[0], base[1], base[2], tor_full, k):
+        M.moe_check_grouping(cfg, dev(i), dev(o), dev(r), dev(t), ws)
+        assert M.moe_read_device_error(ws) == M.MOE_ERR_DEVICE_CHECK, what
+    # and the check's own counters were left clean
+    M.moe_check_grouping(cfg, *(dev(a) for a in (base[0], base[1], base[2], tor_full)), ws)
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_F32])
+def test_grouped_gemm_refuses_inconsistent_offsets(dtype):
+    """Offsets that decrease, or end past the grouped buffer, set the error
+    word and the grouped GEMM writes nothing (tensor-core and CUDA-core)."""
+    N, E, k, d, F = 256, 8, 2, 64, 64
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d, d_ff=F, dtype=dtype)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    xp = D.empty(N * k, d)
+    good = np.linspace(0, N * k, E + 1).astype(np.int32)
+    for what, off in (("decreasing", np.r_[good[:3], good[2] - 5, good[4:]]),
+                      ("past the buffer", np.r_[good[:-1], N * k + 64])):
+        assert off.min() >= 0 and len(off) == E + 1, what
+        h = torch.full((N * k, F), 3.0, dtype=D.tdtype, device="cuda")
+        M.moe_expert_up(D.cfg, xp, dev(off.astype(np.int32)), D.weights, h, D.ws)
+        torch.cuda.synchronize()
+        assert D.device_error() == M.MOE_ERR_DEVICE_CHECK, what
+        assert bool((h == 3.0).all()), what
+
+
 # ---------------------------------------------------------- expert FFNs
 FFN_CASES = [("toy_top2_fp32", 64), ("capacity_top2_fp32", 700),
              ("capacity_top2_bf16", 700), ("deepseek_v3_block", 300),
              ("qwen3_moe", 200),
              # enough rows per expert for CTA pairs, with short group tails
              # left to the single-CTA pass
-             ("deepseek_v3_block", 1536)]
+             ("deepseek_v3_block", 1536),
+             # a few rows per expert: the swapped-operand kernel (weights on
+             # the MMA's M side), SwiGLU and SiLU + bias
+             ("decode_stream", None), ("capacity_top2_bf16", 48)]
 
 
 def _oracle_dispatch_inputs(shape, inp, zipf=1.1, seed=77):
@@ -361,12 +487,14 @@ def test_router_topk_parity(name, N):
     M.moe_router_topk(D.cfg, D.t["x"], D.weights, None, idx2, w2, None, D.ws)
     torch.cuda.synchronize()
     assert torch.equal(idx2, idx) and torch.equal(w2, w)
-    # the counts are those of the GPU's own selection
+    # the counts are those of the GPU's own selection, and the balance
+    # statistic is the oracle's on the GPU's own logits and counts (near-ties
+    # or not)
     cnt = np.bincount(ig.reshape(-1), minlength=E)
     assert np.array_equal(to_np(st["counts"]), cnt)
-    if not amb.any():
-        b_ref = O.balance_statistic(cnt, p_o, n, shape.balance_coef)
-        assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
+    _, _, p_g = O.route(lg, shape.route, k, v.get("sel_bias"))
+    b_ref = O.balance_statistic(cnt, p_g, n, shape.balance_coef)
+    assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
@@ -407,12 +535,15 @@ def test_router_ties_from_duplicated_experts(mode, dtype):
 # --------------------------------------------------------- whole layer
 FORWARD_CASES = [("toy_top2_fp32", None), ("capacity_top2_fp32", None),
                  ("capacity_top2_bf16", None), ("deepseek_v3_block", 640),
-                 ("qwen3_moe", 640), ("decode_stream", None)]
+                 ("qwen3_moe", 640), ("decode_stream", None),
+                 # a few rows per expert, biases and a capacity that drops:
+                 # the swapped-operand up and compact down projections
+                 ("capacity_top2_bf16", 48), ("deepseek_v3_block", 96)]
 
 
-def _router_margin(D, ref_logits):
-    """The near-tie margin of this layer's router: from the GPU router's
-    logits (the same kernel moe_forward runs) against the oracle's."""
+def _gpu_logits(D):
+    """The router logits moe_forward works from: the same router kernels
+    (chosen by the token count), written out by moe_router_topk."""
     shape = D.shape
     n, E, k = shape.n_tokens, shape.n_experts, shape.top_k
     logits = torch.zeros(n, E, device="cuda")
@@ -420,7 +551,30 @@ def _router_margin(D, ref_logits):
     w = torch.zeros(n, k, device="cuda")
     M.moe_router_topk(D.cfg, D.t["x"], D.weights, logits, idx, w, None, D.ws)
     torch.cuda.synchronize()
-    return logit_margin(to_np(logits), ref_logits)
+    return to_np(logits)
+
+
+def _router_margin(D, ref_logits):
+    """The near-tie margin of this layer's router: from the GPU router's
+    logits (the same kernel moe_forward runs) against the oracle's."""
+    return logit_margin(_gpu_logits(D), ref_logits)
+
+
+def _check_forward_statistics(D, st, lg_gpu, values):
+    """The forward's selection counts and balance statistic against the
+    oracle's selection and statistic computed on the GPU's own logits: the
+    counts bit-exact, the statistic within 1e-4 relative, whatever near-ties
+    the layer holds.  With a capacity, kept/dropped must then equal the
+    oracle's grouping of that same selection."""
+    shape = D.shape
+    i_g, _, p_g = O.route(lg_gpu, shape.route, shape.top_k, values.get("sel_bias"))
+    cnt = np.bincount(i_g.reshape(-1), minlength=shape.n_experts)
+    assert np.array_equal(to_np(st["counts"]), cnt)
+    b_ref = O.balance_statistic(cnt, p_g, shape.n_tokens, shape.balance_coef)
+    assert abs(float(to_np(st["balance"])[0]) - b_ref) <= BALANCE_REL * abs(b_ref)
+    disp = O.dispatch(i_g, shape.n_experts, float(np.float32(shape.capacity_factor)))
+    for name in ("kept", "dropped"):
+        assert np.array_equal(to_np(st[name]), disp[name]), name
 
 
 def _forward(D, stats=True):
@@ -439,7 +593,9 @@ def test_forward_parity(name, N):
     D = Device(inp)
     out, st = _forward(D)
     ref = O.forward(shape, inp.values)
-    margin = _router_margin(D, ref["logits"])
+    lg_gpu = _gpu_logits(D)
+    margin = logit_margin(lg_gpu, ref["logits"])
+    _check_forward_statistics(D, st, lg_gpu, inp.values)
     keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
     # a near-tie at the k-th key may swap one expert for another; with a
     # capacity that also moves later drops of the experts involved, so those
@@ -458,9 +614,46 @@ def test_forward_parity(name, N):
     cnt = to_np(st["counts"])
     assert cnt.sum() == shape.n_tokens * shape.top_k
     assert np.abs(cnt - ref["counts"]).sum() <= 2 * amb.sum()
-    b = float(to_np(st["balance"])[0])
-    if not amb.any():
-        assert abs(b - ref["balance"]) <= BALANCE_REL * abs(ref["balance"])
+    assert D.device_error() == M.MOE_OK
+
+
+@pytest.mark.parametrize("name,N", [("qwen3_moe", 4096), ("deepseek_v3_block", 4096)])
+def test_forward_whole_output_large(name, N):
+    """Every output of a 4096-token layer against the oracle: the expert
+    GEMMs run on CTA pairs with the compact, weighted, slot-ordered down
+    projection, and the selection sums its statistic over 32-token CTAs
+    (the path of the full-size layers)."""
+    inp = inputs_for(name, N)
+    shape = inp.shape
+    D = Device(inp)
+    out, st = _forward(D)
+    ref = O.forward(shape, inp.values)
+    lg_gpu = _gpu_logits(D)
+    _check_forward_statistics(D, st, lg_gpu, inp.values)
+    keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
+    amb, _ = set_ambiguous_tokens(keys, shape.top_k, logit_margin(lg_gpu, ref["logits"]))
+    assert (~amb).mean() > 0.9
+    assert_output_close(to_np(out)[~amb], ref["out_exact"][~amb], shape.dtype, name)
+    # near-tie tokens: the GPU's own selection, weights and output from the
+    # oracle's experts on those same choices
+    if amb.any():
+        tok = np.nonzero(amb)[0]
+        i_g, w_g, _ = O.route(lg_gpu[tok], shape.route, shape.top_k,
+                              inp.values.get("sel_bias"))
+        v = inp.values
+        exact = np.zeros((len(tok), shape.d_model))
+        for i, t in enumerate(tok):
+            for j in range(shape.top_k):
+                e = int(i_g[i, j])
+                _, y = O.expert_ffn(v["x"][t:t + 1], v["w1"][e], v["w2"][e], shape.expert,
+                                    shape.dtype, w3=v["w3"][e])
+                exact[i] += w_g[i, j] * y[0]
+        if shape.n_shared > 0:
+            exact += O.round_f32(O.shared_ffn(v["x"][tok], v["ws1"], v["ws3"], v["ws2"],
+                                              shape.dtype))
+        rms = float(np.sqrt(np.mean(ref["out_exact"] ** 2)))
+        err = np.abs(to_np(out)[tok] - exact)
+        assert (err <= 2e-2 * rms + np.abs(exact) * 2.0 ** -8).all()
     assert D.device_error() == M.MOE_OK
 
 
@@ -668,6 +861,9 @@ def test_forward_full_size_sampled(name):
     assert_output_close(o[~amb], ref["out_exact"][~amb], shape.dtype, name)
     cnt = to_np(st["counts"])
     assert cnt.sum() == shape.n_tokens * shape.top_k
+    # counts and balance statistic of the whole layer (32-token selection
+    # CTAs) against the oracle's on the GPU's own logits of every token
+    _check_forward_statistics(D, st, _gpu_logits(D), inp.values)
     assert D.device_error() == M.MOE_OK
 
 
@@ -734,3 +930,65 @@ def test_selection_bias_update_from_forward_counts():
     torch.cuda.synchronize()
     ref = O.selection_bias_update(bias0, to_np(st["counts"]), 1e-3)
     assert np.array_equal(db.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------- grouping with a per-expert room
+@pytest.mark.parametrize("N,E,k,cf,zipf", DISPATCH_CASES)
+def test_dispatch_room_bit_exact(N, E, k, cf, zipf):
+    """Grouping with one capacity per expert (room [E]: zero, negative, below
+    and above the expert's load) equals the oracle's grouping with those
+    capacities, bit for bit; a room of the scalar capacity everywhere equals
+    moe_dispatch_permute with capacity_factor."""
+    d = 32
+    idx = W.make_assignments(N, E, k, seed=N + E + k + 1, zipf_s=zipf)
+    x = np.random.default_rng(N + 1).standard_normal((N, d)).astype(np.float32)
+    shape = _cfg(n_tokens=N, n_experts=E, top_k=k, d_model=d, capacity_factor=cf,
+                 dtype=W.DTYPE_BF16)
+    cfg = M.make_config(shape)
+    cfg_nocap = M.make_config(shape.replace(capacity_factor=0.0))
+    ws = M.MoEWorkspace(cfg, forward=False)
+    xd, di = dev(x, W.DTYPE_BF16), dev(idx)
+    load = np.bincount(idx.reshape(-1), minlength=E)
+    rng = np.random.default_rng(E + k)
+    rooms = [rng.integers(-3, max(2, int(load.max()) + 3), E).astype(np.int32),
+             np.zeros(E, np.int32), (load // 2).astype(np.int32)]
+    cap = O.capacity(float(np.float32(cf)), N, E)
+    if cap is not None:
+        rooms.append(np.full(E, cap, np.int32))
+
+    def run(room):
+        o = dict(offsets=torch.full((E + 1,), -5, dtype=torch.int32, device="cuda"),
+                 ros=torch.full((N * k,), -5, dtype=torch.int32, device="cuda"),
+                 tor=torch.full((N * k,), -5, dtype=torch.int32, device="cuda"),
+                 xp=torch.zeros((N * k, d), dtype=torch.bfloat16, device="cuda"))
+        st = {n: torch.full((E,), -5, dtype=torch.int32, device="cuda")
+              for n in ("counts", "kept", "dropped")}
+        if room is None:
+            M.moe_dispatch_permute(cfg, di, xd, o["offsets"], o["ros"], o["tor"], o["xp"],
+                                   M.make_stats(**st), ws)
+        else:
+            M.moe_dispatch_permute_room(cfg, di, xd, dev(room), o["offsets"], o["ros"],
+                                        o["tor"], o["xp"], M.make_stats(**st), ws)
+        # (a per-expert room may exceed the config's capacity: the check
+        # runs on a config without one)
+        M.moe_check_grouping(cfg_nocap, di, o["offsets"], o["ros"], o["tor"], ws)
+        torch.cuda.synchronize()
+        assert M.moe_read_device_error(ws) == M.MOE_OK
+        o.update(st)
+        return o
+
+    for room in rooms:
+        got = run(room)
+        res = O.dispatch(idx, E, expert_capacity=room)
+        m = int(res["offsets"][-1])
+        assert np.array_equal(to_np(got["offsets"]), res["offsets"])
+        assert np.array_equal(to_np(got["ros"]), res["row_of_slot"])
+        assert np.array_equal(to_np(got["tor"])[:m], res["token_of_row"])
+        for n in ("counts", "kept", "dropped"):
+            assert np.array_equal(to_np(got[n]), res[n]), n
+        ref = xd[torch.from_numpy(res["token_of_row"]).cuda()] if m else got["xp"][:0]
+        assert torch.equal(got["xp"][:m].view(torch.int16), ref.view(torch.int16))
+    if cap is not None:
+        a, b = run(None), run(rooms[-1])
+        for key in a:
+            assert torch.equal(a[key], b[key]), key
