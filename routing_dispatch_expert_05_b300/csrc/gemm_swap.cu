@@ -14,21 +14,21 @@
 //
 // Structure (one persistent CTA per SM, 10 warps, the pipeline of the
 // single-CTA kernel): warp 0 loads, per k-block of 64, the weight tile (128 x
-// 64 bf16) and the token tile (16-row boxes, up to 64 rows) into an 8-stage
-// ring; one lane of warp 1 issues tcgen05.mma (M = 128, N = tokens, K = 16)
-// into one of two TMEM accumulators of 64 columns; warps 2-9 read them back
-// (TMEM lane = output feature, column = token row).
+// 64 bf16; for SwiGLU the gate and the up tile of the same 128 features) and
+// the token tile (16-row boxes, up to 64 rows) into a ring of stages; one
+// lane of warp 1 issues tcgen05.mma (M = 128, N = tokens, K = 16) into one
+// of two TMEM accumulators (SwiGLU: a gate and an up accumulator side by
+// side); warps 2-9 read them back (TMEM lane = output feature, column =
+// token row).  Few, large copies per stage: the copy engine's cost per
+// instruction, not per byte, limits 16-row boxes.
 //
 // Tiles are (expert, block of 64 token rows, block of output features); the
 // feature block is fastest, so CTAs working at the same time share the
 // token rows and stream disjoint weight rows.
 //
 // Epilogues:
-//   * SwiGLU: the weight tile interleaves 16 gate rows (W1) and 16 up rows
-//     (W3) of the same features per TMEM lane quadrant, so lanes j and
-//     j + 16 of a warp hold gate and up of one feature: one shuffle pairs
-//     them, h = silu(gate) * up (64 features per tile), staged in shared
-//     memory and written as 32-byte row pieces;
+//   * SwiGLU: the same TMEM lane of the gate and the up accumulator holds
+//     one feature, h = silu(gate) * up (128 features per tile);
 //   * SiLU + bias: h = silu(v + b1), 128 features per tile;
 //   * compact (down projection): each warp's 32 lanes are one 32-column block
 //     of an output row, scaled by the row's routing weight; the block's
@@ -53,21 +53,26 @@ using namespace tc;
 
 constexpr int kWRows = 128;                         // MMA M: weight rows per tile
 constexpr int kTokRows = 64;                        // token rows per tile (MMA N <= 64)
-constexpr int kStages = 8;
-constexpr uint32_t kTileW = kWRows * BK * 2;        // 16 KB
+constexpr uint32_t kTileW1 = kWRows * BK * 2;       // one weight tile: 16 KB
 constexpr uint32_t kTileX = kTokRows * BK * 2;      // 8 KB
-constexpr uint32_t kStageBytes = kTileW + kTileX;   // 24 KB
-constexpr uint32_t kBox = 16 * BK * 2;              // one 16-row box: 2 KB
+constexpr uint32_t kBox = 16 * BK * 2;              // one 16-row token box: 2 KB
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr uint32_t kTmemCols = 2 * kTokRows;        // two accumulators
 constexpr int kBarBytes = 1024;
 constexpr int kTableBytes = (2 * (kMaxExperts + 1) * 4 + 127) / 128 * 128;
-constexpr int kStgWarpBytes = 16 * 16 * 2;          // 16 token rows x 16 features bf16
-constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kTableBytes +
-                           kEpiWarps * kStgWarpBytes + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert((kStages * kTileW) % 1024 == 0 && kTileX % 1024 == 0, "swizzle atoms");
+// Ring geometry: SwiGLU stages hold a gate and an up weight tile (5 stages
+// of 40 KB), the others one weight tile (8 stages of 24 KB).  TMEM: two
+// accumulators of 64 columns (SwiGLU: gate at +0, up at +64 of each).
+template <bool SWIGLU> struct Geo {
+  static constexpr int kStages = SWIGLU ? 5 : 8;
+  static constexpr uint32_t kTileW = (SWIGLU ? 2 : 1) * kTileW1;
+  static constexpr uint32_t kStageBytes = kTileW + kTileX;
+  static constexpr uint32_t kAccCols = (SWIGLU ? 2 : 1) * kTokRows;
+  static constexpr uint32_t kTmemCols = SWIGLU ? 256 : 128;
+  static constexpr int kSmem = kStages * kStageBytes + kBarBytes + kTableBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  static_assert((kStages * kTileW) % 1024 == 0 && kTileX % 1024 == 0, "swizzle atoms");
+};
 
 struct Params {
   const int32_t* offsets;     // [G+1] device
@@ -113,37 +118,21 @@ __device__ __forceinline__ int tile_n(const Tile& tl) {
 }
 
 // ---------------------------------------------------------------- epilogues
-// SwiGLU, one 16-column chunk: lane j (< 16) holds gate, lane j + 16 up, of
-// feature f0 + 16 q + (j & 15), for token columns c0 .. c0 + 15.
+// SwiGLU, one 16-column chunk: lane j holds gate (g) and up (u) of feature
+// f0 + 32 q + j for token columns c0 .. c0 + 15.
 __device__ __forceinline__ void swiglu_chunk(const Params& p, const Tile& tl, int lane, int q,
-                                             int c0, const uint32_t (&r)[16], uint16_t* stg) {
-  const bool lo = lane < 16;
-  float h[8];
+                                             int c0, const uint32_t (&g)[16],
+                                             const uint32_t (&u)[16]) {
+  const int f = tl.fb * kWRows + q * 32 + lane;
+  if (f >= p.n_out) return;
+  bf16* C = static_cast<bf16*>(p.C);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float mine = __uint_as_float(lo ? r[8 + i] : r[i]);
-    const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-    // lo lanes: columns c0 + i (gate r[i], up from the partner); hi lanes:
-    // columns c0 + 8 + i (gate from the partner, up r[8 + i])
-    h[i] = lo ? silu_f32(__uint_as_float(r[i])) * other
-              : silu_f32(other) * __uint_as_float(r[8 + i]);
+  for (int i = 0; i < 16; ++i) {
+    const int row = tl.row0 + c0 + i;
+    if (row < tl.row_end)
+      C[(int64_t)row * p.n_out + f] =
+          __float2bfloat16_rn(silu_f32(__uint_as_float(g[i])) * __uint_as_float(u[i]));
   }
-  // stage [16 token rows][16 features] and write 32-byte row pieces
-  const int fl = lane & 15, cb = lo ? 0 : 8;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(h[i]);
-    stg[(cb + i) * 16 + fl] = *reinterpret_cast<const uint16_t*>(&b);
-  }
-  __syncwarp();
-  const int rr = lane >> 1, part = lane & 1;
-  const int row = tl.row0 + c0 + rr;
-  const int f = tl.fb * 64 + q * 16 + part * 8;
-  if (row < tl.row_end && f < p.n_out) {
-    const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 16 + part * 8);
-    st_vec16(static_cast<uint16_t*>(p.C) + (int64_t)row * p.n_out + f, v);
-  }
-  __syncwarp();
 }
 
 // SiLU + bias, one 16-column chunk: lane j holds feature f0 + 32 q + j.
@@ -199,10 +188,17 @@ __device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, i
 }
 
 // ---------------------------------------------------------------- kernel
+template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
 swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
                  const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params p) {
+  using Gm = Geo<SWIGLU>;
+  constexpr int kStages = Gm::kStages;
+  constexpr uint32_t kTileW = Gm::kTileW;
+  constexpr uint32_t kStageBytes = Gm::kStageBytes;
+  constexpr uint32_t kAccCols = Gm::kAccCols;
+  constexpr uint32_t kTmemCols = Gm::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,12 +213,10 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_tile_start = reinterpret_cast<int*>(smem + kStages * kStageBytes + kBarBytes);
   int* s_off = s_tile_start + kMaxExperts + 1;
-  uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.n_groups;
-  const int fb_rows = p.swiglu ? 64 : kWRows;        // output features per tile
-  const int nfb = (p.n_out + fb_rows - 1) / fb_rows;
+  const int nfb = (p.n_out + kWRows - 1) / kWRows;   // 128 output features per tile
   const int nkb = (p.K + BK - 1) / BK;
 
   if (warp == 0 && lane == 0) {
@@ -238,7 +232,7 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&tmW0);
-    if (p.swiglu) prefetch_map(&tmW1);
+    if (SWIGLU) prefetch_map(&tmW1);
     prefetch_map(&tmX);
   }
   if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
@@ -292,23 +286,14 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
         const Tile tl = tile_of(t, s_tile_start, s_off, G, nfb);
         const int nb = tile_n(tl) >> 4;               // 16-row token boxes
-        const int wrow = tl.g * p.n_out + tl.fb * fb_rows;
+        const int wrow = tl.g * p.n_out + tl.fb * kWRows;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
           mbar_expect_tx(&full[stage], kTileW + (uint32_t)nb * kBox);
           uint8_t* w = sW + stage * kTileW;
-          if (p.swiglu) {
-            // lane quadrant q: 16 gate rows, then the 16 up rows of the same
-            // features
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              tma_load_2d(w + (2 * q) * kBox, &tmW0, &full[stage], kb * BK, wrow + 16 * q);
-              tma_load_2d(w + (2 * q + 1) * kBox, &tmW1, &full[stage], kb * BK, wrow + 16 * q);
-            }
-          } else {
-            tma_load_2d(w, &tmW0, &full[stage], kb * BK, wrow);
-          }
+          tma_load_2d(w, &tmW0, &full[stage], kb * BK, wrow);
+          if (SWIGLU) tma_load_2d(w + kTileW1, &tmW1, &full[stage], kb * BK, wrow);
           uint8_t* x = sX + stage * kTileX;
           for (int i = 0; i < nb; ++i)
             tma_load_2d(x + i * kBox, &tmX, &full[stage], kb * BK, tl.row0 + 16 * i);
@@ -342,7 +327,7 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
         const uint32_t idesc = idesc_bf16(kWRows, tile_n(tl));
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * kTokRows);
+        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(&full[stage], phase, s_abort, p.err)) { ok = false; break; }
@@ -350,9 +335,13 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
           const uint32_t a0 = smem_u32(sW + stage * kTileW);
           const uint32_t b0 = smem_u32(sX + stage * kTileX);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
+          for (int kk = 0; kk < BK / 16; ++kk) {
             umma(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
                  (kb | kk) != 0);
+            if (SWIGLU)         // the up accumulator, 64 columns on
+              umma(d + kTokRows, sdesc_sw128(a0 + kTileW1 + kk * 32), sdesc_sw128(b0 + kk * 32),
+                   idesc, (kb | kk) != 0);
+          }
           umma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -375,22 +364,28 @@ swap_gemm_kernel(const __grid_constant__ CUtensorMap tmW0,
     // ------------------------------------------------------ epilogue
     const int q = warp & 3;                          // TMEM lane quadrant
     const int half = (warp - 2) >> 2;                // which 16-column chunks
-    uint16_t* stg = reinterpret_cast<uint16_t*>(s_stage + (warp - 2) * kStgWarpBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = tile_of(t, s_tile_start, s_off, G, nfb);
       if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (uint32_t)(acc * kTokRows) + ((uint32_t)(q * 32) << 16);
+      const uint32_t tb = tmem_base + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
       const int nch = tile_n(tl) >> 4;
       for (int ch = half; ch < nch; ch += 2) {
         uint32_t r[16];
         MOE_TMEM_LD16(tb + ch * 16, r);
-        MOE_TMEM_WAIT16(r);
-        if (p.epilogue == kEpiSwiglu) swiglu_chunk(p, tl, lane, q, ch * 16, r, stg);
-        else if (p.c_e8 != nullptr) compact_chunk(p, tl, lane, q, ch * 16, r);
-        else silu_bias_chunk(p, tl, lane, q, ch * 16, r);
+        if constexpr (SWIGLU) {
+          uint32_t u[16];
+          MOE_TMEM_LD16(tb + kTokRows + ch * 16, u);
+          MOE_TMEM_WAIT16(r);
+          MOE_TMEM_WAIT16(u);
+          swiglu_chunk(p, tl, lane, q, ch * 16, r, u);
+        } else {
+          MOE_TMEM_WAIT16(r);
+          if (p.c_e8 != nullptr) compact_chunk(p, tl, lane, q, ch * 16, r);
+          else silu_bias_chunk(p, tl, lane, q, ch * 16, r);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -439,24 +434,27 @@ bool launch_swap_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.c_row_map = q.c_row_map;
   p.c_row_scale = q.c_row_scale;
   p.err = q.err;
-  // weights [G * n_out, K] (16-row boxes for the SwiGLU interleave, else one
-  // 128-row box); token rows [rows, K] in 16-row boxes
+  // weights [G * n_out, K] in 128-row boxes; token rows [rows, K] in 16-row
+  // boxes
   const uint64_t wrows = (uint64_t)q.n_groups * q.n_out;
   CUtensorMap mw0, mw1, mx;
-  const uint32_t wbox = q.swiglu ? 16u : (uint32_t)kWRows;
-  if (!make_map(&mw0, q.B0, (uint64_t)q.K, wrows, (uint64_t)q.K * 2, wbox)) return false;
+  if (!make_map(&mw0, q.B0, (uint64_t)q.K, wrows, (uint64_t)q.K * 2, (uint32_t)kWRows))
+    return false;
   if (q.swiglu) {
-    if (!make_map(&mw1, q.B1, (uint64_t)q.K, wrows, (uint64_t)q.K * 2, wbox)) return false;
+    if (!make_map(&mw1, q.B1, (uint64_t)q.K, wrows, (uint64_t)q.K * 2, (uint32_t)kWRows))
+      return false;
   } else {
     mw1 = mw0;
   }
   if (!make_map(&mx, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2, 16u))
     return false;
-  if (cudaFuncSetAttribute(swap_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
+  auto kern = q.swiglu ? swap_gemm_kernel<true> : swap_gemm_kernel<false>;
+  const int smem = q.swiglu ? Geo<true>::kSmem : Geo<false>::kSmem;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
     return false;
-  return launch_pdl(swap_gemm_kernel, dim3(num_sms), dim3(kThreads), kSmemBytes, st, mw0, mw1,
-                    mx, p) == cudaSuccess;
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, st, mw0, mw1, mx, p) ==
+         cudaSuccess;
 }
 
 }  // namespace moe
