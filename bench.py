@@ -354,6 +354,37 @@ def workload_entry(shape, peaks, args, dev):
     if shape.n_shared > 0:
         sf = 2.0 * N * d * 3 * shape.n_shared * shape.d_ff_shared
         entry["shared_tflops"] = round(sf / (med["shared"] * 1e-3) / 1e12, 1)
+    # the same forward replayed from a CUDA graph (how a decode loop runs
+    # it: no per-launch host cost, no events between stages), each replay
+    # timed between its own events, after the flush when there is one
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                M.moe_forward(cfg, t["x"], weights, out, fstats, ws)
+        stream.wait_stream(cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        spans = []
+        for s_ in range(args.steps):
+            if flush is not None:
+                flush.fill_(s_ & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            spans.append((a, b))
+        torch.cuda.synchronize()
+        graph_ms = sum(a.elapsed_time(b) for a, b in spans) / args.steps
+        entry["graph_ms_per_step"] = round(graph_ms, 4)
+        entry["graph_tokens_per_s"] = round(N / (graph_ms * 1e-3), 1)
+    except Exception as exc:  # report, do not hide, a capture failure
+        graph_ms = None
+        entry["graph_ms_per_step"] = f"capture failed: {exc}"
     if flush is not None:
         # expert weights the step streams: every expert some token chose
         idx = torch.empty(N, k, dtype=torch.int32, device=dev)
@@ -369,6 +400,10 @@ def workload_entry(shape, peaks, args, dev):
         entry["hbm_frac_expert_gemms"] = round(wbytes / (gemm_ms * 1e-3) / 1e9 /
                                                peaks["hbm_gbs"], 4)
         entry["hbm_frac_step"] = round(wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+        if graph_ms is not None:
+            entry["weight_gbs_graph"] = round(wbytes / (graph_ms * 1e-3) / 1e9, 1)
+            entry["hbm_frac_graph"] = round(wbytes / (graph_ms * 1e-3) / 1e9 /
+                                            peaks["hbm_gbs"], 4)
     del t, ws, out
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
