@@ -364,9 +364,14 @@ MOE_API moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_hos
  * over the selected logits, or s_sel / sum s_sel in the sigmoid mode) and
  * the balance statistic (through p; the counts are constant) are
  * differentiated through the logits; dropped assignments pass nothing to
- * their expert.  All outputs fp32, device memory, overwritten:
+ * their expert; the shared experts (weight one) take dout itself.  All
+ * outputs fp32, device memory, overwritten:
  *   dx [N, d], d_w_router [E, d], d_b_router [E] (nullable; only with a
- *   router bias), d_w1 / d_w3 [E, F, d], d_w2 [E, d, F]. */
+ *   router bias), d_w1 [E, F, d], d_w3 [E, F, d] (SwiGLU only, else
+ *   ignored), d_w2 [E, d, F];
+ *   d_b1 [E, F], d_b2 [E, d] (SiLU-MLP with has_bias only, else ignored);
+ *   d_ws1 / d_ws3 [S, Fs, d], d_ws2 [S, d, Fs] (n_shared > 0 only, else
+ *   ignored). */
 typedef struct {
   float *dx;
   float *d_w_router;
@@ -374,6 +379,11 @@ typedef struct {
   float *d_w1;
   float *d_w3;
   float *d_w2;
+  float *d_b1;
+  float *d_b2;
+  float *d_ws1;
+  float *d_ws3;
+  float *d_ws2;
 } moe_grads_t;
 
 /* Bytes of workspace moe_backward needs (the forward's plus the gradient
@@ -382,13 +392,15 @@ MOE_API moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t
 
 /* The backward pass: recomputes the forward's routing, grouping and expert
  * activations from x, then runs the gradients back through the combine, the
- * experts (data and weight gradients on the tensor cores) and the router.
- * x [N, d] and dout [N, d] are bf16 device arrays; x, dout and the
- * gradient arrays 16-byte aligned (else MOE_ERR_INVALID_ARG).  Supported: bf16 SwiGLU
- * experts without expert biases or shared experts, d and F multiples of 64,
- * E a multiple of 8, N > 0 (else MOE_ERR_UNSUPPORTED, nothing enqueued).
- * With a capacity the drops are those of the forward.  Enqueued on
- * `stream`; ws as for moe_forward, moe_backward_workspace_size bytes. */
+ * experts and shared experts (data and weight gradients on the tensor
+ * cores) and the router.  x [N, d] and dout [N, d] are bf16 device arrays;
+ * x, dout and the gradient arrays 16-byte aligned (else
+ * MOE_ERR_INVALID_ARG).  Supported: bf16 layers of either expert kind
+ * (SwiGLU; SiLU-MLP with or without biases), with or without shared
+ * experts, d, F and Fs multiples of 64, E a multiple of 8, N > 0 (else
+ * MOE_ERR_UNSUPPORTED, nothing enqueued).  With a capacity the drops are
+ * those of the forward.  Enqueued on `stream`; ws as for moe_forward,
+ * moe_backward_workspace_size bytes. */
 MOE_API moe_status_t moe_backward(const moe_config_t *cfg, const void *x,
                                   const moe_weights_t *weights, const void *dout,
                                   float d_balance, moe_grads_t *grads, void *ws,

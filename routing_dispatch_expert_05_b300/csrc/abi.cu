@@ -902,7 +902,9 @@ struct BwLayout {
   Layout fw;
   int64_t kt, nt;        // columns of the transposed grouped / token operands
   size_t counts, koff, koff_n, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, xpT, dyT, hT,
-      dguT, dzT, xT, w2T, w13T, wrT, total;
+      dguT, dzT, xT, w2T, w13T, wrT;
+  // shared experts (S * Fs columns, one group of all tokens)
+  size_t gs, us, hs, dhs, dgus, dxs, ws13T, ws2T, doutT, hsT, dgusT, total;
 };
 
 BwLayout bw_layout_of(const moe_config_t& c) {
@@ -940,6 +942,20 @@ BwLayout bw_layout_of(const moe_config_t& c) {
   B.w2T = take((size_t)E * F * d * 2);
   B.w13T = take((size_t)E * 2 * d * F * 2);
   B.wrT = take((size_t)d * E * 2);
+  const int64_t SF = (int64_t)c.n_shared * c.d_ff_shared;
+  if (SF > 0) {
+    B.gs = take((size_t)N * SF * 2);
+    B.us = take((size_t)N * SF * 2);
+    B.hs = take((size_t)N * SF * 2);
+    B.dhs = take((size_t)N * SF * 2);
+    B.dgus = take((size_t)N * 2 * SF * 2);
+    B.dxs = take((size_t)N * d * 4);
+    B.ws13T = take((size_t)2 * d * SF * 2);
+    B.ws2T = take((size_t)SF * d * 2);
+    B.doutT = take((size_t)d * B.nt * 2);
+    B.hsT = take((size_t)SF * B.nt * 2);
+    B.dgusT = take((size_t)2 * SF * B.nt * 2);
+  }
   B.total = o;
   return B;
 }
@@ -947,14 +963,14 @@ BwLayout bw_layout_of(const moe_config_t& c) {
 moe_status_t check_backward_args(const moe_config_t* cfg, const moe_weights_t* w) {
   MOE_TRY(check_config(cfg));
   const moe_config_t& c = *cfg;
-  // the tensor-core path: bf16 SwiGLU experts without biases or shared
-  // experts, feature widths in whole k-blocks, E a multiple of 8 (the
-  // router's gradient GEMMs read E-wide rows)
-  if (c.dtype != MOE_BF16 || c.expert != MOE_EXPERT_SWIGLU || c.has_bias || c.n_shared > 0 ||
-      c.d_ff % 64 != 0 || c.d_model % 64 != 0 || c.n_experts % 8 != 0)
+  // the tensor-core path: bf16 layers, feature widths in whole k-blocks, E a
+  // multiple of 8 (the router's gradient GEMMs read E-wide rows)
+  if (c.dtype != MOE_BF16 || c.d_ff % 64 != 0 || c.d_model % 64 != 0 ||
+      c.n_experts % 8 != 0 || (c.n_shared > 0 && c.d_ff_shared % 64 != 0))
     return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_router_weights(c, w));
   MOE_TRY(check_up_weights(c, w));
+  MOE_TRY(check_shared_weights(c, w));
   return check_down_weights(c, w);
 }
 
@@ -1046,19 +1062,30 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   char* wrT = at<char>(ws, B.wrT);
   const int ns = num_sms();
 
+  const bool swiglu = c.expert == MOE_EXPERT_SWIGLU;
+  const int S = c.n_shared, SF = c.n_shared * c.d_ff_shared;
+  float* dxs = SF > 0 ? at<float>(ws, B.dxs) : nullptr;
+
   // 1. recompute: routing (counts for the balance term), grouping, x_perm,
-  //    g = x W1^T, u = x W3^T, h = silu(g) u, y = h W2^T (compact, row order)
+  //    SwiGLU: g = x W1^T, u = x W3^T, h = silu(g) u; SiLU-MLP: g = a =
+  //    x W1^T + b1, h = silu(a); y = h W2^T (+ b2) (compact, row order)
   moe_stats_t rs{};
   rs.counts = counts;
   router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true);
   dispatch_body(c, idx, x, offsets, ros, tor, x_perm, nullptr, sc, st);
   TcProblem q = plain_problem(x_perm, M, d, w.w1, E, F, offsets, E, M, F, g, 0, sc.err);
   q.use_pairs = pairs_pay(c);
+  if (!swiglu && c.has_bias) {
+    q.bias = w.b1;
+    q.bias_stride = F;
+  }
   MOE_TRY(tc_run(q, st));
-  q.B0 = w.w3;
-  q.C = u;
-  MOE_TRY(tc_run(q, st));
-  launch_silu_mul(g, u, h, offsets, E, F, ns, st);
+  if (swiglu) {
+    q.B0 = w.w3;
+    q.C = u;
+    MOE_TRY(tc_run(q, st));
+  }
+  launch_silu_mul(g, swiglu ? u : nullptr, h, offsets, E, 0, F, ns, st);
   MOE_TRY(down_body(c, h, offsets, w, y, y_e8, sc.err, st));
 
   // 2. combine and router: dw, dy = w dout, dlogits
@@ -1066,41 +1093,103 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   launch_router_backward(sc.logits, idx, wts, dw, counts, N, E, k, c.route, c.balance_coef,
                          d_balance, dz, dz16, st);
 
-  // 3. data gradients: dh = dy W2, [dg | du] = SwiGLU', dx_perm = dg W1 + du W3,
-  //    dx = sum over slots + dlogits Wr
+  // 3. data gradients: dh = dy W2; SwiGLU: [dg | du] = SwiGLU', dx_perm =
+  //    dg W1 + du W3; SiLU-MLP: da = dh silu'(a), dx_perm = da W1; the shared
+  //    experts' part of dx (below); dx = sum over slots + dlogits Wr (+ shared)
   launch_transpose_batched(w.w2, E, d, F, w2T, (int64_t)F * d, st);
-  launch_transpose_batched(w.w1, E, F, d, w13T, (int64_t)2 * d * F, st);
-  launch_transpose_batched(w.w3, E, F, d, w13T + (size_t)d * F * 2, (int64_t)2 * d * F, st);
+  const int64_t w13_stride = (int64_t)(swiglu ? 2 : 1) * d * F;
+  launch_transpose_batched(w.w1, E, F, d, w13T, w13_stride, st);
+  if (swiglu)
+    launch_transpose_batched(w.w3, E, F, d, w13T + (size_t)d * F * 2, w13_stride, st);
   launch_transpose_batched(w.w_router, 1, E, d, wrT, (int64_t)d * E, st);
   q = plain_problem(dy, M, d, w2T, E, F, offsets, E, M, F, dh, 0, sc.err);
   q.use_pairs = pairs_pay(c);
   MOE_TRY(tc_run(q, st));
-  launch_swiglu_backward(dh, g, u, dgu, offsets, E, F, ns, st);
-  q = plain_problem(dgu, M, 2 * F, w13T, E, d, offsets, E, M, d, dxp, 0, sc.err);
-  q.k_sub = F;
-  q.n_sub = 2;
+  launch_swiglu_backward(dh, g, swiglu ? u : nullptr, dgu, offsets, E, 0, F, ns, st);
+  q = plain_problem(dgu, M, swiglu ? 2 * F : F, w13T, E, d, offsets, E, M, d, dxp, 0, sc.err);
+  if (swiglu) {
+    q.k_sub = F;
+    q.n_sub = 2;
+  }
   q.use_pairs = pairs_pay(c);
   MOE_TRY(tc_run(q, st));
   q = plain_problem(dz16, N, E, wrT, 1, d, nullptr, 1, N, d, dxr, 1, sc.err);
   MOE_TRY(tc_run(q, st));
-  launch_dx_reduce(dxp, ros, dxr, N, k, d, gr.dx, ns, st);
+  if (SF > 0) {
+    // shared experts: one SwiGLU of width S*Fs over all tokens, weight one,
+    // so its output gradient is dout itself.  gs = x Ws1^T, us = x Ws3^T,
+    // hs = silu(gs) us; dhs = dout Ws2 (Ws2 [S, d, Fs] transposed to the
+    // K-major [S*Fs, d]); [dgs | dus]; dxs = dgs Ws1 + dus Ws3
+    char* gs = at<char>(ws, B.gs);
+    char* us = at<char>(ws, B.us);
+    char* hs = at<char>(ws, B.hs);
+    char* dhs = at<char>(ws, B.dhs);
+    char* dgus = at<char>(ws, B.dgus);
+    char* ws13T = at<char>(ws, B.ws13T);
+    char* ws2T = at<char>(ws, B.ws2T);
+    const int Fs = c.d_ff_shared;
+    q = plain_problem(x, N, d, w.ws1, 1, SF, nullptr, 1, N, SF, gs, 0, sc.err);
+    q.use_pairs = N >= 128;
+    MOE_TRY(tc_run(q, st));
+    q.B0 = w.ws3;
+    q.C = us;
+    MOE_TRY(tc_run(q, st));
+    launch_silu_mul(gs, us, hs, nullptr, 0, N, SF, ns, st);
+    launch_transpose_batched(w.ws2, S, d, Fs, ws2T, (int64_t)Fs * d, st);
+    q = plain_problem(dout, N, d, ws2T, 1, SF, nullptr, 1, N, SF, dhs, 0, sc.err);
+    q.use_pairs = N >= 128;
+    MOE_TRY(tc_run(q, st));
+    launch_swiglu_backward(dhs, gs, us, dgus, nullptr, 0, N, SF, ns, st);
+    launch_transpose_batched(w.ws1, 1, SF, d, ws13T, (int64_t)d * SF, st);
+    launch_transpose_batched(w.ws3, 1, SF, d, ws13T + (size_t)d * SF * 2, (int64_t)d * SF, st);
+    q = plain_problem(dgus, N, 2 * SF, ws13T, 1, d, nullptr, 1, N, d, dxs, 1, sc.err);
+    q.k_sub = SF;
+    q.n_sub = 2;
+    q.use_pairs = N >= 128;
+    MOE_TRY(tc_run(q, st));
+  }
+  launch_dx_reduce(dxp, ros, dxr, dxs, N, k, d, gr.dx, ns, st);
 
   // 4. weight gradients over each expert's rows (transposed, zero-padded)
   launch_pad_offsets(offsets, M, E, koff, st);
   launch_transpose_grouped(x_perm, d, offsets, M, E, koff, B.kt, xpT, st);
   launch_transpose_grouped(dy, d, offsets, M, E, koff, B.kt, dyT, st);
   launch_transpose_grouped(h, F, offsets, M, E, koff, B.kt, hT, st);
-  launch_transpose_grouped(dgu, 2 * F, offsets, M, E, koff, B.kt, dguT, st);
+  launch_transpose_grouped(dgu, swiglu ? 2 * F : F, offsets, M, E, koff, B.kt, dguT, st);
   MOE_TRY(wgrad_run(dyT, d, hT, F, B.kt, koff, E, gr.d_w2, sc.err, st));
   MOE_TRY(wgrad_run(dguT, F, xpT, d, B.kt, koff, E, gr.d_w1, sc.err, st));
-  MOE_TRY(wgrad_run(dguT + (size_t)F * B.kt * 2, F, xpT, d, B.kt, koff, E, gr.d_w3, sc.err,
-                    st));
+  if (swiglu)
+    MOE_TRY(wgrad_run(dguT + (size_t)F * B.kt * 2, F, xpT, d, B.kt, koff, E, gr.d_w3, sc.err,
+                      st));
+  if (c.has_bias) {
+    // db1[e] = sum of da, db2[e] = sum of dy over expert e's rows
+    launch_group_sums(dgu, F, offsets, E, F, gr.d_b1, st);
+    launch_group_sums(dy, d, offsets, E, d, gr.d_b2, st);
+  }
   // router: d_w_router = dlogits^T x over all tokens (one group)
   launch_pad_offsets(nullptr, N, 1, koff_n, st);
   launch_transpose_grouped(dz16, E, nullptr, N, 1, koff_n, B.nt, dzT, st);
   launch_transpose_grouped(x, d, nullptr, N, 1, koff_n, B.nt, xT, st);
   MOE_TRY(wgrad_run(dzT, E, xT, d, B.nt, koff_n, 1, gr.d_w_router, sc.err, st));
   if (gr.d_b_router != nullptr) launch_column_sums(dz, N, E, gr.d_b_router, st);
+  if (SF > 0) {
+    // shared: dWs2[s] = dout^T hs[:, s], dWs1 = dgs^T x, dWs3 = dus^T x, all
+    // tokens one group
+    char* doutT = at<char>(ws, B.doutT);
+    char* hsT = at<char>(ws, B.hsT);
+    char* dgusT = at<char>(ws, B.dgusT);
+    const int Fs = c.d_ff_shared;
+    launch_transpose_grouped(dout, d, nullptr, N, 1, koff_n, B.nt, doutT, st);
+    launch_transpose_grouped(at<char>(ws, B.hs), SF, nullptr, N, 1, koff_n, B.nt, hsT, st);
+    launch_transpose_grouped(at<char>(ws, B.dgus), 2 * SF, nullptr, N, 1, koff_n, B.nt, dgusT,
+                             st);
+    for (int sx = 0; sx < S; ++sx)
+      MOE_TRY(wgrad_run(doutT, d, hsT + (size_t)sx * Fs * B.nt * 2, Fs, B.nt, koff_n, 1,
+                        gr.d_ws2 + (size_t)sx * d * Fs, sc.err, st));
+    MOE_TRY(wgrad_run(dgusT, SF, xT, d, B.nt, koff_n, 1, gr.d_ws1, sc.err, st));
+    MOE_TRY(wgrad_run(dgusT + (size_t)SF * B.nt * 2, SF, xT, d, B.nt, koff_n, 1, gr.d_ws3,
+                      sc.err, st));
+  }
   return last_cuda();
 }
 
@@ -1185,13 +1274,11 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (grads == nullptr || !std::isfinite(d_balance)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(ws, ws_bytes, bw_layout_of(c).total));
   if (c.n_tokens == 0) return MOE_ERR_UNSUPPORTED;
-  MOE_TRY(need({x, dout, grads->dx, grads->d_w_router, grads->d_w1, grads->d_w3,
-                grads->d_w2}));
+  MOE_TRY(need({x, dout, grads->dx, grads->d_w_router, grads->d_w1, grads->d_w2}));
+  if (c.expert == MOE_EXPERT_SWIGLU) MOE_TRY(need({grads->d_w3}));
+  if (c.has_bias) MOE_TRY(need({grads->d_b1, grads->d_b2}));
+  if (c.n_shared > 0) MOE_TRY(need({grads->d_ws1, grads->d_ws3, grads->d_ws2}));
   MOE_TRY(maybe({grads->d_b_router}));
-  for (const void* q : {x, dout, (const void*)grads->dx, (const void*)grads->d_w_router,
-                        (const void*)grads->d_w1, (const void*)grads->d_w3,
-                        (const void*)grads->d_w2})
-    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (grads->d_b_router != nullptr && weights->b_router == nullptr) return MOE_ERR_INVALID_ARG;
   return backward_impl(c, x, *weights, dout, d_balance, *grads, ws,
                        static_cast<cudaStream_t>(stream));
@@ -1252,6 +1339,6 @@ const char* moe_status_string(moe_status_t s) {
   }
 }
 
-int32_t moe_version(void) { return 100; }
+int32_t moe_version(void) { return 200; }
 
 }  // extern "C"

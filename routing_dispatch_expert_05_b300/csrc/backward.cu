@@ -12,6 +12,10 @@
 //   balance term:  p (g - <p, g>) (softmax), or through s / sum s (sigmoid),
 //                  g_e = d_balance * coef * count_e / N^2
 //   SwiGLU:        dg = dh u silu'(g), du = dh silu(g)
+//   SiLU-MLP:      da = dh silu'(a), a = W1 x + b1; db1 = sum of da, db2 = sum
+//                  of dy over each expert's rows
+//   shared experts (weight 1): the SwiGLU terms with dy = dout, one group of
+//                  all tokens
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -134,46 +138,68 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
-// h = silu(g) * u for the kept rows (offsets[E] rows of F), 8 per thread
+// h = silu(g) * u (SwiGLU) or h = silu(g) (u null: SiLU-MLP, g = W1 x + b1)
+// for the kept rows (offsets[E] rows of F; `rows` when offsets is null), 8
+// per thread
 __global__ void silu_mul_kernel(const bf16* __restrict__ g, const bf16* __restrict__ u,
                                 bf16* __restrict__ h, const int32_t* __restrict__ offsets,
-                                int n_experts, int F) {
-  const int64_t n8 = (int64_t)offsets[n_experts] * F / 8;
+                                int n_experts, int64_t rows, int F) {
+  const int64_t n8 = (offsets ? (int64_t)offsets[n_experts] : rows) * F / 8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     float gv[8], uv[8], hv[8];
     unpack8(ld_vec16_nc(g + 8 * i), gv);
-    unpack8(ld_vec16_nc(u + 8 * i), uv);
+    if (u != nullptr) unpack8(ld_vec16_nc(u + 8 * i), uv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) hv[j] = gv[j] * sigmoid_fast(gv[j]) * uv[j];
+    for (int j = 0; j < 8; ++j)
+      hv[j] = gv[j] * sigmoid_fast(gv[j]) * (u != nullptr ? uv[j] : 1.f);
     st_vec16(h + 8 * i, pack8(hv));
   }
 }
 
-// dgu[r] = [dg | du]: dg = dh u silu'(g), du = dh silu(g); 8 per thread
+// SwiGLU: dgu[r] = [dg | du] (row stride 2F), dg = dh u silu'(g),
+// du = dh silu(g).  SiLU-MLP (u null): dgu[r] = da (row stride F),
+// da = dh silu'(a) with a = g.  Rows as in silu_mul_kernel; 8 per thread.
 __global__ void swiglu_backward_kernel(const bf16* __restrict__ dh, const bf16* __restrict__ g,
                                        const bf16* __restrict__ u, bf16* __restrict__ dgu,
                                        const int32_t* __restrict__ offsets, int n_experts,
-                                       int F) {
-  const int64_t n8 = (int64_t)offsets[n_experts] * F / 8;
+                                       int64_t rows, int F) {
+  const int64_t n8 = (offsets ? (int64_t)offsets[n_experts] : rows) * F / 8;
   const int f8 = F / 8;
+  const int ld = u != nullptr ? 2 * F : F;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / f8;
     const int f = (int)(i - r * f8) * 8;
     float gv[8], uv[8], dv[8], dg[8], du[8];
     unpack8(ld_vec16_nc(g + 8 * i), gv);
-    unpack8(ld_vec16_nc(u + 8 * i), uv);
+    if (u != nullptr) unpack8(ld_vec16_nc(u + 8 * i), uv);
     unpack8(ld_vec16_nc(dh + 8 * i), dv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float sg = sigmoid_fast(gv[j]);
-      dg[j] = dv[j] * uv[j] * sg * (1.f + gv[j] * (1.f - sg));
+      const float dsilu = sg * (1.f + gv[j] * (1.f - sg));
+      dg[j] = dv[j] * (u != nullptr ? uv[j] : 1.f) * dsilu;
       du[j] = dv[j] * gv[j] * sg;
     }
-    st_vec16(dgu + r * 2 * F + f, pack8(dg));
-    st_vec16(dgu + r * 2 * F + F + f, pack8(du));
+    st_vec16(dgu + r * ld + f, pack8(dg));
+    if (u != nullptr) st_vec16(dgu + r * ld + F + f, pack8(du));
   }
+}
+
+// out[g, c] = sum over rows offsets[g] .. offsets[g+1] of in[row, c] (bf16
+// in, fp32 out): the bias gradients.  One thread per column, the rows of a
+// group in order, so the sums are the same run to run.
+__global__ void __launch_bounds__(256)
+group_sums_kernel(const bf16* __restrict__ in, int64_t ld, const int32_t* __restrict__ offsets,
+                  int C, float* __restrict__ out) {
+  const int g = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  const int64_t r0 = offsets[g], r1 = offsets[g + 1];
+  float acc = 0.f;
+  for (int64_t r = r0; r < r1; ++r) acc += __bfloat162float(in[r * ld + c]);
+  out[(int64_t)g * C + c] = acc;
 }
 
 // ---------------------------------------------------------------- combine
@@ -316,8 +342,8 @@ router_backward_kernel(const float* __restrict__ logits, const int32_t* __restri
 // thread
 __global__ void __launch_bounds__(256)
 dx_reduce_kernel(const bf16* __restrict__ dxp, const int32_t* __restrict__ row_of_slot,
-                 const float* __restrict__ dxr, int64_t n_tokens, int top_k, int d,
-                 float* __restrict__ dx) {
+                 const float* __restrict__ dxr, const float* __restrict__ dxs,
+                 int64_t n_tokens, int top_k, int d, float* __restrict__ dx) {
   for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
     for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
       float acc[8];
@@ -325,6 +351,12 @@ dx_reduce_kernel(const bf16* __restrict__ dxp, const int32_t* __restrict__ row_o
       const float4 a0 = xr[0], a1 = xr[1];
       acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
       acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+      if (dxs != nullptr) {                          // the shared experts' part
+        const float4* xs = reinterpret_cast<const float4*>(dxs + t * d + c);
+        const float4 s0 = xs[0], s1 = xs[1];
+        acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+        acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+      }
       for (int j = 0; j < top_k; ++j) {
         const int r = row_of_slot[t * top_k + j];
         if (r < 0) continue;
@@ -385,18 +417,26 @@ void launch_transpose_batched(const void* in, int batch, int rows, int cols, voi
 }
 
 void launch_silu_mul(const void* g, const void* u, void* h, const int32_t* offsets,
-                     int n_experts, int F, int num_sms, cudaStream_t st) {
+                     int n_experts, int64_t rows, int F, int num_sms, cudaStream_t st) {
   silu_mul_kernel<<<num_sms * 8, 256, 0, st>>>(static_cast<const bf16*>(g),
                                                static_cast<const bf16*>(u),
-                                               static_cast<bf16*>(h), offsets, n_experts, F);
+                                               static_cast<bf16*>(h), offsets, n_experts, rows,
+                                               F);
 }
 
 void launch_swiglu_backward(const void* dh, const void* g, const void* u, void* dgu,
-                            const int32_t* offsets, int n_experts, int F, int num_sms,
-                            cudaStream_t st) {
+                            const int32_t* offsets, int n_experts, int64_t rows, int F,
+                            int num_sms, cudaStream_t st) {
   swiglu_backward_kernel<<<num_sms * 8, 256, 0, st>>>(
       static_cast<const bf16*>(dh), static_cast<const bf16*>(g), static_cast<const bf16*>(u),
-      static_cast<bf16*>(dgu), offsets, n_experts, F);
+      static_cast<bf16*>(dgu), offsets, n_experts, rows, F);
+}
+
+void launch_group_sums(const void* in, int64_t ld, const int32_t* offsets, int G, int C,
+                       float* out, cudaStream_t st) {
+  if (G <= 0 || C <= 0) return;
+  const dim3 grid((unsigned)((C + 255) / 256), (unsigned)G);
+  group_sums_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), ld, offsets, C, out);
 }
 
 void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
@@ -433,12 +473,12 @@ void launch_router_backward(const float* logits, const int32_t* idx, const float
 }
 
 void launch_dx_reduce(const void* dxp, const int32_t* row_of_slot, const float* dxr,
-                      int64_t n_tokens, int top_k, int d, float* dx, int num_sms,
-                      cudaStream_t st) {
+                      const float* dxs, int64_t n_tokens, int top_k, int d, float* dx,
+                      int num_sms, cudaStream_t st) {
   if (n_tokens <= 0) return;
   const int blocks = (int)std::min<int64_t>(n_tokens, (int64_t)num_sms * 8);
   dx_reduce_kernel<<<blocks, 256, 0, st>>>(static_cast<const bf16*>(dxp), row_of_slot, dxr,
-                                           n_tokens, top_k, d, dx);
+                                           dxs, n_tokens, top_k, d, dx);
 }
 
 }  // namespace moe

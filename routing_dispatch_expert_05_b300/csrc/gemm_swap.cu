@@ -154,6 +154,10 @@ __device__ __forceinline__ void silu_bias_chunk(const Params& p, const Tile& tl,
 // token columns c0 .. c0 + 15; the warp's 32 lanes are one exponent block.
 __device__ __forceinline__ void compact_chunk(const Params& p, const Tile& tl, int lane, int q,
                                               int c0, const uint32_t (&r)[16]) {
+  // n_out is a multiple of 32, so a warp's block of features lies wholly
+  // inside or wholly past it; past it there is nothing to write (not even
+  // the exponent byte, which would land on the next row's)
+  if (tl.fb * kWRows + q * 32 >= p.n_out) return;
   const int f = tl.fb * kWRows + q * 32 + lane;
   const bool f_ok = f < p.n_out;
   const float b = (p.bias && f_ok)

@@ -210,11 +210,17 @@ void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int
 // out[b][c][r] = in[b][r][c] (bf16), batch b of the output at out + b * out_stride
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
                               int64_t out_stride, cudaStream_t st);
+// rows: offsets[E] (offsets non-null) or `rows`; u null selects the SiLU-MLP
+// forms (h = silu(g); da = dh silu'(g), row stride F)
 void launch_silu_mul(const void* g, const void* u, void* h, const int32_t* offsets,
-                     int n_experts, int F, int num_sms, cudaStream_t st);
+                     int n_experts, int64_t rows, int F, int num_sms, cudaStream_t st);
 void launch_swiglu_backward(const void* dh, const void* g, const void* u, void* dgu,
-                            const int32_t* offsets, int n_experts, int F, int num_sms,
-                            cudaStream_t st);
+                            const int32_t* offsets, int n_experts, int64_t rows, int F,
+                            int num_sms, cudaStream_t st);
+// out[g, c] = sum of in[r, c] over the rows of group g (bf16 in, row stride
+// ld; fp32 out [G, C]); fixed order
+void launch_group_sums(const void* in, int64_t ld, const int32_t* offsets, int G, int C,
+                       float* out, cudaStream_t st);
 void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
                              const float* w, const void* dout, int64_t n_tokens, int top_k,
                              int d, float* dw, void* dy, int num_sms, cudaStream_t st);
@@ -222,9 +228,10 @@ void launch_router_backward(const float* logits, const int32_t* idx, const float
                             const float* dw, const int32_t* counts, int64_t n_tokens, int E,
                             int k, int mode, float coef, float d_balance, float* dz,
                             void* dz16 /* nullable bf16 copy */, cudaStream_t st);
+// dx = dxr (+ dxs, nullable) + the token's kept rows of dxp
 void launch_dx_reduce(const void* dxp, const int32_t* row_of_slot, const float* dxr,
-                      int64_t n_tokens, int top_k, int d, float* dx, int num_sms,
-                      cudaStream_t st);
+                      const float* dxs, int64_t n_tokens, int top_k, int d, float* dx,
+                      int num_sms, cudaStream_t st);
 // d_b_router[e] = sum_t dz[t, e] (fixed-order tree per expert)
 void launch_column_sums(const float* dz, int64_t n_tokens, int E, float* out, cudaStream_t st);
 

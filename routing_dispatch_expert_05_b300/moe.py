@@ -65,7 +65,8 @@ class MoEStats(ctypes.Structure):
 
 class MoEGrads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("dx", "d_w_router", "d_b_router", "d_w1",
-                                               "d_w3", "d_w2")]
+                                               "d_w3", "d_w2", "d_b1", "d_b2", "d_ws1",
+                                               "d_ws3", "d_ws2")]
 
 
 _lib = None
@@ -329,9 +330,10 @@ def backward_workspace_size(cfg: MoEConfig) -> int:
     return n.value
 
 
-def make_grads(dx, d_w_router, d_w1, d_w3, d_w2, d_b_router=None) -> MoEGrads:
+def make_grads(dx, d_w_router, d_w1, d_w2, d_w3=None, d_b_router=None, d_b1=None,
+               d_b2=None, d_ws1=None, d_ws3=None, d_ws2=None) -> MoEGrads:
     return MoEGrads(ptr(dx), ptr(d_w_router), ptr(d_b_router), ptr(d_w1), ptr(d_w3),
-                    ptr(d_w2))
+                    ptr(d_w2), ptr(d_b1), ptr(d_b2), ptr(d_ws1), ptr(d_ws3), ptr(d_ws2))
 
 
 def moe_backward(cfg, x, weights: MoEWeights, dout, d_balance, grads: MoEGrads, ws,

@@ -155,28 +155,40 @@ def test_bias_update_rejects_bad_arguments(lib):
 
 
 def test_backward_rejects_unsupported_layers(lib):
-    """fp32 layers, SiLU-MLP experts and shared experts get
-    MOE_ERR_UNSUPPORTED before anything is enqueued (no GPU needed)."""
+    """fp32 layers and widths the tensor-core backward does not tile (d, F or
+    Fs not a multiple of 64, E not a multiple of 8) get MOE_ERR_UNSUPPORTED
+    before anything is enqueued; a supported layer with a gradient output
+    missing (d_w3 of SwiGLU, d_b1 / d_b2 with expert biases, the shared
+    experts' gradients) gets MOE_ERR_INVALID_ARG (no GPU needed)."""
     buf = ctypes.create_string_buffer(4096)
     addr = (ctypes.addressof(buf) + 255) // 256 * 256
     w = M.MoEWeights()
     g = M.MoEGrads()
-    for name in ("toy_top2_fp32", "capacity_top2_bf16", "deepseek_v3_block"):
-        cfg = M.make_config(W.WORKLOADS[name])
+    bf = W.WORKLOADS["capacity_top2_bf16"]
+    for shape in (W.WORKLOADS["toy_top2_fp32"], bf.replace(d_model=72),
+                  bf.replace(d_ff=96), bf.replace(n_experts=4),
+                  W.WORKLOADS["deepseek_v3_block"].replace(d_ff_shared=96)):
+        cfg = M.make_config(shape)
         st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(w), addr, 0.0,
                               ctypes.byref(g), addr, 1 << 20, None)
-        assert st == M.MOE_ERR_UNSUPPORTED, name
-    cfg = M.make_config(W.WORKLOADS["qwen3_moe"])
-    n = ctypes.c_size_t()
-    assert lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0
-    fw = ctypes.c_size_t()
-    lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(fw))
-    assert n.value > fw.value
-    # missing gradient outputs
-    w.w_router = w.w1 = w.w3 = w.w2 = addr
-    st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(w), addr, 0.0,
-                          ctypes.byref(g), addr, n.value, None)
-    assert st == M.MOE_ERR_INVALID_ARG
+        assert st == M.MOE_ERR_UNSUPPORTED, shape
+    full = dict(dx=addr, d_w_router=addr, d_w1=addr, d_w3=addr, d_w2=addr, d_b1=addr,
+                d_b2=addr, d_ws1=addr, d_ws3=addr, d_ws2=addr)
+    cases = [("qwen3_moe", "d_w3"), ("capacity_top2_bf16", "d_b1"),
+             ("capacity_top2_bf16", "d_b2"), ("deepseek_v3_block", "d_ws2")]
+    for name, missing in cases:
+        cfg = M.make_config(W.WORKLOADS[name])
+        n = ctypes.c_size_t()
+        assert lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0
+        fw = ctypes.c_size_t()
+        lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(fw))
+        assert n.value > fw.value
+        ww = M.MoEWeights(w_router=addr, w1=addr, w3=addr, w2=addr, b1=addr, b2=addr,
+                          ws1=addr, ws3=addr, ws2=addr, sel_bias=addr)
+        gg = M.MoEGrads(**{k: (None if k == missing else v) for k, v in full.items()})
+        st = lib.moe_backward(ctypes.byref(cfg), addr, ctypes.byref(ww), addr, 0.0,
+                              ctypes.byref(gg), addr, n.value, None)
+        assert st == M.MOE_ERR_INVALID_ARG, (name, missing)
 
 
 def test_wait_check_rejects_bad_arguments(lib):

@@ -52,11 +52,34 @@ def _lib():
     torch.cuda.init()
 
 
-def _shape(route, N=256, E=16, k=4, d=256, F=128, cf=0.0, router_bias="normal", seed=21):
+def _shape(route, N=256, E=16, k=4, d=256, F=128, cf=0.0, router_bias="normal", seed=21,
+           expert=W.EXPERT_SWIGLU, has_bias=False, n_shared=0, d_ff_shared=0):
     return W.MoEShape(name="bwd", n_tokens=N, d_model=d, n_experts=E, top_k=k, d_ff=F,
-                      expert=W.EXPERT_SWIGLU, route=route, dtype=W.DTYPE_BF16,
+                      expert=expert, route=route, dtype=W.DTYPE_BF16, has_bias=has_bias,
                       router_bias=router_bias, sel_bias_range=0.1, capacity_factor=cf,
-                      balance_coef=0.01, seed=seed)
+                      n_shared=n_shared, d_ff_shared=d_ff_shared, balance_coef=0.01, seed=seed)
+
+
+def _grad_buffers(shape, inp):
+    """NaN-filled fp32 gradient outputs for every parameter the layer has."""
+    N, d, E, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.d_ff
+    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
+    g = dict(dx=z(N, d), d_w_router=z(E, d), d_w1=z(E, F, d), d_w2=z(E, d, F))
+    if shape.expert == W.EXPERT_SWIGLU:
+        g["d_w3"] = z(E, F, d)
+    if shape.has_bias:
+        g["d_b1"] = z(E, F)
+        g["d_b2"] = z(E, d)
+    if shape.n_shared > 0:
+        S, Fs = shape.n_shared, shape.d_ff_shared
+        g.update(d_ws1=z(S, Fs, d), d_ws3=z(S, Fs, d), d_ws2=z(S, d, Fs))
+    if "b_router" in inp.values:
+        g["d_b_router"] = z(E)
+    return g
+
+
+GRAD_NAMES = ("dx", "d_w_router", "d_b_router", "d_w1", "d_w3", "d_w2", "d_b1", "d_b2",
+              "d_ws1", "d_ws3", "d_ws2")
 
 
 def _run(shape, d_balance, dout_seed=3):
@@ -68,10 +91,7 @@ def _run(shape, d_balance, dout_seed=3):
     dout = np.random.default_rng(dout_seed).standard_normal((N, d)).astype(np.float32)
     dout = W.bits_to_f32(W.bf16_bits(dout))              # exactly representable in bf16
     dout_t = torch.from_numpy(dout).to(torch.bfloat16).cuda()
-    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
-    g = dict(dx=z(N, d), d_w_router=z(E, d), d_w1=z(E, F, d), d_w3=z(E, F, d), d_w2=z(E, d, F))
-    if "b_router" in inp.values:
-        g["d_b_router"] = z(E)
+    g = _grad_buffers(shape, inp)
     grads = M.make_grads(**g)
     ws = M.MoEWorkspace(cfg, backward=True)
     M.moe_backward(cfg, t["x"], weights, dout_t, d_balance, grads, ws)
@@ -94,7 +114,18 @@ CASES = [(W.ROUTE_SOFTMAX_TOPK, {}), (W.ROUTE_TOPK_SOFTMAX, dict(E=64, k=6)),
          (W.ROUTE_SIGMOID_BIAS, dict(E=32, k=3, router_bias="none")),
          (W.ROUTE_SOFTMAX_TOPK, dict(E=8, k=2, cf=1.0, N=320)),
          # enough rows per expert for the CTA-pair GEMMs
-         (W.ROUTE_TOPK_SOFTMAX, dict(N=2048))]
+         (W.ROUTE_TOPK_SOFTMAX, dict(N=2048)),
+         # SiLU-MLP experts with biases ("Expert Networks", In[7]), with a
+         # capacity that drops; and without biases
+         (W.ROUTE_SOFTMAX_TOPK, dict(E=8, k=2, N=320, cf=1.25, expert=W.EXPERT_SILU_MLP,
+                                     has_bias=True)),
+         (W.ROUTE_TOPK_SOFTMAX, dict(E=16, k=4, expert=W.EXPERT_SILU_MLP)),
+         # shared SwiGLU experts beside sigmoid routing ("DeepSeek 5.7", s.4),
+         # one and two of them, CTA pairs for the latter
+         (W.ROUTE_SIGMOID_BIAS, dict(E=16, k=4, router_bias="none", n_shared=1,
+                                     d_ff_shared=128)),
+         (W.ROUTE_SIGMOID_BIAS, dict(E=32, k=6, N=1024, router_bias="none", n_shared=2,
+                                     d_ff_shared=64))]
 
 
 @pytest.mark.parametrize("d_balance", [0.0, 0.7])
@@ -102,10 +133,40 @@ CASES = [(W.ROUTE_SOFTMAX_TOPK, {}), (W.ROUTE_TOPK_SOFTMAX, dict(E=64, k=6)),
 def test_backward_matches_oracle(route, kw, d_balance):
     shape = _shape(route, **kw)
     g, ref, _, _ = _run(shape, d_balance)
-    for name in ("dx", "d_w_router", "d_w1", "d_w3", "d_w2", "d_b_router"):
+    for name in GRAD_NAMES:
         if name not in g:
             continue
         assert_grad_close(to_np(g[name]), ref[name], name)
+
+
+@pytest.mark.parametrize("k", [2, 8])
+def test_backward_worked_example(k):
+    """"DeepSeek 5.7", Worked example: B = 2, T = 4, top-2 routing, one shared
+    expert; router gradients exist, experts no token selected receive no
+    gradient, and with top-k over every expert the layer is the dense
+    all-expert sum.  At the nearest size the tensor-core backward tiles: d = 64
+    (the page: 16), 8 routed experts (the page: 4), F = Fs = 64; SwiGLU
+    experts, sigmoid routing with a selection bias.  k = 8 is the dense case
+    (every expert selected)."""
+    shape = _shape(W.ROUTE_SIGMOID_BIAS, N=8, E=8, k=k, d=64, F=64, router_bias="none",
+                   n_shared=1, d_ff_shared=64, seed=5)
+    g, ref, _, _ = _run(shape, 0.3)
+    for name in GRAD_NAMES:
+        if name in g:
+            assert_grad_close(to_np(g[name]), ref[name], name)
+    # router gradients exist
+    assert float(g["d_w_router"].abs().max()) > 0
+    # each token has exactly k routed assignments; experts no token chose
+    # receive exact zeros
+    inp = W.make_inputs(shape)
+    idx, _, _ = OB.fixed_route(shape, inp.values)
+    assert idx.shape == (8, k) and all(len(set(r)) == k for r in idx.tolist())
+    unused = sorted(set(range(8)) - set(idx.reshape(-1).tolist()))
+    if k == 2:
+        assert unused, "8 tokens x 2 slots left every expert chosen"
+    for e in unused:
+        for name in ("d_w1", "d_w3", "d_w2"):
+            assert torch.count_nonzero(g[name][e]) == 0, (name, e)
 
 
 def test_backward_unused_expert_gets_zero():
@@ -117,10 +178,9 @@ def test_backward_unused_expert_gets_zero():
     t = M.upload(inp)
     cfg = M.make_config(shape)
     weights = M.make_weights(t)
-    N, d, E, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.d_ff
+    N, d = shape.n_tokens, shape.d_model
     dout = torch.randn(N, d, device="cuda").to(torch.bfloat16)
-    z = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
-    g = dict(dx=z(N, d), d_w_router=z(E, d), d_w1=z(E, F, d), d_w3=z(E, F, d), d_w2=z(E, d, F))
+    g = _grad_buffers(shape, inp)
     ws = M.MoEWorkspace(cfg, backward=True)
     M.moe_backward(cfg, t["x"], weights, dout, 0.0, M.make_grads(**g), ws)
     torch.cuda.synchronize()

@@ -992,3 +992,75 @@ def test_dispatch_room_bit_exact(N, E, k, cf, zipf):
         a, b = run(None), run(rooms[-1])
         for key in a:
             assert torch.equal(a[key], b[key]), key
+
+
+# --------------------------------------------- the pages' worked example
+@pytest.mark.parametrize("k", [2, 4])
+def test_forward_worked_example(k):
+    """"DeepSeek 5.7", Worked example, at its own sizes: B = 2, T = 4,
+    d = 16, four routed SwiGLU experts, top-2 (and top-4: every expert),
+    one shared expert, sigmoid routing with a selection bias.  The output is
+    [2, 4, 16] (one row per token), each token has exactly k routed
+    assignments, and the layer matches the oracle on the GPU's own routing;
+    with k = E it is the dense all-expert sum with weights s_e / sum s."""
+    shape = W.MoEShape(name="worked", n_tokens=8, d_model=16, n_experts=4, top_k=k, d_ff=64,
+                       expert=W.EXPERT_SWIGLU, route=W.ROUTE_SIGMOID_BIAS,
+                       dtype=W.DTYPE_BF16, sel_bias_range=0.1, n_shared=1, d_ff_shared=32,
+                       seed=5)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, st = _forward(D)
+    assert tuple(out.reshape(2, 4, 16).shape) == (2, 4, 16)
+    assert np.array_equal(to_np(st["counts"]).sum(), 8 * k)
+    v = inp.values
+    lg = _gpu_logits(D)
+    i_g, w_g, _ = O.route(lg, shape.route, k, v["sel_bias"])
+    assert all(len(set(r)) == k for r in i_g.tolist())
+    exact = np.zeros((8, 16))
+    for t in range(8):
+        for j in range(k):
+            e = int(i_g[t, j])
+            _, y = O.expert_ffn(v["x"][t:t + 1], v["w1"][e], v["w2"][e], shape.expert,
+                                shape.dtype, w3=v["w3"][e])
+            exact[t] += w_g[t, j] * y[0]
+    exact += O.round_f32(O.shared_ffn(v["x"], v["ws1"], v["ws3"], v["ws2"], shape.dtype))
+    assert_output_close(to_np(out), exact, shape.dtype, "worked example")
+    if k == shape.n_experts:
+        # dense: every expert, weight sigmoid(l_e) / sum over all experts
+        s = O.sigmoid_f32(lg).astype(np.float64)
+        dense = np.zeros((8, 16))
+        for e in range(4):
+            _, y = O.expert_ffn(v["x"], v["w1"][e], v["w2"][e], shape.expert, shape.dtype,
+                                w3=v["w3"][e])
+            dense += (s[:, e] / s.sum(axis=1))[:, None] * y
+        dense += O.round_f32(O.shared_ffn(v["x"], v["ws1"], v["ws3"], v["ws2"], shape.dtype))
+        assert_output_close(to_np(out), dense, shape.dtype, "dense all-expert sum")
+    _check_forward_statistics(D, st, lg, v)
+    assert D.device_error() == M.MOE_OK
+
+
+@pytest.mark.parametrize("d", [64, 96, 160])
+def test_forward_swapped_gemm_feature_tail(d):
+    """A few rows per expert (the swapped-operand GEMMs) with d_model not a
+    multiple of the 128 features a weight tile holds: the tile's last lane
+    quadrants lie past d and must write nothing, neither values nor the
+    compact output's block exponents (which would land on the next row's).
+    Every output against the oracle on the GPU's own routing."""
+    shape = _cfg(n_tokens=40, n_experts=16, top_k=2, d_model=d, d_ff=64,
+                 route=W.ROUTE_TOPK_SOFTMAX, dtype=W.DTYPE_BF16)
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, st = _forward(D)
+    v = inp.values
+    lg = _gpu_logits(D)
+    i_g, w_g, _ = O.route(lg, shape.route, shape.top_k)
+    exact = np.zeros((shape.n_tokens, d))
+    for t in range(shape.n_tokens):
+        for j in range(shape.top_k):
+            e = int(i_g[t, j])
+            _, y = O.expert_ffn(v["x"][t:t + 1], v["w1"][e], v["w2"][e], shape.expert,
+                                shape.dtype, w3=v["w3"][e])
+            exact[t] += w_g[t, j] * y[0]
+    assert_output_close(to_np(out), exact, shape.dtype, f"d={d}")
+    _check_forward_statistics(D, st, lg, v)
+    assert D.device_error() == M.MOE_OK
