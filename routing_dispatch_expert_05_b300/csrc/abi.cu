@@ -902,9 +902,9 @@ struct BwLayout {
   Layout fw;
   int64_t kt, nt;        // columns of the transposed grouped / token operands
   size_t counts, koff, koff_n, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, xpT, dyT, hT,
-      dguT, dzT, xT, w2T, w13T, wrT;
+      dguT, dzT, xT, wrT;
   // shared experts (S * Fs columns, one group of all tokens)
-  size_t gs, us, hs, dhs, dgus, dxs, ws13T, ws2T, doutT, hsT, dgusT, total;
+  size_t gs, us, hs, dhs, dgus, dxs, ws2T, doutT, hsT, dgusT, total;
 };
 
 BwLayout bw_layout_of(const moe_config_t& c) {
@@ -939,8 +939,6 @@ BwLayout bw_layout_of(const moe_config_t& c) {
   B.dguT = take((size_t)2 * F * B.kt * 2);
   B.dzT = take((size_t)E * B.nt * 2);
   B.xT = take((size_t)d * B.nt * 2);
-  B.w2T = take((size_t)E * F * d * 2);
-  B.w13T = take((size_t)E * 2 * d * F * 2);
   B.wrT = take((size_t)d * E * 2);
   const int64_t SF = (int64_t)c.n_shared * c.d_ff_shared;
   if (SF > 0) {
@@ -950,7 +948,6 @@ BwLayout bw_layout_of(const moe_config_t& c) {
     B.dhs = take((size_t)N * SF * 2);
     B.dgus = take((size_t)N * 2 * SF * 2);
     B.dxs = take((size_t)N * d * 4);
-    B.ws13T = take((size_t)2 * d * SF * 2);
     B.ws2T = take((size_t)SF * d * 2);
     B.doutT = take((size_t)d * B.nt * 2);
     B.hsT = take((size_t)SF * B.nt * 2);
@@ -1057,8 +1054,6 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   char* dguT = at<char>(ws, B.dguT);
   char* dzT = at<char>(ws, B.dzT);
   char* xT = at<char>(ws, B.xT);
-  char* w2T = at<char>(ws, B.w2T);
-  char* w13T = at<char>(ws, B.w13T);
   char* wrT = at<char>(ws, B.wrT);
   const int ns = num_sms();
 
@@ -1096,19 +1091,21 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   // 3. data gradients: dh = dy W2; SwiGLU: [dg | du] = SwiGLU', dx_perm =
   //    dg W1 + du W3; SiLU-MLP: da = dh silu'(a), dx_perm = da W1; the shared
   //    experts' part of dx (below); dx = sum over slots + dlogits Wr (+ shared)
-  launch_transpose_batched(w.w2, E, d, F, w2T, (int64_t)F * d, st);
-  const int64_t w13_stride = (int64_t)(swiglu ? 2 : 1) * d * F;
-  launch_transpose_batched(w.w1, E, F, d, w13T, w13_stride, st);
-  if (swiglu)
-    launch_transpose_batched(w.w3, E, F, d, w13T + (size_t)d * F * 2, w13_stride, st);
+  // The expert weights are read in place as MN-major B operands: W2 [E, d, F]
+  // is, per expert, d K-rows of F output columns; W1 / W3 [E, F, d] are F
+  // K-rows of d columns (the two K sub-blocks of [dg | du]).  Only the
+  // router's small [E, d] is transposed (its E K-rows need not fill k-blocks).
   launch_transpose_batched(w.w_router, 1, E, d, wrT, (int64_t)d * E, st);
-  q = plain_problem(dy, M, d, w2T, E, F, offsets, E, M, F, dh, 0, sc.err);
+  q = plain_problem(dy, M, d, w.w2, E, F, offsets, E, M, F, dh, 0, sc.err);
+  q.b_mn_major = 1;
   q.use_pairs = pairs_pay(c);
   MOE_TRY(tc_run(q, st));
   launch_swiglu_backward(dh, g, swiglu ? u : nullptr, dgu, offsets, E, 0, F, ns, st);
-  q = plain_problem(dgu, M, swiglu ? 2 * F : F, w13T, E, d, offsets, E, M, d, dxp, 0, sc.err);
+  q = plain_problem(dgu, M, swiglu ? 2 * F : F, w.w1, E, d, offsets, E, M, d, dxp, 0, sc.err);
+  q.b_mn_major = 1;
+  q.k_sub = F;
   if (swiglu) {
-    q.k_sub = F;
+    q.B1 = w.w3;
     q.n_sub = 2;
   }
   q.use_pairs = pairs_pay(c);
@@ -1125,7 +1122,6 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
     char* hs = at<char>(ws, B.hs);
     char* dhs = at<char>(ws, B.dhs);
     char* dgus = at<char>(ws, B.dgus);
-    char* ws13T = at<char>(ws, B.ws13T);
     char* ws2T = at<char>(ws, B.ws2T);
     const int Fs = c.d_ff_shared;
     q = plain_problem(x, N, d, w.ws1, 1, SF, nullptr, 1, N, SF, gs, 0, sc.err);
@@ -1140,9 +1136,10 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
     q.use_pairs = N >= 128;
     MOE_TRY(tc_run(q, st));
     launch_swiglu_backward(dhs, gs, us, dgus, nullptr, 0, N, SF, ns, st);
-    launch_transpose_batched(w.ws1, 1, SF, d, ws13T, (int64_t)d * SF, st);
-    launch_transpose_batched(w.ws3, 1, SF, d, ws13T + (size_t)d * SF * 2, (int64_t)d * SF, st);
-    q = plain_problem(dgus, N, 2 * SF, ws13T, 1, d, nullptr, 1, N, d, dxs, 1, sc.err);
+    // Ws1 / Ws3 [S*Fs, d] read in place (MN-major: S*Fs K-rows of d columns)
+    q = plain_problem(dgus, N, 2 * SF, w.ws1, 1, d, nullptr, 1, N, d, dxs, 1, sc.err);
+    q.b_mn_major = 1;
+    q.B1 = w.ws3;
     q.k_sub = SF;
     q.n_sub = 2;
     q.use_pairs = N >= 128;

@@ -65,15 +65,18 @@ __device__ __forceinline__ void tile_store_t(const bf16 (*tile)[kTp], int i, bf1
   st_vec16(dst_row0 + (int64_t)c * ld + r8, v);
 }
 
-// out[c, koff[g] + l] = in[off[g] + l, c] for l < m_g, 0 on the padding
+// out[c, koff[g] + l] = in[off[g] + l, c] for l < m_g, 0 on the padding.
+// A block owns 64 padded columns of the output (64 source rows, found once
+// by a binary search over koff) and walks every 64-column tile of C with two
+// tiles in flight (double-buffered shared memory), so the per-block set-up
+// is paid once per 64 rows, not once per 8 KB tile.
 __global__ void __launch_bounds__(256)
 transpose_grouped_kernel(const bf16* __restrict__ in, int C, const int32_t* __restrict__ offsets,
                          int64_t rows, int G, const int32_t* __restrict__ koff,
                          int64_t k_total, bf16* __restrict__ out) {
-  __shared__ __align__(16) bf16 tile[64][kTp];
+  __shared__ __align__(16) bf16 tile[2][64][kTp];
   __shared__ int64_t s_src[64];
   const int64_t pc0 = (int64_t)blockIdx.x * 64;
-  const int c0 = blockIdx.y * 64;
   if (pc0 >= koff[G]) return;
   if (threadIdx.x < 64) {
     const int64_t pc = pc0 + threadIdx.x;
@@ -88,38 +91,66 @@ transpose_grouped_kernel(const bf16* __restrict__ in, int C, const int32_t* __re
     s_src[threadIdx.x] = (pc < koff[G] && l < m) ? o0 + l : -1;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-    const int r = i >> 3, c8 = (i & 7) * 8;
-    const int64_t src = s_src[r];
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (src >= 0 && c0 + c8 < C) v = ld_vec16_nc(in + src * C + c0 + c8);
-    *reinterpret_cast<uint4*>(&tile[r][c8]) = v;
+  // each thread moves 16 bytes of two rows per tile: rows r and r + 32
+  const int r = threadIdx.x >> 3, c8 = (threadIdx.x & 7) * 8;
+  const int64_t src0 = s_src[r], src1 = s_src[r + 32];
+  const int n_ct = (C + 63) / 64;
+  uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+  auto load = [&](int ct) {
+    const int c = ct * 64 + c8;
+    v0 = (src0 >= 0 && c < C) ? ld_vec16_nc(in + src0 * C + c) : make_uint4(0u, 0u, 0u, 0u);
+    v1 = (src1 >= 0 && c < C) ? ld_vec16_nc(in + src1 * C + c) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  load(0);
+  for (int ct = 0; ct < n_ct; ++ct) {
+    bf16 (*t)[kTp] = tile[ct & 1];
+    *reinterpret_cast<uint4*>(&t[r][c8]) = v0;
+    *reinterpret_cast<uint4*>(&t[r + 32][c8]) = v1;
+    if (ct + 1 < n_ct) load(ct + 1);               // the next tile's loads in flight
+    __syncthreads();
+    const int c0 = ct * 64;
+    for (int i = threadIdx.x; i < 64 * 8; i += 256)
+      tile_store_t(t, i, out + (int64_t)c0 * k_total + pc0, k_total, c0 + (i >> 3) < C);
+    // (two buffers: a thread writes this one again only after the next
+    // tile's barrier, which every thread reaches after its reads here)
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 8; i += 256)
-    tile_store_t(tile, i, out + (int64_t)c0 * k_total + pc0, k_total, c0 + (i >> 3) < C);
 }
 
 // out[b][c][r] = in[b][r][c]: batched [rows, cols] -> [cols, rows], output
-// batch b at out + b * out_stride
+// batch b at out + b * out_stride.  A block owns 64 source rows and walks
+// every 64-column tile with the next tile's loads in flight (two shared
+// buffers, one barrier per tile).
 __global__ void __launch_bounds__(256)
 transpose_batched_kernel(const bf16* __restrict__ in, int rows, int cols,
                          bf16* __restrict__ out, int64_t out_stride) {
-  __shared__ __align__(16) bf16 tile[64][kTp];
+  __shared__ __align__(16) bf16 tile[2][64][kTp];
   const int b = blockIdx.z;
-  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const int r0 = blockIdx.y * 64;
   const bf16* src = in + (int64_t)b * rows * cols;
   bf16* dst = out + (int64_t)b * out_stride;
-  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-    const int r = i >> 3, c8 = (i & 7) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r0 + r < rows && c0 + c8 < cols) v = ld_vec16_nc(src + (int64_t)(r0 + r) * cols + c0 + c8);
-    *reinterpret_cast<uint4*>(&tile[r][c8]) = v;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-    const int c = i >> 3, r8 = (i & 7) * 8;
-    tile_store_t(tile, i, dst + (int64_t)c0 * rows + r0, rows, c0 + c < cols && r0 + r8 < rows);
+  const int r = threadIdx.x >> 3, c8 = (threadIdx.x & 7) * 8;
+  const bool ok0 = r0 + r < rows, ok1 = r0 + r + 32 < rows;
+  const int n_ct = (cols + 63) / 64;
+  uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+  auto load = [&](int ct) {
+    const int c = ct * 64 + c8;
+    v0 = (ok0 && c < cols) ? ld_vec16_nc(src + (int64_t)(r0 + r) * cols + c)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    v1 = (ok1 && c < cols) ? ld_vec16_nc(src + (int64_t)(r0 + r + 32) * cols + c)
+                           : make_uint4(0u, 0u, 0u, 0u);
+  };
+  load(0);
+  for (int ct = 0; ct < n_ct; ++ct) {
+    bf16 (*t)[kTp] = tile[ct & 1];
+    *reinterpret_cast<uint4*>(&t[r][c8]) = v0;
+    *reinterpret_cast<uint4*>(&t[r + 32][c8]) = v1;
+    if (ct + 1 < n_ct) load(ct + 1);
+    __syncthreads();
+    const int c0 = ct * 64;
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+      const int c = i >> 3, rr8 = (i & 7) * 8;
+      tile_store_t(t, i, dst + (int64_t)c0 * rows + r0, rows, c0 + c < cols && r0 + rr8 < rows);
+    }
   }
 }
 
@@ -402,7 +433,7 @@ void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int
                               int G, const int32_t* koff, int64_t k_total, void* out,
                               cudaStream_t st) {
   if (k_total <= 0 || C <= 0) return;
-  const dim3 grid((unsigned)(k_total / 64), (unsigned)((C + 63) / 64));
+  const dim3 grid((unsigned)(k_total / 64));
   transpose_grouped_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), C, offsets,
                                                  rows, G, koff, k_total,
                                                  static_cast<bf16*>(out));
@@ -411,7 +442,7 @@ void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
                               int64_t out_stride, cudaStream_t st) {
   if (batch <= 0 || rows <= 0 || cols <= 0) return;
-  const dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64), (unsigned)batch);
+  const dim3 grid(1u, (unsigned)((rows + 63) / 64), (unsigned)batch);
   transpose_batched_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), rows, cols,
                                                  static_cast<bf16*>(out), out_stride);
 }

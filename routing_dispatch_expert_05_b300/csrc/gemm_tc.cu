@@ -103,6 +103,7 @@ struct Params {
   int c_is_f32;
   uint8_t* c_e8;              // compact fp16 output: per (row, 32 columns) exponent
   int e8_cols;                // ceil(n_out / 32)
+  int b_mn;                   // B MN-major (TMA boxes of 64 columns x 64 K-rows)
   int mma_n;                  // MMA N / B rows per tile (single CTA, no SwiGLU):
                               // 256, or n_out rounded up to 16 when a single n-tile
                               // is narrower (the router: N = E)
@@ -540,10 +541,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (!good) { ok = false; break; }
           uint8_t* a = sA + stage * kTileA;
           if (lane == 0) {
-            mbar_expect_tx(&full[stage], kTileA + (uint32_t)p.mma_n * BK * 2);
+            // an MN-major B arrives as 64-column boxes of 8 KB
+            const uint32_t b_bytes = p.b_mn ? (uint32_t)((p.mma_n + 63) / 64) * 8192u
+                                            : (uint32_t)p.mma_n * BK * 2;
+            mbar_expect_tx(&full[stage], kTileA + b_bytes);
             uint8_t* b = sB + stage * kTileB;
             if (!gather) tma_load_2d(a, &tmA, &full[stage], kb * BK, tl.row0);
-            if (!NARROW && p.swiglu) {
+            if (p.b_mn) {
+              // group g, sub-block s: K-rows g*k_sub + kk of B0 / B1
+              const int sub = p.n_sub > 1 ? kb / kb_per_sub : 0;
+              const int kk = (kb - sub * kb_per_sub) * BK;
+              const int krow = tl.g * p.k_sub + kk;
+              for (int pc = 0; pc * 64 < p.mma_n; ++pc)
+                tma_load_2d(b + pc * 8192, sub ? &tmB1 : &tmB0, &full[stage],
+                            tl.n * BN + pc * 64, krow);
+            } else if (!NARROW && p.swiglu) {
               const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
               tma_load_2d(b, &tmB0, &full[stage], kb * BK, brow);
               tma_load_2d(b + kTileB / 2, &tmB1, &full[stage], kb * BK, brow);
@@ -584,7 +596,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, p.mma_n);
+      const uint32_t idesc = idesc_bf16(BM, p.mma_n) | (p.b_mn ? kIdescBMnMajor : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -601,7 +613,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t b0 = smem_u32(sB + stage * kTileB);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
+            umma(d, sdesc_sw128(a0 + kk * 32),
+                 p.b_mn ? sdesc_sw128_mn(b0 + kk * 2048) : sdesc_sw128(b0 + kk * 32), idesc,
                  (kb | kk) != 0);
           umma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -1002,7 +1015,16 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (leader) mbar_expect_tx(&full[stage], 2 * kStageBytes2);
             uint8_t* b = sB + stage * kTileB2;
             if (!gather) tma_load_2d_pair(a, &tmA, bar, kb * BK, tl.row0 + (int)rank * 128);
-            if (p.swiglu) {
+            if (p.b_mn) {
+              // this CTA's 128 columns as two 64-column boxes, K-rows
+              // g*k_sub + kk of B0 / B1
+              const int sub = p.n_sub > 1 ? kb / kb_per_sub : 0;
+              const int kk = (kb - sub * kb_per_sub) * BK;
+              const int krow = tl.g * p.k_sub + kk;
+              const int col = tl.n * BN + (int)rank * 128;
+              tma_load_2d_pair(b, sub ? &tmB1 : &tmB0, bar, col, krow);
+              tma_load_2d_pair(b + 8192, sub ? &tmB1 : &tmB0, bar, col + 64, krow);
+            } else if (p.swiglu) {
               const int brow = tl.g * p.b_rows + tl.n * (BN / 2);
               tma_load_2d_pair(b, rank ? &tmB1 : &tmB0, bar, kb * BK, brow);
             } else {
@@ -1043,7 +1065,7 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer (leader)
     if (leader && lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM2, BN);
+      const uint32_t idesc = idesc_bf16(BM2, BN) | (p.b_mn ? kIdescBMnMajor : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -1060,8 +1082,9 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t b0 = smem_u32(sB + stage * kTileB2);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_pair(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
-                      (kb | kk) != 0);
+            umma_pair(d, sdesc_sw128(a0 + kk * 32),
+                      p.b_mn ? sdesc_sw128_mn(b0 + kk * 2048) : sdesc_sw128(b0 + kk * 32),
+                      idesc, (kb | kk) != 0);
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == kStages2) { stage = 0; phase ^= 1; }
         }
@@ -1184,6 +1207,10 @@ bool tc_gemm_supported(const TcProblem& q) {
   // compact output: one exponent per 32 columns, no SwiGLU pairing
   if (q.c_e8 != nullptr && (q.swiglu || q.e8_cols != (q.n_out + 31) / 32)) return false;
   if (q.c_e8 == nullptr && (q.c_row_map != nullptr || q.c_row_scale != nullptr)) return false;
+  // MN-major B: whole k-blocks per sub-block, not with SwiGLU or a gathered A
+  if (q.b_mn_major && (q.swiglu || q.a_row_map != nullptr || q.k_sub % tc::BK != 0 ||
+                       (q.n_sub > 1 && q.B1 == nullptr)))
+    return false;
   return tc::encode_fn() != nullptr;
 }
 
@@ -1231,6 +1258,7 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.e8_cols = q.e8_cols;
   // a single n-tile narrower than 256 columns multiplies only its own width
   p.mma_n = (!q.swiglu && q.n_out < BN) ? (q.n_out + 15) / 16 * 16 : BN;
+  p.b_mn = q.b_mn_major;
   p.err = q.err;
   p.a_row_map = q.a_row_map;
   p.c_row_map = q.c_row_map;
@@ -1243,6 +1271,16 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
     if (!make_map(ma, q.A, (uint64_t)q.K, (uint64_t)q.a_rows, (uint64_t)q.K * 2,
                   q.a_row_map ? 1u : (uint32_t)BM))
       return false;
+    if (q.b_mn_major) {
+      // [b_groups * k_sub K-rows, n_out columns], boxes of 64 columns x 64 rows
+      const uint64_t krows = (uint64_t)q.b_groups * q.k_sub;
+      if (!make_map(mb0, q.B0, (uint64_t)q.n_out, krows, (uint64_t)q.n_out * 2, 64u))
+        return false;
+      if (q.n_sub > 1)
+        return make_map(mb1, q.B1, (uint64_t)q.n_out, krows, (uint64_t)q.n_out * 2, 64u);
+      *mb1 = *mb0;
+      return true;
+    }
     if (q.swiglu)
       return make_map(mb0, q.B0, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2) &&
              make_map(mb1, q.B1, (uint64_t)ksub, brows_total, (uint64_t)ksub * 2, BN / 2);

@@ -153,6 +153,10 @@ struct TcProblem {
   // c_row_scale[output row] (e.g. the routing weight) before compacting.
   const int32_t* c_row_map;
   const float* c_row_scale;
+  // 1: B is MN-major: group g (sub-block s) is rows g*k_sub .. of B0 (s = 0)
+  // or B1 (s = 1), each row n_out contiguous elements -- e.g. a weight
+  // [E, K, N] used without a transpose.  Not with SwiGLU.
+  int b_mn_major;
 };
 bool tc_gemm_supported(const TcProblem& p);
 bool launch_tc_gemm(const TcProblem& p, int num_sms, cudaStream_t st);

@@ -113,11 +113,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                             // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle, as a
+// TMA box of 64 MN-elements x 64 K-rows lands it: K-rows of 128 bytes, 8-row
+// groups 1024 bytes apart (stride offset), consecutive 64-element MN atoms
+// 8 KB apart (leading offset).  A K-step of 16 moves 16 rows: 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)(8192 >> 4) << 16;                   // leading byte offset: next MN atom
+  d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset: next 8 K-rows
+  d |= (uint64_t)1 << 46;                             // descriptor version
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
+// bit 16 of the instruction descriptor: B is MN-major (transposed)
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b,
                                      uint32_t idesc, uint32_t accumulate) {
   asm volatile(
