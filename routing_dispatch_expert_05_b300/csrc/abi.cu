@@ -32,7 +32,8 @@ struct Layout {
   int chunks;
 };
 
-Layout layout_of(const moe_config_t& c) {
+// extra_rows: room for groups padded past N*k rows (the backward's grouping)
+Layout layout_of(const moe_config_t& c, int64_t extra_rows = 0) {
   Layout L{};
   size_t o = 0;
   auto take = [&o](size_t bytes) {
@@ -57,14 +58,15 @@ Layout layout_of(const moe_config_t& c) {
   L.w = take((size_t)N * k * 4);
   L.offsets = take((size_t)(E + 1) * 4);
   L.row_of_slot = take((size_t)N * k * 4);
-  L.token_of_row = take((size_t)N * k * 4);
-  L.slot_of_row = take((size_t)N * k * 4);
-  L.x_perm = take((size_t)N * k * d * es);
-  L.h = take((size_t)N * k * F * es);
+  const int64_t R = N * k + extra_rows;            // grouped rows
+  L.token_of_row = take((size_t)R * 4);
+  L.slot_of_row = take((size_t)R * 4);
+  L.x_perm = take((size_t)R * d * es);
+  L.h = take((size_t)R * F * es);
   // expert outputs: fp32, or (bf16 layers on the tensor cores) fp16 with an
   // exponent byte per (row, 32-column block) -- either fits here
-  L.y = take((size_t)N * k * d * 4);
-  L.y_e8 = take((size_t)N * k * ceil_div64(d, kYScaleBlock));
+  L.y = take((size_t)R * d * 4);
+  L.y_e8 = take((size_t)R * ceil_div64(d, kYScaleBlock));
   if (c.n_shared > 0) {
     L.h_shared = take((size_t)N * c.n_shared * c.d_ff_shared * es);
     L.shared_out = take((size_t)N * d * 4);
@@ -283,11 +285,12 @@ void router_body(const moe_config_t& c, const void* x, const moe_weights_t& w,
 void dispatch_body(const moe_config_t& c, const int32_t* idx, const void* x,
                    int32_t* offsets, int32_t* ros, int32_t* tor, void* x_perm,
                    moe_stats_t* stats, const Scratch& sc, cudaStream_t st,
-                   int32_t* slot_of_row = nullptr, const int32_t* room = nullptr) {
+                   int32_t* slot_of_row = nullptr, const int32_t* room = nullptr,
+                   int pad = 1, int32_t* kept = nullptr) {
   launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity_of(c), sc.chunk_cnt,
                   sc.chunk_base, offsets, ros, tor, stats ? stats->counts : nullptr,
-                  stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr, sc.err, st,
-                  slot_of_row, room);
+                  kept != nullptr ? kept : (stats ? stats->kept : nullptr),
+                  stats ? stats->dropped : nullptr, sc.err, st, slot_of_row, room, pad);
   if (x_perm != nullptr)
     launch_scatter_rows(x, (int64_t)c.d_model * elem_size(c), ros, c.n_tokens, c.top_k,
                         x_perm, num_sms(), st);
@@ -378,7 +381,8 @@ moe_status_t up_body(const moe_config_t& c, const void* a, const int32_t* row_ma
 moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offsets,
                        const moe_weights_t& w, void* y, uint8_t* y_e8, int32_t* err,
                        cudaStream_t st, const int32_t* slot_of_row = nullptr,
-                       const float* wts = nullptr) {
+                       const float* wts = nullptr, int64_t rows = -1) {
+  if (rows < 0) rows = c.n_tokens * c.top_k;
   GemmProblem p{};
   p.A = h;
   p.B0 = w.w2;
@@ -390,14 +394,14 @@ moe_status_t down_body(const moe_config_t& c, const void* h, const int32_t* offs
   p.c_is_f32 = 1;
   p.offsets = offsets;
   p.n_groups = c.n_experts;
-  p.rows = c.n_tokens * c.top_k;
+  p.rows = rows;
   p.N = c.d_model;
   p.K = c.d_ff;
   p.epilogue = kEpiNone;
   p.is_bf16 = c.dtype == MOE_BF16;
   TcProblem q{};
   q.A = h;
-  q.a_rows = c.n_tokens * c.top_k;
+  q.a_rows = rows;
   q.K = c.d_ff;
   q.B0 = w.w2;
   q.b_groups = c.n_experts;
@@ -898,48 +902,66 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
 // ---- backward -------------------------------------------------------------
 // Buffers of moe_backward after the forward's own layout (which holds the
 // recomputed routing, grouping, x_perm, h and compact y).
+// The backward's grouping pads every expert's rows to whole 16-row slices
+// (zero rows), so the weight-gradient MMAs can stop at a group's end.
+constexpr int kBwPad = 16;
+
+// The router's weight-gradient problem: dWr [E, d] = dlogits^T x over all
+// tokens, one group, K split over CTA pairs (partials in the workspace).
+WgradProblem router_wgrad_problem(const moe_config_t& c, const void* dz16, const void* x,
+                                  float* d_wr, float* partial, int32_t* err) {
+  WgradProblem q{};
+  q.P = dz16;
+  q.p_ld = c.n_experts;
+  q.m_dim = c.n_experts;
+  q.Q = x;
+  q.q_ld = c.d_model;
+  q.n_dim = c.d_model;
+  q.rows = c.n_tokens;
+  q.n_groups = 1;
+  q.C0 = d_wr;
+  q.partial = partial;
+  q.err = err;
+  return q;
+}
+
 struct BwLayout {
-  Layout fw;
-  int64_t kt, nt;        // columns of the transposed grouped / token operands
-  size_t counts, koff, koff_n, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, xpT, dyT, hT,
-      dguT, dzT, xT, wrT;
+  Layout fw;             // grouped buffers with room for the padded rows
+  int64_t rows;          // grouped rows: N*k + (kBwPad - 1) * E
+  size_t counts, kept, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, wrT, part;
   // shared experts (S * Fs columns, one group of all tokens)
-  size_t gs, us, hs, dhs, dgus, dxs, ws2T, doutT, hsT, dgusT, total;
+  size_t gs, us, hs, dhs, dgus, dxs, ws2T, total;
 };
 
 BwLayout bw_layout_of(const moe_config_t& c) {
   BwLayout B{};
-  B.fw = layout_of(c);
+  const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
+  B.rows = N * k + (kBwPad - 1) * E;
+  B.fw = layout_of(c, (kBwPad - 1) * E);
   size_t o = B.fw.total;
   auto take = [&o](size_t bytes) {
     const size_t at = o;
     o = align_up(o + bytes);
     return at;
   };
-  const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
-  const int64_t M = N * k;
-  B.kt = (M + 64 * E + 63) / 64 * 64;                 // every group padded to 64
-  B.nt = (N + 63) / 64 * 64 + 64;
+  const int64_t R = B.rows;
   B.counts = take((size_t)E * 4);
-  B.koff = take((size_t)(E + 1) * 4);
-  B.koff_n = take(2 * 4);
-  B.g = take((size_t)M * F * 2);
-  B.u = take((size_t)M * F * 2);
-  B.dy = take((size_t)M * d * 2);
-  B.dh = take((size_t)M * F * 2);
-  B.dgu = take((size_t)M * 2 * F * 2);
-  B.dxp = take((size_t)M * d * 2);
+  B.kept = take((size_t)E * 4);
+  B.g = take((size_t)R * F * 2);
+  B.u = take((size_t)R * F * 2);
+  B.dy = take((size_t)R * d * 2);
+  B.dh = take((size_t)R * F * 2);
+  B.dgu = take((size_t)R * 2 * F * 2);
+  B.dxp = take((size_t)R * d * 2);
   B.dz = take((size_t)N * E * 4);
   B.dz16 = take((size_t)N * E * 2);
   B.dxr = take((size_t)N * d * 4);
   B.dw = take((size_t)N * k * 4);
-  B.xpT = take((size_t)d * B.kt * 2);
-  B.dyT = take((size_t)d * B.kt * 2);
-  B.hT = take((size_t)F * B.kt * 2);
-  B.dguT = take((size_t)2 * F * B.kt * 2);
-  B.dzT = take((size_t)E * B.nt * 2);
-  B.xT = take((size_t)d * B.nt * 2);
   B.wrT = take((size_t)d * E * 2);
+  B.part = take(std::max<size_t>(
+      4, wgrad_partial_floats(router_wgrad_problem(c, nullptr, nullptr, nullptr, nullptr,
+                                                   nullptr),
+                              num_sms()) * 4));
   const int64_t SF = (int64_t)c.n_shared * c.d_ff_shared;
   if (SF > 0) {
     B.gs = take((size_t)N * SF * 2);
@@ -949,9 +971,6 @@ BwLayout bw_layout_of(const moe_config_t& c) {
     B.dgus = take((size_t)N * 2 * SF * 2);
     B.dxs = take((size_t)N * d * 4);
     B.ws2T = take((size_t)SF * d * 2);
-    B.doutT = take((size_t)d * B.nt * 2);
-    B.hsT = take((size_t)SF * B.nt * 2);
-    B.dgusT = take((size_t)2 * SF * B.nt * 2);
   }
   B.total = o;
   return B;
@@ -999,20 +1018,8 @@ moe_status_t tc_run(const TcProblem& q, cudaStream_t st) {
   return launch_tc_gemm(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status_t wgrad_run(const void* A, int rows_a, const void* B, int rows_b, int64_t k_total,
-                       const int32_t* koff, int groups, float* C, int32_t* err,
-                       cudaStream_t st) {
-  WgradProblem q{};
-  q.A = A;
-  q.B = B;
-  q.rows_a = rows_a;
-  q.rows_b = rows_b;
-  q.k_total = k_total;
-  q.k_offsets = koff;
-  q.n_groups = groups;
-  q.C = C;
-  q.err = err;
-  return launch_tc_wgrad(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
+moe_status_t wgrad_run(const WgradProblem& q, cudaStream_t st) {
+  return launch_wgrad(q, num_sms(), st) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // The backward pass (routing held fixed): the forward's routing, grouping
@@ -1024,7 +1031,7 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   const BwLayout B = bw_layout_of(c);
   const Layout& L = B.fw;
   const Scratch sc = scratch_of(L, ws);
-  const int64_t N = c.n_tokens, M = N * c.top_k;
+  const int64_t N = c.n_tokens, M = B.rows;        // M: grouped rows (padded)
   const int E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
   int32_t* idx = at<int32_t>(ws, L.idx);
   float* wts = at<float>(ws, L.w);
@@ -1036,8 +1043,7 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   void* y = at<char>(ws, L.y);
   uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
   int32_t* counts = at<int32_t>(ws, B.counts);
-  int32_t* koff = at<int32_t>(ws, B.koff);
-  int32_t* koff_n = at<int32_t>(ws, B.koff_n);
+  int32_t* kept = at<int32_t>(ws, B.kept);
   void* g = at<char>(ws, B.g);
   void* u = at<char>(ws, B.u);
   void* dy = at<char>(ws, B.dy);
@@ -1048,12 +1054,6 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   void* dz16 = at<char>(ws, B.dz16);
   float* dxr = at<float>(ws, B.dxr);
   float* dw = at<float>(ws, B.dw);
-  char* xpT = at<char>(ws, B.xpT);
-  char* dyT = at<char>(ws, B.dyT);
-  char* hT = at<char>(ws, B.hT);
-  char* dguT = at<char>(ws, B.dguT);
-  char* dzT = at<char>(ws, B.dzT);
-  char* xT = at<char>(ws, B.xT);
   char* wrT = at<char>(ws, B.wrT);
   const int ns = num_sms();
 
@@ -1061,13 +1061,17 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   const int S = c.n_shared, SF = c.n_shared * c.d_ff_shared;
   float* dxs = SF > 0 ? at<float>(ws, B.dxs) : nullptr;
 
-  // 1. recompute: routing (counts for the balance term), grouping, x_perm,
-  //    SwiGLU: g = x W1^T, u = x W3^T, h = silu(g) u; SiLU-MLP: g = a =
-  //    x W1^T + b1, h = silu(a); y = h W2^T (+ b2) (compact, row order)
+  // 1. recompute: routing (counts for the balance term), grouping (each
+  //    expert's rows padded to whole 16-row slices, the padding zero in
+  //    x_perm and dy), x_perm, SwiGLU: g = x W1^T, u = x W3^T, h = silu(g) u;
+  //    SiLU-MLP: g = a = x W1^T + b1, h = silu(a); y = h W2^T (+ b2)
+  //    (compact, row order)
   moe_stats_t rs{};
   rs.counts = counts;
   router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true);
-  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, nullptr, sc, st);
+  dispatch_body(c, idx, x, offsets, ros, tor, x_perm, nullptr, sc, st, nullptr, nullptr,
+                kBwPad, kept);
+  launch_zero_pad_rows(offsets, kept, E, (int64_t)d * 2, x_perm, dy, st);
   TcProblem q = plain_problem(x_perm, M, d, w.w1, E, F, offsets, E, M, F, g, 0, sc.err);
   q.use_pairs = pairs_pay(c);
   if (!swiglu && c.has_bias) {
@@ -1081,7 +1085,7 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
     MOE_TRY(tc_run(q, st));
   }
   launch_silu_mul(g, swiglu ? u : nullptr, h, offsets, E, 0, F, ns, st);
-  MOE_TRY(down_body(c, h, offsets, w, y, y_e8, sc.err, st));
+  MOE_TRY(down_body(c, h, offsets, w, y, y_e8, sc.err, st, nullptr, nullptr, M));
 
   // 2. combine and router: dw, dy = w dout, dlogits
   launch_combine_backward(y, y_e8, ros, wts, dout, N, k, d, dw, dy, ns, st);
@@ -1147,45 +1151,73 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   }
   launch_dx_reduce(dxp, ros, dxr, dxs, N, k, d, gr.dx, ns, st);
 
-  // 4. weight gradients over each expert's rows (transposed, zero-padded)
-  launch_pad_offsets(offsets, M, E, koff, st);
-  launch_transpose_grouped(x_perm, d, offsets, M, E, koff, B.kt, xpT, st);
-  launch_transpose_grouped(dy, d, offsets, M, E, koff, B.kt, dyT, st);
-  launch_transpose_grouped(h, F, offsets, M, E, koff, B.kt, hT, st);
-  launch_transpose_grouped(dgu, swiglu ? 2 * F : F, offsets, M, E, koff, B.kt, dguT, st);
-  MOE_TRY(wgrad_run(dyT, d, hT, F, B.kt, koff, E, gr.d_w2, sc.err, st));
-  MOE_TRY(wgrad_run(dguT, F, xpT, d, B.kt, koff, E, gr.d_w1, sc.err, st));
-  if (swiglu)
-    MOE_TRY(wgrad_run(dguT + (size_t)F * B.kt * 2, F, xpT, d, B.kt, koff, E, gr.d_w3, sc.err,
-                      st));
+  // 4. weight gradients, read in place: dW2[e] = dy_e^T h_e; [dW1 | dW3][e]
+  //    = [dg | du]_e^T x_e (one launch, rows F.. of each group's output to
+  //    dW3); the router's dWr = dlogits^T x and the shared experts' over all
+  //    tokens as one group
+  WgradProblem wq{};
+  wq.P = dy;
+  wq.p_ld = d;
+  wq.m_dim = d;
+  wq.Q = h;
+  wq.q_ld = F;
+  wq.n_dim = F;
+  wq.rows = M;
+  wq.offsets = offsets;
+  wq.n_groups = E;
+  wq.C0 = gr.d_w2;
+  wq.err = sc.err;
+  MOE_TRY(wgrad_run(wq, st));
+  wq.P = dgu;
+  wq.p_ld = swiglu ? 2 * F : F;
+  wq.m_dim = swiglu ? 2 * F : F;
+  wq.Q = x_perm;
+  wq.q_ld = d;
+  wq.n_dim = d;
+  wq.C0 = gr.d_w1;
+  if (swiglu) {
+    wq.C1 = gr.d_w3;
+    wq.m_split = F;
+  }
+  MOE_TRY(wgrad_run(wq, st));
   if (c.has_bias) {
-    // db1[e] = sum of da, db2[e] = sum of dy over expert e's rows
+    // db1[e] = sum of da, db2[e] = sum of dy over expert e's rows (the
+    // padding rows are zero)
     launch_group_sums(dgu, F, offsets, E, F, gr.d_b1, st);
     launch_group_sums(dy, d, offsets, E, d, gr.d_b2, st);
   }
-  // router: d_w_router = dlogits^T x over all tokens (one group)
-  launch_pad_offsets(nullptr, N, 1, koff_n, st);
-  launch_transpose_grouped(dz16, E, nullptr, N, 1, koff_n, B.nt, dzT, st);
-  launch_transpose_grouped(x, d, nullptr, N, 1, koff_n, B.nt, xT, st);
-  MOE_TRY(wgrad_run(dzT, E, xT, d, B.nt, koff_n, 1, gr.d_w_router, sc.err, st));
+  WgradProblem rq = router_wgrad_problem(c, dz16, x, gr.d_w_router, at<float>(ws, B.part),
+                                         sc.err);
+  rq.partial_floats = wgrad_partial_floats(rq, ns);
+  MOE_TRY(wgrad_run(rq, st));
   if (gr.d_b_router != nullptr) launch_column_sums(dz, N, E, gr.d_b_router, st);
   if (SF > 0) {
-    // shared: dWs2[s] = dout^T hs[:, s], dWs1 = dgs^T x, dWs3 = dus^T x, all
-    // tokens one group
-    char* doutT = at<char>(ws, B.doutT);
-    char* hsT = at<char>(ws, B.hsT);
-    char* dgusT = at<char>(ws, B.dgusT);
+    // shared: dWs2[s] = dout^T hs[:, s], [dWs1 | dWs3] = [dgs | dus]^T x
     const int Fs = c.d_ff_shared;
-    launch_transpose_grouped(dout, d, nullptr, N, 1, koff_n, B.nt, doutT, st);
-    launch_transpose_grouped(at<char>(ws, B.hs), SF, nullptr, N, 1, koff_n, B.nt, hsT, st);
-    launch_transpose_grouped(at<char>(ws, B.dgus), 2 * SF, nullptr, N, 1, koff_n, B.nt, dgusT,
-                             st);
-    for (int sx = 0; sx < S; ++sx)
-      MOE_TRY(wgrad_run(doutT, d, hsT + (size_t)sx * Fs * B.nt * 2, Fs, B.nt, koff_n, 1,
-                        gr.d_ws2 + (size_t)sx * d * Fs, sc.err, st));
-    MOE_TRY(wgrad_run(dgusT, SF, xT, d, B.nt, koff_n, 1, gr.d_ws1, sc.err, st));
-    MOE_TRY(wgrad_run(dgusT + (size_t)SF * B.nt * 2, SF, xT, d, B.nt, koff_n, 1, gr.d_ws3,
-                      sc.err, st));
+    WgradProblem sq{};
+    sq.rows = N;
+    sq.n_groups = 1;
+    sq.err = sc.err;
+    sq.P = dout;
+    sq.p_ld = d;
+    sq.m_dim = d;
+    sq.q_ld = SF;
+    sq.n_dim = Fs;
+    for (int sx = 0; sx < S; ++sx) {
+      sq.Q = at<char>(ws, B.hs) + (size_t)sx * Fs * 2;
+      sq.C0 = gr.d_ws2 + (size_t)sx * d * Fs;
+      MOE_TRY(wgrad_run(sq, st));
+    }
+    sq.P = at<char>(ws, B.dgus);
+    sq.p_ld = 2 * SF;
+    sq.m_dim = 2 * SF;
+    sq.Q = x;
+    sq.q_ld = d;
+    sq.n_dim = d;
+    sq.C0 = gr.d_ws1;
+    sq.C1 = gr.d_ws3;
+    sq.m_split = SF;
+    MOE_TRY(wgrad_run(sq, st));
   }
   return last_cuda();
 }

@@ -1,6 +1,6 @@
 // The layer's backward pass outside the GEMMs: the weighted combine's and the
 // router's gradients, the SwiGLU derivative, the reduction of the expert rows
-// back to tokens, and the layout changes the gradient GEMMs need.
+// back to tokens, and the small layout changes the gradient GEMMs need.
 //
 // The gradient is that of <dout, out> + d_balance * B with the routing held
 // fixed ("DeepSeek 5.7: MoE from scratch", Worked example and study lab: the
@@ -31,17 +31,21 @@ constexpr unsigned kFull = 0xffffffffu;
 __device__ __forceinline__ float sigmoid_fast(float z) { return 1.f / (1.f + __expf(-z)); }
 
 // ---------------------------------------------------------------- layouts
-// koff[g+1] = koff[g] + max(64, 64 * ceil(m_g / 64)): every group's span of
-// the transposed activations is a non-zero number of whole k-blocks.
-__global__ void pad_offsets_kernel(const int32_t* __restrict__ offsets, int64_t rows, int G,
-                                   int32_t* __restrict__ koff) {
-  if (threadIdx.x != 0) return;
-  int acc = 0;
-  koff[0] = 0;
-  for (int g = 0; g < G; ++g) {
-    const int m = offsets ? offsets[g + 1] - offsets[g] : (int)rows;
-    acc += max(64, (m + 63) / 64 * 64);
-    koff[g + 1] = acc;
+// Rows [offsets[e] + kept[e], offsets[e+1]) of buf0 / buf1 set to zero: the
+// rows that round each expert's group up to whole 16-row slices of the
+// weight-gradient MMAs.  One block per expert; at most pad - 1 rows each.
+__global__ void __launch_bounds__(256)
+zero_pad_rows_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ kept,
+                     int64_t row_bytes, uint8_t* __restrict__ buf0, uint8_t* __restrict__ buf1) {
+  const int e = blockIdx.x;
+  const int64_t r0 = (int64_t)offsets[e] + kept[e], r1 = offsets[e + 1];
+  const int64_t n16 = row_bytes / 16;
+  const int64_t total = r1 > r0 ? (r1 - r0) * n16 : 0;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = threadIdx.x; i < total; i += blockDim.x) {
+    const int64_t off = (r0 + i / n16) * row_bytes + (i % n16) * 16;
+    *reinterpret_cast<uint4*>(buf0 + off) = z;
+    if (buf1 != nullptr) *reinterpret_cast<uint4*>(buf1 + off) = z;
   }
 }
 
@@ -63,57 +67,6 @@ __device__ __forceinline__ void tile_store_t(const bf16 (*tile)[kTp], int i, bf1
     w[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
   }
   st_vec16(dst_row0 + (int64_t)c * ld + r8, v);
-}
-
-// out[c, koff[g] + l] = in[off[g] + l, c] for l < m_g, 0 on the padding.
-// A block owns 64 padded columns of the output (64 source rows, found once
-// by a binary search over koff) and walks every 64-column tile of C with two
-// tiles in flight (double-buffered shared memory), so the per-block set-up
-// is paid once per 64 rows, not once per 8 KB tile.
-__global__ void __launch_bounds__(256)
-transpose_grouped_kernel(const bf16* __restrict__ in, int C, const int32_t* __restrict__ offsets,
-                         int64_t rows, int G, const int32_t* __restrict__ koff,
-                         int64_t k_total, bf16* __restrict__ out) {
-  __shared__ __align__(16) bf16 tile[2][64][kTp];
-  __shared__ int64_t s_src[64];
-  const int64_t pc0 = (int64_t)blockIdx.x * 64;
-  if (pc0 >= koff[G]) return;
-  if (threadIdx.x < 64) {
-    const int64_t pc = pc0 + threadIdx.x;
-    int lo = 0, hi = G - 1;                        // largest g with koff[g] <= pc
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (koff[mid] <= pc) lo = mid; else hi = mid - 1;
-    }
-    const int64_t o0 = offsets ? offsets[lo] : 0;
-    const int64_t m = offsets ? offsets[lo + 1] - o0 : rows;
-    const int64_t l = pc - koff[lo];
-    s_src[threadIdx.x] = (pc < koff[G] && l < m) ? o0 + l : -1;
-  }
-  __syncthreads();
-  // each thread moves 16 bytes of two rows per tile: rows r and r + 32
-  const int r = threadIdx.x >> 3, c8 = (threadIdx.x & 7) * 8;
-  const int64_t src0 = s_src[r], src1 = s_src[r + 32];
-  const int n_ct = (C + 63) / 64;
-  uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-  auto load = [&](int ct) {
-    const int c = ct * 64 + c8;
-    v0 = (src0 >= 0 && c < C) ? ld_vec16_nc(in + src0 * C + c) : make_uint4(0u, 0u, 0u, 0u);
-    v1 = (src1 >= 0 && c < C) ? ld_vec16_nc(in + src1 * C + c) : make_uint4(0u, 0u, 0u, 0u);
-  };
-  load(0);
-  for (int ct = 0; ct < n_ct; ++ct) {
-    bf16 (*t)[kTp] = tile[ct & 1];
-    *reinterpret_cast<uint4*>(&t[r][c8]) = v0;
-    *reinterpret_cast<uint4*>(&t[r + 32][c8]) = v1;
-    if (ct + 1 < n_ct) load(ct + 1);               // the next tile's loads in flight
-    __syncthreads();
-    const int c0 = ct * 64;
-    for (int i = threadIdx.x; i < 64 * 8; i += 256)
-      tile_store_t(t, i, out + (int64_t)c0 * k_total + pc0, k_total, c0 + (i >> 3) < C);
-    // (two buffers: a thread writes this one again only after the next
-    // tile's barrier, which every thread reaches after its reads here)
-  }
 }
 
 // out[b][c][r] = in[b][r][c]: batched [rows, cols] -> [cols, rows], output
@@ -424,19 +377,12 @@ void launch_column_sums(const float* dz, int64_t n_tokens, int E, float* out, cu
   column_sums_kernel<<<E, 256, 0, st>>>(dz, n_tokens, E, out);
 }
 
-void launch_pad_offsets(const int32_t* offsets, int64_t rows, int G, int32_t* koff,
-                        cudaStream_t st) {
-  pad_offsets_kernel<<<1, 32, 0, st>>>(offsets, rows, G, koff);
-}
-
-void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int64_t rows,
-                              int G, const int32_t* koff, int64_t k_total, void* out,
-                              cudaStream_t st) {
-  if (k_total <= 0 || C <= 0) return;
-  const dim3 grid((unsigned)(k_total / 64));
-  transpose_grouped_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), C, offsets,
-                                                 rows, G, koff, k_total,
-                                                 static_cast<bf16*>(out));
+void launch_zero_pad_rows(const int32_t* offsets, const int32_t* kept, int n_experts,
+                          int64_t row_bytes, void* buf0, void* buf1, cudaStream_t st) {
+  if (n_experts < 1) return;
+  zero_pad_rows_kernel<<<n_experts, 256, 0, st>>>(offsets, kept, row_bytes,
+                                                  static_cast<uint8_t*>(buf0),
+                                                  static_cast<uint8_t*>(buf1));
 }
 
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,

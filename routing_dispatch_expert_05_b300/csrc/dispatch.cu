@@ -62,7 +62,7 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top
 __global__ void __launch_bounds__(kMaxExperts)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
                      int n_experts, int64_t capacity, const int32_t* __restrict__ room,
-                     int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
+                     int pad, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                      int32_t* __restrict__ dropped) {
   pdl_wait();
@@ -89,7 +89,7 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
     int acc = 0;
     for (int q = 0; q < n_experts; ++q) {
       offsets[q] = acc;
-      acc += s_kept[q];
+      acc += (s_kept[q] + pad - 1) / pad * pad;   // pad > 1: zero rows after the kept
     }
     offsets[n_experts] = acc;
   }
@@ -98,11 +98,13 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
 // An assignment of rank r (arrival index among expert e's) is kept iff
 // r < kept_e = offsets[e+1] - offsets[e]: kept_e = min(total_e, capacity_e)
 // and r < total_e, so this is r < capacity_e, whichever capacity applied.
+// With padded groups kept_e comes from kept_rows instead.
 __global__ void __launch_bounds__(kRankWarps * 32)
 dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
                      int n_experts,
                      const int32_t* __restrict__ chunk_base,
                      const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ kept_rows,
                      int32_t* __restrict__ row_of_slot,
                      int32_t* __restrict__ token_of_row,
                      int32_t* __restrict__ slot_of_row) {
@@ -156,7 +158,8 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
     __syncwarp();
     if (s < ws1) {
       int32_t row = -1;
-      if (e >= 0 && offsets[e] + rank < offsets[e + 1]) {
+      if (e >= 0 && (kept_rows != nullptr ? rank < kept_rows[e]
+                                          : offsets[e] + rank < offsets[e + 1])) {
         row = offsets[e] + rank;
         token_of_row[row] = (int32_t)(s / top_k);
         if (slot_of_row != nullptr) slot_of_row[row] = (int32_t)s;
@@ -316,16 +319,19 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* chunk_base, int32_t* offsets, int32_t* row_of_slot,
                      int32_t* token_of_row, int32_t* counts, int32_t* kept,
                      int32_t* dropped, int32_t* err, cudaStream_t st,
-                     int32_t* slot_of_row, const int32_t* room) {
+                     int32_t* slot_of_row, const int32_t* room, int pad) {
   const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
   if (chunks > 0)
     launch_pdl(dispatch_count_kernel, dim3(chunks), dim3(256), 0, st, idx, n_tokens, top_k,
                n_experts, chunk_cnt, err);
+  pad = pad > 1 && kept != nullptr ? pad : 1;      // padding needs the kept counts
   launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, chunk_cnt, chunks,
-             n_experts, capacity, room, chunk_base, offsets, counts, kept, dropped);
+             n_experts, capacity, room, pad, chunk_base, offsets, counts, kept, dropped);
   if (chunks > 0)
     launch_pdl(dispatch_rank_kernel, dim3(chunks), dim3(kRankWarps * 32), 0, st, idx, n_tokens,
-               top_k, n_experts, chunk_base, offsets, row_of_slot, token_of_row, slot_of_row);
+               top_k, n_experts, chunk_base, offsets,
+               pad > 1 ? static_cast<const int32_t*>(kept) : nullptr, row_of_slot,
+               token_of_row, slot_of_row);
 }
 
 void launch_check_grouping(const int32_t* idx, const int32_t* offsets,

@@ -114,11 +114,6 @@ struct Params {
                               // c_row_map[r] (null: row r)
   const float* c_row_scale;   // compact output only: output row o is scaled by
                               // c_row_scale[o] before compacting (null: 1)
-  // weight-gradient kernel: group g contracts columns k_offsets[g] ..
-  // k_offsets[g+1] (non-zero multiples of BK) of A [wg_rows, *] and B
-  // [n_out, *] into rows g * wg_rows .. of C
-  const int32_t* k_offsets;
-  int wg_rows;
 };
 
 // ---------------------------------------------------------------- tiles
@@ -669,170 +664,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
-// ------------------------------------------------------- weight gradients
-// Per group g: C[g*R + i, j] = sum over c in [k_offsets[g], k_offsets[g+1])
-// of A[i, c] * B[j, c], fp32 out (R = wg_rows rows of A, n_out rows of B).
-// A and B are the grouped activations transposed (feature-major, the tokens'
-// rows as columns, each group's span zero-padded to whole k-blocks), so the
-// contraction over a group's rows is an ordinary K-major MMA loop whose
-// length differs per group.  The pipeline is the single-CTA kernel's: one
-// CTA per SM walks the (g, m, n) tiles; TMA producer, one MMA thread, eight
-// epilogue warps, two TMEM accumulators, bounded waits.
-__global__ void __launch_bounds__(kThreads, 1)
-tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kTileA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  uint8_t* s_stage = smem + kStages * kStageBytes + kBarBytes + kTableBytes;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = p.wg_rows;
-  const int mt = (R + BM - 1) / BM;
-  const int nt = (p.n_out + BN - 1) / BN;
-  const int per_g = mt * nt;
-  const int total = p.n_groups * per_g;
-
-  if (warp == 0 && lane == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], kEpiWarps);
-    }
-    mbar_init(drain, 1);
-    *s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    prefetch_map(&tmA);
-    prefetch_map(&tmB);
-  }
-  if (warp == 1) tmem_alloc(s_tmem, kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *s_tmem;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t used = 0, last_phases = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const int g = t / per_g, l = t - g * per_g;
-        const int m = l / nt, n = l - m * nt;
-        const int k0 = p.k_offsets[g];
-        const int nkb = (p.k_offsets[g + 1] - k0) / BK;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
-          mbar_expect_tx(&full[stage], kTileA + (uint32_t)BN * BK * 2);
-          tma_load_2d(sA + stage * kTileA, &tmA, &full[stage], k0 + kb * BK, m * BM);
-          tma_load_2d(sB + stage * kTileB, &tmB, &full[stage], k0 + kb * BK, n * BN);
-          used |= 1u << stage;
-          last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-        if (!ok) break;
-      }
-      for (int s = 0; s < kStages; ++s) {
-        if (!(used >> s & 1u)) continue;
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&full[s], last_phases >> s & 1u)) {
-          if (globaltimer() - t0 > kTimeoutNs) {
-            set_device_error(p.err, kDevTimeout);
-            break;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const int g = t / per_g;
-        const int nkb = (p.k_offsets[g + 1] - p.k_offsets[g]) / BK;
-        if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&full[stage], phase, s_abort, p.err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * kTileA);
-          const uint32_t b0 = smem_u32(sB + stage * kTileB);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc,
-                 (kb | kk) != 0);
-          umma_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-        if (!ok) break;
-        umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
-      }
-      umma_commit(drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(drain, 0)) {
-        if (globaltimer() - t0 > kTimeoutNs) {
-          set_device_error(p.err, kDevTimeout);
-          break;
-        }
-      }
-    }
-  } else {
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    float* stg_f = reinterpret_cast<float*>(s_stage + (warp - 2) * kStgWarpBytes);
-    uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg_f);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int g = t / per_g, l = t - g * per_g;
-      const int m = l / nt;
-      Tile tl;
-      tl.g = g;
-      tl.row0 = g * R + m * BM;
-      tl.row_end = (g + 1) * R;
-      tl.n = l - m * nt;
-      if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
-      tc_fence_after();
-      const int row_base = tl.row0 + q * 32;
-      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      store_tile(p, tl, lane, half, row_base, tb, stg_f, stg_w);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// ---------------------------------------------------------------- CTA pairs
 // The same grouped GEMM on pairs of SMs (a cluster of two CTAs) with
 // tcgen05.mma.cta_group::2: a pair computes a 256-row x 256-column tile.
 // CTA r of the pair loads rows 128r..128r+127 of A and half of the B tile
@@ -857,71 +688,6 @@ constexpr int kSmemBytes2 =
     kStages2 * kStageBytes2 + kBarBytes + kTableBytes + kEpiWarps * kStgWarpBytes + 1024;
 static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA (pairs)");
 static_assert((kStages2 * kStageBytes2 + kBarBytes + kTableBytes) % 16 == 0, "staging alignment");
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// shared::cluster address of the same shared variable in CTA `rank`
-__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
-  uint32_t d;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
-  return d;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// tile load into this CTA's shared memory, completing on an mbarrier of
-// either CTA of the pair (a shared::cluster address)
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
-                                                 uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".cta_group::2 [%0], [%1, {%3, %4}], [%2];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-// gather4 (four rows of one box each) completing on either CTA's barrier
-__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map, uint32_t bar,
-                                                 int c0, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar),
-        "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
-__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// arrive once on `bar` (same offset) in every CTA of `mask` when all prior
-// MMAs of this thread are complete
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-               ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
-               ::"r"(taddr), "r"(ncols) : "memory");
-}
 
 template <int EK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1168,32 +934,6 @@ wait_check_kernel(int32_t* err, uint64_t limit_ns, int32_t* flags) {
 }
 
 }  // namespace tc
-
-bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
-  using namespace tc;
-  if (q.rows_a < 1 || q.rows_b < 8 || q.rows_b % 8 != 0 || q.k_total % BK != 0 ||
-      q.n_groups < 1 || encode_fn() == nullptr)
-    return false;
-  Params p{};
-  p.n_out = q.rows_b;
-  p.wg_rows = q.rows_a;
-  p.n_groups = q.n_groups;
-  p.k_offsets = q.k_offsets;
-  p.epilogue = kEpiNone;
-  p.C = q.C;
-  p.c_is_f32 = 1;
-  p.mma_n = BN;
-  p.err = q.err;
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, q.A, (uint64_t)q.k_total, (uint64_t)q.rows_a, (uint64_t)q.k_total * 2, BM) ||
-      !make_map(&mb, q.B, (uint64_t)q.k_total, (uint64_t)q.rows_b, (uint64_t)q.k_total * 2, BN))
-    return false;
-  if (cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
-    return false;
-  tc_wgrad_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(ma, mb, p);
-  return cudaGetLastError() == cudaSuccess;
-}
 
 bool launch_wait_check(int32_t* err, uint64_t limit_ns, int32_t* flags, cudaStream_t st) {
   tc::wait_check_kernel<<<1, 64, 0, st>>>(err, limit_ns, flags);

@@ -49,14 +49,17 @@ void launch_bias_update(const int32_t* counts, int n_experts, float gamma, float
 
 // ---- dispatch -------------------------------------------------------------
 // capacity: one for every expert (< 0: none); room (device [E], nullable):
-// a capacity per expert instead
+// a capacity per expert instead.  pad > 1 (with kept non-null): each
+// expert's group of rows is rounded up to a multiple of pad, so
+// offsets[e+1] - offsets[e] = pad * ceil(kept[e] / pad); the rows after the
+// kept ones are not written (launch_zero_pad_rows clears them)
 void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int n_experts, int64_t capacity /* <0: none */,
                      int32_t* chunk_cnt, int32_t* chunk_base, int32_t* offsets,
                      int32_t* row_of_slot, int32_t* token_of_row,
                      int32_t* counts, int32_t* kept, int32_t* dropped,
                      int32_t* err, cudaStream_t st, int32_t* slot_of_row = nullptr,
-                     const int32_t* room = nullptr);
+                     const int32_t* room = nullptr, int pad = 1);
 // x_perm[row_of_slot[t*k + j]] = x[t] for every kept slot (one warp per token,
 // 32- or 16-byte vectors; a TMA bulk-copy version measured slower)
 void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,
@@ -173,17 +176,35 @@ bool launch_swap_gemm(const TcProblem& p, int num_sms, cudaStream_t st);
 // A [rows_a, k_total] and B [rows_b, k_total] bf16 row-major (the grouped
 // activations transposed, every group's column span a non-zero multiple of
 // 64, zero-padded); C fp32 [n_groups * rows_a, rows_b].
+// Weight gradients, per group g of rows [offsets[g], offsets[g+1]) of P and
+// Q (null offsets: one group of all rows): C_g = P_g^T Q_g in fp32, from the
+// first m_dim columns of P [rows, p_ld] and n_dim of Q [rows, q_ld] (bf16),
+// both read in place (MN-major tcgen05 operands, CTA pairs).  Output rows i
+// < m_split of group g go to C0[g][i][:], the rest (C1 non-null) to
+// C1[g][i - m_split][:]; without C1, C0 is [G][m_dim][n_dim].  Each group's
+// row count must be a multiple of 16, or the group must end at `rows`, and
+// the rows that pad a group to 16 must be zero.  One group over few tiles is
+// split over K into `partial` (wgrad_partial_floats(q) floats) and summed.
 struct WgradProblem {
-  const void* A;
-  const void* B;
-  int rows_a, rows_b;
-  int64_t k_total;            // columns of A and B (multiple of 64)
-  const int32_t* k_offsets;   // [n_groups + 1], device
+  const void* P;
+  int64_t p_ld;
+  int m_dim;
+  const void* Q;
+  int64_t q_ld;
+  int n_dim;
+  int64_t rows;
+  const int32_t* offsets;
   int n_groups;
-  float* C;
+  float* C0;
+  float* C1;
+  int m_split;
+  float* partial;
+  size_t partial_floats;      // room at `partial` (fewer splits if it holds less)
   int32_t* err;
 };
-bool launch_tc_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st);
+int wgrad_splits(const WgradProblem& q, int num_sms);
+size_t wgrad_partial_floats(const WgradProblem& q, int num_sms);
+bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st);
 // the GEMM kernels' bounded mbarrier wait, run out on purpose (see moe.h)
 bool launch_wait_check(int32_t* err, uint64_t limit_ns, int32_t* flags, cudaStream_t st);
 
@@ -202,15 +223,10 @@ void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* r
 constexpr int kYScaleBlock = 32;    // columns per compact-output exponent
 
 // ---- backward (backward.cu) -----------------------------------------------
-// koff[g+1] = koff[g] + max(64, 64 * ceil(m_g / 64)), m_g from offsets (or
-// one group of `rows` rows when offsets is null)
-void launch_pad_offsets(const int32_t* offsets, int64_t rows, int G, int32_t* koff,
-                        cudaStream_t st);
-// out [C, k_total] bf16: column koff[g] + l = row offsets[g] + l of in [*, C]
-// (bf16; C and k_total multiples of 8), zeros on each group's padding
-void launch_transpose_grouped(const void* in, int C, const int32_t* offsets, int64_t rows,
-                              int G, const int32_t* koff, int64_t k_total, void* out,
-                              cudaStream_t st);
+// zero rows [offsets[e] + kept[e], offsets[e+1]) of buf0 and buf1 (rows of
+// row_bytes, a multiple of 16; buf1 nullable): the padding of a padded grouping
+void launch_zero_pad_rows(const int32_t* offsets, const int32_t* kept, int n_experts,
+                          int64_t row_bytes, void* buf0, void* buf1, cudaStream_t st);
 // out[b][c][r] = in[b][r][c] (bf16), batch b of the output at out + b * out_stride
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
                               int64_t out_stride, cudaStream_t st);

@@ -2,8 +2,8 @@
 oracle.
 
 The oracle differentiates in float64 without storage roundings; the GPU
-path keeps its intermediates (g, u, h, dy, dh, [dg|du], dx_perm, the
-transposed operands) in bf16 with fp32 accumulation.  A gradient passes
+path keeps its intermediates (g, u, h, dy, dh, [dg|du], dx_perm) in bf16
+with fp32 accumulation.  A gradient passes
 through about five such roundings, each within 2^-9 relative, so each
 tensor is compared as ||gpu - oracle|| / ||oracle|| <= BWD_NORM (2e-2, a
 few times the compounded rounding) and max |gpu - oracle| <= BWD_MAX *
@@ -125,7 +125,12 @@ CASES = [(W.ROUTE_SOFTMAX_TOPK, {}), (W.ROUTE_TOPK_SOFTMAX, dict(E=64, k=6)),
          (W.ROUTE_SIGMOID_BIAS, dict(E=16, k=4, router_bias="none", n_shared=1,
                                      d_ff_shared=128)),
          (W.ROUTE_SIGMOID_BIAS, dict(E=32, k=6, N=1024, router_bias="none", n_shared=2,
-                                     d_ff_shared=64))]
+                                     d_ff_shared=64)),
+         # widths over several 256-wide weight-gradient tiles with ragged
+         # edges (d = 384, F = 320: the dW1 / dW3 split inside a tile)
+         (W.ROUTE_SOFTMAX_TOPK, dict(N=1024, E=8, k=2, d=384, F=320)),
+         (W.ROUTE_SIGMOID_BIAS, dict(N=512, E=8, k=2, d=320, F=192, router_bias="none",
+                                     n_shared=1, d_ff_shared=320))]
 
 
 @pytest.mark.parametrize("d_balance", [0.0, 0.7])
