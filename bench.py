@@ -691,9 +691,12 @@ def run_backward(args, shape, peaks, peaks_kind):
     """Time moe_backward (one GPU): recompute + data and weight gradients.
 
     Algorithmic FLOPs per step, SwiGLU experts: the recomputed g, u (2 d F)
-    and y (d F) per kept assignment, the data gradients dh (d F) and dx_perm
-    (2 d F), the weight gradients dW2 (d F) and dW1, dW3 (2 d F) -- 18 d F
-    FLOP per assignment -- plus the router's three N x E x d products.
+    per kept assignment, the data gradients dh (d F) and dx_perm (2 d F), the
+    weight gradients dW2 (d F) and dW1, dW3 (2 d F) -- 16 d F FLOP per
+    assignment (two each per multiply-add) -- plus the router's three
+    N x E x d products.  The expert outputs y are not recomputed: the routing
+    weights' gradient <dout, y> is taken as <dout W2, h>, a row dot of the
+    dh product with h, so no down projection is counted or run.
     """
     import torch
     from routing_dispatch_expert_05_b300 import moe as M
@@ -723,7 +726,7 @@ def run_backward(args, shape, peaks, peaks_kind):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    flop = 18.0 * d * F * N * k + 3 * 2.0 * N * E * d
+    flop = 16.0 * d * F * N * k + 3 * 2.0 * N * E * d
     tflops = flop / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     assert M.moe_read_device_error(ws) == M.MOE_OK

@@ -32,8 +32,9 @@ struct Layout {
   int chunks;
 };
 
-// extra_rows: room for groups padded past N*k rows (the backward's grouping)
-Layout layout_of(const moe_config_t& c, int64_t extra_rows = 0) {
+// extra_rows: room for groups padded past N*k rows (the backward's grouping);
+// backward: without the forward's expert outputs and staging buffers
+Layout layout_of(const moe_config_t& c, int64_t extra_rows = 0, bool backward = false) {
   Layout L{};
   size_t o = 0;
   auto take = [&o](size_t bytes) {
@@ -65,6 +66,10 @@ Layout layout_of(const moe_config_t& c, int64_t extra_rows = 0) {
   L.h = take((size_t)R * F * es);
   // expert outputs: fp32, or (bf16 layers on the tensor cores) fp16 with an
   // exponent byte per (row, 32-column block) -- either fits here
+  if (backward) {
+    L.total = o;
+    return L;
+  }
   L.y = take((size_t)R * d * 4);
   L.y_e8 = take((size_t)R * ceil_div64(d, kYScaleBlock));
   if (c.n_shared > 0) {
@@ -928,7 +933,7 @@ WgradProblem router_wgrad_problem(const moe_config_t& c, const void* dz16, const
 struct BwLayout {
   Layout fw;             // grouped buffers with room for the padded rows
   int64_t rows;          // grouped rows: N*k + (kBwPad - 1) * E
-  size_t counts, kept, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, wrT, part;
+  size_t counts, kept, g, u, dy, dh, dgu, dxp, dz, dz16, dxr, dw, w_row, dw_row, wrT, part;
   // shared experts (S * Fs columns, one group of all tokens)
   size_t gs, us, hs, dhs, dgus, dxs, ws2T, total;
 };
@@ -937,7 +942,7 @@ BwLayout bw_layout_of(const moe_config_t& c) {
   BwLayout B{};
   const int64_t N = c.n_tokens, E = c.n_experts, k = c.top_k, d = c.d_model, F = c.d_ff;
   B.rows = N * k + (kBwPad - 1) * E;
-  B.fw = layout_of(c, (kBwPad - 1) * E);
+  B.fw = layout_of(c, (kBwPad - 1) * E, true);
   size_t o = B.fw.total;
   auto take = [&o](size_t bytes) {
     const size_t at = o;
@@ -957,6 +962,8 @@ BwLayout bw_layout_of(const moe_config_t& c) {
   B.dz16 = take((size_t)N * E * 2);
   B.dxr = take((size_t)N * d * 4);
   B.dw = take((size_t)N * k * 4);
+  B.w_row = take((size_t)R * 4);
+  B.dw_row = take((size_t)R * 4);
   B.wrT = take((size_t)d * E * 2);
   B.part = take(std::max<size_t>(
       4, wgrad_partial_floats(router_wgrad_problem(c, nullptr, nullptr, nullptr, nullptr,
@@ -1039,14 +1046,14 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   int32_t* ros = at<int32_t>(ws, L.row_of_slot);
   int32_t* tor = at<int32_t>(ws, L.token_of_row);
   void* x_perm = at<char>(ws, L.x_perm);
-  void* h = at<char>(ws, L.h);
-  void* y = at<char>(ws, L.y);
-  uint8_t* y_e8 = at<uint8_t>(ws, L.y_e8);
+  void* hw = at<char>(ws, L.h);                     // w h, per grouped row
   int32_t* counts = at<int32_t>(ws, B.counts);
   int32_t* kept = at<int32_t>(ws, B.kept);
   void* g = at<char>(ws, B.g);
   void* u = at<char>(ws, B.u);
-  void* dy = at<char>(ws, B.dy);
+  void* dy_u = at<char>(ws, B.dy);                  // dout per grouped row
+  float* w_row = at<float>(ws, B.w_row);
+  float* dw_row = at<float>(ws, B.dw_row);
   void* dh = at<char>(ws, B.dh);
   void* dgu = at<char>(ws, B.dgu);
   void* dxp = at<char>(ws, B.dxp);
@@ -1063,15 +1070,16 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
 
   // 1. recompute: routing (counts for the balance term), grouping (each
   //    expert's rows padded to whole 16-row slices, the padding zero in
-  //    x_perm and dy), x_perm, SwiGLU: g = x W1^T, u = x W3^T, h = silu(g) u;
-  //    SiLU-MLP: g = a = x W1^T + b1, h = silu(a); y = h W2^T (+ b2)
-  //    (compact, row order)
+  //    x_perm and dy_u), x_perm, g = x W1^T (+ b1 for the SiLU-MLP: a), and
+  //    for SwiGLU u = x W3^T.  Neither h nor y is recomputed: the gradient of
+  //    the routing weights is a row dot of dh_u and h, formed from g and u
+  //    where they are read anyway.
   moe_stats_t rs{};
   rs.counts = counts;
   router_body(c, x, w, nullptr, idx, wts, &rs, sc, st, true);
   dispatch_body(c, idx, x, offsets, ros, tor, x_perm, nullptr, sc, st, nullptr, nullptr,
                 kBwPad, kept);
-  launch_zero_pad_rows(offsets, kept, E, (int64_t)d * 2, x_perm, dy, st);
+  launch_zero_pad_rows(offsets, kept, E, (int64_t)d * 2, x_perm, dy_u, st);
   TcProblem q = plain_problem(x_perm, M, d, w.w1, E, F, offsets, E, M, F, g, 0, sc.err);
   q.use_pairs = pairs_pay(c);
   if (!swiglu && c.has_bias) {
@@ -1084,27 +1092,32 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
     q.C = u;
     MOE_TRY(tc_run(q, st));
   }
-  launch_silu_mul(g, swiglu ? u : nullptr, h, offsets, E, 0, F, ns, st);
-  MOE_TRY(down_body(c, h, offsets, w, y, y_e8, sc.err, st, nullptr, nullptr, M));
 
-  // 2. combine and router: dw, dy = w dout, dlogits
-  launch_combine_backward(y, y_e8, ros, wts, dout, N, k, d, dw, dy, ns, st);
-  launch_router_backward(sc.logits, idx, wts, dw, counts, N, E, k, c.route, c.balance_coef,
-                         d_balance, dz, dz16, st);
+  // 2. dout to the expert rows: dy_u[row] = dout[t] (unweighted), w_row[row]
+  //    = w[t, j] (0 on the padding), dw = <dout, b2> (biases) or 0
+  cudaMemsetAsync(w_row, 0, (size_t)M * 4, st);
+  MOE_TRY(last_cuda());
+  launch_scatter_dout(dout, ros, wts, idx, c.has_bias ? w.b2 : nullptr, N, k, d, dy_u, w_row,
+                      dw, ns, st);
 
-  // 3. data gradients: dh = dy W2; SwiGLU: [dg | du] = SwiGLU', dx_perm =
-  //    dg W1 + du W3; SiLU-MLP: da = dh silu'(a), dx_perm = da W1; the shared
-  //    experts' part of dx (below); dx = sum over slots + dlogits Wr (+ shared)
-  // The expert weights are read in place as MN-major B operands: W2 [E, d, F]
-  // is, per expert, d K-rows of F output columns; W1 / W3 [E, F, d] are F
-  // K-rows of d columns (the two K sub-blocks of [dg | du]).  Only the
-  // router's small [E, d] is transposed (its E K-rows need not fill k-blocks).
-  launch_transpose_batched(w.w_router, 1, E, d, wrT, (int64_t)d * E, st);
-  q = plain_problem(dy, M, d, w.w2, E, F, offsets, E, M, F, dh, 0, sc.err);
+  // 3. data gradients: dh_u = dy_u W2; per row dw += <dh_u, h>, dh = w dh_u,
+  //    SwiGLU: [dg | du] = SwiGLU', SiLU-MLP: da = dh silu'(a), and hw = w h
+  //    (for dW2); dlogits from dw; dx_perm = dg W1 + du W3 (SiLU-MLP: da W1);
+  //    the shared experts' part of dx (below); dx = sum over slots +
+  //    dlogits Wr (+ shared).  The expert weights are read in place as
+  //    MN-major B operands: W2 [E, d, F] is, per expert, d K-rows of F
+  //    output columns; W1 / W3 [E, F, d] are F K-rows of d columns (the two
+  //    K sub-blocks of [dg | du]); Wr [E, d] likewise when E fills whole
+  //    k-blocks, else it is transposed.
+  q = plain_problem(dy_u, M, d, w.w2, E, F, offsets, E, M, F, dh, 0, sc.err);
   q.b_mn_major = 1;
   q.use_pairs = pairs_pay(c);
   MOE_TRY(tc_run(q, st));
-  launch_swiglu_backward(dh, g, swiglu ? u : nullptr, dgu, offsets, E, 0, F, ns, st);
+  launch_expert_rows_backward(dh, g, swiglu ? u : nullptr, w_row, offsets, E, 0, F, dgu, hw,
+                              dw_row, ns, st);
+  launch_slot_dw(dw_row, ros, N * k, dw, ns, st);
+  launch_router_backward(sc.logits, idx, wts, dw, counts, N, E, k, c.route, c.balance_coef,
+                         d_balance, dz, dz16, st);
   q = plain_problem(dgu, M, swiglu ? 2 * F : F, w.w1, E, d, offsets, E, M, d, dxp, 0, sc.err);
   q.b_mn_major = 1;
   q.k_sub = F;
@@ -1114,13 +1127,20 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   }
   q.use_pairs = pairs_pay(c);
   MOE_TRY(tc_run(q, st));
-  q = plain_problem(dz16, N, E, wrT, 1, d, nullptr, 1, N, d, dxr, 1, sc.err);
+  if (E % 64 == 0) {                               // whole 64-row k-blocks of Wr
+    q = plain_problem(dz16, N, E, w.w_router, 1, d, nullptr, 1, N, d, dxr, 1, sc.err);
+    q.b_mn_major = 1;
+  } else {
+    launch_transpose_batched(w.w_router, 1, E, d, wrT, (int64_t)d * E, st);
+    q = plain_problem(dz16, N, E, wrT, 1, d, nullptr, 1, N, d, dxr, 1, sc.err);
+  }
   MOE_TRY(tc_run(q, st));
   if (SF > 0) {
     // shared experts: one SwiGLU of width S*Fs over all tokens, weight one,
-    // so its output gradient is dout itself.  gs = x Ws1^T, us = x Ws3^T,
-    // hs = silu(gs) us; dhs = dout Ws2 (Ws2 [S, d, Fs] transposed to the
-    // K-major [S*Fs, d]); [dgs | dus]; dxs = dgs Ws1 + dus Ws3
+    // so its output gradient is dout itself.  gs = x Ws1^T, us = x Ws3^T;
+    // dhs = dout Ws2 (one shared expert: Ws2 [d, Fs] read MN-major; more:
+    // Ws2 [S, d, Fs] transposed to the K-major [S*Fs, d]); [dgs | dus] and
+    // hs = silu(gs) us; dxs = dgs Ws1 + dus Ws3
     char* gs = at<char>(ws, B.gs);
     char* us = at<char>(ws, B.us);
     char* hs = at<char>(ws, B.hs);
@@ -1134,12 +1154,17 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
     q.B0 = w.ws3;
     q.C = us;
     MOE_TRY(tc_run(q, st));
-    launch_silu_mul(gs, us, hs, nullptr, 0, N, SF, ns, st);
-    launch_transpose_batched(w.ws2, S, d, Fs, ws2T, (int64_t)Fs * d, st);
-    q = plain_problem(dout, N, d, ws2T, 1, SF, nullptr, 1, N, SF, dhs, 0, sc.err);
+    if (S == 1) {
+      q = plain_problem(dout, N, d, w.ws2, 1, SF, nullptr, 1, N, SF, dhs, 0, sc.err);
+      q.b_mn_major = 1;
+    } else {
+      launch_transpose_batched(w.ws2, S, d, Fs, ws2T, (int64_t)Fs * d, st);
+      q = plain_problem(dout, N, d, ws2T, 1, SF, nullptr, 1, N, SF, dhs, 0, sc.err);
+    }
     q.use_pairs = N >= 128;
     MOE_TRY(tc_run(q, st));
-    launch_swiglu_backward(dhs, gs, us, dgus, nullptr, 0, N, SF, ns, st);
+    launch_expert_rows_backward(dhs, gs, us, nullptr, nullptr, 0, N, SF, dgus, hs, nullptr, ns,
+                                st);
     // Ws1 / Ws3 [S*Fs, d] read in place (MN-major: S*Fs K-rows of d columns)
     q = plain_problem(dgus, N, 2 * SF, w.ws1, 1, d, nullptr, 1, N, d, dxs, 1, sc.err);
     q.b_mn_major = 1;
@@ -1151,15 +1176,16 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   }
   launch_dx_reduce(dxp, ros, dxr, dxs, N, k, d, gr.dx, ns, st);
 
-  // 4. weight gradients, read in place: dW2[e] = dy_e^T h_e; [dW1 | dW3][e]
+  // 4. weight gradients, read in place: dW2[e] = dy_u,e^T hw_e (= dy^T h);
+  //    [dW1 | dW3][e]
   //    = [dg | du]_e^T x_e (one launch, rows F.. of each group's output to
   //    dW3); the router's dWr = dlogits^T x and the shared experts' over all
   //    tokens as one group
   WgradProblem wq{};
-  wq.P = dy;
+  wq.P = dy_u;
   wq.p_ld = d;
   wq.m_dim = d;
-  wq.Q = h;
+  wq.Q = hw;
   wq.q_ld = F;
   wq.n_dim = F;
   wq.rows = M;
@@ -1181,10 +1207,10 @@ moe_status_t backward_impl(const moe_config_t& c, const void* x, const moe_weigh
   }
   MOE_TRY(wgrad_run(wq, st));
   if (c.has_bias) {
-    // db1[e] = sum of da, db2[e] = sum of dy over expert e's rows (the
+    // db1[e] = sum of da, db2[e] = sum of w dy_u over expert e's rows (the
     // padding rows are zero)
     launch_group_sums(dgu, F, offsets, E, F, gr.d_b1, st);
-    launch_group_sums(dy, d, offsets, E, d, gr.d_b2, st);
+    launch_group_sums(dy_u, d, offsets, E, d, gr.d_b2, st, w_row);
   }
   WgradProblem rq = router_wgrad_problem(c, dz16, x, gr.d_w_router, at<float>(ws, B.part),
                                          sc.err);

@@ -7,6 +7,9 @@
 // router receives gradients through the contribution weights, the top-k
 // choice itself is not differentiable, an expert no token chose gets none):
 //   dw[t,j] = <dout[t], y[t,j]>,      dy[t,j] = w[t,j] dout[t]
+//   with y = h W2^T + b2 the first is <dout[t] W2, h> + <dout[t], b2>: the
+//   data-gradient GEMM's dh_u = dout W2 (unweighted) gives it as a row dot
+//   with h, so y is never recomputed; dh = w dh_u
 //   softmax modes: dlogit = w * (dw - <w, dw>) on the selected experts
 //   sigmoid mode:  dlogit = s (1 - s) (dw - <w, dw>) / sum_sel s
 //   balance term:  p (g - <p, g>) (softmax), or through s / sum s (sigmoid),
@@ -122,113 +125,134 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
-// h = silu(g) * u (SwiGLU) or h = silu(g) (u null: SiLU-MLP, g = W1 x + b1)
-// for the kept rows (offsets[E] rows of F; `rows` when offsets is null), 8
-// per thread
-__global__ void silu_mul_kernel(const bf16* __restrict__ g, const bf16* __restrict__ u,
-                                bf16* __restrict__ h, const int32_t* __restrict__ offsets,
-                                int n_experts, int64_t rows, int F) {
-  const int64_t n8 = (offsets ? (int64_t)offsets[n_experts] : rows) * F / 8;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    float gv[8], uv[8], hv[8];
-    unpack8(ld_vec16_nc(g + 8 * i), gv);
-    if (u != nullptr) unpack8(ld_vec16_nc(u + 8 * i), uv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      hv[j] = gv[j] * sigmoid_fast(gv[j]) * (u != nullptr ? uv[j] : 1.f);
-    st_vec16(h + 8 * i, pack8(hv));
-  }
-}
-
-// SwiGLU: dgu[r] = [dg | du] (row stride 2F), dg = dh u silu'(g),
-// du = dh silu(g).  SiLU-MLP (u null): dgu[r] = da (row stride F),
-// da = dh silu'(a) with a = g.  Rows as in silu_mul_kernel; 8 per thread.
-__global__ void swiglu_backward_kernel(const bf16* __restrict__ dh, const bf16* __restrict__ g,
-                                       const bf16* __restrict__ u, bf16* __restrict__ dgu,
-                                       const int32_t* __restrict__ offsets, int n_experts,
-                                       int64_t rows, int F) {
-  const int64_t n8 = (offsets ? (int64_t)offsets[n_experts] : rows) * F / 8;
-  const int f8 = F / 8;
+// Per grouped row r (offsets[E] rows, or `rows` when offsets is null; one
+// warp each), from dh_u = dout W2 (unweighted), g, u and the row's routing
+// weight w_r (1 when w_row is null: the shared experts):
+//   h = silu(g) u (SwiGLU) or silu(g) (u null: SiLU-MLP, g = a = W1 x + b1)
+//   dw_row[r] = <dh_u, h>              (the weight's gradient, less <dout, b2>)
+//   dh = w_r dh_u;  SwiGLU: dgu[r] = [dg | du] (row stride 2F), dg = dh u
+//   silu'(g), du = dh silu(g);  SiLU-MLP: dgu[r] = da = dh silu'(a) (stride F)
+//   hw[r] = w_r h                      (dW2 = dout_rows^T hw)
+// hw and dw_row are nullable.  Lanes take 8 features at a time (16-byte
+// loads and stores).
+__global__ void __launch_bounds__(256)
+expert_rows_backward_kernel(const bf16* __restrict__ dh_u, const bf16* __restrict__ g,
+                            const bf16* __restrict__ u, const float* __restrict__ w_row,
+                            const int32_t* __restrict__ offsets, int n_experts, int64_t n_rows,
+                            int F, bf16* __restrict__ dgu, bf16* __restrict__ hw,
+                            float* __restrict__ dw_row) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = offsets != nullptr ? (int64_t)offsets[n_experts] : n_rows;
   const int ld = u != nullptr ? 2 * F : F;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / f8;
-    const int f = (int)(i - r * f8) * 8;
-    float gv[8], uv[8], dv[8], dg[8], du[8];
-    unpack8(ld_vec16_nc(g + 8 * i), gv);
-    if (u != nullptr) unpack8(ld_vec16_nc(u + 8 * i), uv);
-    unpack8(ld_vec16_nc(dh + 8 * i), dv);
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    const float wr = w_row != nullptr ? w_row[r] : 1.f;
+    float part = 0.f;
+    for (int c = lane * 8; c < F; c += 256) {
+      float gv[8], uv[8], dv[8], dg[8], du[8], hv[8];
+      unpack8(ld_vec16_nc(g + r * F + c), gv);
+      if (u != nullptr) unpack8(ld_vec16_nc(u + r * F + c), uv);
+      unpack8(ld_vec16_nc(dh_u + r * F + c), dv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float sg = sigmoid_fast(gv[j]);
-      const float dsilu = sg * (1.f + gv[j] * (1.f - sg));
-      dg[j] = dv[j] * (u != nullptr ? uv[j] : 1.f) * dsilu;
-      du[j] = dv[j] * gv[j] * sg;
+      for (int j = 0; j < 8; ++j) {
+        const float sg = sigmoid_fast(gv[j]);
+        const float sl = gv[j] * sg;                 // silu(g)
+        const float uj = u != nullptr ? uv[j] : 1.f;
+        const float h = sl * uj;
+        part = fmaf(dv[j], h, part);
+        const float dh = wr * dv[j];
+        dg[j] = dh * uj * sg * (1.f + gv[j] * (1.f - sg));
+        du[j] = dh * sl;
+        hv[j] = wr * h;
+      }
+      st_vec16(dgu + r * ld + c, pack8(dg));
+      if (u != nullptr) st_vec16(dgu + r * ld + F + c, pack8(du));
+      if (hw != nullptr) st_vec16(hw + r * F + c, pack8(hv));
     }
-    st_vec16(dgu + r * ld + f, pack8(dg));
-    if (u != nullptr) st_vec16(dgu + r * ld + F + f, pack8(du));
+    if (dw_row != nullptr) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+      if (lane == 0) dw_row[r] = part;
+    }
   }
 }
 
-// out[g, c] = sum over rows offsets[g] .. offsets[g+1] of in[row, c] (bf16
-// in, fp32 out): the bias gradients.  One thread per column, the rows of a
-// group in order, so the sums are the same run to run.
+// out[g, c] = sum over rows offsets[g] .. offsets[g+1] of in[row, c] (times
+// row_w[row] when row_w is non-null; bf16 in, fp32 out): the bias gradients.
+// One thread per column, the rows of a group in order, so the sums are the
+// same run to run.
 __global__ void __launch_bounds__(256)
 group_sums_kernel(const bf16* __restrict__ in, int64_t ld, const int32_t* __restrict__ offsets,
-                  int C, float* __restrict__ out) {
+                  const float* __restrict__ row_w, int C, float* __restrict__ out) {
   const int g = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= C) return;
   const int64_t r0 = offsets[g], r1 = offsets[g + 1];
   float acc = 0.f;
-  for (int64_t r = r0; r < r1; ++r) acc += __bfloat162float(in[r * ld + c]);
+  for (int64_t r = r0; r < r1; ++r) {
+    const float v = __bfloat162float(in[r * ld + c]);
+    acc = row_w != nullptr ? fmaf(row_w[r], v, acc) : acc + v;
+  }
   out[(int64_t)g * C + c] = acc;
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per assignment (t, j): dw[t,j] = <dout[t], y[row]> with y compact
-// (fp16 and an exponent per 32 columns, row order), dy[row] = w[t,j] dout[t]
-// (bf16); lanes take 8 columns at a time (16-byte loads and stores).
+// One warp per token t: for each kept slot s = (t, j) with row r,
+// dy_u[r] = dout[t] (bf16 rows, unweighted) and w_row[r] = w[s]; dw[s] =
+// <dout[t], b2[idx[s]]> (0 without expert biases, and for a dropped slot,
+// which has no output).  dout is read once per token (16-byte pieces).
 __global__ void __launch_bounds__(256)
-combine_backward_kernel(const __half* __restrict__ y, const uint8_t* __restrict__ y_e8,
-                        const int32_t* __restrict__ row_of_slot, const float* __restrict__ w,
-                        const bf16* __restrict__ dout, int64_t n_tokens, int top_k, int d,
-                        float* __restrict__ dw, bf16* __restrict__ dy) {
+scatter_dout_kernel(const bf16* __restrict__ dout, const int32_t* __restrict__ row_of_slot,
+                    const float* __restrict__ w, const int32_t* __restrict__ idx,
+                    const bf16* __restrict__ b2, int64_t n_tokens, int top_k, int d,
+                    bf16* __restrict__ dy_u, float* __restrict__ w_row, float* __restrict__ dw) {
   const int lane = threadIdx.x & 31;
-  const int e8_cols = (d + kYScaleBlock - 1) / kYScaleBlock;
-  const int64_t n_slots = n_tokens * top_k;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < n_slots;
-       s += warps) {
-    const int r = row_of_slot[s];
-    if (r < 0) {                                   // dropped: no output, no gradient
-      if (lane == 0) dw[s] = 0.f;
-      continue;
-    }
-    const int64_t t = s / top_k;
-    const float ws = w[s];
-    float part = 0.f;
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tokens;
+       t += warps) {
+    const int64_t s0 = t * top_k;
     for (int c = lane * 8; c < d; c += 256) {
-      float dv[8];
-      unpack8(ld_vec16_nc(dout + t * d + c), dv);
-      const uint4 yv = ld_vec16_nc(y + (int64_t)r * d + c);
-      const float sc = __uint_as_float((uint32_t)y_e8[(int64_t)r * e8_cols + c / kYScaleBlock] << 23);
-      const __half2* yh = reinterpret_cast<const __half2*>(&yv);
-      float dyv[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(yh[j]);
-        part = fmaf(dv[2 * j], f.x * sc, part);
-        part = fmaf(dv[2 * j + 1], f.y * sc, part);
+      const uint4 v = ld_vec16_nc(dout + t * d + c);
+      for (int j = 0; j < top_k; ++j) {
+        const int r = __ldg(row_of_slot + s0 + j);
+        if (r >= 0) st_vec16(dy_u + (int64_t)r * d + c, v);
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) dyv[j] = ws * dv[j];
-      st_vec16(dy + (int64_t)r * d + c, pack8(dyv));
     }
+    for (int j = lane; j < top_k; j += 32) {
+      const int r = row_of_slot[s0 + j];
+      if (r >= 0) w_row[r] = w[s0 + j];
+      if (b2 == nullptr || r < 0) dw[s0 + j] = 0.f;
+    }
+    if (b2 != nullptr) {
+      for (int j = 0; j < top_k; ++j) {
+        const int r = __ldg(row_of_slot + s0 + j);
+        if (r < 0) continue;
+        const bf16* bp = b2 + (int64_t)idx[s0 + j] * d;
+        float part = 0.f;
+        for (int c = lane * 8; c < d; c += 256) {
+          float dv[8], bv[8];
+          unpack8(ld_vec16_nc(dout + t * d + c), dv);
+          unpack8(ld_vec16_nc(bp + c), bv);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-    if (lane == 0) dw[s] = part;
+          for (int q = 0; q < 8; ++q) part = fmaf(dv[q], bv[q], part);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+        if (lane == 0) dw[s0 + j] = part;
+      }
+    }
+  }
+}
+
+// dw[s] += dw_row[row_of_slot[s]] for the kept slots
+__global__ void __launch_bounds__(256)
+slot_dw_kernel(const float* __restrict__ dw_row, const int32_t* __restrict__ row_of_slot,
+               int64_t n_slots, float* __restrict__ dw) {
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_slots;
+       s += (int64_t)gridDim.x * blockDim.x) {
+    const int r = row_of_slot[s];
+    if (r >= 0) dw[s] += dw_row[r];
   }
 }
 
@@ -393,37 +417,39 @@ void launch_transpose_batched(const void* in, int batch, int rows, int cols, voi
                                                  static_cast<bf16*>(out), out_stride);
 }
 
-void launch_silu_mul(const void* g, const void* u, void* h, const int32_t* offsets,
-                     int n_experts, int64_t rows, int F, int num_sms, cudaStream_t st) {
-  silu_mul_kernel<<<num_sms * 8, 256, 0, st>>>(static_cast<const bf16*>(g),
-                                               static_cast<const bf16*>(u),
-                                               static_cast<bf16*>(h), offsets, n_experts, rows,
-                                               F);
-}
-
-void launch_swiglu_backward(const void* dh, const void* g, const void* u, void* dgu,
-                            const int32_t* offsets, int n_experts, int64_t rows, int F,
-                            int num_sms, cudaStream_t st) {
-  swiglu_backward_kernel<<<num_sms * 8, 256, 0, st>>>(
-      static_cast<const bf16*>(dh), static_cast<const bf16*>(g), static_cast<const bf16*>(u),
-      static_cast<bf16*>(dgu), offsets, n_experts, rows, F);
+void launch_expert_rows_backward(const void* dh_u, const void* g, const void* u,
+                                 const float* w_row, const int32_t* offsets, int n_experts,
+                                 int64_t rows, int F, void* dgu, void* hw, float* dw_row,
+                                 int num_sms, cudaStream_t st) {
+  expert_rows_backward_kernel<<<num_sms * 8, 256, 0, st>>>(
+      static_cast<const bf16*>(dh_u), static_cast<const bf16*>(g), static_cast<const bf16*>(u),
+      w_row, offsets, n_experts, rows, F, static_cast<bf16*>(dgu), static_cast<bf16*>(hw),
+      dw_row);
 }
 
 void launch_group_sums(const void* in, int64_t ld, const int32_t* offsets, int G, int C,
-                       float* out, cudaStream_t st) {
+                       float* out, cudaStream_t st, const float* row_w) {
   if (G <= 0 || C <= 0) return;
   const dim3 grid((unsigned)((C + 255) / 256), (unsigned)G);
-  group_sums_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), ld, offsets, C, out);
+  group_sums_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(in), ld, offsets, row_w, C,
+                                          out);
 }
 
-void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
-                             const float* w, const void* dout, int64_t n_tokens, int top_k,
-                             int d, float* dw, void* dy, int num_sms, cudaStream_t st) {
+void launch_scatter_dout(const void* dout, const int32_t* row_of_slot, const float* w,
+                         const int32_t* idx, const void* b2, int64_t n_tokens, int top_k, int d,
+                         void* dy_u, float* w_row, float* dw, int num_sms, cudaStream_t st) {
   if (n_tokens <= 0) return;
-  const int blocks = (int)std::min<int64_t>(ceil_div64(n_tokens * top_k, 8), (int64_t)num_sms * 8);
-  combine_backward_kernel<<<blocks, 256, 0, st>>>(
-      static_cast<const __half*>(y16), y_e8, row_of_slot, w, static_cast<const bf16*>(dout),
-      n_tokens, top_k, d, dw, static_cast<bf16*>(dy));
+  const int blocks = (int)std::min<int64_t>(ceil_div64(n_tokens, 8), (int64_t)num_sms * 8);
+  scatter_dout_kernel<<<blocks, 256, 0, st>>>(
+      static_cast<const bf16*>(dout), row_of_slot, w, idx, static_cast<const bf16*>(b2),
+      n_tokens, top_k, d, static_cast<bf16*>(dy_u), w_row, dw);
+}
+
+void launch_slot_dw(const float* dw_row, const int32_t* row_of_slot, int64_t n_slots, float* dw,
+                    int num_sms, cudaStream_t st) {
+  if (n_slots <= 0) return;
+  const int blocks = (int)std::min<int64_t>(ceil_div64(n_slots, 256), (int64_t)num_sms * 4);
+  slot_dw_kernel<<<blocks, 256, 0, st>>>(dw_row, row_of_slot, n_slots, dw);
 }
 
 void launch_router_backward(const float* logits, const int32_t* idx, const float* w,

@@ -230,20 +230,26 @@ void launch_zero_pad_rows(const int32_t* offsets, const int32_t* kept, int n_exp
 // out[b][c][r] = in[b][r][c] (bf16), batch b of the output at out + b * out_stride
 void launch_transpose_batched(const void* in, int batch, int rows, int cols, void* out,
                               int64_t out_stride, cudaStream_t st);
-// rows: offsets[E] (offsets non-null) or `rows`; u null selects the SiLU-MLP
-// forms (h = silu(g); da = dh silu'(g), row stride F)
-void launch_silu_mul(const void* g, const void* u, void* h, const int32_t* offsets,
-                     int n_experts, int64_t rows, int F, int num_sms, cudaStream_t st);
-void launch_swiglu_backward(const void* dh, const void* g, const void* u, void* dgu,
-                            const int32_t* offsets, int n_experts, int64_t rows, int F,
-                            int num_sms, cudaStream_t st);
-// out[g, c] = sum of in[r, c] over the rows of group g (bf16 in, row stride
-// ld; fp32 out [G, C]); fixed order
+// Per grouped row (offsets[E] rows, or `rows` with offsets null): from dh_u
+// (= dout W2, unweighted), g, u (null: SiLU-MLP) and the row's routing weight
+// (w_row null: 1), h = silu(g) u; dw_row = <dh_u, h>; dh = w dh_u; dgu =
+// [dh u silu'(g) | dh silu(g)] (SiLU-MLP: dh silu'(g), row stride F); hw = w h.
+// hw and dw_row nullable.
+void launch_expert_rows_backward(const void* dh_u, const void* g, const void* u,
+                                 const float* w_row, const int32_t* offsets, int n_experts,
+                                 int64_t rows, int F, void* dgu, void* hw, float* dw_row,
+                                 int num_sms, cudaStream_t st);
+// out[g] = sum over group g's rows of in[row] (times row_w[row] if non-null)
 void launch_group_sums(const void* in, int64_t ld, const int32_t* offsets, int G, int C,
-                       float* out, cudaStream_t st);
-void launch_combine_backward(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
-                             const float* w, const void* dout, int64_t n_tokens, int top_k,
-                             int d, float* dw, void* dy, int num_sms, cudaStream_t st);
+                       float* out, cudaStream_t st, const float* row_w = nullptr);
+// dy_u[row] = dout[t] and w_row[row] = w[s] for each kept slot s = (t, j);
+// dw[s] = <dout[t], b2[idx[s]]> (b2 non-null) or 0
+void launch_scatter_dout(const void* dout, const int32_t* row_of_slot, const float* w,
+                         const int32_t* idx, const void* b2, int64_t n_tokens, int top_k, int d,
+                         void* dy_u, float* w_row, float* dw, int num_sms, cudaStream_t st);
+// dw[s] += dw_row[row_of_slot[s]] for the kept slots
+void launch_slot_dw(const float* dw_row, const int32_t* row_of_slot, int64_t n_slots, float* dw,
+                    int num_sms, cudaStream_t st);
 void launch_router_backward(const float* logits, const int32_t* idx, const float* w,
                             const float* dw, const int32_t* counts, int64_t n_tokens, int E,
                             int k, int mode, float coef, float d_balance, float* dz,
