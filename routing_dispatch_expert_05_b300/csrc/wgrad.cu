@@ -24,8 +24,13 @@
 // loads its halves into a 6-stage ring (completing on the leader's full
 // barrier), the leader's warp 1 issues tcgen05.mma.cta_group::2 and commits
 // to both CTAs' barriers, and eight epilogue warps per CTA read the fp32
-// accumulator (two of them in TMEM, 512 columns) and store it; every wait
-// is bounded.  With one group, K may be split into chunks whose partial
+// accumulator (two of them in TMEM, 512 columns); every wait is bounded.
+// An epilogue warp loads its 32 rows x 128 columns into registers and hands
+// the accumulator back at once (the MMA never waits for stores), then writes
+// each 32 x 32 chunk with a TMA tensor store from a 128-byte-swizzled
+// staging buffer.  The output maps are 3-D (group, row, column), so a chunk
+// is clipped at its group's last row and column; the weight gradients are
+// written once, in fp32, without a pass through the load/store unit.  With one group, K may be split into chunks whose partial
 // sums go to a scratch buffer and are added afterwards (the router's
 // gradient: E x d outputs over all N tokens would otherwise be 8 tiles).
 #include <cuda_bf16.h>
@@ -48,12 +53,42 @@ constexpr uint32_t kWgStageBytes = 2 * kWgHalf;     // P half + Q half
 constexpr int kWgEpiWarps = 8;
 constexpr int kWgThreads = (2 + kWgEpiWarps) * 32;
 constexpr uint32_t kWgTmemCols = 2 * kWgTile;       // two accumulators
-constexpr int kWgBarBytes = 1024;
-constexpr int kWgStgStride = 20;                    // words per staged row (16 fp32 + pad)
-constexpr int kWgStgWarpBytes = 32 * kWgStgStride * 4;
+constexpr int kWgBarBytes = 1024;                   // barriers; group order at +512
+constexpr int kWgStgWarpBytes = 32 * 32 * 4;        // one 32 x 32 fp32 chunk, swizzled
 constexpr int kWgSmem =
     kWgStages * kWgStageBytes + kWgBarBytes + kWgEpiWarps * kWgStgWarpBytes + 1024;
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
+static_assert((kWgStages * kWgStageBytes + kWgBarBytes) % 1024 == 0,
+              "swizzled staging must start on a 1024-byte boundary");
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the staging buffer may be written again once the stores have read it
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
 
 struct WgParams {
   int64_t rows;               // rows of P and Q
@@ -63,9 +98,8 @@ struct WgParams {
   int mt, nt;                 // 256-wide tiles over m_dim / n_dim
   int splits;                 // chunks of kc rows per group (one group only)
   int64_t kc;
-  float* C0;                  // rows i < m_split of each group
-  float* C1;                  // rows i >= m_split (null: m_split == m_dim)
-  int m_split;
+  int has_c1;                 // rows i >= m_split go to the second output
+  int m_split;                // (m_dim without it); a multiple of 32
   int32_t* err;
 };
 
@@ -76,12 +110,17 @@ struct WgItem {
   bool bad;
 };
 
-__device__ __forceinline__ WgItem wg_item(const WgParams& p, int t) {
+// Tile t belongs to the group of rank t / per_g in order of decreasing row
+// count (s_order; equal counts by index): a tile's cost is its group's rows,
+// and with the heaviest groups' tiles dealt out first the pairs' loads even
+// out (the routing of a real layer is far from uniform).
+__device__ __forceinline__ WgItem wg_item(const WgParams& p, const uint8_t* s_order, int t) {
   WgItem it;
   const int per_s = p.mt * p.nt;
   const int per_g = p.splits * per_s;
-  it.g = t / per_g;
-  int l = t - it.g * per_g;
+  const int gi = t / per_g;
+  it.g = p.G > 1 ? (int)s_order[gi] : gi;
+  int l = t - gi * per_g;
   it.s = l / per_s;
   l -= it.s * per_s;
   it.m = l / p.nt;
@@ -104,18 +143,10 @@ __device__ __forceinline__ WgItem wg_item(const WgParams& p, int t) {
   return it;
 }
 
-// output row pointer of accumulator row i (i < m_dim) of item `it`
-__device__ __forceinline__ float* wg_row(const WgParams& p, const WgItem& it, int i) {
-  if (p.splits > 1) return p.C0 + ((int64_t)it.s * p.m_dim + i) * p.n_dim;
-  if (p.C1 != nullptr && i >= p.m_split)
-    return p.C1 + ((int64_t)it.g * (p.m_dim - p.m_split) + (i - p.m_split)) * p.n_dim;
-  const int rows_c0 = p.C1 != nullptr ? p.m_split : p.m_dim;
-  return p.C0 + ((int64_t)it.g * rows_c0 + i) * p.n_dim;
-}
-
 __global__ void __launch_bounds__(kWgThreads, 1)
 tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                 const __grid_constant__ WgParams p) {
+                 const __grid_constant__ CUtensorMap tmC0,
+                 const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ WgParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,7 +159,8 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
   uint64_t* drain = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  float* s_stage = reinterpret_cast<float*>(smem + kWgStages * kWgStageBytes + kWgBarBytes);
+  uint8_t* s_order = reinterpret_cast<uint8_t*>(smem + kWgStages * kWgStageBytes + 512);
+  uint8_t* s_stage = smem + kWgStages * kWgStageBytes + kWgBarBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -150,10 +182,29 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&tmP);
     prefetch_map(&tmQ);
+    prefetch_map(&tmC0);
+    if (p.has_c1) prefetch_map(&tmC1);
   }
   if (warp == 1) tmem_alloc_pair(s_tmem, kWgTmemCols);
   pdl_wait();
   pdl_launch_dependents();
+  if (p.G > 1) {
+    // group ranks by decreasing rows (the staging area is free until the
+    // epilogue starts); every CTA computes the same order
+    int* s_rows = reinterpret_cast<int*>(s_stage);
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x)
+      s_rows[g] = __ldg(p.offsets + g + 1) - __ldg(p.offsets + g);
+    __syncthreads();
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+      const int rg = s_rows[g];
+      int rank = 0;
+      for (int h = 0; h < p.G; ++h) {
+        const int rh = s_rows[h];
+        rank += (rh > rg) | ((rh == rg) & (h < g));
+      }
+      s_order[rank] = (uint8_t)g;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();                                  // both CTAs' barriers exist
@@ -167,7 +218,7 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
       uint32_t phase = 0;
       uint32_t used = 0, last_phases = 0;
       for (int t = pair; t < total; t += n_pairs) {
-        const WgItem it = wg_item(p, t);
+        const WgItem it = wg_item(p, s_order, t);
         if (it.bad && leader) set_device_error(p.err, kDevBadRow);
         const int nkb = (it.cnt + BK - 1) / BK;
         const int colP = it.m * kWgTile + (int)rank * 128;
@@ -213,7 +264,7 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = pair; t < total; t += n_pairs) {
-        const WgItem it = wg_item(p, t);
+        const WgItem it = wg_item(p, s_order, t);
         const int nkb = (it.cnt + BK - 1) / BK;
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
         tc_fence_after();
@@ -251,64 +302,62 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
     // warp w reads TMEM lanes 32*(w%4).. (its rows), half (w-2)/4 of the columns
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    float* stg = s_stage + (warp - 2) * (kWgStgWarpBytes / 4);
+    uint8_t* stg = s_stage + (warp - 2) * kWgStgWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < total; t += n_pairs) {
-      const WgItem it = wg_item(p, t);
+      const WgItem it = wg_item(p, s_order, t);
       if (!wait_bounded(&tfull[acc], acc_phase, s_abort, p.err)) break;
       tc_fence_after();
-      const int i_base = it.m * kWgTile + (int)rank * 128 + q * 32;  // rows of this warp
       const uint32_t tb = tmem_base + (uint32_t)(acc * kWgTile) + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int ci = 0; ci < 4; ++ci) {
-        const int c_acc = half * 128 + ci * 32;    // accumulator column
-        const int col0 = it.n * kWgTile + c_acc;   // output column
-        uint32_t r[32];
-        if (it.cnt > 0) {
-          MOE_TMEM_LD32(tb + (uint32_t)c_acc, r);
-          MOE_TMEM_WAIT32(r);
-        } else {
+      uint32_t r[4][32];
+      if (it.cnt > 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = 0u;
-        }
-        if (col0 >= p.n_dim) continue;
-        // two halves of 16 columns through the staging rows: lane = row
-        // when staging, then (row of an 8-row group, 16-byte piece) when
-        // storing, so each row's 64 bytes go out as one segment
+        for (int ci = 0; ci < 4; ++ci) MOE_TMEM_LD32(tb + (uint32_t)(half * 128 + ci * 32), r[ci]);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float4* dst = reinterpret_cast<float4*>(stg + lane * kWgStgStride);
+        for (int ci = 0; ci < 4; ++ci) MOE_TMEM_WAIT32(r[ci]);
+      } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__uint_as_float(r[16 * hh + 4 * j]),
-                                 __uint_as_float(r[16 * hh + 4 * j + 1]),
-                                 __uint_as_float(r[16 * hh + 4 * j + 2]),
-                                 __uint_as_float(r[16 * hh + 4 * j + 3]));
-          __syncwarp();
-          const int c4 = lane & 3;
-          const int col = col0 + 16 * hh + c4 * 4;
+        for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8) {
-            const int rr = k8 * 8 + (lane >> 2);
-            const int i = i_base + rr;
-            if (i < p.m_dim && col < p.n_dim) {
-              const float4 v = *reinterpret_cast<const float4*>(stg + rr * kWgStgStride + c4 * 4);
-              *reinterpret_cast<float4*>(wg_row(p, it, i) + col) = v;
-            }
-          }
-          __syncwarp();
-        }
+          for (int j = 0; j < 32; ++j) r[ci][j] = 0u;
       }
+      // the accumulator is in registers: hand it back before any store
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (leader) mbar_arrive(&tempty[acc]);
-        else mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
+        if (leader) mbar_arrive_relaxed(&tempty[acc]);
+        else mbar_arrive_relaxed_cluster(map_to_rank(&tempty[acc], 0));
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+      // rows i0 .. i0+31 of the group's output, in the first or second map
+      const int i0 = it.m * kWgTile + (int)rank * 128 + q * 32;
+      if (i0 >= p.m_dim) continue;
+      const bool second = p.has_c1 && i0 >= p.m_split;
+      const CUtensorMap* map = second ? &tmC1 : &tmC0;
+      const int y = second ? i0 - p.m_split : i0;
+      const int z = p.splits > 1 ? it.s : it.g;
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) {
+        const int col0 = it.n * kWgTile + half * 128 + ci * 32;
+        if (col0 >= p.n_dim) continue;
+        if (lane == 0) bulk_wait_read();           // the previous chunk has left
+        __syncwarp();
+        // row `lane` = 128 bytes; its 16-byte piece j sits at j ^ (lane % 8)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(r[ci][4 * j], r[ci][4 * j + 1], r[ci][4 * j + 2], r[ci][4 * j + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(map, stg, col0, y, z);
+          bulk_commit();
+        }
+      }
     }
+    if (lane == 0) bulk_wait_all();                // every store of this warp is done
   }
 
   tc_fence_before();
@@ -339,6 +388,19 @@ sum_partials_kernel(const float* __restrict__ part, int splits, int64_t n,
     }
     reinterpret_cast<float4*>(out)[i] = a;
   }
+}
+
+// 3-D fp32 map [z][rows][cols] with 32 x 32 boxes in the 128-byte swizzle
+bool make_out_map(CUtensorMap* m, const float* base, uint64_t cols, uint64_t rows, uint64_t z) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, z};
+  const cuuint64_t strides[2] = {cols * 4, cols * rows * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int wg_pairs(int num_sms) {
@@ -386,9 +448,10 @@ bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
   if (q.rows < 1 || q.m_dim < 8 || q.n_dim < 8 || q.m_dim % 8 != 0 || q.n_dim % 8 != 0 ||
       q.p_ld < q.m_dim || q.q_ld < q.n_dim || q.p_ld % 8 != 0 || q.q_ld % 8 != 0 ||
       !aligned(q.P) || !aligned(q.Q) || !aligned(q.C0) || q.n_groups < 1 ||
-      q.rows > (int64_t)INT32_MAX - 2 * BK || encode_fn() == nullptr)
+      q.rows > (int64_t)INT32_MAX - 2 * BK || q.n_groups > 256 || encode_fn() == nullptr)
     return false;
-  if (q.C1 != nullptr && (q.m_split <= 0 || q.m_split >= q.m_dim || !aligned(q.C1)))
+  if (q.C1 != nullptr && (q.m_split <= 0 || q.m_split >= q.m_dim || q.m_split % 32 != 0 ||
+                         !aligned(q.C1)))
     return false;
   WgParams p{};
   p.rows = q.rows;
@@ -407,17 +470,24 @@ bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
   if (p.splits > 1) {
     if (q.partial == nullptr || q.C1 != nullptr || !aligned(q.partial)) return false;
     p.splits = (int)((q.rows + p.kc - 1) / p.kc);  // chunks that hold rows
-    p.C0 = q.partial;
-  } else {
-    p.C0 = q.C0;
   }
-  p.C1 = q.C1;
+  float* c0 = p.splits > 1 ? q.partial : q.C0;
+  p.has_c1 = q.C1 != nullptr;
   p.m_split = q.C1 != nullptr ? q.m_split : q.m_dim;
   p.err = q.err;
-  CUtensorMap mp, mq;
+  CUtensorMap mp, mq, mc0, mc1;
   if (!make_map(&mp, q.P, (uint64_t)q.m_dim, (uint64_t)q.rows, (uint64_t)q.p_ld * 2, 64u) ||
       !make_map(&mq, q.Q, (uint64_t)q.n_dim, (uint64_t)q.rows, (uint64_t)q.q_ld * 2, 64u))
     return false;
+  // outputs: [z][rows][n_dim] fp32, z = group (or split), boxes 32 x 32
+  const uint64_t zc = p.splits > 1 ? (uint64_t)p.splits : (uint64_t)p.G;
+  if (!make_out_map(&mc0, c0, (uint64_t)q.n_dim, (uint64_t)p.m_split, zc)) return false;
+  if (p.has_c1) {
+    if (!make_out_map(&mc1, q.C1, (uint64_t)q.n_dim, (uint64_t)(q.m_dim - q.m_split), zc))
+      return false;
+  } else {
+    mc1 = mc0;
+  }
   if (cudaFuncSetAttribute(tc2_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kWgSmem) != cudaSuccess)
     return false;
@@ -437,7 +507,8 @@ bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, tc2_wgrad_kernel, mp, mq, p) != cudaSuccess) return false;
+  if (cudaLaunchKernelEx(&cfg, tc2_wgrad_kernel, mp, mq, mc0, mc1, p) != cudaSuccess)
+    return false;
   if (p.splits > 1) {
     const int64_t n = (int64_t)q.m_dim * q.n_dim;
     const int blocks = (int)std::min<int64_t>((n / 4 + 255) / 256, (int64_t)num_sms * 4);
