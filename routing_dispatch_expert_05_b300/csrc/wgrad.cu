@@ -30,9 +30,10 @@
 // each 32 x 32 chunk with a TMA tensor store from a 128-byte-swizzled
 // staging buffer.  The output maps are 3-D (group, row, column), so a chunk
 // is clipped at its group's last row and column; the weight gradients are
-// written once, in fp32, without a pass through the load/store unit.  With one group, K may be split into chunks whose partial
-// sums go to a scratch buffer and are added afterwards (the router's
-// gradient: E x d outputs over all N tokens would otherwise be 8 tiles).
+// written once, in fp32, without a pass through the load/store unit.
+// With one group, K may be split into chunks whose partial sums go to a
+// scratch buffer and are added afterwards (the router's gradient: E x d
+// outputs over all N tokens would otherwise be 8 tiles).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
