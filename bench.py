@@ -627,6 +627,11 @@ def run_ours(args, shape, peaks, peaks_kind):
         for name in EXTRA_WORKLOADS:
             if name != shape.name:
                 extra[name] = workload_entry(W.WORKLOADS[name], peaks, args, dev)
+        # the backward pass of the same layer (moe_backward, routing held
+        # fixed), outside the timed forward steps
+        if (shape.expert == W.EXPERT_SWIGLU and shape.dtype == W.DTYPE_BF16 and
+                shape.n_shared == 0 and not shape.has_bias):
+            extra["backward_" + shape.name] = backward_times(shape, peaks, steps=10, warmup=3)
         res["config"]["workloads"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         n_s, el = oracle_sample(shape, inputs, target_s=args.cpu_seconds)
@@ -687,7 +692,7 @@ def run_reference(args, shape):
     return res, rank
 
 
-def run_backward(args, shape, peaks, peaks_kind):
+def backward_times(shape, peaks, steps, warmup):
     """Time moe_backward (one GPU): recompute + data and weight gradients.
 
     Algorithmic FLOPs per step, SwiGLU experts: the recomputed g, u (2 d F)
@@ -715,29 +720,38 @@ def run_backward(args, shape, peaks, peaks_kind):
         g["d_b_router"] = f32(E)
     grads = M.make_grads(**g)
     ws = M.MoEWorkspace(cfg, backward=True)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         M.moe_backward(cfg, t["x"], weights, dout, 1.0, grads, ws)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         M.moe_backward(cfg, t["x"], weights, dout, 1.0, grads, ws)
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     flop = 16.0 * d * F * N * k + 3 * 2.0 * N * E * d
     tflops = flop / (ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
     assert M.moe_read_device_error(ws) == M.MOE_OK
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(N / (ms * 1e-3), 1),
+            "gemm_tflops_effective": round(tflops, 1),
+            "frac_of_burst_bf16": round(tflops / peaks["bf16_tflops"], 4),
+            "steps": steps, "warmup": warmup}
+
+
+def run_backward(args, shape, peaks, peaks_kind):
+    """Time moe_backward alone (one GPU) as the bench line's metric."""
+    bt = backward_times(shape, peaks, args.steps, args.warmup)
+    N, d, E, k, F = shape.n_tokens, shape.d_model, shape.n_experts, shape.top_k, shape.d_ff
     return {"metric": "MoE-layer bwd tokens/s on 1 B300 (routing held fixed)",
-            "value": round(N / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "value": bt["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": bt["ms_per_step"],
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": shape.name, "n_tokens": N, "d_model": d, "n_experts": E,
                        "top_k": k, "d_ff": F},
-            "gemm_tflops_effective": round(tflops, 1),
-            "frac_of_burst_bf16": round(tflops / peak, 4),
+            "gemm_tflops_effective": bt["gemm_tflops_effective"],
+            "frac_of_burst_bf16": bt["frac_of_burst_bf16"],
             "peak_kind": f"{peaks_kind} burst bf16"}
 
 
