@@ -202,3 +202,63 @@ def test_backward_is_deterministic():
     torch.cuda.synchronize()
     for name, v in g.items():
         assert torch.equal(v, first[name]), name
+
+
+def test_backward_full_size_sampled():
+    """The Qwen3-style layer at full size (16384 tokens, 128 experts, top-8,
+    the skewed grouping of the workload: 2 to ~16,000 rows per expert), the
+    backward as the bench times it, checked on samples the oracle computes
+    exactly from the GPU's own routing:
+    - dx of 16 tokens: with d_balance = 0 a token's input gradient depends on
+      that token alone, so the oracle runs on those tokens;
+    - the weight gradients of two experts (one of a few dozen rows, one of a
+      few hundred): an expert's gradient sums over the assignments routed to
+      it, so the oracle runs on exactly the tokens that chose it, with every
+      other assignment of theirs marked as not kept (their routing weights
+      still normalise over all of a token's selected logits)."""
+    shape = W.WORKLOADS["qwen3_moe"]
+    assert shape.expert == W.EXPERT_SWIGLU and shape.n_shared == 0
+    inp = W.make_inputs(shape)
+    t = M.upload(inp)
+    cfg = M.make_config(shape)
+    weights = M.make_weights(t)
+    N, d, E, k = shape.n_tokens, shape.d_model, shape.n_experts, shape.top_k
+    dout = np.random.default_rng(11).standard_normal((N, d)).astype(np.float32)
+    dout = W.bits_to_f32(W.bf16_bits(dout))
+    dout_t = torch.from_numpy(dout).to(torch.bfloat16).cuda()
+    g = _grad_buffers(shape, inp)
+    ws = M.MoEWorkspace(cfg, backward=True)
+    M.moe_backward(cfg, t["x"], weights, dout_t, 0.0, M.make_grads(**g), ws)
+    fws = M.MoEWorkspace(cfg)
+    idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(N, k, dtype=torch.float32, device="cuda")
+    M.moe_router_topk(cfg, t["x"], weights, None, idx, w, None, fws)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_error(ws) == M.MOE_OK
+    idx_np = to_np(idx).astype(np.int64)
+    disp = O.dispatch(idx_np, E, shape.capacity_factor)
+    kept = (disp["row_of_slot"] >= 0).reshape(idx_np.shape)
+    counts = disp["counts"]
+
+    def oracle_on(tokens, kept_sub):
+        vals = dict(inp.values)
+        vals["x"] = inp.values["x"][tokens]
+        sub = shape.replace(n_tokens=len(tokens))
+        return OB.layer_backward(sub, vals, dout[tokens], 0.0,
+                                 route_fixed=(idx_np[tokens], kept_sub, counts))
+
+    toks = np.sort(np.random.default_rng(5).choice(N, 16, replace=False))
+    ref = oracle_on(toks, kept[toks])
+    assert_grad_close(to_np(g["dx"])[toks], ref["dx"], "dx (16 sampled tokens)")
+    del ref
+
+    rows = counts.astype(np.int64)
+    small = int(np.nonzero((rows >= 20) & (rows <= 80))[0][0])
+    medium = int(np.nonzero((rows >= 200) & (rows <= 600))[0][0])
+    for e in (small, medium):
+        tok_e = np.nonzero((idx_np == e).any(axis=1))[0]
+        kept_e = kept[tok_e] & (idx_np[tok_e] == e)
+        ref = oracle_on(tok_e, kept_e)
+        for name in ("d_w1", "d_w3", "d_w2"):
+            assert_grad_close(to_np(g[name][e]), ref[name][e], f"{name}[{e}] ({rows[e]} rows)")
+        del ref
