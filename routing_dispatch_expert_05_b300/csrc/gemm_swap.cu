@@ -131,7 +131,7 @@ __device__ __forceinline__ void swiglu_chunk(const Params& p, const Tile& tl, in
     const int row = tl.row0 + c0 + i;
     if (row < tl.row_end)
       C[(int64_t)row * p.n_out + f] =
-          __float2bfloat16_rn(silu_f32(__uint_as_float(g[i])) * __uint_as_float(u[i]));
+          __float2bfloat16_rn(silu_fast(__uint_as_float(g[i])) * __uint_as_float(u[i]));
   }
 }
 
@@ -146,7 +146,7 @@ __device__ __forceinline__ void silu_bias_chunk(const Params& p, const Tile& tl,
   for (int i = 0; i < 16; ++i) {
     const int row = tl.row0 + c0 + i;
     if (row < tl.row_end)
-      C[(int64_t)row * p.n_out + f] = __float2bfloat16_rn(silu_f32(__uint_as_float(r[i]) + b));
+      C[(int64_t)row * p.n_out + f] = __float2bfloat16_rn(silu_fast(__uint_as_float(r[i]) + b));
   }
 }
 

@@ -371,7 +371,7 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int 
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          v[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+          v[j] = silu_fast(__uint_as_float(g[j])) * __uint_as_float(u[j]);
         store_chunk(p, tl, lane, row_base, col0, v, stg_f, stg_w);
       }
       if (ci + 1 < kCh) {
@@ -411,7 +411,7 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tl, int 
       }
       if (p.epilogue == kEpiSiluBias) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
+        for (int j = 0; j < 32; ++j) v[j] = silu_fast(v[j]);
       }
       store_chunk(p, tl, lane, row_base, col0, v, stg_f, stg_w);
     }
