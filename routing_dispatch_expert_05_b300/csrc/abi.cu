@@ -774,7 +774,8 @@ moe_status_t forward_core(const moe_config_t& c, const Layout& L, const Scratch&
   // without a capacity nothing is dropped: the combine need not read row_of_slot
   if (compact)
     launch_combine_slots(y, y_e8, capacity_of(c) < 0 ? nullptr : ros, shared_out, out,
-                         c.n_tokens, c.top_k, c.d_model, c.dtype == MOE_BF16, num_sms(), st);
+                         c.n_tokens, c.top_k, c.d_model, c.dtype == MOE_BF16, num_sms(), st,
+                         sc.err);
   else
     launch_combine(y, ros, wts, shared_out, out, c.n_tokens, c.top_k, c.d_model,
                    c.dtype == MOE_BF16, num_sms(), st);

@@ -217,9 +217,12 @@ void launch_combine(const float* y, const int32_t* row_of_slot, const float* w,
 // y_e8 [N*k, ceil(d/32)] (value = y16 * 2^(y_e8 - 127) for its 32 columns)
 // compact expert outputs already weighted and in slot order (row t*k + j);
 // row_of_slot null: no slot was dropped (a layer without capacity)
+// err (nullable): the bulk-copy kernel's timeout word; without it, or where
+// a token's rows do not fit a stage, the register-fed kernel runs
 void launch_combine_slots(const void* y16, const uint8_t* y_e8, const int32_t* row_of_slot,
                           const float* shared, void* out, int64_t n_tokens, int top_k,
-                          int d_model, int is_bf16, int num_sms, cudaStream_t st);
+                          int d_model, int is_bf16, int num_sms, cudaStream_t st,
+                          int32_t* err = nullptr);
 constexpr int kYScaleBlock = 32;    // columns per compact-output exponent
 
 // ---- backward (backward.cu) -----------------------------------------------
