@@ -117,9 +117,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 // TMA box of 64 MN-elements x 64 K-rows lands it: K-rows of 128 bytes, 8-row
 // groups 1024 bytes apart (stride offset), consecutive 64-element MN atoms
 // 8 KB apart (leading offset).  A K-step of 16 moves 16 rows: 2048 bytes.
-__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo = 8192) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= (uint64_t)(8192 >> 4) << 16;                   // leading byte offset: next MN atom
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;        // leading byte offset: next MN atom
   d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset: next 8 K-rows
   d |= (uint64_t)1 << 46;                             // descriptor version
   d |= (uint64_t)2 << 61;                             // 128-byte swizzle

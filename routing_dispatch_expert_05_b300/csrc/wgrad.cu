@@ -9,10 +9,10 @@
 //
 // Both operands are read in place as MN-major tcgen05 operands: a k-block is
 // 64 token rows, and the pair's 256 x 256 tile takes, per CTA, 128 columns
-// of P (two TMA boxes of 64 columns x 64 rows, 128-byte swizzle) and 128
+// of P (two TMA boxes of 64 columns x 128 rows, 128-byte swizzle) and 128
 // columns of Q the same way, so no transposed copy of any activation is
 // made.  Groups are contiguous row ranges of any start; a group whose row
-// count is not a multiple of 64 has a last k-block of which only the first
+// count is not a multiple of 128 has a last stage of which only the first
 // ceil(rem / 16) slices of 16 rows are multiplied.  The rows after a group
 // inside such a slice must be zero: the grouped buffers of the backward pass
 // pad every group to a multiple of 16 rows with zero rows, and a group that
@@ -21,7 +21,7 @@
 // kDevBadRow and its tiles are written as zeros.
 //
 // The pipeline is the pair kernel's of the grouped GEMM: warp 0 of each CTA
-// loads its halves into a 6-stage ring (completing on the leader's full
+// loads its halves into a 3-stage ring (completing on the leader's full
 // barrier), the leader's warp 1 issues tcgen05.mma.cta_group::2 and commits
 // to both CTAs' barriers, and eight epilogue warps per CTA read the fp32
 // accumulator (two of them in TMEM, 512 columns); every wait is bounded.
@@ -48,8 +48,13 @@ namespace tc {
 namespace {
 
 constexpr int kWgTile = 256;                        // output tile (M and N)
-constexpr int kWgStages = 6;
-constexpr uint32_t kWgHalf = 128 * BK * 2;          // one operand half per CTA: 16 KB
+// A stage holds 128 token rows: per CTA and operand two TMA boxes of 64
+// columns x 128 rows (16 KB each).  (With 64-row k-blocks, four 8 KB boxes
+// per CTA and k-block, issuing the copies took nearly as long as the MMAs.)
+constexpr int kWgK = 128;                            // token rows per stage
+constexpr int kWgStages = 3;
+constexpr uint32_t kWgBox = 64 * kWgK * 2;           // one 64-column box: 16 KB
+constexpr uint32_t kWgHalf = 2 * kWgBox;             // one operand half per CTA: 32 KB
 constexpr uint32_t kWgStageBytes = 2 * kWgHalf;     // P half + Q half
 constexpr int kWgEpiWarps = 8;
 constexpr int kWgThreads = (2 + kWgEpiWarps) * 32;
@@ -192,7 +197,7 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
       for (int t = pair; t < total; t += n_pairs) {
         const WgItem it = wg_item(p, s_order, t);
         if (it.bad && leader) set_device_error(p.err, kDevBadRow);
-        const int nkb = (it.cnt + BK - 1) / BK;
+        const int nkb = (it.cnt + kWgK - 1) / kWgK;
         const int colP = it.m * kWgTile + (int)rank * 128;
         const int colQ = it.n * kWgTile + (int)rank * 128;
         bool ok = true;
@@ -200,13 +205,13 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
           if (!wait_bounded(&empty[stage], phase ^ 1, s_abort, p.err)) { ok = false; break; }
           const uint32_t bar = map_to_rank(&full[stage], 0);
           if (leader) mbar_expect_tx(&full[stage], 2 * kWgStageBytes);
-          const int krow = (int)(it.k0 + (int64_t)kb * BK);
+          const int krow = (int)(it.k0 + (int64_t)kb * kWgK);
           uint8_t* a = sP + stage * kWgHalf;
           uint8_t* b = sQ + stage * kWgHalf;
           tma_load_2d_pair(a, &tmP, bar, colP, krow);
-          tma_load_2d_pair(a + 8192, &tmP, bar, colP + 64, krow);
+          tma_load_2d_pair(a + kWgBox, &tmP, bar, colP + 64, krow);
           tma_load_2d_pair(b, &tmQ, bar, colQ, krow);
-          tma_load_2d_pair(b + 8192, &tmQ, bar, colQ + 64, krow);
+          tma_load_2d_pair(b + kWgBox, &tmQ, bar, colQ + 64, krow);
           used |= 1u << stage;
           last_phases = (last_phases & ~(1u << stage)) | (phase << stage);
           if (++stage == kWgStages) { stage = 0; phase ^= 1; }
@@ -237,7 +242,7 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
       uint32_t acc_phase = 0;
       for (int t = pair; t < total; t += n_pairs) {
         const WgItem it = wg_item(p, s_order, t);
-        const int nkb = (it.cnt + BK - 1) / BK;
+        const int nkb = (it.cnt + kWgK - 1) / kWgK;
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kWgTile);
@@ -248,10 +253,10 @@ tc2_wgrad_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant_
           const uint32_t a0 = smem_u32(sP + stage * kWgHalf);
           const uint32_t b0 = smem_u32(sQ + stage * kWgHalf);
           // slices of 16 rows that hold rows of this group
-          const int n16 = kb + 1 < nkb ? BK / 16 : (it.cnt - kb * BK + 15) / 16;
+          const int n16 = kb + 1 < nkb ? kWgK / 16 : (it.cnt - kb * kWgK + 15) / 16;
           for (int kk = 0; kk < n16; ++kk)
-            umma_pair(d, sdesc_sw128_mn(a0 + kk * 2048), sdesc_sw128_mn(b0 + kk * 2048), idesc,
-                      (kb | kk) != 0);
+            umma_pair(d, sdesc_sw128_mn(a0 + kk * 2048, kWgBox),
+                      sdesc_sw128_mn(b0 + kk * 2048, kWgBox), idesc, (kb | kk) != 0);
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == kWgStages) { stage = 0; phase ^= 1; }
         }
@@ -420,7 +425,7 @@ bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
   if (q.rows < 1 || q.m_dim < 8 || q.n_dim < 8 || q.m_dim % 8 != 0 || q.n_dim % 8 != 0 ||
       q.p_ld < q.m_dim || q.q_ld < q.n_dim || q.p_ld % 8 != 0 || q.q_ld % 8 != 0 ||
       !aligned(q.P) || !aligned(q.Q) || !aligned(q.C0) || q.n_groups < 1 ||
-      q.rows > (int64_t)INT32_MAX - 2 * BK || q.n_groups > 256 || encode_fn() == nullptr)
+      q.rows > (int64_t)INT32_MAX - 2 * kWgK || q.n_groups > 256 || encode_fn() == nullptr)
     return false;
   if (q.C1 != nullptr && (q.m_split <= 0 || q.m_split >= q.m_dim || q.m_split % 32 != 0 ||
                          !aligned(q.C1)))
@@ -448,8 +453,10 @@ bool launch_wgrad(const WgradProblem& q, int num_sms, cudaStream_t st) {
   p.m_split = q.C1 != nullptr ? q.m_split : q.m_dim;
   p.err = q.err;
   CUtensorMap mp, mq, mc0, mc1;
-  if (!make_map(&mp, q.P, (uint64_t)q.m_dim, (uint64_t)q.rows, (uint64_t)q.p_ld * 2, 64u) ||
-      !make_map(&mq, q.Q, (uint64_t)q.n_dim, (uint64_t)q.rows, (uint64_t)q.q_ld * 2, 64u))
+  if (!make_map(&mp, q.P, (uint64_t)q.m_dim, (uint64_t)q.rows, (uint64_t)q.p_ld * 2,
+                (uint32_t)kWgK) ||
+      !make_map(&mq, q.Q, (uint64_t)q.n_dim, (uint64_t)q.rows, (uint64_t)q.q_ld * 2,
+                (uint32_t)kWgK))
     return false;
   // outputs: [z][rows][n_dim] fp32, z = group (or split), boxes 32 x 32
   const uint64_t zc = p.splits > 1 ? (uint64_t)p.splits : (uint64_t)p.G;
