@@ -617,6 +617,25 @@ def test_forward_parity(name, N):
     assert D.device_error() == M.MOE_OK
 
 
+def test_forward_combine_register_path():
+    """A token whose k compact rows do not fit a bulk-copy stage (d = 2304,
+    top-8: 37.4 KB per token) takes the register-fed combine; the whole
+    output against the oracle."""
+    shape = W.WORKLOADS["qwen3_moe"].replace(name="wide_d", n_tokens=512, n_experts=16,
+                                             d_model=2304)
+    assert shape.top_k * shape.d_model * 2 + shape.top_k * shape.d_model // 32 > 36 * 1024
+    inp = W.make_inputs(shape)
+    D = Device(inp)
+    out, st = _forward(D)
+    ref = O.forward(shape, inp.values)
+    lg_gpu = _gpu_logits(D)
+    keys = O.selection_keys(ref["logits"], shape.route, inp.values.get("sel_bias"))
+    amb, _ = set_ambiguous_tokens(keys, shape.top_k, logit_margin(lg_gpu, ref["logits"]))
+    assert (~amb).mean() > 0.9
+    assert_output_close(to_np(out)[~amb], ref["out_exact"][~amb], shape.dtype, "wide_d")
+    assert D.device_error() == M.MOE_OK
+
+
 @pytest.mark.parametrize("name,N", [("qwen3_moe", 4096), ("deepseek_v3_block", 4096)])
 def test_forward_whole_output_large(name, N):
     """Every output of a 4096-token layer against the oracle: the expert
