@@ -386,14 +386,19 @@ typedef struct {
   float *d_ws2;
 } moe_grads_t;
 
-/* Bytes of workspace moe_backward needs (the forward's plus the gradient
- * intermediates: recomputed activations, transposed operands). */
+/* Bytes of workspace moe_backward needs: the forward's routing and grouping
+ * (each expert's rows padded to a multiple of 16), the recomputed
+ * activations and the gradient intermediates, all in grouped row order. */
 MOE_API moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
 /* The backward pass: recomputes the forward's routing, grouping and expert
  * activations from x, then runs the gradients back through the combine, the
  * experts and shared experts (data and weight gradients on the tensor
- * cores) and the router.  x [N, d] and dout [N, d] are bf16 device arrays;
+ * cores; the weights and activations are read in place, the weight
+ * gradients accumulated per expert over its rows in fp32) and the router.
+ * The routing weights' gradient <dout, y> is formed as <dout W2, h> +
+ * <dout, b2>, so the expert outputs y are not recomputed.  x [N, d] and
+ * dout [N, d] are bf16 device arrays;
  * x, dout and the gradient arrays 16-byte aligned (else
  * MOE_ERR_INVALID_ARG).  Supported: bf16 layers of either expert kind
  * (SwiGLU; SiLU-MLP with or without biases), with or without shared
