@@ -7,8 +7,8 @@
 // and backward passes ("DeepSeek 5.7: MoE from scratch", Backward pass: each
 // expert's weight gradient is accumulated over the tokens routed to it).
 //
-// Both operands are read in place as MN-major tcgen05 operands: a k-block is
-// 64 token rows, and the pair's 256 x 256 tile takes, per CTA, 128 columns
+// Both operands are read in place as MN-major tcgen05 operands: a stage is
+// 128 token rows, and the pair's 256 x 256 tile takes, per CTA, 128 columns
 // of P (two TMA boxes of 64 columns x 128 rows, 128-byte swizzle) and 128
 // columns of Q the same way, so no transposed copy of any activation is
 // made.  Groups are contiguous row ranges of any start; a group whose row
