@@ -204,20 +204,24 @@ def test_backward_is_deterministic():
         assert torch.equal(v, first[name]), name
 
 
-def test_backward_full_size_sampled():
-    """The Qwen3-style layer at full size (16384 tokens, 128 experts, top-8,
-    the skewed grouping of the workload: 2 to ~16,000 rows per expert), the
-    backward as the bench times it, checked on samples the oracle computes
-    exactly from the GPU's own routing:
+@pytest.mark.parametrize("name", ["qwen3_moe", "deepseek_v3_block"])
+def test_backward_full_size_sampled(name):
+    """A full-size layer -- Qwen3-style (16384 tokens, 128 experts, top-8,
+    the skewed grouping of the workload: 2 to ~16,000 rows per expert) or
+    DeepSeek-style (8192 tokens, 64 experts, top-6, sigmoid routing with a
+    selection bias, two shared experts) -- the backward as the bench times
+    it, checked on samples the oracle computes exactly from the GPU's own
+    routing:
     - dx of 16 tokens: with d_balance = 0 a token's input gradient depends on
       that token alone, so the oracle runs on those tokens;
-    - the weight gradients of two experts (one of a few dozen rows, one of a
-      few hundred): an expert's gradient sums over the assignments routed to
-      it, so the oracle runs on exactly the tokens that chose it, with every
-      other assignment of theirs marked as not kept (their routing weights
-      still normalise over all of a token's selected logits)."""
-    shape = W.WORKLOADS["qwen3_moe"]
-    assert shape.expert == W.EXPERT_SWIGLU and shape.n_shared == 0
+    - the weight gradients of two experts (the smallest of at least 20
+      rows, and one of a few hundred): an expert's gradient sums over the
+      assignments routed to it, so the oracle runs on exactly the tokens
+      that chose it, with every other assignment of theirs marked as not
+      kept (their routing weights still normalise over all of a token's
+      selected logits)."""
+    shape = W.WORKLOADS[name]
+    assert shape.expert == W.EXPERT_SWIGLU and not shape.has_bias
     inp = W.make_inputs(shape)
     t = M.upload(inp)
     cfg = M.make_config(shape)
@@ -253,7 +257,9 @@ def test_backward_full_size_sampled():
     del ref
 
     rows = counts.astype(np.int64)
-    small = int(np.nonzero((rows >= 20) & (rows <= 80))[0][0])
+    # the smallest expert of at least 20 rows, and one of a few hundred
+    cand = np.nonzero(rows >= 20)[0]
+    small = int(cand[np.argmin(rows[cand])])
     medium = int(np.nonzero((rows >= 200) & (rows <= 600))[0][0])
     for e in (small, medium):
         tok_e = np.nonzero((idx_np == e).any(axis=1))[0]
