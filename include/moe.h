@@ -178,7 +178,10 @@ MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
 /* ---- stages ----------------------------------------------------------- */
 
-/* Router GEMM plus selection.
+/* Router GEMM plus selection ("Implementing Mixed Expert (MoE) layers", the
+ * gate and its top-k routing probabilities; "Hands-on build guide", step 2:
+ * the gate is a Linear layer, then softmax and top-k; "DeepSeek 5.7",
+ * section 2: sigmoid affinities with a selection-only bias).
  * x [N, d] (device, layer dtype); weights->w_router, ->b_router,
  * ->sel_bias used.  Writes idx [N, k] int32 and w [N, k] fp32 (device), and
  * if non-NULL logits [N, E] fp32 (device).  stats->counts receives the
@@ -317,8 +320,12 @@ MOE_API moe_status_t moe_combine(const moe_config_t *cfg, const float *y,
 
 /* ---- the whole layer ---------------------------------------------------- */
 
-/* All stages above on one stream, intermediates in `ws`
- * (moe_workspace_size bytes).  x [N, d] and out [N, d] are device memory. */
+/* The sparse-MoE FFN layer ("DeepSeek 5.7: MoE from scratch", sections 1-5:
+ * route, group tokens by expert, run each expert on its tokens, combine the
+ * weighted outputs, plus the always-on shared experts; "Tutorial -- MoE SER
+ * Expert Routing", section 4: the load-balance statistic).  All stages
+ * above on one stream, intermediates in `ws` (moe_workspace_size bytes).
+ * x [N, d] and out [N, d] are device memory. */
 MOE_API moe_status_t moe_forward(const moe_config_t *cfg, const void *x,
                          const moe_weights_t *weights, void *out,
                          moe_stats_t *stats, void *ws, size_t ws_bytes,

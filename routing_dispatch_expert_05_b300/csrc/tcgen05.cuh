@@ -223,7 +223,9 @@ __device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a, uint64_t 
       : "memory");
 }
 // arrive once on `bar` (same offset) in every CTA of `mask` when all prior
-// MMAs of this thread are complete
+// MMAs of this thread are complete.  The `multicast::cluster` form is an
+// mbarrier arrive delivered to both CTAs of the pair, not a multicast load:
+// no data moves between the CTAs' memories through it.
 __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
