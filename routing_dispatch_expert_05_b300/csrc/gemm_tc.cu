@@ -90,6 +90,7 @@ struct Params {
   const int32_t* offsets;     // [G+1] device or null (one group of `rows`)
   int n_groups;
   int rows;
+  int a_rows;                 // rows of the A tensor map (a row past them reads zeros)
   int K;                      // reduction length (multiple of 64 per sub-block)
   int n_out;                  // output columns
   int swiglu;                 // 1: B = (W1 rows, W3 rows), epilogue silu(g)*u
@@ -799,7 +800,14 @@ tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (lane == 0) {
             if (leader) mbar_expect_tx(&full[stage], 2 * kStageBytes2);
             uint8_t* b = sB + stage * kTileB2;
-            if (!gather) tma_load_2d_pair(a, &tmA, bar, kb * BK, tl.row0 + (int)rank * 128);
+            if (!gather) {
+              // a CTA whose 128 rows all lie past the group's end multiplies
+              // padding: it loads from past the end of A, which TMA fills
+              // with zeros without reading memory (no traffic, and zero
+              // operands cost the tensor cores less power)
+              const int arow = tl.row0 + (int)rank * 128;
+              tma_load_2d_pair(a, &tmA, bar, kb * BK, arow < tl.row_end ? arow : p.a_rows);
+            }
             if (p.b_mn) {
               // this CTA's 128 columns as two 64-column boxes, K-rows
               // g*k_sub + kk of B0 / B1
@@ -1002,6 +1010,7 @@ bool launch_tc_gemm(const TcProblem& q, int num_sms, cudaStream_t st) {
   p.offsets = q.offsets;
   p.n_groups = q.n_groups;
   p.rows = (int)q.rows;
+  p.a_rows = (int)q.a_rows;
   p.K = q.K;
   p.n_out = q.n_out;
   p.swiglu = q.swiglu;
