@@ -348,8 +348,9 @@ MOE_API moe_status_t moe_forward_timed(const moe_config_t *cfg, const void *x,
  * out_host [N, d] (use page-locked host memory for asynchronous copies).
  * Weights and stats are device memory.  The results equal moe_forward's.
  *   - Without a capacity limit and with N >= 8192, the tokens are split into
- *     up to four chunks (whole 32-token statistics groups) and the copies of
- *     one chunk overlap the compute of another: the copies run on two
+ *     up to four chunks (whole 32-token statistics groups; two equal ones,
+ *     or 3:5:3 / 3:5:5:3 so that the first and last are short) and the
+ *     copies of one chunk overlap the compute of another: the copies run on two
  *     streams that the library creates, with some events, on the first such
  *     call on each device (kept until exit); the compute runs on `stream`;
  *     the statistics are reduced once over all chunks.  When the call

@@ -858,11 +858,25 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
   char* xd = at<char>(ws, L.x_stage);
   char* od = at<char>(ws, L.out_stage);
   const int nch = (int)std::min<int64_t>(kHostChunks, c.n_tokens / kHostChunkMin);
-  // chunks start on selection-CTA boundaries (the same per-CTA sums as one
-  // launch over all tokens)
-  const int64_t chunk =
-      ceil_div64(ceil_div64(c.n_tokens, nch), kRouteTokensPerCta) * kRouteTokensPerCta;
-  const int nrun = (int)ceil_div64(c.n_tokens, chunk);   // chunks holding tokens
+  // Chunk sizes in the proportions kChunkShare[nch]: the first chunk's copy
+  // in (the fill) and the last chunk's compute and copy out (the drain)
+  // overlap nothing, so with three or four chunks those two are smaller.
+  // Chunks start on selection-CTA boundaries (the same per-CTA sums as one
+  // launch over all tokens).
+  static constexpr int kChunkShare[kHostChunks + 1][kHostChunks] = {
+      {0, 0, 0, 0}, {1, 0, 0, 0}, {1, 1, 0, 0}, {3, 5, 3, 0}, {3, 5, 5, 3}};
+  int64_t bound[kHostChunks + 1] = {};
+  {
+    int total = 0, acc = 0;
+    for (int i = 0; i < nch; ++i) total += kChunkShare[nch][i];
+    for (int i = 1; i < nch; ++i) {
+      acc += kChunkShare[nch][i - 1];
+      const int64_t b = c.n_tokens * acc / total;
+      bound[i] = b / kRouteTokensPerCta * kRouteTokensPerCta;
+    }
+    bound[nch] = c.n_tokens;
+  }
+  const int nrun = nch;
   bool ok = cudaEventRecord(hp.start, st) == cudaSuccess &&
             cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(hp.d2h, hp.start, 0) == cudaSuccess;
@@ -875,8 +889,8 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
     last.balance = stats->balance;
   }
   for (int i = 0; ok && i < nrun; ++i) {
-    const int64_t s0 = (int64_t)i * chunk;
-    const int64_t n = std::min(chunk, c.n_tokens - s0);
+    const int64_t s0 = bound[i];
+    const int64_t n = bound[i + 1] - s0;
     ok = cudaMemcpyAsync(xd + s0 * row, xh + s0 * row, n * row, cudaMemcpyHostToDevice,
                          hp.h2d) == cudaSuccess &&
          cudaEventRecord(hp.in[i], hp.h2d) == cudaSuccess &&

@@ -182,6 +182,20 @@ def workspace_size(cfg: MoEConfig) -> int:
     return n.value
 
 
+def _rows_arg(t, cfg, name):
+    """A token-row argument ([n_tokens, d_model] in the layer dtype) as an
+    address.  A tensor smaller than the config declares is refused here: the
+    library takes plain pointers and would read or write past its end."""
+    if isinstance(t, torch.Tensor):
+        es = 2 if cfg.dtype == MOE_BF16 else 4
+        need = int(cfg.n_tokens) * int(cfg.d_model) * es
+        have = t.numel() * t.element_size()
+        if have < need:
+            raise ValueError(f"{name}: {have} bytes, the config needs {need} "
+                             f"({cfg.n_tokens} tokens x {cfg.d_model})")
+    return ptr(t)
+
+
 def _ws(ws):
     if ws is None:
         return None, 0
@@ -194,7 +208,8 @@ def _ws(ws):
 def moe_router_topk(cfg, x, weights: MoEWeights, logits, idx, w, stats, ws, stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_router_topk(
-        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(logits), ptr(idx),
+        ctypes.byref(cfg), _rows_arg(x, cfg, "x"), ctypes.byref(weights), ptr(logits),
+        ptr(idx),
         ptr(w), ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_router_topk")
 
@@ -211,7 +226,7 @@ def moe_dispatch_permute(cfg, idx, x, offsets, row_of_slot, token_of_row, x_perm
                          stats, ws, stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_dispatch_permute(
-        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(offsets), ptr(row_of_slot),
+        ctypes.byref(cfg), ptr(idx), _rows_arg(x, cfg, "x"), ptr(offsets), ptr(row_of_slot),
         ptr(token_of_row), ptr(x_perm),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_dispatch_permute")
@@ -222,7 +237,8 @@ def moe_dispatch_permute_room(cfg, idx, x, room, offsets, row_of_slot, token_of_
     """moe_dispatch_permute with a per-expert capacity room [E] (int32)."""
     wp, wb = _ws(ws)
     _check(load_library().moe_dispatch_permute_room(
-        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(room), ptr(offsets), ptr(row_of_slot),
+        ctypes.byref(cfg), ptr(idx), _rows_arg(x, cfg, "x"), ptr(room), ptr(offsets),
+        ptr(row_of_slot),
         ptr(token_of_row), ptr(x_perm),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_dispatch_permute_room")
@@ -234,7 +250,7 @@ def moe_dispatch_permute_noalloc(cfg, idx, x, offsets, row_of_slot, token_of_row
     the library device memory (its scratch is a fixed array in the library:
     n_tokens <= 65536; overlapping calls race)."""
     _check(load_library().moe_dispatch_permute_noalloc(
-        ctypes.byref(cfg), ptr(idx), ptr(x), ptr(offsets), ptr(row_of_slot),
+        ctypes.byref(cfg), ptr(idx), _rows_arg(x, cfg, "x"), ptr(offsets), ptr(row_of_slot),
         ptr(token_of_row), ptr(x_perm),
         ctypes.byref(stats) if stats is not None else None, _stream(stream)),
         "moe_dispatch_permute_noalloc")
@@ -251,7 +267,7 @@ def moe_expert_up_gather(cfg, x, token_of_row, offsets, weights: MoEWeights, h, 
                          stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_expert_up_gather(
-        ctypes.byref(cfg), ptr(x), ptr(token_of_row), ptr(offsets),
+        ctypes.byref(cfg), _rows_arg(x, cfg, "x"), ptr(token_of_row), ptr(offsets),
         ctypes.byref(weights), ptr(h), wp, wb, _stream(stream)), "moe_expert_up_gather")
 
 
@@ -272,7 +288,7 @@ def moe_grouped_ffn(cfg, x_perm, offsets, weights: MoEWeights, h, y, ws, stream=
 def moe_shared_ffn(cfg, x, weights: MoEWeights, h_shared, shared_out, ws, stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_shared_ffn(
-        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(h_shared),
+        ctypes.byref(cfg), _rows_arg(x, cfg, "x"), ctypes.byref(weights), ptr(h_shared),
         ptr(shared_out), wp, wb, _stream(stream)), "moe_shared_ffn")
 
 
@@ -280,13 +296,14 @@ def moe_combine(cfg, y, row_of_slot, w, shared_out, out, ws, stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_combine(
         ctypes.byref(cfg), ptr(y), ptr(row_of_slot), ptr(w), ptr(shared_out),
-        ptr(out), wp, wb, _stream(stream)), "moe_combine")
+        _rows_arg(out, cfg, "out"), wp, wb, _stream(stream)), "moe_combine")
 
 
 def moe_forward(cfg, x, weights: MoEWeights, out, stats, ws, stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_forward(
-        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(out),
+        ctypes.byref(cfg), _rows_arg(x, cfg, "x"), ctypes.byref(weights),
+        _rows_arg(out, cfg, "out"),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_forward")
 
@@ -309,7 +326,8 @@ def moe_forward_timed(cfg, x, weights: MoEWeights, out, stats, ws, events, strea
     arr = (ctypes.c_void_p * len(handles))(*handles)
     wp, wb = _ws(ws)
     _check(load_library().moe_forward_timed(
-        ctypes.byref(cfg), ptr(x), ctypes.byref(weights), ptr(out),
+        ctypes.byref(cfg), _rows_arg(x, cfg, "x"), ctypes.byref(weights),
+        _rows_arg(out, cfg, "out"),
         ctypes.byref(stats) if stats is not None else None, wp, wb, _stream(stream),
         arr, len(handles)), "moe_forward_timed")
 
@@ -318,7 +336,8 @@ def moe_forward_host(cfg, x_host, weights: MoEWeights, out_host, stats, ws,
                      stream=None):
     wp, wb = _ws(ws)
     _check(load_library().moe_forward_host(
-        ctypes.byref(cfg), ptr(x_host), ctypes.byref(weights), ptr(out_host),
+        ctypes.byref(cfg), _rows_arg(x_host, cfg, "x_host"), ctypes.byref(weights),
+        _rows_arg(out_host, cfg, "out_host"),
         ctypes.byref(stats) if stats is not None else None, wp, wb,
         _stream(stream)), "moe_forward_host")
 
@@ -341,9 +360,10 @@ def moe_backward(cfg, x, weights: MoEWeights, dout, d_balance, grads: MoEGrads, 
     """Gradients of <dout, out> + d_balance * balance (routing held fixed)
     into the fp32 arrays of `grads`; ws holds backward_workspace_size bytes."""
     wp, wb = _ws(ws)
-    _check(load_library().moe_backward(ctypes.byref(cfg), ptr(x), ctypes.byref(weights),
-                                       ptr(dout), float(d_balance), ctypes.byref(grads), wp,
-                                       wb, _stream(stream)), "moe_backward")
+    _check(load_library().moe_backward(ctypes.byref(cfg), _rows_arg(x, cfg, "x"),
+                                       ctypes.byref(weights), _rows_arg(dout, cfg, "dout"),
+                                       float(d_balance), ctypes.byref(grads), wp, wb,
+                                       _stream(stream)), "moe_backward")
 
 
 def moe_update_selection_bias(cfg, counts, sel_bias, gamma, load_cv=None, stream=None):

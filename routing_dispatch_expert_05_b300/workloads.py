@@ -152,6 +152,9 @@ class MoEInputs:
 
     def first_tokens(self, n: int) -> "MoEInputs":
         """The same layer applied to the first n tokens only (views, no copy)."""
+        have = self.values["x"].shape[0]
+        if not 0 <= n <= have:
+            raise ValueError(f"first_tokens({n}): these inputs hold {have} tokens")
         v = dict(self.values)
         b = dict(self.bits)
         v["x"] = self.values["x"][:n]

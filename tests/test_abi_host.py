@@ -129,6 +129,37 @@ def test_stage_calls_reject_bad_pointers_before_the_device(lib):
     assert st == -1
 
 
+def test_binding_refuses_token_rows_smaller_than_the_config(lib):
+    """The Python binding checks each [n_tokens, d_model] tensor against the
+    config before the call: the library takes plain pointers and would read
+    (or write) past the end of a shorter buffer."""
+    import torch
+    shape = W.WORKLOADS["capacity_top2_bf16"]
+    cfg = M.make_config(shape)
+    short = torch.zeros(shape.n_tokens - 1, shape.d_model, dtype=torch.bfloat16)
+    full = torch.zeros(shape.n_tokens, shape.d_model, dtype=torch.bfloat16)
+    w = M.MoEWeights()
+    sts = None
+    with pytest.raises(ValueError, match="x:"):
+        M.moe_forward(cfg, short, w, full, sts, None)
+    with pytest.raises(ValueError, match="out:"):
+        M.moe_forward(cfg, full, w, short, sts, None)
+    with pytest.raises(ValueError, match="x_host:"):
+        M.moe_forward_host(cfg, short, w, full, sts, None)
+    with pytest.raises(ValueError, match="x:"):
+        M.moe_router_topk(cfg, short, w, None, None, None, None, None)
+    with pytest.raises(ValueError, match="x:"):
+        M.moe_dispatch_permute(cfg, None, short, None, None, None, None, None, None)
+    with pytest.raises(ValueError, match="out:"):
+        M.moe_combine(cfg, None, None, None, None, short, None)
+    with pytest.raises(ValueError, match="dout:"):
+        M.moe_backward(cfg, full, w, short, 0.0, M.MoEGrads(), None)
+    # big enough: the call reaches the library, which rejects the missing
+    # workspace on the host
+    with pytest.raises(M.MoEError):
+        M.moe_forward(cfg, full, w, full, sts, None)
+
+
 def test_forward_timed_rejects_a_wrong_event_count(lib):
     cfg = M.make_config(W.WORKLOADS["toy_top2_fp32"])
     w = M.MoEWeights()

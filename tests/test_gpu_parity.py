@@ -688,12 +688,13 @@ def test_forward_host_matches_forward():
     assert torch.equal(oh, out.cpu())
 
 
-@pytest.mark.parametrize("N", [12288 + 96, 8200])
+@pytest.mark.parametrize("N", [16384, 12288 + 96, 8200])
 def test_forward_host_pipelined_matches_forward(N):
     """Without a capacity, moe_forward_host splits the tokens into chunks and
     overlaps the host copies with the compute; the output and every
-    statistic equal one moe_forward over all tokens, bit for bit (three
-    chunks with a ragged tail; two chunks, the last under 4096 tokens)."""
+    statistic equal one moe_forward over all tokens, bit for bit (four
+    chunks in the proportions 3:5:5:3 over the whole layer; three in 3:5:3;
+    two equal chunks with a ragged tail)."""
     inp = inputs_for("qwen3_moe", N)
     D = Device(inp)
     shape = inp.shape
