@@ -606,6 +606,14 @@ def run_ours(args, shape, peaks, peaks_kind):
                    "forward_graph_ms_per_step": (round(graph_ms, 4)
                                                  if isinstance(graph_ms, float) else graph_ms),
                    "timed_api": "moe_forward_timed (events between stages)",
+                   "timed_region": {
+                       "seconds": round(h_end - h_start, 3),
+                       "regime": ("power-capped (sw_power_cap seen in the region)"
+                                  if clocks and "sw_power_cap" in clocks.get("reasons", [])
+                                  else "no power cap seen in the region"),
+                       "note": "the default 200 steps are long enough for clock samples "
+                               "inside the region; short bursts (--steps 20) run faster "
+                               "before the power cap engages"},
                    "grouped_gemm_tflops": round(grouped_flop / (grouped_ms * 1e-3) / 1e12, 1),
                    "grouped_gemm_frac_of_burst": round(
                        grouped_flop / (grouped_ms * 1e-3) / 1e12 / peak_tf, 4),
