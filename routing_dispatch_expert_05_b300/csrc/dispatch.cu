@@ -35,15 +35,15 @@ constexpr int kRankWarps = 8;
 
 __global__ void __launch_bounds__(256)
 dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
-                      int n_experts, int32_t* __restrict__ chunk_cnt,
+                      int n_experts, int tpc, int32_t* __restrict__ chunk_cnt,
                       int32_t* __restrict__ err) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ int s_cnt[kMaxExperts];
   for (int e = threadIdx.x; e < n_experts; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  const int64_t t0 = (int64_t)blockIdx.x * kDispatchTokensPerChunk;
-  const int64_t t1 = min(n_tokens, t0 + kDispatchTokensPerChunk);
+  const int64_t t0 = (int64_t)blockIdx.x * tpc;
+  const int64_t t1 = min(n_tokens, t0 + tpc);
   for (int64_t s = t0 * top_k + threadIdx.x; s < t1 * top_k; s += blockDim.x) {
     const int e = idx[s];
     if (e < 0 || e >= n_experts) {
@@ -59,7 +59,14 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top
 
 // The capacity of expert e is `capacity` (< 0: none), or room[e] when a
 // per-expert room is given (what a shard of a larger batch may still keep).
-__global__ void __launch_bounds__(kMaxExperts)
+// One CTA.  The chunks are split into `slices` runs per expert (thread
+// (slice, e), experts warp-contiguous so the loads coalesce); each thread
+// sums its run, the runs' sums are scanned in slice order, and each thread
+// then writes its run's chunk bases.  The group starts are a two-level
+// shuffle scan over the experts.  All integer: the order of the additions
+// does not change any result.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
                      int n_experts, int64_t capacity, const int32_t* __restrict__ room,
                      int pad, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
@@ -67,31 +74,61 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
                      int32_t* __restrict__ dropped) {
   pdl_wait();
   pdl_launch_dependents();
+  __shared__ int s_part[kScanThreads];             // run sums, [slice][e_span]
   __shared__ int s_kept[kMaxExperts];
-  const int e = threadIdx.x;
-  if (e < n_experts) {
+  __shared__ int s_wsum[kMaxExperts / 32];
+  const int e_span = (n_experts + 31) / 32 * 32;   // <= kMaxExperts
+  const int slices = kScanThreads / e_span;        // >= 4
+  const int e = threadIdx.x % e_span, sl = threadIdx.x / e_span;
+  const bool mine = sl < slices && e < n_experts;
+  const int per = (n_chunks + slices - 1) / slices;
+  const int c0 = min(n_chunks, sl * per), c1 = min(n_chunks, c0 + per);
+  int sum = 0;
+  if (mine)
+    for (int c = c0; c < c1; ++c) sum += chunk_cnt[(int64_t)c * n_experts + e];
+  if (sl < slices) s_part[sl * e_span + e] = sum;
+  __syncthreads();
+  if (mine) {
     int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
+    for (int q = 0; q < sl; ++q) run += s_part[q * e_span + e];
+    for (int c = c0; c < c1; ++c) {
       const int64_t o = (int64_t)c * n_experts + e;
       const int v = chunk_cnt[o];
       chunk_base[o] = run;
       run += v;
     }
+  }
+  if (sl == 0 && e < n_experts) {
+    int total = 0;
+    for (int q = 0; q < slices; ++q) total += s_part[q * e_span + e];
     const int64_t cap = room != nullptr ? (int64_t)max(room[e], 0) : capacity;
-    const int kp = cap < 0 ? run : (int)min((int64_t)run, cap);
+    const int kp = cap < 0 ? total : (int)min((int64_t)total, cap);
     s_kept[e] = kp;
-    if (counts) counts[e] = run;
+    if (counts) counts[e] = total;
     if (kept) kept[e] = kp;
-    if (dropped) dropped[e] = run - kp;
+    if (dropped) dropped[e] = total - kp;
   }
   __syncthreads();
-  if (e == 0) {
-    int acc = 0;
-    for (int q = 0; q < n_experts; ++q) {
-      offsets[q] = acc;
-      acc += (s_kept[q] + pad - 1) / pad * pad;   // pad > 1: zero rows after the kept
+  // offsets = exclusive scan of the kept rows (pad > 1: rounded up to
+  // multiples of pad, zero rows after the kept)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int v = 0, incl = 0;
+  if (threadIdx.x < kMaxExperts) {
+    v = threadIdx.x < n_experts ? (s_kept[threadIdx.x] + pad - 1) / pad * pad : 0;
+    incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
     }
-    offsets[n_experts] = acc;
+    if (lane == 31) s_wsum[w] = incl;
+  }
+  __syncthreads();
+  if (threadIdx.x < n_experts) {
+    int base = 0;
+    for (int q = 0; q < w; ++q) base += s_wsum[q];
+    offsets[threadIdx.x] = base + incl - v;
+    if (threadIdx.x == n_experts - 1) offsets[n_experts] = base + incl;
   }
 }
 
@@ -101,7 +138,7 @@ dispatch_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks,
 // With padded groups kept_e comes from kept_rows instead.
 __global__ void __launch_bounds__(kRankWarps * 32)
 dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_k,
-                     int n_experts,
+                     int n_experts, int tpc,
                      const int32_t* __restrict__ chunk_base,
                      const int32_t* __restrict__ offsets,
                      const int32_t* __restrict__ kept_rows,
@@ -116,8 +153,8 @@ dispatch_rank_kernel(const int32_t* __restrict__ idx, int64_t n_tokens, int top_
     (&s_w[0][0])[i] = 0;
   __syncthreads();
 
-  const int64_t t0 = (int64_t)blockIdx.x * kDispatchTokensPerChunk;
-  const int64_t t1 = min(n_tokens, t0 + kDispatchTokensPerChunk);
+  const int64_t t0 = (int64_t)blockIdx.x * tpc;
+  const int64_t t1 = min(n_tokens, t0 + tpc);
   const int64_t s0 = t0 * top_k, s1 = t1 * top_k;
   const int64_t per_warp = ceil_div64(s1 - s0, kRankWarps);
   const int64_t ws0 = s0 + warp * per_warp;
@@ -319,17 +356,17 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* chunk_base, int32_t* offsets, int32_t* row_of_slot,
                      int32_t* token_of_row, int32_t* counts, int32_t* kept,
                      int32_t* dropped, int32_t* err, cudaStream_t st,
-                     int32_t* slot_of_row, const int32_t* room, int pad) {
-  const int chunks = (int)ceil_div64(n_tokens, kDispatchTokensPerChunk);
+                     int32_t* slot_of_row, const int32_t* room, int pad, int tpc) {
+  const int chunks = (int)ceil_div64(n_tokens, tpc);
   if (chunks > 0)
     launch_pdl(dispatch_count_kernel, dim3(chunks), dim3(256), 0, st, idx, n_tokens, top_k,
-               n_experts, chunk_cnt, err);
+               n_experts, tpc, chunk_cnt, err);
   pad = pad > 1 && kept != nullptr ? pad : 1;      // padding needs the kept counts
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, chunk_cnt, chunks,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, chunk_cnt, chunks,
              n_experts, capacity, room, pad, chunk_base, offsets, counts, kept, dropped);
   if (chunks > 0)
     launch_pdl(dispatch_rank_kernel, dim3(chunks), dim3(kRankWarps * 32), 0, st, idx, n_tokens,
-               top_k, n_experts, chunk_base, offsets,
+               top_k, n_experts, tpc, chunk_base, offsets,
                pad > 1 ? static_cast<const int32_t*>(kept) : nullptr, row_of_slot,
                token_of_row, slot_of_row);
 }

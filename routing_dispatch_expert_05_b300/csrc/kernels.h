@@ -13,7 +13,7 @@ namespace moe {
 // same tokens either way.
 constexpr int kRouteTokensPerCta = 32;
 // Tokens per dispatch chunk (the unit of the per-chunk histogram).
-constexpr int kDispatchTokensPerChunk = 256;
+constexpr int kDispatchTokensPerChunk = 128;
 constexpr int kMaxExperts = 256;
 
 // ---- router ---------------------------------------------------------------
@@ -59,7 +59,8 @@ void launch_dispatch(const int32_t* idx, int64_t n_tokens, int top_k,
                      int32_t* row_of_slot, int32_t* token_of_row,
                      int32_t* counts, int32_t* kept, int32_t* dropped,
                      int32_t* err, cudaStream_t st, int32_t* slot_of_row = nullptr,
-                     const int32_t* room = nullptr, int pad = 1);
+                     const int32_t* room = nullptr, int pad = 1,
+                     int tokens_per_chunk = kDispatchTokensPerChunk);
 // x_perm[row_of_slot[t*k + j]] = x[t] for every kept slot (one warp per token,
 // 32- or 16-byte vectors; a TMA bulk-copy version measured slower)
 void launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* row_of_slot,

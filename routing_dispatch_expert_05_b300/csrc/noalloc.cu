@@ -23,10 +23,13 @@ namespace moe {
 namespace {
 
 constexpr int64_t kNoAllocMaxTokens = 65536;
-constexpr int64_t kNoAllocMaxChunks = kNoAllocMaxTokens / kDispatchTokensPerChunk;  // 256
+// tokens per histogram chunk here: wider than moe_dispatch_permute's, so the
+// fixed array stays at 512 KB
+constexpr int kNoAllocTokensPerChunk = 256;
+constexpr int64_t kNoAllocMaxChunks = kNoAllocMaxTokens / kNoAllocTokensPerChunk;  // 256
 // per-chunk counts and per-chunk bases, [chunks][E] int32 each
 constexpr size_t kNoAllocBytes = 2 * (size_t)kNoAllocMaxChunks * kMaxExperts * 4;
-static_assert(kNoAllocMaxTokens % kDispatchTokensPerChunk == 0, "whole chunks");
+static_assert(kNoAllocMaxTokens % kNoAllocTokensPerChunk == 0, "whole chunks");
 
 // The scratch.  In host code this name is only a stand-in for the device
 // array: its device address comes from cudaGetSymbolAddress, per device.
@@ -94,7 +97,7 @@ extern "C" moe_status_t moe_dispatch_permute_noalloc(const moe_config_t* cfg,
   void* scratch = nullptr;
   const moe_status_t s = scratch_address(&scratch);
   if (s != MOE_OK) return s;
-  const int chunks = (int)ceil_div64(c.n_tokens, kDispatchTokensPerChunk);
+  const int chunks = (int)ceil_div64(c.n_tokens, kNoAllocTokensPerChunk);
   int32_t* chunk_cnt = static_cast<int32_t*>(scratch);
   int32_t* chunk_base = chunk_cnt + (size_t)chunks * c.n_experts;
   int64_t capacity = -1;
@@ -107,7 +110,8 @@ extern "C" moe_status_t moe_dispatch_permute_noalloc(const moe_config_t* cfg,
   launch_dispatch(idx, c.n_tokens, c.top_k, c.n_experts, capacity, chunk_cnt, chunk_base,
                   offsets, row_of_slot, token_of_row, stats ? stats->counts : nullptr,
                   stats ? stats->kept : nullptr, stats ? stats->dropped : nullptr,
-                  /*err=*/nullptr, st);
+                  /*err=*/nullptr, st, /*slot_of_row=*/nullptr, /*room=*/nullptr, /*pad=*/1,
+                  kNoAllocTokensPerChunk);
   if (x_perm != nullptr) {
     // the row copy from the token side, as moe_dispatch_permute makes it:
     // each token row is read once and written to each of its kept rows
