@@ -82,6 +82,21 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def build_library():
+    """Build the CUDA library if it is out of date, once per host: ranks
+    started together take a file lock in turn, so the first compiles and the
+    others find the library up to date."""
+    import fcntl
+    from routing_dispatch_expert_05_b300 import build as B
+    os.makedirs(B.BUILD_DIR, exist_ok=True)
+    with open(os.path.join(B.BUILD_DIR, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return B.build()
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -793,8 +808,7 @@ def main(argv=None):
     if args.impl == "reference":
         res, rank = run_reference(args, shape)
     else:
-        from routing_dispatch_expert_05_b300 import build as B
-        B.build()
+        build_library()
         peaks, kind = load_peaks()
         if args.backward:
             res, rank = run_backward(args, shape, peaks, kind), 0

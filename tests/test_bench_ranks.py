@@ -127,3 +127,28 @@ def test_bench_rejects_too_few_warmup_steps():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--impl", "reference", "--warmup", "2"])
+
+
+def _build_main(out, i):
+    sys.path.insert(0, ROOT)
+    import bench
+    out[i] = bench.build_library()
+
+
+def test_ranks_started_together_build_the_library_in_turn():
+    """bench.py under torchrun: every rank calls the build step at once; the
+    file lock lets them through one at a time and all get the library."""
+    sys.path.insert(0, ROOT)
+    from routing_dispatch_expert_05_b300 import build as B
+    B.build()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_build_main, args=(out, i)) for i in range(3)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(600)
+            assert p.exitcode == 0
+        res = dict(out)
+    assert sorted(res) == [0, 1, 2] and set(res.values()) == {B.LIB_PATH}
