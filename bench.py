@@ -431,10 +431,10 @@ def run_ours(args, shape, peaks, peaks_kind):
     from routing_dispatch_expert_05_b300 import moe as M
 
     ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)            # before the group, so NCCL binds this GPU
+    dev = torch.device("cuda", local)
     if ws_n > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
 
     inputs = W.make_inputs(shape)
     t = M.upload(inputs, device=dev)
