@@ -888,7 +888,8 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
     last.counts = stats->counts ? stats->counts : stats->kept;
     last.balance = stats->balance;
   }
-  for (int i = 0; ok && i < nrun; ++i) {
+  moe_status_t status = MOE_OK;
+  for (int i = 0; ok && status == MOE_OK && i < nrun; ++i) {
     const int64_t s0 = bound[i];
     const int64_t n = bound[i + 1] - s0;
     ok = cudaMemcpyAsync(xd + s0 * row, xh + s0 * row, n * row, cudaMemcpyHostToDevice,
@@ -899,24 +900,30 @@ moe_status_t forward_host_pipelined(const moe_config_t& c, const char* xh,
     moe_config_t ci = c;
     ci.n_tokens = n;
     const bool fin = i == nrun - 1;
-    MOE_TRY(forward_core(ci, L, sc, fin, c.n_tokens, xd + s0 * row, w, od + s0 * row,
-                         fin ? &last : &none, ws, st, nullptr));
+    status = forward_core(ci, L, sc, fin, c.n_tokens, xd + s0 * row, w, od + s0 * row,
+                          fin ? &last : &none, ws, st, nullptr);
+    if (status != MOE_OK) break;
     ok = cudaEventRecord(hp.done[i], st) == cudaSuccess &&
          cudaStreamWaitEvent(hp.d2h, hp.done[i], 0) == cudaSuccess &&
          cudaMemcpyAsync(oh + s0 * row, od + s0 * row, n * row, cudaMemcpyDeviceToHost,
                          hp.d2h) == cudaSuccess;
   }
-  if (ok && stats != nullptr) {
+  if (ok && status == MOE_OK && stats != nullptr) {
     int32_t* counts = last.counts;
     const size_t eb = (size_t)c.n_experts * 4;
     if (stats->kept && counts != stats->kept)
       ok = cudaMemcpyAsync(stats->kept, counts, eb, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
     if (ok && stats->dropped) ok = cudaMemsetAsync(stats->dropped, 0, eb, st) == cudaSuccess;
   }
-  // the caller's stream completes with the last copy back
-  ok = ok && cudaEventRecord(hp.out_done, hp.d2h) == cudaSuccess &&
-       cudaStreamWaitEvent(st, hp.out_done, 0) == cudaSuccess;
-  return ok ? last_cuda() : MOE_ERR_CUDA;
+  // The caller's stream completes with the last copy back, and with every
+  // other copy the call enqueued even when an enqueue above failed, so the
+  // caller's buffers outlive the copies whatever the call returns.
+  const bool joined = cudaEventRecord(hp.out_done, hp.d2h) == cudaSuccess &&
+                      cudaStreamWaitEvent(st, hp.out_done, 0) == cudaSuccess &&
+                      cudaEventRecord(hp.start, hp.h2d) == cudaSuccess &&
+                      cudaStreamWaitEvent(st, hp.start, 0) == cudaSuccess;
+  if (status != MOE_OK) return status;
+  return ok && joined ? last_cuda() : MOE_ERR_CUDA;
 }
 
 // ---- backward -------------------------------------------------------------
